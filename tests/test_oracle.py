@@ -1,0 +1,224 @@
+"""Pins of the CPU oracle against things other than itself (no GPU needed).
+
+Every check compares the oracle with an independent fact: LAPACK / scipy on the
+dense or banded matrix assembled from the band definition, a closed form of
+the discrete scheme, an invariant of the scheme, or the convergence order the
+cuPentBatch page reports for its exact-solution test (eq. (14), Fig. 2).
+"""
+import os
+
+import numpy as np
+import pytest
+import scipy.linalg
+
+import oracle
+from implicit_pde_stepping_gb300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def dense(bands, cyclic):
+    """Assemble the N x N matrix: row i holds bands a..e at columns i-2..i+2."""
+    bands = np.asarray(bands, dtype=np.float64)
+    N = bands.shape[1]
+    A = np.zeros((N, N))
+    for i in range(N):
+        for k in range(5):
+            col = i + k - 2
+            if cyclic:
+                A[i, col % N] += bands[k, i]
+            elif 0 <= col < N:
+                A[i, col] += bands[k, i]
+    return A
+
+
+def random_dd_bands(N, rng):
+    b = rng.uniform(-1, 1, size=(5, N))
+    for i in range(N):
+        b[2, i] = 1.0 + np.abs(b[[0, 1, 3, 4], i]).sum() + rng.uniform(0, 1)
+    return b
+
+
+def rel(x, ref):
+    return np.max(np.abs(x - ref)) / max(np.max(np.abs(ref)), 1e-300)
+
+
+# ---------------------------------------------------------------------------
+# non-cyclic LR solve against LAPACK / scipy
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("N", list(range(1, 17)) + [33, 128])
+@pytest.mark.parametrize("kind", ["dd", "s0.1", "s1", "s10"])
+def test_noncyclic_matches_lapack(N, kind):
+    rng = np.random.default_rng(1000 + N)
+    bands = random_dd_bands(N, rng) if kind == "dd" else inputs.hyper_bands(N, float(kind[1:]))
+    f = rng.uniform(-1, 1, N)
+    x = oracle.solve(*bands, f)
+    ref = np.linalg.solve(dense(bands, False), f)
+    assert rel(x, ref) < 1e-12
+
+
+def test_noncyclic_config_matrix_matches_solve_banded():
+    """N=1024, sigma=1 (the shared-matrix throughput matrix) against scipy's banded LU."""
+    N = 1024
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, 8)
+    X = oracle.batch_shared(bands, F, cyclic=False)
+    ab = np.zeros((5, N))          # scipy's diagonal-ordered form, ab[2 + i - j, j] = A[i, j]
+    for k, off in enumerate((-2, -1, 0, 1, 2)):
+        # band k of row i sits at column j = i + off -> ab[2 - off, i + off]
+        for i in range(N):
+            j = i + off
+            if 0 <= j < N:
+                ab[2 - off, j] = bands[k, i]
+    ref = scipy.linalg.solve_banded((2, 2), ab, F)
+    assert rel(X, ref) < 1e-12
+
+
+def test_noncyclic_factor_reproduces_matrix():
+    """L R with the factor vectors equals A (L: alpha diag, beta sub, eps subsub; R: unit, gamma, delta)."""
+    rng = np.random.default_rng(7)
+    N = 12
+    bands = random_dd_bands(N, rng)
+    alpha, beta, gamma, delta, eps = oracle.factor(*bands)
+    Lm = np.diag(alpha) + np.diag(beta[1:], -1) + np.diag(eps[2:], -2)
+    Rm = np.eye(N) + np.diag(gamma[:-1], 1) + np.diag(delta[:-2], 2)
+    assert np.max(np.abs(Lm @ Rm - dense(bands, False))) < 1e-13
+
+
+# ---------------------------------------------------------------------------
+# cyclic (bordered) solve
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("N", list(range(5, 17)) + [64, 257])
+@pytest.mark.parametrize("kind", ["dd", "s0.5", "s10.48576"])
+def test_cyclic_matches_lapack(N, kind):
+    rng = np.random.default_rng(2000 + N)
+    bands = random_dd_bands(N, rng) if kind == "dd" else inputs.hyper_bands(N, float(kind[1:]))
+    f = rng.uniform(-1, 1, N)
+    x = oracle.solve(*bands, f, cyclic=True)
+    ref = np.linalg.solve(dense(bands, True), f)
+    assert rel(x, ref) < 1e-12
+
+
+def test_cyclic_rejects_small_n():
+    with pytest.raises(oracle.OracleError):
+        oracle.solve(*inputs.hyper_bands(4, 1.0), np.ones(4), cyclic=True)
+
+
+def test_zero_pivot_reported():
+    bands = np.zeros((5, 6))
+    with pytest.raises(oracle.OracleError):
+        oracle.solve(*bands, np.ones(6))
+
+
+# ---------------------------------------------------------------------------
+# manufactured solutions and symmetry
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cyclic", [False, True])
+def test_manufactured_solution_persys(cyclic):
+    rng = np.random.default_rng(3)
+    N, batch = 40, 16
+    xs = rng.uniform(-1, 1, (N, batch))
+    bands_all = [random_dd_bands(N, rng) for _ in range(batch)]
+    for s in range(batch):
+        f = dense(bands_all[s], cyclic) @ xs[:, s]
+        x = oracle.solve(*bands_all[s], f, cyclic=cyclic)
+        assert rel(x, xs[:, s]) < 1e-13
+
+
+def test_batch_persys_matches_single():
+    N, batch = 24, 6
+    a, b, c, d, e = inputs.persys_bands(N, batch, seed=3)
+    F = inputs.rhs_uniform(N, batch, seed=3).astype(np.float32)
+    X = oracle.batch_persys(a, b, c, d, e, F)
+    for s in range(batch):
+        bands = np.stack([v[:, s].astype(np.float64) for v in (a, b, c, d, e)])
+        ref = np.linalg.solve(dense(bands, False), F[:, s].astype(np.float64))
+        assert rel(X[:, s], ref) < 1e-12
+
+
+def test_persymmetry_constant_bands():
+    """For symmetric constant bands J A J = A, so reversing f reverses x."""
+    N = 301
+    bands = inputs.hyper_bands(N, 1.0)
+    f = np.random.default_rng(5).uniform(-1, 1, N)
+    x = oracle.solve(*bands, f)
+    xr = oracle.solve(*bands, f[::-1].copy())
+    assert rel(xr[::-1], x) < 1e-13
+
+
+# ---------------------------------------------------------------------------
+# closed forms of the discrete schemes
+# ---------------------------------------------------------------------------
+def test_hyperdiffusion_discrete_amplification():
+    """Periodic Fourier data: each mode k is multiplied by 1/(1 + 16 sigma sin^4(pi k/N)) per step."""
+    N, sigma, steps, batch = 512, 0.5, 100, 4
+    C0 = inputs.fourier_initial(N, batch)
+    CT = oracle.batch_hyperdiffusion(C0, sigma, steps)
+    a, b = inputs.fourier_modes(N, batch)
+    k = np.arange(1, 9)
+    G = 1.0 / (1.0 + 16.0 * sigma * np.sin(np.pi * k / N) ** 4)
+    x = np.arange(N) / N
+    ph = 2 * np.pi * k[:, None] * x[None, :]
+    ref = np.cos(ph).T @ (a * (G ** steps)[:, None]) + np.sin(ph).T @ (b * (G ** steps)[:, None])
+    assert rel(CT, ref) < 1e-12
+    # the damping is visible: mode 8 loses ~0.46% over 100 steps
+    assert abs(G[7] ** steps - 0.99541) < 1e-4
+
+
+def test_ch_mass_conservation():
+    N, batch, steps = 1024, 4, 200
+    sigma, k2 = inputs.ch_params(N)
+    C0 = inputs.ch_initial(N, batch)
+    CT = oracle.batch_ch(C0, sigma, k2, steps)
+    assert np.max(np.abs(CT.mean(axis=0) - C0.mean(axis=0))) < 1e-12
+    assert np.max(np.abs(CT - C0)) > 1e-6     # it did evolve
+
+
+def test_ch_linearised_single_mode():
+    """Amplitude 1e-7: the cubic term is ~1e-14 relative, so each step multiplies mode k by
+    (1 + 4 (dt/dx^2) sin^2(pi k/N)) / (1 + 16 sigma sin^4(pi k/N))."""
+    N = 1024
+    sigma, k2 = inputs.ch_params(N)
+    x = np.arange(N) / N
+    for kk, steps in ((3, 20), (40, 20), (71, 20), (200, 2)):
+        # steps kept small enough that G^steps >= 1e-3: a mode damped further
+        # sinks below the rounding noise of the others
+        C0 = 1e-7 * np.cos(2 * np.pi * kk * x)[:, None]
+        CT = oracle.batch_ch(C0, sigma, k2, steps)
+        s = np.sin(np.pi * kk / N)
+        G = (1.0 + 4.0 * k2 * s * s) / (1.0 + 16.0 * sigma * s ** 4)
+        assert G ** steps > 1e-3
+        assert rel(CT, C0 * G ** steps) < 1e-9
+
+
+def _golden(name):
+    vals = {}
+    with open(os.path.join(GOLDEN, name)) as fh:
+        for line in fh:
+            line = line.split("#", 1)[0].strip()
+            if line:
+                k, v = line.split()
+                vals[k] = float(v)
+    return vals
+
+
+def test_hyperdiffusion_exact_solution_convergence_order():
+    """The page's validation set-up (eq. (14), Figs. 1–2): the L2 error against
+    A cos(kx) exp(-gamma D k^4 T) falls as N^-2.  Backward Euler with a small
+    dt keeps the time error below the spatial one."""
+    g = _golden("hyperdiffusion_exact.txt")
+    k = 2 * np.pi * g["n"] / g["L"]
+    lam = g["gamma"] * g["D"] * k ** 4
+    T, dt = g["T"], 1e-9
+    steps = int(round(T / dt))
+    errs = []
+    Ns = (32, 64, 128)
+    for N in Ns:
+        dx = g["L"] / N
+        x = np.arange(N) * dx
+        C0 = (g["A"] * np.cos(k * x + g["phi"]))[:, None]
+        CT = oracle.batch_hyperdiffusion(C0, g["gamma"] * g["D"] * dt / dx ** 4, steps)[:, 0]
+        exact = g["A"] * np.cos(k * x + g["phi"]) * np.exp(-lam * T)
+        errs.append(np.sqrt(np.sum((CT - exact) ** 2) * dx))
+    orders = [np.log2(errs[i] / errs[i + 1]) for i in range(len(errs) - 1)]
+    assert all(abs(o - g["error_order"]) < 0.15 for o in orders), (errs, orders)
