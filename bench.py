@@ -1,0 +1,481 @@
+#!/usr/bin/env python
+"""Benchmark of the batched pentadiagonal solves on GB300.
+
+Default workload: the shared-matrix solve, N = 1024, batch = 65536, fp64,
+bands [1, -4, 7, -4, 1] (sigma = 1, non-cyclic), factored once; one step = one
+solve of the whole batch (read f, write x: 2 x 512 MB).  Other workloads
+(--workload small | cyclic | persys | ch) time the other rows of the hot path.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  `value` is whole-job throughput with inputs
+resident in HBM; `e2e` is the same metric through the public Python API with
+pinned host buffers, both copies inside the timed region; `roofline` is the
+dominant kernel's algorithmic bandwidth against the measured HBM peak;
+`cpu_baseline` times the CPU oracle on a bounded sample.  With --gpus > 1 (under
+torchrun) every rank solves its own batch (weak scaling, no collective on the
+data path); the timed region is bracketed by barriers and the max over ranks is
+taken.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "pentadiagonal system-solves/s (N=1024, fp64) and HBM GB/s vs GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+
+WORKLOADS = {
+    "shared": dict(N=1024, batch=65536, kind="shared", sigma=1.0, cyclic=False, dtype="f64",
+                   desc="shared-matrix pentadiagonal solve, N=1024, batch=65536, fp64, "
+                        "bands [1,-4,7,-4,1] (sigma=1), non-cyclic, factor once"),
+    "small": dict(N=128, batch=1024, kind="shared", sigma=1.0, cyclic=False, dtype="f64",
+                  desc="shared-matrix pentadiagonal solve, N=128, batch=1024, fp64, sigma=1"),
+    "cyclic": dict(N=512, batch=4096, kind="hyper", sigma=0.5, cyclic=True, dtype="f64",
+                   desc="periodic hyperdiffusion step, cyclic I+0.5*D4, N=512, batch=4096, fp64"),
+    "persys": dict(N=256, batch=262144, kind="persys", dtype="f32",
+                   desc="per-system factor+solve, N=256, batch=262144, fp32, diagonally dominant"),
+    "ch": dict(N=1024, batch=16384, kind="ch", cyclic=True, dtype="f64",
+               desc="semi-implicit Cahn-Hilliard step (fused RHS + cyclic solve), N=1024, "
+                    "batch=16384, fp64, gamma=1e-4, dt=0.1dx^2"),
+}
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+# ----------------------------------------------------------------------------
+# distributed plumbing (one process per GPU, NCCL only for barrier / max)
+# ----------------------------------------------------------------------------
+class Dist:
+    def __init__(self, ngpus: int):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        if self.pg is None:
+            return v
+        import torch
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def shard(batch: int, world: int, rank: int, weak: bool = True):
+    """Systems of this rank.  Weak scaling: every rank gets the full per-GPU batch."""
+    if weak:
+        return batch
+    base, rem = divmod(batch, world)
+    return base + (1 if rank < rem else 0)
+
+
+# ----------------------------------------------------------------------------
+# clocks during the timed region
+# ----------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+        return False
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append(dict(sm=float(parts[0]), max=float(parts[1]), power=float(parts[2]),
+                                 hw=parts[4], hwt=parts[5], swt=parts[6], swp=parts[7]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("swp", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        loaded = [r["sm"] for r in rows if r["power"] > 0] or [r["sm"] for r in rows]
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows),
+                "power_w_max": max(r["power"] for r in rows)}
+
+
+# ----------------------------------------------------------------------------
+# peaks and ncu traffic
+# ----------------------------------------------------------------------------
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(kernel_file: str) -> str:
+    h = hashlib.sha256()
+    for name in (kernel_file, "pent_internal.cuh", "df64.cuh"):
+        path = os.path.join(ROOT, "implicit_pde_stepping_gb300", "csrc", name)
+        if os.path.exists(path):
+            with open(path, "rb") as fh:
+                h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, kernel_file: str, workload: str, units: int):
+    """DRAM bytes per launch from the committed ncu summary, scaled to `units` systems when
+    the capture was taken on a smaller case; None if the kernel changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as fh:
+            table = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    rec = table.get(f"{kernel}@{workload}")
+    if not rec or rec.get("source_digest") != source_digest(kernel_file):
+        return None
+    return float(rec["dram_bytes_per_launch"]) * units / float(rec["units"])
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, W: dict, dist: Dist):
+    import numpy as np
+    import torch
+
+    from implicit_pde_stepping_gb300 import inputs, pent
+
+    dev_index = dist.local if dist.world > 1 else 0
+    torch.cuda.set_device(dev_index)
+    stream = torch.cuda.Stream()
+    N = W["N"]
+    batch = shard(args.batch or W["batch"], dist.world, dist.rank, weak=True)
+    kind = W["kind"]
+    seed = dist.rank
+    fdt = torch.float64 if W["dtype"] == "f64" else torch.float32
+    elem = 8 if W["dtype"] == "f64" else 4
+
+    # ---- inputs (host generator -> HBM), plan
+    plan = None
+    k2 = None
+    if kind in ("shared", "hyper"):
+        plan = pent.pent_factor(inputs.hyper_bands(N, W["sigma"]), batch, cyclic=W["cyclic"])
+        bufs = [torch.from_numpy(inputs.rhs_uniform(N, batch, seed=seed + r) if kind == "shared"
+                                 else inputs.fourier_initial(N, batch, seed=seed + r)).to("cuda")
+                for r in range(2)]
+    elif kind == "ch":
+        sigma, k2 = inputs.ch_params(N)
+        plan = pent.pent_factor(inputs.hyper_bands(N, sigma), batch, cyclic=True)
+        bufs = [torch.from_numpy(inputs.ch_initial(N, batch, seed=seed + r)).to("cuda")
+                for r in range(2)]
+    else:  # persys
+        bands = [torch.from_numpy(v).to("cuda") for v in inputs.persys_bands(N, batch, seed=seed)]
+        bufs = [torch.from_numpy(inputs.rhs_uniform(N, batch, seed=seed + r).astype(np.float32))
+                .to("cuda") for r in range(2)]
+        work = torch.empty(pent.pent_factor_solve_work_bytes(N, batch, pent.F32),
+                           dtype=torch.uint8, device="cuda")
+    if plan is not None and args.variant != "auto":
+        plan.set_variant(args.variant)
+    variant = plan.variant(batch) if plan is not None else pent.VARIANT_THREAD
+    torch.cuda.synchronize()
+
+    def step(k, X=None):
+        X = bufs[k % 2] if X is None else X
+        if kind == "shared":
+            pent.pent_solve(plan, X, stream=stream)
+        elif kind == "hyper":
+            pent.hyperdiffusion_step(plan, X, 1, stream=stream)
+        elif kind == "ch":
+            pent.ch_step(plan, X, k2, 1, stream=stream)
+        else:
+            pent.pent_factor_solve(*bands, X, work=work, stream=stream)
+
+    # ---- device-resident timing
+    with torch.cuda.stream(stream):
+        for k in range(args.warmup):
+            step(k)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    dist.barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = pent.launch_count()
+    with ClockSampler(dev_index) as clocks:
+        with torch.cuda.stream(stream):
+            t_start.record(stream)
+            for k in range(args.steps):
+                ev[k][0].record(stream)
+                step(k)
+                ev[k][1].record(stream)
+            t_end.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+    launches = pent.launch_count() - l0
+    dist.barrier()
+    ms_local = t_start.elapsed_time(t_end)
+    ms = dist.max(ms_local)
+    kernel_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    total_units = batch * args.steps * dist.world
+    value = total_units / (ms / 1e3)
+
+    # ---- end to end through the public API: pinned host in, host out, every step
+    e2e = None
+    if not args.no_e2e:
+        host_in = bufs[0].cpu().pin_memory()
+        host_out = torch.empty_like(host_in).pin_memory()
+        Xd = torch.empty_like(bufs[0])
+        ke = max(1, min(args.steps, args.e2e_steps))
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                Xd.copy_(host_in, non_blocking=True)
+                step(0, Xd)
+                host_out.copy_(Xd, non_blocking=True)
+        stream.synchronize()
+        dist.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(ke):
+                Xd.copy_(host_in, non_blocking=True)
+                step(0, Xd)
+                host_out.copy_(Xd, non_blocking=True)
+            e1.record(stream)
+        stream.synchronize()
+        dist.barrier()
+        ems = dist.max(e0.elapsed_time(e1))
+        nbytes = host_in.numel() * host_in.element_size()
+        e2e = {"value": batch * ke * dist.world / (ems / 1e3), "unit": "system-solves/s"
+               if kind in ("shared", "persys") else "system-steps/s",
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": ke,
+               "ms_per_step": ems / ke}
+
+    # ---- roofline of the dominant kernel (one kernel per step on every path)
+    per_unit = {"shared": 2 * N * elem, "hyper": 2 * N * elem, "ch": 2 * N * elem,
+                "persys": 7 * N * elem}[kind]
+    alg_bytes = per_unit * batch
+    achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    kernel_names = {
+        ("shared", pent.VARIANT_THREAD): ("k_shared_thread", "pent_shared.cu"),
+        ("hyper", pent.VARIANT_THREAD): ("k_shared_thread", "pent_shared.cu"),
+        ("ch", pent.VARIANT_THREAD): ("k_ch_thread_f64", "pent_ch.cu"),
+        ("persys", pent.VARIANT_THREAD): ("k_persys_thread", "pent_persys.cu"),
+        ("shared", pent.VARIANT_THREAD_DF): ("k_shared_df", "pent_shared_df.cu"),
+        ("hyper", pent.VARIANT_THREAD_DF): ("k_shared_df", "pent_shared_df.cu"),
+        ("ch", pent.VARIANT_THREAD_DF): ("k_ch_df", "pent_ch_df.cu"),
+        ("shared", pent.VARIANT_SPLIT): ("k_shared_split", "pent_split.cu"),
+    }
+    kname, kfile = kernel_names.get((kind, variant), ("?", "?"))
+    traffic = ncu_traffic(kname, kfile, args.workload, batch)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
+                "measured" else "fallback 6.8 TB/s",
+                "kernel": kname, "kernel_ms": round(kernel_ms, 4),
+                "algorithmic_bytes_per_launch": alg_bytes,
+                "bytes_per_unit": per_unit, "units_per_launch": batch}
+
+    unit = "system-solves/s" if kind in ("shared", "persys") else "system-steps/s"
+    res = {
+        "metric": METRIC if args.workload == "shared" else f"{W['desc']} throughput",
+        "value": value, "unit": unit, "n_gpus": dist.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": W["dtype"],
+        "data": "synthetic (seeded SplitMix64 counter-based generator)",
+        "config": {"workload": W["desc"], "N": N, "batch_per_gpu": batch,
+                   "global_batch": batch * dist.world, "parallelism": f"replicas x{dist.world} "
+                   "(batch split, no collective)", "variant": variant,
+                   "l2": "inputs larger than L2 (two 512 MB buffers alternated)" if kind ==
+                   "shared" else "two input buffers alternated",
+                   "solves_per_second_whole_job": value},
+        "clocks": clocks.summary(), "gpu_launches": int(launches) * dist.world,
+        "e2e": e2e, "roofline": roofline,
+    }
+    return res
+
+
+def run_cpu_baseline(W: dict, seconds: float):
+    """The oracle as it stands, on this host's cores, on a bounded sample of the workload."""
+    import numpy as np
+
+    import oracle
+    from implicit_pde_stepping_gb300 import inputs
+    N, kind = W["N"], W["kind"]
+    if kind == "shared":
+        S = 4096
+        bands = inputs.hyper_bands(N, W["sigma"])
+        F = inputs.rhs_uniform(N, S, seed=0)
+        fn = lambda: oracle.batch_shared(bands, F, cyclic=W["cyclic"])  # noqa: E731
+    elif kind == "hyper":
+        S = 512
+        F = inputs.fourier_initial(N, S)
+        fn = lambda: oracle.batch_hyperdiffusion(F, W["sigma"], 1)  # noqa: E731
+    elif kind == "ch":
+        S = 256
+        sigma, k2 = inputs.ch_params(N)
+        F = inputs.ch_initial(N, S)
+        fn = lambda: oracle.batch_ch(F, sigma, k2, 1)  # noqa: E731
+    else:
+        S = 8192
+        a, b, c, d, e = inputs.persys_bands(N, S)
+        F = inputs.rhs_uniform(N, S).astype(np.float32)
+        fn = lambda: oracle.batch_persys(a, b, c, d, e, F)  # noqa: E731
+    fn()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    unit = "system-solves/s" if kind in ("shared", "persys") else "system-steps/s"
+    return {"value": S * reps / el, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{S} systems of the workload (N={N}) x {reps} repetitions, {el:.1f} s"}
+
+
+def run_reference(args, W: dict, dist: Dist):
+    """Reference arm: the CPU oracle as it stands, timed on this host's cores."""
+    import oracle
+    from implicit_pde_stepping_gb300 import inputs
+    N, kind = W["N"], W["kind"]
+    S = {"shared": 1024, "hyper": 256, "ch": 64, "persys": 2048}[kind]
+    if kind == "shared":
+        bands = inputs.hyper_bands(N, W["sigma"])
+        F = inputs.rhs_uniform(N, S, seed=0)
+        fn = lambda: oracle.batch_shared(bands, F, cyclic=W["cyclic"])  # noqa: E731
+    elif kind == "hyper":
+        F = inputs.fourier_initial(N, S)
+        fn = lambda: oracle.batch_hyperdiffusion(F, W["sigma"], 1)  # noqa: E731
+    elif kind == "ch":
+        sigma, k2 = inputs.ch_params(N)
+        F = inputs.ch_initial(N, S)
+        fn = lambda: oracle.batch_ch(F, sigma, k2, 1)  # noqa: E731
+    else:
+        import numpy as np
+        a, b, c, d, e = inputs.persys_bands(N, S)
+        F = inputs.rhs_uniform(N, S).astype(np.float32)
+        fn = lambda: oracle.batch_persys(a, b, c, d, e, F)  # noqa: E731
+    for _ in range(args.warmup):
+        fn()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        fn()
+    el = time.perf_counter() - t0
+    unit = "system-solves/s" if kind in ("shared", "persys") else "system-steps/s"
+    value = S * args.steps / el
+    sample = f"{S} systems of the workload (N={N}) per step"
+    return {
+        "impl": "reference", "metric": METRIC if args.workload == "shared" else
+        f"{W['desc']} throughput", "value": value, "unit": unit, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64 counter-based generator)",
+        "config": {"workload": W["desc"], "N": N, "sample_systems_per_step": S},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="shared")
+    ap.add_argument("--variant", default="auto", choices=["auto", "thread", "thread_df", "split"])
+    ap.add_argument("--batch", type=int, default=0, help="override the per-GPU batch")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        log("warning: fewer than 3 warm-up steps")
+    W = WORKLOADS[args.workload]
+    dist = Dist(args.gpus)
+    try:
+        if args.impl == "reference":
+            if dist.rank == 0:
+                print(json.dumps(run_reference(args, W, dist)), flush=True)
+            return 0
+        from implicit_pde_stepping_gb300 import build as b
+        if dist.rank == 0:
+            b.build()
+        dist.barrier()
+        res = run_ours(args, W, dist)
+        if dist.rank == 0:
+            if dist.world == 1 and not args.no_cpu_baseline:
+                res["cpu_baseline"] = run_cpu_baseline(W, args.cpu_seconds)
+            else:
+                res["cpu_baseline"] = None
+            print(json.dumps(res), flush=True)
+        return 0
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,219 @@
+// C ABI of libpent: argument checks, plan lifecycle and dispatch to the kernels.
+// Every declaration is documented in include/pent.h.
+#include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "pent_internal.cuh"
+
+namespace pent {
+
+static std::atomic<unsigned long long> g_launches{0};
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+
+inline cudaStream_t as_stream(void* s) { return static_cast<cudaStream_t>(s); }
+
+inline pent_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return PENT_OK;
+  if (e == cudaErrorMemoryAllocation) return PENT_ERR_ALLOC;
+  return PENT_ERR_CUDA;
+}
+
+inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// The kernel variant a plan uses for `batch` systems.
+pent_variant resolve(const pent_plan_s& p, int batch) {
+  if (p.variant != PENT_VARIANT_AUTO) return p.variant;
+  (void)batch;
+  return PENT_VARIANT_THREAD;
+}
+
+bool variant_exists(const pent_plan_s& p, pent_variant v) {
+  switch (v) {
+    case PENT_VARIANT_AUTO:
+    case PENT_VARIANT_THREAD:
+      return true;
+    default:
+      return false;
+  }
+}
+
+}  // namespace
+}  // namespace pent
+
+using namespace pent;
+
+extern "C" {
+
+const char* pent_status_string(pent_status s) {
+  switch (s) {
+    case PENT_OK: return "PENT_OK";
+    case PENT_ERR_INVALID_ARG: return "PENT_ERR_INVALID_ARG";
+    case PENT_ERR_ZERO_PIVOT: return "PENT_ERR_ZERO_PIVOT";
+    case PENT_ERR_CUDA: return "PENT_ERR_CUDA";
+    case PENT_ERR_ALLOC: return "PENT_ERR_ALLOC";
+    case PENT_ERR_UNSUPPORTED: return "PENT_ERR_UNSUPPORTED";
+  }
+  return "PENT_ERR_UNKNOWN";
+}
+
+unsigned long long pent_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+pent_status pent_sync(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(as_stream(stream));
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return from_cuda(e);
+}
+
+void pent_destroy(pent_plan p) {
+  if (!p) return;
+  if (p->arena) cudaFree(p->arena);
+  delete p;
+}
+
+pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, pent_dtype dtype,
+                        pent_plan* out) {
+  if (!out) return PENT_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!bands_host || N < 1 || batch < 1 || (cyclic != 0 && cyclic != 1)) return PENT_ERR_INVALID_ARG;
+  if (dtype != PENT_F64 && dtype != PENT_F32) return PENT_ERR_INVALID_ARG;
+  if (cyclic && N < 5) return PENT_ERR_INVALID_ARG;
+  if (N > (1 << 26)) return PENT_ERR_UNSUPPORTED;
+
+  pent_plan_s* p = new (std::nothrow) pent_plan_s;
+  if (!p) return PENT_ERR_ALLOC;
+  p->N = N;
+  p->M = cyclic ? N - 2 : N;
+  p->batch = batch;
+  p->cyclic = cyclic;
+  p->dtype = dtype;
+  cudaGetDevice(&p->device);
+
+  // one arena: coef64 | tail64 | coef32 | tail32 | coefdf | taildf | bands | work | status
+  const size_t nc = (size_t)kCoefCount * p->M;
+  size_t off = 0;
+  const size_t o_coef64 = off; off = round_up(off + nc * sizeof(double), 256);
+  const size_t o_tail64 = off; off = round_up(off + kTailCount * sizeof(double), 256);
+  const size_t o_coef32 = off; off = round_up(off + nc * sizeof(float), 256);
+  const size_t o_tail32 = off; off = round_up(off + kTailCount * sizeof(float), 256);
+  const size_t o_coefdf = off; off = round_up(off + nc * sizeof(float2), 256);
+  const size_t o_taildf = off; off = round_up(off + kTailCount * sizeof(float2), 256);
+  const size_t o_bands = off; off = round_up(off + 5 * (size_t)N * sizeof(double), 256);
+  const size_t o_work = off; off = round_up(off + 4 * (size_t)p->M * sizeof(double), 256);
+  const size_t o_status = off; off = round_up(off + sizeof(int), 256);
+  char* arena = nullptr;
+  cudaError_t e = cudaMalloc(&arena, off);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return PENT_ERR_ALLOC;
+  }
+  p->arena = arena;
+  p->coef64 = reinterpret_cast<double*>(arena + o_coef64);
+  p->tail64 = reinterpret_cast<double*>(arena + o_tail64);
+  p->coef32 = reinterpret_cast<float*>(arena + o_coef32);
+  p->tail32 = reinterpret_cast<float*>(arena + o_tail32);
+  p->coefdf = reinterpret_cast<float2*>(arena + o_coefdf);
+  p->taildf = reinterpret_cast<float2*>(arena + o_taildf);
+  double* d_bands = reinterpret_cast<double*>(arena + o_bands);
+  double* d_work = reinterpret_cast<double*>(arena + o_work);
+  int* d_status = reinterpret_cast<int*>(arena + o_status);
+
+  int status = 0;
+  e = cudaMemset(arena, 0, off);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(d_bands, bands_host, 5 * (size_t)N * sizeof(double), cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = factor_shared(d_bands, N, cyclic, p->coef64, p->tail64, d_work, d_status, 0);
+  if (e == cudaSuccess)
+    e = pack_coefficients(p->coef64, p->tail64, (int)nc, p->coef32, p->tail32, p->coefdf, p->taildf, 0);
+  if (e == cudaSuccess) e = cudaMemcpy(&status, d_status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    pent_destroy(p);
+    return from_cuda(e);
+  }
+  if (status != 0) {
+    pent_destroy(p);
+    return PENT_ERR_ZERO_PIVOT;
+  }
+  *out = p;
+  return PENT_OK;
+}
+
+pent_status pent_set_variant(pent_plan p, pent_variant v) {
+  if (!p) return PENT_ERR_INVALID_ARG;
+  if (!variant_exists(*p, v)) return PENT_ERR_UNSUPPORTED;
+  p->variant = v;
+  return PENT_OK;
+}
+
+pent_variant pent_get_variant(pent_plan p, int batch) {
+  if (!p) return PENT_VARIANT_AUTO;
+  return resolve(*p, batch);
+}
+
+pent_status pent_solve(pent_plan p, void* rhs, int batch, void* stream) {
+  if (!p || !rhs || batch < 1) return PENT_ERR_INVALID_ARG;
+  if (!aligned(rhs, 16)) return PENT_ERR_INVALID_ARG;
+  const pent_variant v = resolve(*p, batch);
+  cudaError_t e;
+  if (p->dtype == PENT_F32) {
+    if (v != PENT_VARIANT_THREAD) return PENT_ERR_UNSUPPORTED;
+    e = shared_thread_f32(*p, static_cast<float*>(rhs), batch, as_stream(stream));
+  } else {
+    switch (v) {
+      case PENT_VARIANT_THREAD:
+        e = shared_thread_f64(*p, static_cast<double*>(rhs), batch, as_stream(stream));
+        break;
+      default:
+        return PENT_ERR_UNSUPPORTED;
+    }
+  }
+  return from_cuda(e);
+}
+
+size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {
+  if (N < 1 || batch < 1 || (dtype != PENT_F64 && dtype != PENT_F32)) return 0;
+  return persys_work_bytes(N, batch, dtype);
+}
+
+pent_status pent_factor_solve(const void* a, const void* b, const void* c, const void* d,
+                              const void* e, void* rhs, int N, int batch, pent_dtype dtype,
+                              void* work, size_t work_bytes, int* info, void* stream) {
+  if (!a || !b || !c || !d || !e || !rhs || !work || N < 1 || batch < 1) return PENT_ERR_INVALID_ARG;
+  if (dtype != PENT_F64 && dtype != PENT_F32) return PENT_ERR_INVALID_ARG;
+  if (work_bytes < persys_work_bytes(N, batch, dtype) || !aligned(work, 256)) return PENT_ERR_INVALID_ARG;
+  const void* ptrs[6] = {a, b, c, d, e, rhs};
+  for (const void* q : ptrs)
+    if (!aligned(q, 16)) return PENT_ERR_INVALID_ARG;
+  return from_cuda(persys_thread(a, b, c, d, e, rhs, N, batch, dtype, work, info, as_stream(stream)));
+}
+
+pent_status hyperdiffusion_step(pent_plan p, void* C, int batch, int nsteps, void* stream) {
+  if (!p || !C || batch < 1 || nsteps < 0) return PENT_ERR_INVALID_ARG;
+  if (!p->cyclic || p->dtype != PENT_F64) return PENT_ERR_INVALID_ARG;
+  for (int n = 0; n < nsteps; ++n) {
+    const pent_status s = pent_solve(p, C, batch, stream);
+    if (s != PENT_OK) return s;
+  }
+  return PENT_OK;
+}
+
+pent_status ch_step(pent_plan p, void* C, int batch, double dt_over_dx2, int nsteps, void* stream) {
+  if (!p || !C || batch < 1 || nsteps < 0) return PENT_ERR_INVALID_ARG;
+  if (!p->cyclic || p->dtype != PENT_F64) return PENT_ERR_INVALID_ARG;
+  if (!aligned(C, 16)) return PENT_ERR_INVALID_ARG;
+  for (int n = 0; n < nsteps; ++n) {
+    const cudaError_t e = ch_thread_f64(*p, static_cast<double*>(C), batch, dt_over_dx2, as_stream(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return PENT_OK;
+}
+
+}  // extern "C"

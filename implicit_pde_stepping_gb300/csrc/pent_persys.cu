@@ -1,0 +1,120 @@
+// Per-system matrices: factor + solve in one kernel, one thread per system.
+//
+// "cuPentBatch – A batched pentadiagonal solver for NVIDIA GPUs", the Rewrite
+// variant (a new matrix at every call): factorisation steps 1–14 fused with the
+// forward substitution in one sweep down the rows, then back substitution up
+// the rows.  Diagonally dominant or SPD matrices need no pivoting (the page's
+// stability remark), so none is done; a zero or non-finite pivot is reported
+// per system in `info`.
+//
+// The page overwrites the bands with the factors.  Here the bands are inputs
+// and stay unchanged: gamma_i and delta_i go to the caller's scratch `work`
+// (two interleaved [N][batch] arrays), and g is written over the right-hand
+// side in place, read back by the backward sweep.
+#include "pent_internal.cuh"
+
+namespace pent {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kUnroll = 4;
+
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    k_persys_thread(const T* __restrict__ A, const T* __restrict__ B, const T* __restrict__ C,
+                    const T* __restrict__ D, const T* __restrict__ E, T* __restrict__ X,
+                    T* __restrict__ Wg, T* __restrict__ Wd, int N, int batch, int* __restrict__ info) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= batch) return;
+  const size_t ld = (size_t)batch;
+  T gm1 = T(0), gm2 = T(0), dm1 = T(0), dm2 = T(0), g1 = T(0), g2 = T(0);
+  int bad = 0;
+  for (int i0 = 0; i0 < N; i0 += kUnroll) {
+    T a[kUnroll], b[kUnroll], c[kUnroll], d[kUnroll], e[kUnroll], f[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u;
+      const size_t o = (size_t)i * ld + s;
+      const bool in = i < N;
+      a[u] = (in && i >= 2) ? A[o] : T(0);
+      b[u] = (in && i >= 1) ? B[o] : T(0);
+      c[u] = in ? C[o] : T(1);
+      d[u] = (in && i + 1 < N) ? D[o] : T(0);
+      e[u] = (in && i + 2 < N) ? E[o] : T(0);
+      f[u] = in ? X[o] : T(0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u;
+      if (i < N) {
+        const size_t o = (size_t)i * ld + s;
+        const T beta = b[u] - a[u] * gm2;
+        const T alpha = c[u] - a[u] * dm2 - beta * gm1;
+        if (bad == 0 && !(alpha != T(0) && isfinite(alpha))) bad = i + 1;
+        const T ra = T(1) / alpha;
+        const T gam = (d[u] - beta * dm1) * ra;
+        const T del = e[u] * ra;
+        const T g = (f[u] - a[u] * g2 - beta * g1) * ra;
+        Wg[o] = gam;
+        Wd[o] = del;
+        X[o] = g;
+        gm2 = gm1; gm1 = gam;
+        dm2 = dm1; dm1 = del;
+        g2 = g1; g1 = g;
+      }
+    }
+  }
+  T x1 = T(0), x2 = T(0);
+  for (int i0 = N - 1; i0 >= 0; i0 -= kUnroll) {
+    T gv[kUnroll], gm[kUnroll], dl[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 - u;
+      const size_t o = (size_t)(i >= 0 ? i : 0) * ld + s;
+      gv[u] = (i >= 0) ? X[o] : T(0);
+      gm[u] = (i >= 0) ? Wg[o] : T(0);
+      dl[u] = (i >= 0) ? Wd[o] : T(0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 - u;
+      if (i >= 0) {
+        const T x = gv[u] - gm[u] * x1 - dl[u] * x2;
+        X[(size_t)i * ld + s] = x;
+        x2 = x1;
+        x1 = x;
+      }
+    }
+  }
+  if (info) info[s] = bad;
+}
+
+template <typename T>
+cudaError_t launch(const void* a, const void* b, const void* c, const void* d, const void* e,
+                   void* X, int N, int batch, void* work, int* info, cudaStream_t st) {
+  T* Wg = static_cast<T*>(work);
+  T* Wd = Wg + (size_t)N * batch;
+  const int grid = (batch + kThreads - 1) / kThreads;
+  k_persys_thread<T><<<grid, kThreads, 0, st>>>(
+      static_cast<const T*>(a), static_cast<const T*>(b), static_cast<const T*>(c),
+      static_cast<const T*>(d), static_cast<const T*>(e), static_cast<T*>(X), Wg, Wd, N, batch,
+      info);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t persys_work_bytes(int N, int batch, pent_dtype dt) {
+  const size_t elem = dt == PENT_F64 ? sizeof(double) : sizeof(float);
+  return 2 * (size_t)N * (size_t)batch * elem;
+}
+
+cudaError_t persys_thread(const void* a, const void* b, const void* c, const void* d, const void* e,
+                          void* X, int N, int batch, pent_dtype dt, void* work, int* info,
+                          cudaStream_t st) {
+  if (dt == PENT_F64) return launch<double>(a, b, c, d, e, X, N, batch, work, info, st);
+  return launch<float>(a, b, c, d, e, X, N, batch, work, info, st);
+}
+
+}  // namespace pent

@@ -1,0 +1,163 @@
+/*
+ * pent.h — C ABI of the GB300 batched pentadiagonal solver library (libpent.so).
+ *
+ * The library solves many independent pentadiagonal systems A x = f at once,
+ * the linear solve behind semi-implicit stepping of 1-D hyperdiffusion and
+ * Cahn–Hilliard,  (I + sigma D4) C^{n+1} = RHS^n,  D4 = [1, -4, 6, -4, 1]/dx^4.
+ * Source: "cuPentBatch – A batched pentadiagonal solver for NVIDIA GPUs"
+ * (Gloster et al., arXiv 1807.07382).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Bands.  Row i (0-based) of a matrix holds a[i] at column i-2, b[i] at i-1,
+ *   c[i] at i, d[i] at i+1, e[i] at i+2 — the naming of the page's
+ *   factorisation steps (alpha_1 = c_1, beta_2 = b_2, delta_1 = e_1/alpha_1,
+ *   eps_i = a_i).  Non-cyclic: entries whose column is outside 0..N-1 are
+ *   ignored.  Cyclic (periodic, matrix (7c)): the column wraps modulo N.
+ * Interleaved layout.  A batch of vectors is one array of N rows of `batch`
+ *   elements; element i of system s lives at index i*batch + s (row i holds
+ *   entry i of every system; the page's "interleaved data layout").
+ * Memory.  Pointers named *_host are host memory; every other array pointer
+ *   is device memory of the current CUDA device, owned by the caller, which
+ *   must stay valid until the work queued on `stream` has finished.
+ * Streams.  `stream` is a cudaStream_t passed as void*; NULL is the legacy
+ *   default stream.  Solves are asynchronous (stream ordered).
+ * Errors.  Every call returns a pent_status.  Argument errors are detected on
+ *   the host before anything is queued, and nothing is modified.  A failed
+ *   launch returns PENT_ERR_CUDA.  No entry point aborts, traps or prints.
+ *   No entry point falls back to host computation: every solve runs in the
+ *   library's CUDA kernels.
+ */
+#ifndef PENT_H
+#define PENT_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PENT_OK = 0,
+  PENT_ERR_INVALID_ARG = 1, /* bad size, null pointer, wrong plan kind         */
+  PENT_ERR_ZERO_PIVOT = 2,  /* zero or non-finite pivot / singular 2x2 border  */
+  PENT_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed             */
+  PENT_ERR_ALLOC = 4,       /* device or host allocation failed                */
+  PENT_ERR_UNSUPPORTED = 5  /* valid request this build does not implement     */
+} pent_status;
+
+typedef enum { PENT_F64 = 0, PENT_F32 = 1 } pent_dtype;
+
+/* Kernel variants of the shared-matrix solves (for tests and benchmarks;
+ * PENT_VARIANT_AUTO picks one by shape). */
+typedef enum {
+  PENT_VARIANT_AUTO = 0,
+  PENT_VARIANT_THREAD = 1,    /* one thread per system, native arithmetic of the plan dtype */
+  PENT_VARIANT_THREAD_DF = 2, /* one thread per system, fp64 plans computed in double-float
+                                 (pairs of fp32) on the FP32 pipe                        */
+  PENT_VARIANT_SPLIT = 3      /* each system split over a warp (partitioned solve)       */
+} pent_variant;
+
+typedef struct pent_plan_s* pent_plan;
+
+/*
+ * pent_factor — factor a shared matrix once (the page's factor/solve split,
+ * "cuPentBatchConstant": factorisation steps 1–14 done once, reused by every
+ * solve).  For cyclic = 1 it also precomputes the pieces of Navon's bordering
+ * (eqs. (8)–(12)) that the page says to store once: E = leading (N-2)x(N-2)
+ * block, the 2x2 inverse of B - H^T E^{-1} G and the vectors for H^T E^{-1}
+ * and E^{-1} G.
+ *   bands_host : HOST, 5*N doubles, row-major [5][N] = a, b, c, d, e.
+ *   N          : rows; >= 1 (non-cyclic) or >= 5 (cyclic).
+ *   batch      : number of systems the plan will usually be called with
+ *                (>= 1); used to choose the kernel variant.
+ *   cyclic     : 0 or 1.
+ *   dtype      : PENT_F64 or PENT_F32 — element type of the solve arrays.
+ *                The factorisation itself is always computed in fp64.
+ *   out        : receives the plan (owned by the caller; free with pent_destroy).
+ * The factorisation runs on the current device and the call waits for it.
+ * Returns PENT_ERR_ZERO_PIVOT if a pivot alpha_i is zero or not finite, or
+ * if the 2x2 border block is singular.  On error *out is set to NULL.
+ */
+pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, pent_dtype dtype,
+                        pent_plan* out);
+
+/*
+ * pent_solve — shared-matrix batched solve in place: forward substitution
+ * L g = f then back substitution R x = g (the page's steps for g and x), or
+ * for a cyclic plan the bordered solve (eqs. (11)–(12)).
+ *   rhs_inout : DEVICE, interleaved [N][batch] of the plan dtype; holds f on
+ *               entry and x on return.  Base address 16-byte aligned.
+ *   batch     : >= 1.
+ */
+pent_status pent_solve(pent_plan plan, void* rhs_inout, int batch, void* stream);
+
+/*
+ * pent_factor_solve — per-system matrices, factor + solve in one call
+ * ("cuPentBatchRewrite": a new matrix every call).  Unlike the page, the
+ * bands are left unchanged; the factor coefficients go to `work`.
+ *   a, b, c, d, e : DEVICE, interleaved [N][batch] each, dtype elements.
+ *   rhs_inout     : DEVICE, interleaved [N][batch]; f in, x out.
+ *   N, batch      : >= 1.
+ *   work          : DEVICE scratch of at least pent_factor_solve_work_bytes()
+ *                   bytes, 256-byte aligned; contents undefined afterwards.
+ *   info          : DEVICE int[batch] or NULL.  info[s] = 0 if system s was
+ *                   factored, else the 1-based row of its first zero or
+ *                   non-finite pivot (its x is then not meaningful).
+ * Non-cyclic only.
+ */
+pent_status pent_factor_solve(const void* a, const void* b, const void* c, const void* d,
+                              const void* e, void* rhs_inout, int N, int batch, pent_dtype dtype,
+                              void* work, size_t work_bytes, int* info, void* stream);
+
+/* Bytes of device scratch pent_factor_solve needs for (N, batch, dtype). */
+size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);
+
+/*
+ * hyperdiffusion_step — nsteps of C <- A^{-1} C with a cyclic plan, i.e. the
+ * semi-implicit step (I + sigma D4) C^{n+1} = C^n of the hyperdiffusion
+ * equation (eq. (4)) with periodic boundaries, the plan built from the bands
+ * [sigma, -4 sigma, 1 + 6 sigma, -4 sigma, sigma].
+ *   C_inout : DEVICE, interleaved [N][batch], plan dtype (must be PENT_F64).
+ *   nsteps  : >= 0.
+ */
+pent_status hyperdiffusion_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* stream);
+
+/*
+ * ch_step — nsteps of the semi-implicit Cahn–Hilliard scheme (eqs. (1a),
+ * (2)) with mobility D = 1, periodic on N points:
+ *   (I + gamma dt D4) C^{n+1} = C^n + dt D2[(C^n)^3 - C^n],
+ * D2 = [1, -2, 1]/dx^2.  The plan must be cyclic, PENT_F64, built from the
+ * bands of I + sigma D4 with sigma = gamma dt/dx^4.  The explicit right-hand
+ * side is computed inside the solve kernel (no extra pass over memory).
+ *   C_inout     : DEVICE, interleaved [N][batch] doubles.
+ *   dt_over_dx2 : dt/dx^2 of the explicit D2 term.
+ */
+pent_status ch_step(pent_plan plan, void* C_inout, int batch, double dt_over_dx2, int nsteps,
+                    void* stream);
+
+/* Select the kernel variant of a plan (PENT_VARIANT_AUTO restores the default).
+ * PENT_ERR_UNSUPPORTED if the variant does not exist for this plan. */
+pent_status pent_set_variant(pent_plan plan, pent_variant variant);
+
+/* The variant the next call on this plan with `batch` systems would use. */
+pent_variant pent_get_variant(pent_plan plan, int batch);
+
+/* Free a plan (NULL is allowed).  Waits for nothing: the caller must not free
+ * a plan while work using it is still queued. */
+void pent_destroy(pent_plan plan);
+
+/* cudaStreamSynchronize(stream) and report any pending CUDA error. */
+pent_status pent_sync(void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* pent_status_string(pent_status status);
+
+/* Number of kernel launches this library has queued since it was loaded. */
+unsigned long long pent_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PENT_H */
