@@ -50,6 +50,8 @@ def lib():
             L.pent_factor_solve.argtypes = [vp] * 6 + [i, i, i, vp, sz, vp, vp]
             L.pent_factor_solve_work_bytes.argtypes = [i, i, i]
             L.pent_factor_solve_work_bytes.restype = sz
+            L.pent_factor_solve_noalloc.argtypes = [vp] * 6 + [i, i, i, vp, vp]
+            L.pent_factor_solve_noalloc.restype = i
             L.hyperdiffusion_step.argtypes = [vp, vp, i, i, vp]
             L.ch_step.argtypes = [vp, vp, i, d, i, vp]
             L.pent_set_variant.argtypes = [vp, i]
@@ -187,6 +189,22 @@ def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None):
                                    work.numel() * work.element_size(), ip, _stream(stream)),
            "pent_factor_solve")
     return work
+
+
+def pent_factor_solve_noalloc(a, b, c, d, e, rhs, info=None, stream=None) -> None:
+    """Per-system factor + solve in place, with the library's fixed 16 MiB scratch instead of
+    caller memory (for callers that cannot allocate device memory; see include/pent.h)."""
+    import torch
+    N, batch = rhs.shape
+    code = _dtype_code(rhs)
+    ptrs = [_ptr(t, N, code, n) for t, n in zip((a, b, c, d, e), "abcde")]
+    ip = None
+    if info is not None:
+        if info.dtype != torch.int32 or info.numel() < batch or not info.is_cuda:
+            raise ValueError("info must be a CUDA int32 tensor of >= batch elements")
+        ip = ctypes.c_void_p(info.data_ptr())
+    _check(lib().pent_factor_solve_noalloc(*ptrs, _ptr(rhs, N, code, "rhs"), N, batch, code, ip,
+                                           _stream(stream)), "pent_factor_solve_noalloc")
 
 
 def hyperdiffusion_step(plan: Plan, C, nsteps: int, stream=None) -> None:

@@ -114,6 +114,35 @@ pent_status pent_factor_solve(const void* a, const void* b, const void* c, const
 size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);
 
 /*
+ * pent_factor_solve_noalloc — pent_factor_solve for callers that cannot
+ * allocate device memory.  The paper has no counterpart; this is a library
+ * service.  Some callers cannot call cudaMalloc: an application that reserved
+ * all device memory for its own pool at start-up and does not let libraries
+ * allocate, or a time-critical loop where cudaMalloc/cudaFree are ruled out
+ * because they may synchronise the device and take unbounded time.
+ *
+ * Same kernel and results as pent_factor_solve, but the scratch for the factor
+ * coefficients is a fixed 16 MiB array inside the library (every GPU that
+ * loads the library holds it until the process exits).  Nothing is allocated:
+ * no cudaMalloc, cudaFree or allocating library routine is called.
+ *   a..e, rhs_inout, N, batch, dtype, info : as for pent_factor_solve.
+ * Limit: 2 * N * batch * sizeof(element) must be <= 16 MiB (for example
+ * N = 256 with batch <= 8192 in fp32, or batch <= 4096 in fp64); larger
+ * requests return PENT_ERR_UNSUPPORTED and queue nothing.
+ * Set-up: the first call on each device looks up the device address of the
+ * array (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.
+ * Sharing: every call uses the same array.  The kernel writes each scratch
+ * entry before reading it, so nothing needs clearing between calls, but two
+ * calls whose kernels overlap on the GPU (different streams, or different host
+ * threads without ordering) race on the array; order them on one stream or
+ * with events.
+ */
+pent_status pent_factor_solve_noalloc(const void* a, const void* b, const void* c, const void* d,
+                                      const void* e, void* rhs_inout, int N, int batch,
+                                      pent_dtype dtype, int* info, void* stream);
+
+/*
  * hyperdiffusion_step — nsteps of C <- A^{-1} C with a cyclic plan, i.e. the
  * semi-implicit step (I + sigma D4) C^{n+1} = C^n of the hyperdiffusion
  * equation (eq. (4)) with periodic boundaries, the plan built from the bands
