@@ -27,10 +27,15 @@ inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 
 size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// The kernel variant a plan uses for `batch` systems.
+// Largest sweep length whose double-float tables fit in one CTA's shared memory.
+constexpr int kMaxTwistedRows = 2560;
+
+// The kernel variant a plan uses for `batch` systems: fp64 plans take the
+// double-float twisted kernel when its tables exist, else the native one.
 pent_variant resolve(const pent_plan_s& p, int batch) {
   if (p.variant != PENT_VARIANT_AUTO) return p.variant;
   (void)batch;
+  if (p.dtype == PENT_F64 && p.twist_ok) return PENT_VARIANT_THREAD_DF;
   return PENT_VARIANT_THREAD;
 }
 
@@ -39,9 +44,17 @@ bool variant_exists(const pent_plan_s& p, pent_variant v) {
     case PENT_VARIANT_AUTO:
     case PENT_VARIANT_THREAD:
       return true;
+    case PENT_VARIANT_THREAD_DF:
+      return p.dtype == PENT_F64 && p.twist_ok;
     default:
       return false;
   }
+}
+
+int env_int(const char* name, int dflt) {
+  const char* v = std::getenv(name);
+  if (!v || !*v) return dflt;
+  return std::atoi(v);
 }
 
 }  // namespace
@@ -105,8 +118,10 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   const size_t o_coefdf = off; off = round_up(off + nc * sizeof(float2), 256);
   const size_t o_taildf = off; off = round_up(off + kTailCount * sizeof(float2), 256);
   const size_t o_bands = off; off = round_up(off + 5 * (size_t)N * sizeof(double), 256);
-  const size_t o_work = off; off = round_up(off + 4 * (size_t)p->M * sizeof(double), 256);
+  const size_t o_work = off; off = round_up(off + 18 * (size_t)p->M * sizeof(double), 256);
   const size_t o_status = off; off = round_up(off + sizeof(int), 256);
+  const size_t o_twtab = off; off = round_up(off + (size_t)p->M * kTwK * sizeof(float4), 256);
+  const size_t o_twist = off; off = round_up(off + kTwistCount * sizeof(double), 256);
   char* arena = nullptr;
   cudaError_t e = cudaMalloc(&arena, off);
   if (e != cudaSuccess) {
@@ -121,6 +136,8 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   p->tail32 = reinterpret_cast<float*>(arena + o_tail32);
   p->coefdf = reinterpret_cast<float2*>(arena + o_coefdf);
   p->taildf = reinterpret_cast<float2*>(arena + o_taildf);
+  p->twtab = reinterpret_cast<float4*>(arena + o_twtab);
+  p->twist = reinterpret_cast<double*>(arena + o_twist);
   double* d_bands = reinterpret_cast<double*>(arena + o_bands);
   double* d_work = reinterpret_cast<double*>(arena + o_work);
   int* d_status = reinterpret_cast<int*>(arena + o_status);
@@ -141,6 +158,22 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   if (status != 0) {
     pent_destroy(p);
     return PENT_ERR_ZERO_PIVOT;
+  }
+  // twisted double-float tables (fp64 plans whose sweep fits the kernel)
+  cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  p->df_spb = env_int("PENT_DF_SPB", 128);
+  p->df_ctas = env_int("PENT_DF_CTAS", 0);
+  if (dtype == PENT_F64 && p->M >= 8 && p->M <= kMaxTwistedRows) {
+    p->m = p->M / 2;
+    int tstatus = 0;
+    e = factor_twisted(d_bands, N, cyclic, p->m, p->twtab, p->twist, d_work, d_status, 0);
+    if (e == cudaSuccess) e = cudaMemcpy(&tstatus, d_status, sizeof(int), cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      pent_destroy(p);
+      return from_cuda(e);
+    }
+    p->twist_ok = (tstatus == 0);
   }
   *out = p;
   return PENT_OK;
@@ -170,6 +203,9 @@ pent_status pent_solve(pent_plan p, void* rhs, int batch, void* stream) {
     switch (v) {
       case PENT_VARIANT_THREAD:
         e = shared_thread_f64(*p, static_cast<double*>(rhs), batch, as_stream(stream));
+        break;
+      case PENT_VARIANT_THREAD_DF:
+        e = shared_thread_df(*p, static_cast<double*>(rhs), batch, as_stream(stream));
         break;
       default:
         return PENT_ERR_UNSUPPORTED;
