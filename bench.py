@@ -321,8 +321,8 @@ def run_ours(args, W: dict, dist: Dist):
         ("hyper", pent.VARIANT_THREAD): ("k_shared_thread", "pent_shared.cu"),
         ("ch", pent.VARIANT_THREAD): ("k_ch_thread_f64", "pent_ch.cu"),
         ("persys", pent.VARIANT_THREAD): ("k_persys_thread", "pent_persys.cu"),
-        ("shared", pent.VARIANT_THREAD_DF): ("k_shared_df", "pent_shared_df.cu"),
-        ("hyper", pent.VARIANT_THREAD_DF): ("k_shared_df", "pent_shared_df.cu"),
+        ("shared", pent.VARIANT_THREAD_DF): ("k_twisted_df", "pent_twisted_df.cu"),
+        ("hyper", pent.VARIANT_THREAD_DF): ("k_twisted_df", "pent_twisted_df.cu"),
         ("ch", pent.VARIANT_THREAD_DF): ("k_ch_df", "pent_ch_df.cu"),
         ("shared", pent.VARIANT_SPLIT): ("k_shared_split", "pent_split.cu"),
     }

@@ -46,6 +46,8 @@ bool variant_exists(const pent_plan_s& p, pent_variant v) {
       return true;
     case PENT_VARIANT_THREAD_DF:
       return p.dtype == PENT_F64 && p.twist_ok;
+    case PENT_VARIANT_SPLIT:
+      return p.dtype == PENT_F64 && p.split_ok;
     default:
       return false;
   }
@@ -118,7 +120,14 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   const size_t o_coefdf = off; off = round_up(off + nc * sizeof(float2), 256);
   const size_t o_taildf = off; off = round_up(off + kTailCount * sizeof(float2), 256);
   const size_t o_bands = off; off = round_up(off + 5 * (size_t)N * sizeof(double), 256);
-  const size_t o_work = off; off = round_up(off + 18 * (size_t)p->M * sizeof(double), 256);
+  // partitioned variant: chunk length and count (P a multiple of 4, Mpad = L * P)
+  const int spL = p->M >= 256 ? 32 : 16;
+  const int spP = ((p->M + 4 * spL - 1) / (4 * spL)) * 4;
+  const size_t Mpad = (size_t)spL * spP;
+  const size_t o_work = off; off = round_up(off + 18 * (Mpad > (size_t)p->M ? Mpad : (size_t)p->M) * sizeof(double), 256);
+  const size_t o_sptab = off; off = round_up(off + Mpad * kSpK * sizeof(float4), 256);
+  const size_t o_spchunk = off; off = round_up(off + (size_t)spP * kSpChunk * sizeof(double), 256);
+  const size_t o_spextra = off; off = round_up(off + kSpExtra * sizeof(double), 256);
   const size_t o_status = off; off = round_up(off + sizeof(int), 256);
   const size_t o_twtab = off; off = round_up(off + (size_t)p->M * kTwK * sizeof(float4), 256);
   const size_t o_twist = off; off = round_up(off + kTwistCount * sizeof(double), 256);
@@ -138,6 +147,9 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   p->taildf = reinterpret_cast<float2*>(arena + o_taildf);
   p->twtab = reinterpret_cast<float4*>(arena + o_twtab);
   p->twist = reinterpret_cast<double*>(arena + o_twist);
+  p->sptab = reinterpret_cast<float4*>(arena + o_sptab);
+  p->spchunk = reinterpret_cast<double*>(arena + o_spchunk);
+  p->spextra = reinterpret_cast<double*>(arena + o_spextra);
   double* d_bands = reinterpret_cast<double*>(arena + o_bands);
   double* d_work = reinterpret_cast<double*>(arena + o_work);
   int* d_status = reinterpret_cast<int*>(arena + o_status);
@@ -161,7 +173,9 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   }
   // twisted double-float tables (fp64 plans whose sweep fits the kernel)
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
-  p->df_spb = env_int("PENT_DF_SPB", 128);
+  p->df_spb = env_int("PENT_DF_SPB", 256);
+  p->df_spt = env_int("PENT_DF_SPT", 2);
+  p->df_ku = env_int("PENT_DF_KU", 4);
   p->df_ctas = env_int("PENT_DF_CTAS", 0);
   if (dtype == PENT_F64 && p->M >= 8 && p->M <= kMaxTwistedRows) {
     p->m = p->M / 2;
@@ -174,6 +188,36 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
       return from_cuda(e);
     }
     p->twist_ok = (tstatus == 0);
+  }
+  // partitioned double-float tables
+  {
+    const int SB = (cyclic && spL == 32 && spP <= 32) ? 16 : 8;
+    const bool fits = split_smem_bytes(spL, spP, SB, cyclic) <= 200 * 1024 && SB * spP <= 1024 && spP <= kSpMaxChunks &&
+                      !(cyclic && spL == 32 && spP > 32);
+    if (dtype == PENT_F64 && p->M >= 16 && fits) {
+      p->sp_L = spL;
+      p->sp_P = spP;
+      int sstatus = 0;
+      e = factor_split(d_bands, N, cyclic, spL, (int)Mpad, p->sptab, p->spchunk, p->spextra, d_work,
+                       d_status, 0);
+      if (e == cudaSuccess) e = cudaMemcpy(&sstatus, d_status, sizeof(int), cudaMemcpyDeviceToHost);
+      if (e != cudaSuccess) {
+        cudaGetLastError();
+        pent_destroy(p);
+        return from_cuda(e);
+      }
+      p->split_ok = (sstatus == 0);
+      // PENT_SPLIT_T=0 forces the exact serial chunk scan (testing)
+      if (p->split_ok && std::getenv("PENT_SPLIT_T") && env_int("PENT_SPLIT_T", -1) == 0) {
+        const double zero = 0.0;
+        e = cudaMemcpy(p->spextra + 18, &zero, sizeof(double), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          pent_destroy(p);
+          return from_cuda(e);
+        }
+      }
+    }
   }
   *out = p;
   return PENT_OK;
@@ -205,7 +249,10 @@ pent_status pent_solve(pent_plan p, void* rhs, int batch, void* stream) {
         e = shared_thread_f64(*p, static_cast<double*>(rhs), batch, as_stream(stream));
         break;
       case PENT_VARIANT_THREAD_DF:
-        e = shared_thread_df(*p, static_cast<double*>(rhs), batch, as_stream(stream));
+        e = shared_twisted_df(*p, static_cast<double*>(rhs), batch, as_stream(stream));
+        break;
+      case PENT_VARIANT_SPLIT:
+        e = shared_split_df(*p, static_cast<double*>(rhs), batch, as_stream(stream));
         break;
       default:
         return PENT_ERR_UNSUPPORTED;

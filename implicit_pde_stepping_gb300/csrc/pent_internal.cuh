@@ -36,14 +36,22 @@ struct pent_plan_s {
   float2* coefdf = nullptr;  // [kCoefCount][M] (hi, lo) double-float pairs
   float2* taildf = nullptr;
   void* arena = nullptr;     // single allocation backing all of the above
-  // twisted double-float variant (pent_factor_twisted.cu / pent_shared_df.cu)
+  // twisted double-float variant (pent_factor_twisted.cu / pent_twisted_df.cu)
   int m = 0;                 // meeting row: top rows 0..m-1, bottom rows m..M-1
   int twist_ok = 0;          // tables valid and the 4x4 meeting system nonsingular
   float4* twtab = nullptr;   // [M][kTwK]
   double* twist = nullptr;   // [kTwistCount]
   int num_sms = 0;           // SMs of the plan's device (persistent grid size)
-  int df_spb = 128;          // systems per CTA of the double-float kernels
-  int df_ctas = 0;           // CTAs of the double-float kernels (0: one per SM)
+  int df_spb = 256;          // systems per CTA of the double-float kernels
+  int df_spt = 2;            // systems per thread (2 needs an even batch)
+  int df_ku = 4;             // rows per prefetch block
+  int df_ctas = 0;           // CTAs of the double-float kernels (0: two per SM)
+  // partitioned double-float variant (pent_factor_split.cu / pent_split_df.cu)
+  int split_ok = 0;          // tables valid
+  int sp_L = 0, sp_P = 0;    // chunk length, chunks per system (Mpad = sp_L * sp_P)
+  float4* sptab = nullptr;   // [Mpad][kSpK]
+  double* spchunk = nullptr; // [sp_P][kSpChunk]
+  double* spextra = nullptr; // [kSpExtra]
 };
 
 namespace pent {
@@ -60,9 +68,8 @@ cudaError_t pack_coefficients(const double* coef64, const double* tail64, int n_
 // shared.cu
 cudaError_t shared_thread_f64(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 cudaError_t shared_thread_f32(const pent_plan_s& p, float* X, int batch, cudaStream_t st);
-cudaError_t shared_thread_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
+cudaError_t shared_twisted_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 cudaError_t shared_split_f64(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
-size_t shared_df_smem_bytes(int M);
 
 // persys.cu
 cudaError_t persys_thread(const void* a, const void* b, const void* c, const void* d, const void* e,
@@ -97,5 +104,40 @@ constexpr int kTwistCount = 20;
 
 cudaError_t factor_twisted(const double* d_bands, int N, int cyclic, int m, float4* tab,
                            double* twist, double* d_work, int* d_status, cudaStream_t st);
+
+}  // namespace pent
+
+namespace pent {
+
+// Partitioned ("split") double-float kernel tables (pent_factor_split.cu).
+// The M-row block is padded to Mpad = P * L rows (padding rows are decoupled
+// identity rows) and cut into P chunks of L rows.  Per padded row, kSpK float4
+// of (hi, lo) pairs:
+//   k0 = {r, P}   k1 = {Q, U0}   k2 = {C, D}   k3 = {M1, M2}   k4 = {K1, K2}   k5 = {U1, 0}
+// forward  g_j = r f + P g_{j-2} + Q g_{j-1}; backward y_j = g_j + C y_{j+1} + D y_{j+2};
+// H1/H2 = forward responses of a chunk to its incoming state (g_{a-2}, g_{a-1}),
+// M1/M2 = their local back substitution, K1/K2 = backward responses to the
+// outgoing state (x_b, x_{b+1}); U0/U1 = E^{-1} G (cyclic).
+constexpr int kSpK = 6;
+// Per chunk c, kSpChunk doubles, each 2x2 row-major:
+//   [0]  Phi_c  (H at the chunk's last two rows: s_{c+1} = e_c + Phi_c s_c)
+//   [4]  Mst_c  (M at its first two rows)    [8] Kst_c (K at its first two rows)
+//   [12 + 4(k-2)]  A_{c,k} = Phi_{c-1} ... Phi_{c-k+1},  k = 2..kSpTmax
+//   [24 + 4(k-1)]  B_{c,k} = Kst_{c+1} ... Kst_{c+k},    k = 1..kSpTmax-1
+// so that s_c = sum_{k=1..T} A_{c,k} e_{c-k} (A_{c,1} = I) and
+// t_c = sum_{k=0..T-1} B_{c,k} w_{c+1+k} (B_{c,0} = I), w_c = x'_start(c) + Mst_c s_c.
+constexpr int kSpTmax = 4;
+constexpr int kSpMaxChunks = 64;   // chunks per system the split kernel supports
+constexpr int kSpChunk = 36;
+// Extras: [0..3] S^{-1} (cyclic); [4..6] h0 at rows M-2, M-1, 0; [7..9] h1 at rows
+// M-1, 0, 1; [10..13] M1,M2 at rows M-2 then M-1; [14..17] K1,K2 at rows M-2 then
+// M-1; [18] T, the number of chunk couplings kept (0: exact serial scan).
+constexpr int kSpExtra = 20;
+
+cudaError_t factor_split(const double* d_bands, int N, int cyclic, int L, int Mpad, float4* rowtab,
+                         double* chunktab, double* extra, double* d_work, int* d_status,
+                         cudaStream_t st);
+cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
+size_t split_smem_bytes(int L, int P, int SB, int cyclic);
 
 }  // namespace pent

@@ -1,0 +1,293 @@
+// Partitioned (split-within-system) shared-matrix solve in double-float.
+//
+// Same mathematics as the one-thread-per-system solve (forward substitution
+// L g = f and back substitution R x = g of "cuPentBatch – A batched
+// pentadiagonal solver for NVIDIA GPUs", interleaved layout, factor once), but
+// every system is cut into P chunks of L rows, one thread per chunk, so that
+// the whole system lives in registers and HBM sees only the two-array minimum
+// (read f once, write x once).  Per chunk (tables: pent_factor_split.cu):
+//   1. load the chunk, run the forward and the back substitution locally with
+//      zero boundary values -> x' (registers); publish the local end values
+//      e_c of g;
+//   2. boundary states: s_c (the g entering the chunk) and t_c (the x leaving
+//      it).  With T > 0 every chunk forms them itself from the T nearest
+//      chunks (s_c = sum_k A_{c,k} e_{c-k}, then t_c = sum_k B_{c,k} w_{c+1+k}
+//      with w_c = x'_start(c) + Mst_c s_c); the plan chose T so that the
+//      couplings dropped are below 2^-64.  With T = 0 one thread per system
+//      scans the chunks in order (exact for any matrix);
+//   3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1, joined to fp64 and stored.
+// Cyclic plans carry Navon's bordering (eqs. (8)–(12)): x_t = S^{-1}(f_t -
+// H^T y) from y at rows 0, 1, M-2, M-1, and step 3 subtracts u0 x_t0 + u1 x_t1.
+//
+// Warp layout: 8 consecutive systems x 4 chunks per warp, so every load or
+// store instruction moves four 64-byte runs of one row each (whole sectors).
+// The per-row tables sit in shared memory with one float4 of padding per
+// chunk, so the four chunks a warp reads fall in different banks.  A CTA holds
+// SB systems x P chunks; the grid is persistent.
+#include "df64.cuh"
+#include "pent_internal.cuh"
+
+namespace pent {
+namespace {
+
+using df::D2;
+
+// y += A x for a row-major 2x2 A
+__device__ __forceinline__ void mv2(const double* A, double x0, double x1, double& y0, double& y1) {
+  y0 = fma(A[0], x0, fma(A[1], x1, y0));
+  y1 = fma(A[2], x0, fma(A[3], x1, y1));
+}
+
+template <int L, int SB, int MAXT, bool CYC>
+__global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
+    k_split_df(const float4* __restrict__ growtab, const double* __restrict__ gchunk,
+               const double* __restrict__ gextra, double* __restrict__ X, int M, int P,
+               int batch) {
+  constexpr int K4 = CYC ? kSpK : kSpK - 1;   // float4 per row kept in shared memory
+  constexpr int CS = L * K4 + 1;              // chunk stride (float4), padded
+  constexpr int SG = SB / 8;                  // system groups of 8 per CTA
+  extern __shared__ float4 smem4[];
+  float4* rtab = smem4;                                              // [P][CS]
+  double* ctab = reinterpret_cast<double*>(rtab + (size_t)P * CS);   // [P][kSpChunk]
+  double* sE = ctab + (size_t)P * kSpChunk;      // [SB][P][2] local forward end values e_c
+  double* sW = sE + (size_t)SB * P * 2;          // [SB][P][2] x'_start (serial) or w_c (parallel)
+  double* sS = sW + (size_t)SB * P * 2;          // [SB][P][2] s_c (serial scan)
+  double* sT = sS + (size_t)SB * P * 2;          // [SB][P][2] t_c (serial scan)
+  double* sX = sT + (size_t)SB * P * 2;          // [SB][8]   cyclic: y and x_t
+
+  for (int t = threadIdx.x; t < P * L * K4; t += blockDim.x) {
+    const int row = t / K4, k = t % K4;
+    rtab[(row / L) * CS + (row % L) * K4 + k] = growtab[(size_t)row * kSpK + k];
+  }
+  for (int t = threadIdx.x; t < P * kSpChunk; t += blockDim.x) ctab[t] = gchunk[t];
+  __syncthreads();
+  const int T = (int)gextra[18];
+
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int sys = (w % SG) * 8 + (lane & 7);
+  const int c = (w / SG) * 4 + (lane >> 3);
+  const int row0 = c * L;
+  const float4* ctb = rtab + (size_t)c * CS;     // this chunk's rows
+  const double* ct = ctab + (size_t)c * kSpChunk;
+  const long long ld = batch;
+  const int nblk = (batch + SB - 1) / SB;
+
+  for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    const int s = blk * SB + sys;
+    const bool act = s < batch;
+    double* p = X + (long long)row0 * ld + (act ? s : 0);
+
+    // ---- 1. load, local forward (zero incoming state), local backward
+    D2 v[L];
+    {
+      double fv[L];
+#pragma unroll
+      for (int j = 0; j < L; ++j) fv[j] = (act && row0 + j < M) ? p[j * ld] : 0.0;
+      D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < L; ++j) {
+        const float4 c0 = ctb[j * K4];
+        const float4 c1 = ctb[j * K4 + 1];
+        const D2 g = df::sum3p(D2{c0.x, c0.y}, df::from_double(fv[j]), D2{c0.z, c0.w}, a2,
+                               D2{c1.x, c1.y}, a1);
+        v[j] = g;
+        a2 = a1;
+        a1 = g;
+      }
+    }
+    double* eo = sE + ((size_t)sys * P + c) * 2;
+    eo[0] = df::to_double(v[L - 2]);
+    eo[1] = df::to_double(v[L - 1]);
+    {
+      D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+#pragma unroll
+      for (int j = L - 1; j >= 0; --j) {
+        const float4 c2 = ctb[j * K4 + 2];
+        const D2 y = df::sum3(v[j], D2{c2.x, c2.y}, a1, D2{c2.z, c2.w}, a2);
+        v[j] = y;
+        a2 = a1;
+        a1 = y;
+      }
+    }
+    const double xs0 = df::to_double(v[0]), xs1 = df::to_double(v[1]);   // x'_start(c)
+    // x' at rows M-2, M-1 (cyclic): only the owning chunks keep them
+    double xm2 = 0.0, xm1 = 0.0;
+    if (CYC && row0 <= M - 1 && M - 2 < row0 + L) {
+#pragma unroll
+      for (int j = 0; j < L; ++j) {
+        if (row0 + j == M - 2) xm2 = df::to_double(v[j]);
+        if (row0 + j == M - 1) xm1 = df::to_double(v[j]);
+      }
+    }
+
+    // ---- 2. boundary states s_c (entering) and t_c (leaving), fp64
+    double s0 = 0.0, s1 = 0.0, t0 = 0.0, t1 = 0.0;
+    double* xc = sX + (size_t)sys * 8;
+    if (T > 0) {
+      __syncthreads();                                   // e_c published
+      const double* E = sE + (size_t)sys * P * 2;
+      for (int k = 1; k <= T && k <= c; ++k) {           // s_c = sum_k A_{c,k} e_{c-k}
+        const double ea = E[2 * (c - k)], eb = E[2 * (c - k) + 1];
+        if (k == 1) { s0 += ea; s1 += eb; }
+        else mv2(ct + 12 + 4 * (k - 2), ea, eb, s0, s1);
+      }
+      double w0 = xs0, w1 = xs1;
+      mv2(ct + 4, s0, s1, w0, w1);                       // w_c = x'_start + Mst_c s_c
+      double* wo = sW + ((size_t)sys * P + c) * 2;
+      wo[0] = w0;
+      wo[1] = w1;
+      __syncthreads();                                   // w_c published
+      const double* Wv = sW + (size_t)sys * P * 2;
+      for (int k = 0; k < T && c + 1 + k < P; ++k) {     // t_c = sum_k B_{c,k} w_{c+1+k}
+        const double wa = Wv[2 * (c + 1 + k)], wb = Wv[2 * (c + 1 + k) + 1];
+        if (k == 0) { t0 += wa; t1 += wb; }
+        else mv2(ct + 24 + 4 * (k - 1), wa, wb, t0, t1);
+      }
+      if (CYC) {
+        if (c == 0) {                                    // y at rows 0, 1
+          double y0 = w0, y1 = w1;
+          mv2(ct + 8, t0, t1, y0, y1);
+          xc[2] = y0;
+          xc[3] = y1;
+        }
+        if (row0 <= M - 2 && M - 2 < row0 + L)
+          xc[0] = xm2 + gextra[10] * s0 + gextra[11] * s1 + gextra[14] * t0 + gextra[15] * t1;
+        if (row0 <= M - 1 && M - 1 < row0 + L)
+          xc[1] = xm1 + gextra[12] * s0 + gextra[13] * s1 + gextra[16] * t0 + gextra[17] * t1;
+      }
+    } else {
+      double* wo = sW + ((size_t)sys * P + c) * 2;
+      wo[0] = xs0;
+      wo[1] = xs1;
+      if (CYC) {
+        if (row0 <= M - 2 && M - 2 < row0 + L) xc[0] = xm2;
+        if (row0 <= M - 1 && M - 1 < row0 + L) xc[1] = xm1;
+      }
+      __syncthreads();
+      if (c == 0) {                                      // exact serial scan, one thread per system
+        const double* E = sE + (size_t)sys * P * 2;
+        const double* Wv = sW + (size_t)sys * P * 2;
+        double* S = sS + (size_t)sys * P * 2;
+        double* Tt = sT + (size_t)sys * P * 2;
+        double a0 = 0.0, a1 = 0.0;
+        for (int k = 0; k < P; ++k) {                    // s_{k+1} = e_k + Phi_k s_k
+          S[2 * k] = a0;
+          S[2 * k + 1] = a1;
+          double n0 = E[2 * k], n1 = E[2 * k + 1];
+          mv2(ctab + (size_t)k * kSpChunk, a0, a1, n0, n1);
+          a0 = n0;
+          a1 = n1;
+        }
+        double b0 = 0.0, b1 = 0.0;
+        for (int k = P - 1; k >= 0; --k) {               // x at the start of chunk k
+          Tt[2 * k] = b0;
+          Tt[2 * k + 1] = b1;
+          const double* ck = ctab + (size_t)k * kSpChunk;
+          double x0 = Wv[2 * k], x1 = Wv[2 * k + 1];
+          mv2(ck + 4, S[2 * k], S[2 * k + 1], x0, x1);
+          mv2(ck + 8, b0, b1, x0, x1);
+          b0 = x0;
+          b1 = x1;
+        }
+        if (CYC) {
+          const int k2 = (M - 2) / L, k1 = (M - 1) / L;
+          xc[0] += gextra[10] * S[2 * k2] + gextra[11] * S[2 * k2 + 1] + gextra[14] * Tt[2 * k2] +
+                   gextra[15] * Tt[2 * k2 + 1];
+          xc[1] += gextra[12] * S[2 * k1] + gextra[13] * S[2 * k1 + 1] + gextra[16] * Tt[2 * k1] +
+                   gextra[17] * Tt[2 * k1 + 1];
+          xc[2] = b0;
+          xc[3] = b1;
+        }
+      }
+      __syncthreads();
+      s0 = sS[((size_t)sys * P + c) * 2];
+      s1 = sS[((size_t)sys * P + c) * 2 + 1];
+      t0 = sT[((size_t)sys * P + c) * 2];
+      t1 = sT[((size_t)sys * P + c) * 2 + 1];
+    }
+    // cyclic: x_t = S^{-1}(f_t - H^T y)   (eq. (12))
+    double xt0 = 0.0, xt1 = 0.0;
+    if (CYC) {
+      __syncthreads();                                   // y published
+      if (c == 0) {
+        const double r0 = gextra[4] * xc[0] + gextra[5] * xc[1] + gextra[6] * xc[2];
+        const double r1 = gextra[7] * xc[1] + gextra[8] * xc[2] + gextra[9] * xc[3];
+        double ft0 = 0.0, ft1 = 0.0;
+        if (act) {
+          ft0 = X[(long long)M * ld + s];
+          ft1 = X[(long long)(M + 1) * ld + s];
+        }
+        const double u0 = gextra[0] * (ft0 - r0) + gextra[1] * (ft1 - r1);
+        const double u1 = gextra[2] * (ft0 - r0) + gextra[3] * (ft1 - r1);
+        xc[4] = u0;
+        xc[5] = u1;
+        if (act) {
+          X[(long long)M * ld + s] = u0;
+          X[(long long)(M + 1) * ld + s] = u1;
+        }
+      }
+      __syncthreads();
+      xt0 = xc[4];
+      xt1 = xc[5];
+    }
+
+    // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 (- u0 x_t0 - u1 x_t1), store
+    {
+      const D2 S0 = df::from_double(s0), S1 = df::from_double(s1);
+      const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
+      const D2 X0 = df::from_double(-xt0), X1 = df::from_double(-xt1);
+#pragma unroll
+      for (int j = 0; j < L; ++j) {
+        const float4 c3 = ctb[j * K4 + 3], c4 = ctb[j * K4 + 4];
+        D2 x = df::axpy(v[j], D2{c3.x, c3.y}, S0);
+        x = df::axpy(x, D2{c3.z, c3.w}, S1);
+        x = df::axpy(x, D2{c4.x, c4.y}, T0);
+        x = df::axpy(x, D2{c4.z, c4.w}, T1);
+        if (CYC) {
+          const float4 c1 = ctb[j * K4 + 1], c5 = ctb[j * K4 + 5];
+          x = df::axpy(x, D2{c1.z, c1.w}, X0);
+          x = df::axpy(x, D2{c5.x, c5.y}, X1);
+        }
+        if (act && row0 + j < M) __stcs(p + j * ld, df::to_double(x));
+      }
+    }
+  }
+}
+
+template <int L, int SB, int MAXT, bool CYC>
+cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+  const int P = p.sp_P;
+  const size_t smem = split_smem_bytes(L, P, SB, CYC);
+  auto kern = k_split_df<L, SB, MAXT, CYC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int nblk = (batch + SB - 1) / SB;
+  const int per_sm = (MAXT <= 256 && smem <= 110 * 1024) ? 2 : 1;
+  int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
+  if (grid > nblk) grid = nblk;
+  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t split_smem_bytes(int L, int P, int SB, int cyclic) {
+  const int K4 = cyclic ? kSpK : kSpK - 1;
+  return (size_t)P * (L * K4 + 1) * sizeof(float4) +
+         ((size_t)P * kSpChunk + 4 * (size_t)SB * P * 2 + (size_t)SB * 8) * sizeof(double);
+}
+
+cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+  // p.sp_L and p.sp_P were fixed at plan time (P % 4 == 0, SB * P threads)
+  if (p.sp_L == 16) {
+    if (p.cyclic) return launch<16, 8, 512, true>(p, X, batch, st);
+    return launch<16, 8, 512, false>(p, X, batch, st);
+  }
+  if (p.cyclic) return p.sp_P <= 32 ? launch<32, 16, 512, true>(p, X, batch, st)
+                                    : launch<32, 8, 512, true>(p, X, batch, st);
+  return p.sp_P <= 32 ? launch<32, 8, 256, false>(p, X, batch, st)
+                      : launch<32, 8, 512, false>(p, X, batch, st);
+}
+
+}  // namespace pent

@@ -8,7 +8,7 @@ from tests.gpu_util import TOL_F32, TOL_F64, dev, host, max_rel_err, random_dd_b
 
 pytestmark = pytest.mark.gpu
 
-VARIANTS_F64 = ["thread", "thread_df"]
+VARIANTS_F64 = ["thread", "thread_df", "split"]
 
 
 def solve_gpu(bands, F, cyclic, variant="auto", dtype="f64"):
@@ -115,6 +115,20 @@ def test_df_zero_and_spike_systems(cyclic):
     assert np.max(np.abs(X[:, 0])) < 1e-30
     ref = oracle.batch_shared(bands, F[:, 1:], cyclic=cyclic)
     assert max_rel_err(X[:, 1:], ref) < TOL_F64
+
+
+@pytest.mark.parametrize("cyclic", [False, True])
+@pytest.mark.parametrize("N,sigma", [(1024, 1e4), (300, 50.0), (1024, 1.0)])
+def test_split_serial_and_parallel_scans(cyclic, N, sigma, monkeypatch):
+    """The partitioned kernel with its parallel (truncated-coupling) scan and with the
+    exact serial scan forced; sigma = 1e4 couples chunks too strongly for truncation,
+    so the plan itself falls back to the serial scan there."""
+    bands = inputs.hyper_bands(N, sigma)
+    F = inputs.rhs_uniform(N, 96, seed=N)
+    ref = oracle.batch_shared(bands, F, cyclic=cyclic)
+    assert max_rel_err(solve_gpu(bands, F, cyclic, "split"), ref) < TOL_F64
+    monkeypatch.setenv("PENT_SPLIT_T", "0")
+    assert max_rel_err(solve_gpu(bands, F, cyclic, "split"), ref) < TOL_F64
 
 
 def test_zero_pivot_is_reported():
