@@ -87,6 +87,24 @@ __device__ __forceinline__ D2 axpy(D2 a, D2 c, D2 y) {
   return D2{s, lo};
 }
 
+// a * b (exact product of the hi words, cross terms in the low word)
+__device__ __forceinline__ D2 mul(D2 a, D2 b) {
+  float p, e;
+  two_prod(a.h, b.h, p, e);
+  float lo = __fmaf_rn(a.h, b.l, e);
+  lo = __fmaf_rn(a.l, b.h, lo);
+  return D2{p, lo};
+}
+
+// a + b
+__device__ __forceinline__ D2 add(D2 a, D2 b) {
+  float s, t;
+  two_sum(a.h, b.h, s, t);
+  return D2{s, __fadd_rn(__fadd_rn(a.l, b.l), t)};
+}
+
+__device__ __forceinline__ D2 neg(D2 a) { return D2{-a.h, -a.l}; }
+
 // ---------------------------------------------------------------------------
 // fp64 <-> df64 by integer operations
 // ---------------------------------------------------------------------------

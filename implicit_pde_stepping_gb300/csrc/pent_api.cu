@@ -30,12 +30,17 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 // Largest sweep length whose double-float tables fit in one CTA's shared memory.
 constexpr int kMaxTwistedRows = 2560;
 
-// The kernel variant a plan uses for `batch` systems: fp64 plans take the
-// double-float twisted kernel when its tables exist, else the native one.
+// The kernel variant a plan uses for `batch` systems.  fp64 plans run in
+// double-float: the twisted kernel when the batch alone fills every SM with
+// two CTAs of 256 systems, else the partitioned kernel (fine-grained, so small
+// batches still spread over the GPU); the native kernel when neither exists.
 pent_variant resolve(const pent_plan_s& p, int batch) {
   if (p.variant != PENT_VARIANT_AUTO) return p.variant;
-  (void)batch;
-  if (p.dtype == PENT_F64 && p.twist_ok) return PENT_VARIANT_THREAD_DF;
+  if (p.dtype != PENT_F64) return PENT_VARIANT_THREAD;
+  const long long fill = 2LL * 256 * (p.num_sms > 0 ? p.num_sms : 1);
+  if (p.twist_ok && batch % 2 == 0 && batch >= fill) return PENT_VARIANT_THREAD_DF;
+  if (p.split_ok) return PENT_VARIANT_SPLIT;
+  if (p.twist_ok) return PENT_VARIANT_THREAD_DF;
   return PENT_VARIANT_THREAD;
 }
 
@@ -292,8 +297,14 @@ pent_status ch_step(pent_plan p, void* C, int batch, double dt_over_dx2, int nst
   if (!p || !C || batch < 1 || nsteps < 0) return PENT_ERR_INVALID_ARG;
   if (!p->cyclic || p->dtype != PENT_F64) return PENT_ERR_INVALID_ARG;
   if (!aligned(C, 16)) return PENT_ERR_INVALID_ARG;
+  // the partitioned double-float kernel unless the native one is requested
+  const bool use_split = p->split_ok && p->N >= 8 &&
+                         (p->variant == PENT_VARIANT_AUTO || p->variant == PENT_VARIANT_SPLIT ||
+                          p->variant == PENT_VARIANT_THREAD_DF);
   for (int n = 0; n < nsteps; ++n) {
-    const cudaError_t e = ch_thread_f64(*p, static_cast<double*>(C), batch, dt_over_dx2, as_stream(stream));
+    const cudaError_t e =
+        use_split ? ch_split_df(*p, static_cast<double*>(C), batch, dt_over_dx2, as_stream(stream))
+                  : ch_thread_f64(*p, static_cast<double*>(C), batch, dt_over_dx2, as_stream(stream));
     if (e != cudaSuccess) return from_cuda(e);
   }
   return PENT_OK;

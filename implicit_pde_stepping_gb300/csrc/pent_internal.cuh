@@ -139,5 +139,6 @@ cudaError_t factor_split(const double* d_bands, int N, int cyclic, int L, int Mp
                          cudaStream_t st);
 cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 size_t split_smem_bytes(int L, int P, int SB, int cyclic);
+cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);
 
 }  // namespace pent

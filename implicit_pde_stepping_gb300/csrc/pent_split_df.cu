@@ -38,11 +38,21 @@ __device__ __forceinline__ void mv2(const double* A, double x0, double x1, doubl
   y1 = fma(A[2], x0, fma(A[3], x1, y1));
 }
 
-template <int L, int SB, int MAXT, bool CYC>
+// u = c^3 - c (Cahn–Hilliard chemical potential without the gradient term)
+__device__ __forceinline__ D2 cubic_minus(D2 c) { return df::add(df::mul(df::mul(c, c), c), df::neg(c)); }
+
+// rhs_i = C_i + k2 (u_{i-1} - 2 u_i + u_{i+1})   (eq. (2), D2 = [1, -2, 1]/dx^2, k2 = dt/dx^2)
+__device__ __forceinline__ D2 ch_rhs(D2 c, D2 um, D2 u0, D2 up, D2 k2) {
+  const D2 lap = df::add(df::add(um, up), D2{-2.f * u0.h, -2.f * u0.l});
+  return df::add(c, df::mul(k2, lap));
+}
+
+template <int L, int SB, int MAXT, bool CYC, bool CH>
 __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     k_split_df(const float4* __restrict__ growtab, const double* __restrict__ gchunk,
                const double* __restrict__ gextra, double* __restrict__ X, int M, int P,
-               int batch) {
+               int batch, double k2d) {
+  static_assert(!CH || CYC, "the Cahn-Hilliard step is periodic");
   constexpr int K4 = CYC ? kSpK : kSpK - 1;   // float4 per row kept in shared memory
   constexpr int CS = L * K4 + 1;              // chunk stride (float4), padded
   constexpr int SG = SB / 8;                  // system groups of 8 per CTA
@@ -79,7 +89,37 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
 
     // ---- 1. load, local forward (zero incoming state), local backward
     D2 v[L];
-    {
+    if constexpr (CH) {
+      // right-hand side from C_{i-1}, C_i, C_{i+1} (row -1 wraps to N-1 = M+1);
+      // every load of this block precedes the first store (barriers below)
+      double cv[L + 2];
+#pragma unroll
+      for (int j = 0; j < L + 2; ++j) {
+        const int i = row0 - 1 + j;
+        const int iw = i < 0 ? M + 1 : i;
+        cv[j] = (act && i <= M) ? X[(long long)iw * ld + s] : 0.0;
+      }
+      const D2 k2 = df::from_double(k2d);
+      D2 cc = df::from_double(cv[1]);
+      D2 um = cubic_minus(df::from_double(cv[0])), u0 = cubic_minus(cc);
+      D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < L; ++j) {
+        const D2 cn = df::from_double(cv[j + 2]);
+        const D2 up = cubic_minus(cn);
+        D2 f = ch_rhs(cc, um, u0, up, k2);
+        if (row0 + j >= M) f = D2{0.f, 0.f};
+        const float4 c0 = ctb[j * K4];
+        const float4 c1 = ctb[j * K4 + 1];
+        const D2 g = df::sum3p(D2{c0.x, c0.y}, f, D2{c0.z, c0.w}, a2, D2{c1.x, c1.y}, a1);
+        v[j] = g;
+        a2 = a1;
+        a1 = g;
+        um = u0;
+        u0 = up;
+        cc = cn;
+      }
+    } else {
       double fv[L];
 #pragma unroll
       for (int j = 0; j < L; ++j) fv[j] = (act && row0 + j < M) ? p[j * ld] : 0.0;
@@ -214,8 +254,21 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         const double r1 = gextra[7] * xc[1] + gextra[8] * xc[2] + gextra[9] * xc[3];
         double ft0 = 0.0, ft1 = 0.0;
         if (act) {
-          ft0 = X[(long long)M * ld + s];
-          ft1 = X[(long long)(M + 1) * ld + s];
+          if constexpr (CH) {
+            // tail rows N-2 = M and N-1 = M+1 need C at M-1, M, M+1 and 0
+            const D2 k2 = df::from_double(k2d);
+            const D2 cA = df::from_double(X[(long long)(M - 1) * ld + s]);
+            const D2 cB = df::from_double(X[(long long)M * ld + s]);
+            const D2 cC = df::from_double(X[(long long)(M + 1) * ld + s]);
+            const D2 cD = df::from_double(X[s]);
+            const D2 uA = cubic_minus(cA), uB = cubic_minus(cB), uC = cubic_minus(cC);
+            const D2 uD = cubic_minus(cD);
+            ft0 = df::to_double(ch_rhs(cB, uA, uB, uC, k2));
+            ft1 = df::to_double(ch_rhs(cC, uB, uC, uD, k2));
+          } else {
+            ft0 = X[(long long)M * ld + s];
+            ft1 = X[(long long)(M + 1) * ld + s];
+          }
         }
         const double u0 = gextra[0] * (ft0 - r0) + gextra[1] * (ft1 - r1);
         const double u1 = gextra[2] * (ft0 - r0) + gextra[3] * (ft1 - r1);
@@ -254,18 +307,18 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   }
 }
 
-template <int L, int SB, int MAXT, bool CYC>
-cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+template <int L, int SB, int MAXT, bool CYC, bool CH = false>
+cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st, double k2 = 0.0) {
   const int P = p.sp_P;
   const size_t smem = split_smem_bytes(L, P, SB, CYC);
-  auto kern = k_split_df<L, SB, MAXT, CYC>;
+  auto kern = k_split_df<L, SB, MAXT, CYC, CH>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nblk = (batch + SB - 1) / SB;
   const int per_sm = (MAXT <= 256 && smem <= 110 * 1024) ? 2 : 1;
   int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
   if (grid > nblk) grid = nblk;
-  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch);
+  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch, k2);
   note_launch();
   return cudaGetLastError();
 }
@@ -288,6 +341,12 @@ cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStre
                                     : launch<32, 8, 512, true>(p, X, batch, st);
   return p.sp_P <= 32 ? launch<32, 8, 256, false>(p, X, batch, st)
                       : launch<32, 8, 512, false>(p, X, batch, st);
+}
+
+cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st) {
+  if (p.sp_L == 16) return launch<16, 8, 512, true, true>(p, X, batch, st, k2);
+  return p.sp_P <= 32 ? launch<32, 16, 512, true, true>(p, X, batch, st, k2)
+                      : launch<32, 8, 512, true, true>(p, X, batch, st, k2);
 }
 
 }  // namespace pent
