@@ -282,32 +282,44 @@ def run_ours(args, W: dict, dist: Dist):
     # ---- end to end through the public API: pinned host in, host out, every step
     e2e = None
     if not args.no_e2e:
+        # every input of a step comes from pinned host memory: the right-hand side, and for
+        # per-system matrices also the five bands (the shared matrix lives in the plan)
         host_in = bufs[0].cpu().pin_memory()
         host_out = torch.empty_like(host_in).pin_memory()
         Xd = torch.empty_like(bufs[0])
+        host_bands = [b.cpu().pin_memory() for b in bands] if kind == "persys" else []
+        dev_bands = [torch.empty_like(b) for b in bands] if kind == "persys" else []
+
+        def e2e_step():
+            for hb, db in zip(host_bands, dev_bands):
+                db.copy_(hb, non_blocking=True)
+            Xd.copy_(host_in, non_blocking=True)
+            if kind == "persys":
+                pent.pent_factor_solve(*dev_bands, Xd, work=work, stream=stream)
+            else:
+                step(0, Xd)
+            host_out.copy_(Xd, non_blocking=True)
+
         ke = max(1, min(args.steps, args.e2e_steps))
         with torch.cuda.stream(stream):
             for _ in range(2):
-                Xd.copy_(host_in, non_blocking=True)
-                step(0, Xd)
-                host_out.copy_(Xd, non_blocking=True)
+                e2e_step()
         stream.synchronize()
         dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
             e0.record(stream)
             for _ in range(ke):
-                Xd.copy_(host_in, non_blocking=True)
-                step(0, Xd)
-                host_out.copy_(Xd, non_blocking=True)
+                e2e_step()
             e1.record(stream)
         stream.synchronize()
         dist.barrier()
         ems = dist.max(e0.elapsed_time(e1))
-        nbytes = host_in.numel() * host_in.element_size()
+        nbytes_out = host_in.numel() * host_in.element_size()
+        nbytes = nbytes_out + sum(b.numel() * b.element_size() for b in host_bands)
         e2e = {"value": batch * ke * dist.world / (ems / 1e3), "unit": "system-solves/s"
                if kind in ("shared", "persys") else "system-steps/s",
-               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes, "steps": ke,
+               "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes_out, "steps": ke,
                "ms_per_step": ems / ke}
 
     # ---- roofline of the dominant kernel (one kernel per step on every path)
