@@ -334,6 +334,203 @@ __global__ void __launch_bounds__(2 * SPB / SPT)
   }
 }
 
+// ---- asynchronous row streaming (cp.async: global -> shared, no registers held)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int NPEND>
+__device__ __forceinline__ void cp_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(NPEND) : "memory");
+}
+__device__ __forceinline__ void unpack2(const uint4 r, double* v) {
+  v[0] = __hiloint2double((int)r.y, (int)r.x);
+  v[1] = __hiloint2double((int)r.w, (int)r.z);
+}
+
+// Same sweeps as k_twisted_df with two systems per thread, but every row a
+// thread needs is streamed D rows ahead into its own 16-byte slots of a
+// shared-memory ring by cp.async, so the prefetch depth costs no registers.
+template <int SPB, int D, bool CYC>
+__global__ void __launch_bounds__(SPB, 2)
+    k_twisted_async(const float4* __restrict__ gtab, const double* __restrict__ twist,
+                    double* __restrict__ X, int M, int m, int batch) {
+  constexpr int SPT = 2;
+  constexpr int TPD = SPB / SPT;            // threads per direction
+  constexpr int NT = 2 * TPD;               // threads per CTA
+  constexpr int KT = CYC ? kTwK : 3;        // float4 per table row kept in shared memory
+  constexpr int NX = CYC ? 8 : 4;
+  extern __shared__ float4 sm_tw[];
+  float4* stab = sm_tw;                                          // [M][KT]
+  uint4* ring = reinterpret_cast<uint4*>(stab + (size_t)M * KT);  // [D][NT]
+  __shared__ double sx[TPD][SPT][NX];
+  __shared__ double sT[kTwistCount];
+  for (int t = threadIdx.x; t < M * KT; t += NT) stab[t] = gtab[(size_t)(t / KT) * kTwK + t % KT];
+  if (threadIdx.x < kTwistCount) sT[threadIdx.x] = twist[threadIdx.x];
+  __syncthreads();
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  const bool top = warp < TPD / 32;
+  const int grp = top ? warp : warp - TPD / 32;
+  const int tl = grp * 32 + lane;
+  const float4* tab = stab + (top ? 0 : m * KT);
+  const int rows = top ? m : M - m;
+  const long long ld = batch;
+  const long long stepB = (top ? ld : -ld) * (long long)sizeof(double);
+  const int nblk = (batch + SPB - 1) / SPB;
+  const int jtop = rows - 3;
+  uint4* myring = ring + tid;
+
+  for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    const int s0 = blk * SPB + tl * SPT;
+    const bool act = s0 < batch;
+    char* p0 = reinterpret_cast<char*>(X + (top ? 0 : (long long)(M - 1) * ld) + (act ? s0 : 0));
+    Lane<SPT> st;
+#pragma unroll
+    for (int t = 0; t < SPT; ++t) st.a1[t] = st.a2[t] = st.acc0[t] = st.acc1[t] = D2{0.f, 0.f};
+
+    // ------------------------------------------------ inward sweep
+#pragma unroll
+    for (int u = 0; u < D; ++u) {
+      if (u < rows) cp_async16(myring + u * NT, p0 + (long long)u * stepB);
+      cp_commit();
+    }
+    for (int j0 = 0; j0 < rows; j0 += D) {
+      const bool fullb = j0 + D <= rows;
+#pragma unroll
+      for (int u = 0; u < D; ++u) {
+        const int j = j0 + u;
+        if (fullb || j < rows) {
+          cp_wait<D - 1>();
+          double f[SPT];
+          unpack2(myring[u * NT], f);
+          D2 g[SPT];
+          inward_row<SPT, CYC>(tab + j * KT, f, st, g);
+          char* q = p0 + (long long)j * stepB;
+          if (act) st_g<SPT>(q, g);
+          if (j + D < rows) cp_async16(myring + u * NT, q + (long long)D * stepB);
+        }
+        cp_commit();
+      }
+    }
+    __threadfence();   // this thread's g stores are performed before it streams them back
+
+    // ------------------------------------------------ meeting point (fp64)
+#pragma unroll
+    for (int t = 0; t < SPT; ++t) {
+      if (top) {
+        sx[tl][t][0] = df::to_double(st.a2[t]);
+        sx[tl][t][1] = df::to_double(st.a1[t]);
+        if (CYC) { sx[tl][t][4] = df::to_double(st.acc0[t]); sx[tl][t][5] = df::to_double(st.acc1[t]); }
+      } else {
+        sx[tl][t][2] = df::to_double(st.a1[t]);
+        sx[tl][t][3] = df::to_double(st.a2[t]);
+        if (CYC) { sx[tl][t][6] = df::to_double(st.acc0[t]); sx[tl][t][7] = df::to_double(st.acc1[t]); }
+      }
+    }
+    named_barrier(1 + grp, 64);
+    const double* Ti = sT + (top ? 0 : 8);
+    double v0[SPT], v1[SPT], xt0[SPT], xt1[SPT];
+    D2 nx0[SPT], nx1[SPT];
+#pragma unroll
+    for (int t = 0; t < SPT; ++t) {
+      const double w0 = sx[tl][t][0], w1 = sx[tl][t][1], w2 = sx[tl][t][2], w3 = sx[tl][t][3];
+      v0[t] = Ti[0] * w0 + Ti[1] * w1 + Ti[2] * w2 + Ti[3] * w3;
+      v1[t] = Ti[4] * w0 + Ti[5] * w1 + Ti[6] * w2 + Ti[7] * w3;
+      nx0[t] = nx1[t] = D2{0.f, 0.f};
+    }
+    if (CYC) {
+      double ft0[SPT], ft1[SPT];
+      const char* pt = reinterpret_cast<const char*>(X + (long long)M * ld + (act ? s0 : 0));
+      ld_f<SPT>(pt, ft0);
+      ld_f<SPT>(pt + ld * (long long)sizeof(double), ft1);
+#pragma unroll
+      for (int t = 0; t < SPT; ++t) {
+        const double r0 = ft0[t] - (sx[tl][t][4] + sx[tl][t][6]);
+        const double r1 = ft1[t] - (sx[tl][t][5] + sx[tl][t][7]);
+        xt0[t] = sT[16] * r0 + sT[17] * r1;
+        xt1[t] = sT[18] * r0 + sT[19] * r1;
+        nx0[t] = df::from_double(-xt0[t]);
+        nx1[t] = df::from_double(-xt1[t]);
+      }
+    }
+    named_barrier(1 + grp, 64);   // partner has read sx (and f_t) before reuse / overwrite
+    if (CYC && act && !top) {
+      char* pt = reinterpret_cast<char*>(X + (long long)M * ld + s0);
+      st_x<SPT>(pt, xt0);
+      st_x<SPT>(pt + ld * (long long)sizeof(double), xt1);
+    }
+    {
+      const int jA = top ? rows - 2 : rows - 1;
+      const int jB = top ? rows - 1 : rows - 2;
+      double xa[SPT], xb[SPT];
+#pragma unroll
+      for (int t = 0; t < SPT; ++t) {
+        const D2 a = df::from_double(v0[t]), b = df::from_double(v1[t]);
+        st.a1[t] = top ? a : b;
+        st.a2[t] = top ? b : a;
+        if (CYC) {
+          const float4 cA3 = tab[jA * KT + 3], cA4 = tab[jA * KT + 4];
+          const float4 cB3 = tab[jB * KT + 3], cB4 = tab[jB * KT + 4];
+          xa[t] = df::to_double(df::axpy(df::axpy(a, D2{cA3.z, cA3.w}, nx0[t]), D2{cA4.x, cA4.y}, nx1[t]));
+          xb[t] = df::to_double(df::axpy(df::axpy(b, D2{cB3.z, cB3.w}, nx0[t]), D2{cB4.x, cB4.y}, nx1[t]));
+        } else {
+          xa[t] = v0[t];
+          xb[t] = v1[t];
+        }
+      }
+      if (act) {
+        st_x<SPT>(p0 + (long long)jA * stepB, xa);
+        st_x<SPT>(p0 + (long long)jB * stepB, xb);
+      }
+    }
+
+    // ------------------------------------------------ outward sweep, local rows jtop..0
+#pragma unroll
+    for (int u = 0; u < D; ++u) {
+      if (jtop - u >= 0) cp_async16(myring + u * NT, p0 + (long long)(jtop - u) * stepB);
+      cp_commit();
+    }
+    for (int j0 = jtop; j0 >= 0; j0 -= D) {
+      const bool fullb = j0 - (D - 1) >= 0;
+#pragma unroll
+      for (int u = 0; u < D; ++u) {
+        const int j = j0 - u;
+        if (fullb || j >= 0) {
+          cp_wait<D - 1>();
+          const uint4 r = myring[u * NT];
+          D2 g[SPT] = {D2{__uint_as_float(r.x), __uint_as_float(r.y)},
+                       D2{__uint_as_float(r.z), __uint_as_float(r.w)}};
+          double x[SPT];
+          outward_row<SPT, CYC>(tab + j * KT, g, st, nx0, nx1, x);
+          char* q = p0 + (long long)j * stepB;
+          if (act) st_x<SPT>(q, x);
+          if (j - D >= 0) cp_async16(myring + u * NT, q - (long long)D * stepB);
+        }
+        cp_commit();
+      }
+    }
+    cp_wait<0>();
+  }
+}
+
+template <int SPB, int D, bool CYC>
+cudaError_t launch_async(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+  constexpr int KT = CYC ? kTwK : 3;
+  const size_t smem = (size_t)p.M * KT * sizeof(float4) + (size_t)D * SPB * sizeof(uint4);
+  auto kern = k_twisted_async<SPB, D, CYC>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int nblk = (batch + SPB - 1) / SPB;
+  int grid = p.df_ctas > 0 ? p.df_ctas : 2 * p.num_sms;
+  if (grid > nblk) grid = nblk;
+  kern<<<grid, SPB, smem, st>>>(p.twtab, p.twist, X, p.M, p.m, batch);
+  note_launch();
+  return cudaGetLastError();
+}
+
 template <int SPT, int SPB, int KU, bool CYC>
 cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   const size_t smem = (size_t)p.M * kTwK * sizeof(float4);
@@ -350,6 +547,11 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st) 
 
 template <bool CYC>
 cudaError_t dispatch(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+  if (batch % 2 == 0 && p.df_async > 0) {
+    if (p.df_async == 12) return launch_async<256, 12, CYC>(p, X, batch, st);
+    if (p.df_async == 4) return launch_async<256, 4, CYC>(p, X, batch, st);
+    return launch_async<256, 8, CYC>(p, X, batch, st);
+  }
   if (batch % 2 == 0 && p.df_spt != 1) {
     switch (p.df_spb) {
       case 128: return p.df_ku == 4 ? launch<2, 128, 4, CYC>(p, X, batch, st)
