@@ -46,7 +46,7 @@ struct pent_plan_s {
   int df_spt = 2;            // systems per thread (2 needs an even batch)
   int df_ku = 4;             // rows per prefetch block
   int df_ctas = 0;           // CTAs of the double-float kernels (0: two per SM)
-  int df_async = 8;          // cp.async ring depth of the twisted kernel (0: register ring)
+  int df_async = 6;          // cp.async ring depth of the twisted kernel (0: register ring)
   // partitioned double-float variant (pent_factor_split.cu / pent_split_df.cu)
   int split_ok = 0;          // tables valid
   int sp_L = 0, sp_P = 0;    // chunk length, chunks per system (Mpad = sp_L * sp_P)

@@ -397,22 +397,43 @@ __global__ void __launch_bounds__(SPB, 2)
       if (u < rows) cp_async16(myring + u * NT, p0 + (long long)u * stepB);
       cp_commit();
     }
-    for (int j0 = 0; j0 < rows; j0 += D) {
-      const bool fullb = j0 + D <= rows;
+    {
+      // main blocks: row j and its prefetch row j + D both exist -> no guards
+      const int nmain = rows >= 2 * D ? rows / D - 1 : 0;
+      char* q = p0;
+      const long long pf = (long long)D * stepB;
+      const float4* row = tab;
+      for (int b = 0; b < nmain; ++b) {
 #pragma unroll
-      for (int u = 0; u < D; ++u) {
-        const int j = j0 + u;
-        if (fullb || j < rows) {
+        for (int u = 0; u < D; ++u) {
           cp_wait<D - 1>();
           double f[SPT];
           unpack2(myring[u * NT], f);
           D2 g[SPT];
-          inward_row<SPT, CYC>(tab + j * KT, f, st, g);
-          char* q = p0 + (long long)j * stepB;
+          inward_row<SPT, CYC>(row, f, st, g);
           if (act) st_g<SPT>(q, g);
-          if (j + D < rows) cp_async16(myring + u * NT, q + (long long)D * stepB);
+          cp_async16(myring + u * NT, q + pf);
+          cp_commit();
+          q += stepB;
+          row += KT;
         }
-        cp_commit();
+      }
+      for (int j0 = nmain * D; j0 < rows; j0 += D) {
+#pragma unroll
+        for (int u = 0; u < D; ++u) {
+          const int j = j0 + u;
+          if (j < rows) {
+            cp_wait<D - 1>();
+            double f[SPT];
+            unpack2(myring[u * NT], f);
+            D2 g[SPT];
+            inward_row<SPT, CYC>(tab + j * KT, f, st, g);
+            char* qq = p0 + (long long)j * stepB;
+            if (act) st_g<SPT>(qq, g);
+            if (j + D < rows) cp_async16(myring + u * NT, qq + pf);
+          }
+          cp_commit();
+        }
       }
     }
     __threadfence();   // this thread's g stores are performed before it streams them back
@@ -493,23 +514,45 @@ __global__ void __launch_bounds__(SPB, 2)
       if (jtop - u >= 0) cp_async16(myring + u * NT, p0 + (long long)(jtop - u) * stepB);
       cp_commit();
     }
-    for (int j0 = jtop; j0 >= 0; j0 -= D) {
-      const bool fullb = j0 - (D - 1) >= 0;
+    {
+      const int nrows = jtop + 1;
+      const int nmain = nrows >= 2 * D ? nrows / D - 1 : 0;
+      char* q = p0 + (long long)jtop * stepB;
+      const long long pf = (long long)D * stepB;
+      const float4* row = tab + jtop * KT;
+      for (int b = 0; b < nmain; ++b) {
 #pragma unroll
-      for (int u = 0; u < D; ++u) {
-        const int j = j0 - u;
-        if (fullb || j >= 0) {
+        for (int u = 0; u < D; ++u) {
           cp_wait<D - 1>();
           const uint4 r = myring[u * NT];
           D2 g[SPT] = {D2{__uint_as_float(r.x), __uint_as_float(r.y)},
                        D2{__uint_as_float(r.z), __uint_as_float(r.w)}};
           double x[SPT];
-          outward_row<SPT, CYC>(tab + j * KT, g, st, nx0, nx1, x);
-          char* q = p0 + (long long)j * stepB;
+          outward_row<SPT, CYC>(row, g, st, nx0, nx1, x);
           if (act) st_x<SPT>(q, x);
-          if (j - D >= 0) cp_async16(myring + u * NT, q - (long long)D * stepB);
+          cp_async16(myring + u * NT, q - pf);
+          cp_commit();
+          q -= stepB;
+          row -= KT;
         }
-        cp_commit();
+      }
+      for (int j0 = jtop - nmain * D; j0 >= 0; j0 -= D) {
+#pragma unroll
+        for (int u = 0; u < D; ++u) {
+          const int j = j0 - u;
+          if (j >= 0) {
+            cp_wait<D - 1>();
+            const uint4 r = myring[u * NT];
+            D2 g[SPT] = {D2{__uint_as_float(r.x), __uint_as_float(r.y)},
+                         D2{__uint_as_float(r.z), __uint_as_float(r.w)}};
+            double x[SPT];
+            outward_row<SPT, CYC>(tab + j * KT, g, st, nx0, nx1, x);
+            char* qq = p0 + (long long)j * stepB;
+            if (act) st_x<SPT>(qq, x);
+            if (j - D >= 0) cp_async16(myring + u * NT, qq - pf);
+          }
+          cp_commit();
+        }
       }
     }
     cp_wait<0>();
@@ -550,6 +593,7 @@ cudaError_t dispatch(const pent_plan_s& p, double* X, int batch, cudaStream_t st
   if (batch % 2 == 0 && p.df_async > 0) {
     if (p.df_async == 12) return launch_async<256, 12, CYC>(p, X, batch, st);
     if (p.df_async == 4) return launch_async<256, 4, CYC>(p, X, batch, st);
+    if (p.df_async == 6) return launch_async<256, 6, CYC>(p, X, batch, st);
     return launch_async<256, 8, CYC>(p, X, batch, st);
   }
   if (batch % 2 == 0 && p.df_spt != 1) {
