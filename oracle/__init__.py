@@ -65,9 +65,10 @@ def _load():
             lib.oracle_batch_persys.argtypes = [i, i] + [dp] * 7
             lib.oracle_batch_hyperdiffusion.argtypes = [i, i, d, i, dp]
             lib.oracle_batch_ch.argtypes = [i, i, d, d, i, dp]
+            lib.oracle_batch_cn.argtypes = [i, i, d, i, dp]
             for fn in ("oracle_pent_factor", "oracle_pent_solve", "oracle_cyclic_solve",
                        "oracle_batch_shared", "oracle_batch_persys",
-                       "oracle_batch_hyperdiffusion", "oracle_batch_ch"):
+                       "oracle_batch_hyperdiffusion", "oracle_batch_ch", "oracle_batch_cn"):
                 getattr(lib, fn).restype = i
             _lib = lib
     return _lib
@@ -158,3 +159,12 @@ def batch_ch(C_il, sigma: float, dt_over_dx2: float, nsteps: int) -> np.ndarray:
     _check(_load().oracle_batch_ch(N, batch, float(sigma), float(dt_over_dx2), int(nsteps), _p(X)),
            "batch_ch")
     return np.ascontiguousarray(X.T)
+
+
+def batch_cn(C_il, sigma_x: float, nsteps: int) -> np.ndarray:
+    """nsteps of Crank–Nicolson hyperdiffusion (I + sx D4) C' = (I - sx D4) C, periodic."""
+    X = _rows(C_il)
+    batch, N = X.shape
+    _check(_load().oracle_batch_cn(N, batch, float(sigma_x), int(nsteps), _p(X)), "batch_cn")
+    return np.ascontiguousarray(X.T)
+

@@ -13,7 +13,8 @@
  *   - forward substitution L g = f, steps 1–3;
  *   - back substitution R x = g, steps 1–3;
  *   - periodic (cyclic) matrix (7c) solved by Navon's bordering, eqs. (8)–(12);
- *   - hyperdiffusion / Cahn–Hilliard semi-implicit stepping, eqs. (1)–(2), (4).
+ *   - hyperdiffusion / Cahn–Hilliard semi-implicit stepping, eqs. (1)–(2), (4);
+ *   - Crank–Nicolson hyperdiffusion, eqs. (5)–(6), sigma_x = dt / (2 dx^4).
  *
  * Conventions (0-based; the page is 1-based).  Row i of the matrix holds
  *   a[i] at column i-2, b[i] at i-1, c[i] at i, d[i] at i+1, e[i] at i+2.
@@ -244,6 +245,33 @@ int oracle_ch_steps(int N, double sigma, double dt_over_dx2, int nsteps, double*
   return rc;
 }
 
+/*
+ * nsteps of the Crank–Nicolson scheme for hyperdiffusion, periodic
+ * (eqs. (5)–(6), sigma_x = dt / (2 dx^4)):
+ *   (I + sigma_x D4) C^{n+1} = (I - sigma_x D4) C^n.
+ * The right-hand side is the explicit stencil applied to C^n, indices mod N.
+ */
+int oracle_cn_steps(int N, double sigma_x, int nsteps, double* C) {
+  if (N < 5 || nsteps < 0) return OR_EINVAL;
+  double* w = (double*)malloc(sizeof(double) * 7 * (size_t)N);
+  if (!w) return OR_ENOMEM;
+  double *a = w, *b = w + N, *c = w + 2 * N, *d = w + 3 * N, *e = w + 4 * N, *x = w + 5 * N;
+  double* rhs = w + 6 * N;
+  hyper_bands(N, sigma_x, a, b, c, d, e);
+  int rc = OR_OK;
+  for (int n = 0; n < nsteps && rc == OR_OK; ++n) {
+    for (int i = 0; i < N; ++i) {
+      int im2 = (i + N - 2) % N, im1 = (i + N - 1) % N, ip1 = (i + 1) % N, ip2 = (i + 2) % N;
+      double d4 = C[im2] - 4.0 * C[im1] + 6.0 * C[i] - 4.0 * C[ip1] + C[ip2];
+      rhs[i] = C[i] - sigma_x * d4;
+    }
+    rc = oracle_cyclic_solve(N, a, b, c, d, e, rhs, x);
+    if (rc == OR_OK) memcpy(C, x, sizeof(double) * (size_t)N);
+  }
+  free(w);
+  return rc;
+}
+
 /* ---------------------------------------------------------------------------
  * Batched drivers.  X and F are [batch][N] (one system per row); X may alias F.
  * Each returns the first nonzero per-system code, or 0.
@@ -332,6 +360,20 @@ int oracle_batch_ch(int N, int batch, double sigma, double dt_over_dx2, int nste
 #pragma omp parallel for schedule(static)
   for (long s = 0; s < batch; ++s) {
     int r = oracle_ch_steps(N, sigma, dt_over_dx2, nsteps, C + s * (size_t)N);
+    if (r != OR_OK) {
+#pragma omp critical
+      if (rc == OR_OK) rc = r;
+    }
+  }
+  return rc;
+}
+
+int oracle_batch_cn(int N, int batch, double sigma_x, int nsteps, double* C) {
+  if (N < 5 || batch < 0) return OR_EINVAL;
+  int rc = OR_OK;
+#pragma omp parallel for schedule(static)
+  for (long s = 0; s < batch; ++s) {
+    int r = oracle_cn_steps(N, sigma_x, nsteps, C + s * (size_t)N);
     if (r != OR_OK) {
 #pragma omp critical
       if (rc == OR_OK) rc = r;

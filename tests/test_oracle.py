@@ -222,3 +222,70 @@ def test_hyperdiffusion_exact_solution_convergence_order():
         errs.append(np.sqrt(np.sum((CT - exact) ** 2) * dx))
     orders = [np.log2(errs[i] / errs[i + 1]) for i in range(len(errs) - 1)]
     assert all(abs(o - g["error_order"]) < 0.15 for o in orders), (errs, orders)
+
+
+# ---------------------------------------------------------------------------
+# Crank–Nicolson hyperdiffusion (the page's time scheme, eqs. (5)–(6))
+# ---------------------------------------------------------------------------
+def test_cn_discrete_amplification():
+    """Each periodic Fourier mode k is multiplied per step by
+    (1 - 16 sx sin^4(pi k/N)) / (1 + 16 sx sin^4(pi k/N)).  With sx = 10 on
+    N = 64 the factor of modes 6..8 is negative (they flip sign every step),
+    which a wrong sign in the explicit half would not reproduce."""
+    steps, batch = 40, 4
+    for N, sx in ((512, 0.5), (64, 10.0)):
+        a, b = inputs.fourier_modes(N, batch)
+        C0 = inputs.fourier_initial(N, batch)
+        k = np.arange(1, 9)
+        s4 = np.sin(np.pi * k / N) ** 4
+        x = np.arange(N) / N
+        ph = 2 * np.pi * k[:, None] * x[None, :]
+        CT = oracle.batch_cn(C0, sx, steps)
+        G = ((1 - 16 * sx * s4) / (1 + 16 * sx * s4)) ** steps
+        ref = np.cos(ph).T @ (a * G[:, None]) + np.sin(ph).T @ (b * G[:, None])
+        assert rel(CT, ref) < 1e-12
+    assert (1 - 160 * np.sin(np.pi * 6 / 64) ** 4) < 0
+
+
+def test_cn_conserves_mean_and_matches_one_step_by_hand():
+    """The D4 stencil sums to zero, so both halves keep the mean.  One step on
+    N = 7 equals a dense solve of the two matrices assembled entry by entry."""
+    N, sx = 7, 0.37
+    C = np.random.default_rng(11).uniform(-1, 1, N)
+    D4 = np.zeros((N, N))
+    for i in range(N):
+        for off, w in ((-2, 1.0), (-1, -4.0), (0, 6.0), (1, -4.0), (2, 1.0)):
+            D4[i, (i + off) % N] += w
+    ref = np.linalg.solve(np.eye(N) + sx * D4, (np.eye(N) - sx * D4) @ C)
+    got = oracle.batch_cn(C[:, None], sx, 1)[:, 0]
+    assert rel(got, ref) < 1e-13
+    CT = oracle.batch_cn(inputs.ch_initial(1024, 3), 5.0, 50)
+    assert np.max(np.abs(CT.mean(axis=0) - inputs.ch_initial(1024, 3).mean(axis=0))) < 1e-12
+
+
+def test_cn_exact_solution_second_order():
+    """The page's validation (eq. (14), Figs. 1–2) run with its own scheme,
+    sigma_x = dt / (2 dx^4): the L2 error against the decaying harmonic falls as
+    N^-2.  At fixed N the error against the semi-discrete solution
+    (decay rate 16 sin^4(k dx / 2) / dx^4) falls as dt^2: Crank–Nicolson is
+    second order in time."""
+    g = _golden("hyperdiffusion_exact.txt")
+    k = 2 * np.pi * g["n"] / g["L"]
+    T = g["T"]
+
+    def err(N, steps, semi_discrete=False):
+        dt = T / steps
+        dx = g["L"] / N
+        x = np.arange(N) * dx
+        lam = g["gamma"] * g["D"] * (16 * np.sin(k * dx / 2) ** 4 / dx ** 4 if semi_discrete else k ** 4)
+        C0 = (g["A"] * np.cos(k * x + g["phi"]))[:, None]
+        CT = oracle.batch_cn(C0, g["gamma"] * g["D"] * dt / (2 * dx ** 4), steps)[:, 0]
+        exact = g["A"] * np.cos(k * x + g["phi"]) * np.exp(-lam * T)
+        return np.sqrt(np.sum((CT - exact) ** 2) * dx)
+
+    errs = [err(N, 400) for N in (32, 64, 128)]
+    orders = [np.log2(errs[i] / errs[i + 1]) for i in range(2)]
+    assert all(abs(o - g["error_order"]) < 0.15 for o in orders), (errs, orders)
+    et = [err(64, s, semi_discrete=True) for s in (10, 20, 40)]
+    t_orders = [np.log2(et[i] / et[i + 1]) for i in range(2)]
+    assert all(abs(o - 2.0) < 0.1 for o in t_orders), (et, t_orders)

@@ -38,6 +38,10 @@ MUTATIONS = [
      "rhs[i] = C[i] + dt_over_dx2 * (u[im] - 2.0 * u[i] - u[ip]);"),
     ("cubic sign", "u[i] = C[i] * C[i] * C[i] - C[i];", "u[i] = C[i] * C[i] * C[i] + C[i];"),
     ("D4 band sign", "b[i] = -4.0 * sigma;", "b[i] = 4.0 * sigma;"),
+    ("CN explicit half sign", "rhs[i] = C[i] - sigma_x * d4;", "rhs[i] = C[i] + sigma_x * d4;"),
+    ("CN stencil index", "double d4 = C[im2] - 4.0 * C[im1] + 6.0 * C[i] - 4.0 * C[ip1] + C[ip2];",
+     "double d4 = C[im2] - 4.0 * C[im1] + 6.0 * C[i] - 4.0 * C[ip1] + C[ip1];"),
+    ("CN wrap", "int im2 = (i + N - 2) % N,", "int im2 = (i + N - 1) % N,"),
 ]
 
 
@@ -52,6 +56,8 @@ def _pins():
     T.test_hyperdiffusion_discrete_amplification()
     T.test_ch_mass_conservation()
     T.test_ch_linearised_single_mode()
+    T.test_cn_discrete_amplification()
+    T.test_cn_conserves_mean_and_matches_one_step_by_hand()
     T.test_manufactured_solution_persys(False)
     T.test_manufactured_solution_persys(True)
 
