@@ -156,6 +156,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   p->spchunk = reinterpret_cast<double*>(arena + o_spchunk);
   p->spextra = reinterpret_cast<double*>(arena + o_spextra);
   double* d_bands = reinterpret_cast<double*>(arena + o_bands);
+  p->bands = d_bands;
   double* d_work = reinterpret_cast<double*>(arena + o_work);
   int* d_status = reinterpret_cast<int*>(arena + o_status);
 
@@ -306,6 +307,22 @@ pent_status ch_step(pent_plan p, void* C, int batch, double dt_over_dx2, int nst
     const cudaError_t e =
         use_split ? ch_split_df(*p, static_cast<double*>(C), batch, dt_over_dx2, as_stream(stream))
                   : ch_thread_f64(*p, static_cast<double*>(C), batch, dt_over_dx2, as_stream(stream));
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return PENT_OK;
+}
+
+pent_status cn_step(pent_plan p, void* C, int batch, int nsteps, void* stream) {
+  if (!p || !C || batch < 1 || nsteps < 0) return PENT_ERR_INVALID_ARG;
+  if (!p->cyclic || p->dtype != PENT_F64) return PENT_ERR_INVALID_ARG;
+  if (!aligned(C, 16)) return PENT_ERR_INVALID_ARG;
+  // the partitioned double-float kernel unless the native one is requested
+  const bool use_split = p->split_ok && (p->variant == PENT_VARIANT_AUTO ||
+                                         p->variant == PENT_VARIANT_SPLIT ||
+                                         p->variant == PENT_VARIANT_THREAD_DF);
+  for (int n = 0; n < nsteps; ++n) {
+    const cudaError_t e = use_split ? cn_split_df(*p, static_cast<double*>(C), batch, as_stream(stream))
+                                    : cn_thread_f64(*p, static_cast<double*>(C), batch, as_stream(stream));
     if (e != cudaSuccess) return from_cuda(e);
   }
   return PENT_OK;

@@ -35,6 +35,7 @@ struct pent_plan_s {
   float* tail32 = nullptr;
   float2* coefdf = nullptr;  // [kCoefCount][M] (hi, lo) double-float pairs
   float2* taildf = nullptr;
+  double* bands = nullptr;   // [5][N] the matrix as factored (a, b, c, d, e)
   void* arena = nullptr;     // single allocation backing all of the above
   // twisted double-float variant (pent_factor_twisted.cu / pent_twisted_df.cu)
   int m = 0;                 // meeting row: top rows 0..m-1, bottom rows m..M-1
@@ -70,7 +71,6 @@ cudaError_t pack_coefficients(const double* coef64, const double* tail64, int n_
 cudaError_t shared_thread_f64(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 cudaError_t shared_thread_f32(const pent_plan_s& p, float* X, int batch, cudaStream_t st);
 cudaError_t shared_twisted_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
-cudaError_t shared_split_f64(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 
 // persys.cu
 cudaError_t persys_thread(const void* a, const void* b, const void* c, const void* d, const void* e,
@@ -78,9 +78,9 @@ cudaError_t persys_thread(const void* a, const void* b, const void* c, const voi
                           cudaStream_t st);
 size_t persys_work_bytes(int N, int batch, pent_dtype dt);
 
-// ch.cu
+// ch.cu: fused explicit right-hand side + cyclic solve, one thread per system
 cudaError_t ch_thread_f64(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);
-cudaError_t ch_thread_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);
+cudaError_t cn_thread_f64(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 
 }  // namespace pent
 
@@ -141,5 +141,6 @@ cudaError_t factor_split(const double* d_bands, int N, int cyclic, int L, int Mp
 cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 size_t split_smem_bytes(int L, int P, int SB, int cyclic);
 cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);
+cudaError_t cn_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 
 }  // namespace pent

@@ -19,6 +19,14 @@
 // Cyclic plans carry Navon's bordering (eqs. (8)–(12)): x_t = S^{-1}(f_t -
 // H^T y) from y at rows 0, 1, M-2, M-1, and step 3 subtracts u0 x_t0 + u1 x_t1.
 //
+// Time steps fused into the same kernel (periodic plans):
+//   Cahn–Hilliard (eq. (2)): the load phase builds the right-hand side
+//     C_i + k2 (u_{i-1} - 2 u_i + u_{i+1}), u = C^3 - C, from C_{i-1..i+1};
+//   Crank–Nicolson (eqs. (5)–(6)): with A = I + sigma_x D4 the step
+//     A C' = (2I - A) C equals C' = 2 A^{-1} C - C, so the kernel solves with
+//     f = C and stores 2y - C, re-reading its own C_i (still in L2) at the
+//     store.
+//
 // Warp layout: 8 consecutive systems x 4 chunks per warp, so every load or
 // store instruction moves four 64-byte runs of one row each (whole sectors).
 // The per-row tables sit in shared memory with one float4 of padding per
@@ -47,12 +55,19 @@ __device__ __forceinline__ D2 ch_rhs(D2 c, D2 um, D2 u0, D2 up, D2 k2) {
   return df::add(c, df::mul(k2, lap));
 }
 
-template <int L, int SB, int MAXT, bool CYC, bool CH>
+// right-hand side / output kind of one launch
+constexpr int kRhsPlain = 0;   // solve A x = f in place
+constexpr int kRhsCH = 1;      // one Cahn–Hilliard step
+constexpr int kRhsCN = 2;      // one Crank–Nicolson step
+
+template <int L, int SB, int MAXT, bool CYC, int RHS>
 __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     k_split_df(const float4* __restrict__ growtab, const double* __restrict__ gchunk,
                const double* __restrict__ gextra, double* __restrict__ X, int M, int P,
                int batch, double k2d) {
-  static_assert(!CH || CYC, "the Cahn-Hilliard step is periodic");
+  constexpr bool CH = RHS == kRhsCH;
+  constexpr bool CN = RHS == kRhsCN;
+  static_assert(RHS == kRhsPlain || CYC, "the fused time steps are periodic");
   constexpr int K4 = CYC ? kSpK : kSpK - 1;   // float4 per row kept in shared memory
   constexpr int CS = L * K4 + 1;              // chunk stride (float4), padded
   constexpr int SG = SB / 8;                  // system groups of 8 per CTA
@@ -275,8 +290,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         xc[4] = u0;
         xc[5] = u1;
         if (act) {
-          X[(long long)M * ld + s] = u0;
-          X[(long long)(M + 1) * ld + s] = u1;
+          X[(long long)M * ld + s] = CN ? 2.0 * u0 - ft0 : u0;
+          X[(long long)(M + 1) * ld + s] = CN ? 2.0 * u1 - ft1 : u1;
         }
       }
       __syncthreads();
@@ -289,29 +304,40 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
       const D2 S0 = df::from_double(s0), S1 = df::from_double(s1);
       const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
       const D2 X0 = df::from_double(-xt0), X1 = df::from_double(-xt1);
+      constexpr int G = CN ? 8 : L;                    // rows per group (CN re-reads C)
 #pragma unroll
-      for (int j = 0; j < L; ++j) {
-        const float4 c3 = ctb[j * K4 + 3], c4 = ctb[j * K4 + 4];
-        D2 x = df::axpy(v[j], D2{c3.x, c3.y}, S0);
-        x = df::axpy(x, D2{c3.z, c3.w}, S1);
-        x = df::axpy(x, D2{c4.x, c4.y}, T0);
-        x = df::axpy(x, D2{c4.z, c4.w}, T1);
-        if (CYC) {
-          const float4 c1 = ctb[j * K4 + 1], c5 = ctb[j * K4 + 5];
-          x = df::axpy(x, D2{c1.z, c1.w}, X0);
-          x = df::axpy(x, D2{c5.x, c5.y}, X1);
+      for (int j0 = 0; j0 < L; j0 += G) {
+        double cold[CN ? G : 1];
+        if constexpr (CN) {
+#pragma unroll
+          for (int u = 0; u < G; ++u) cold[u] = (act && row0 + j0 + u < M) ? p[(j0 + u) * ld] : 0.0;
         }
-        if (act && row0 + j < M) __stcs(p + j * ld, df::to_double(x));
+#pragma unroll
+        for (int u = 0; u < G; ++u) {
+          const int j = j0 + u;
+          const float4 c3 = ctb[j * K4 + 3], c4 = ctb[j * K4 + 4];
+          D2 x = df::axpy(v[j], D2{c3.x, c3.y}, S0);
+          x = df::axpy(x, D2{c3.z, c3.w}, S1);
+          x = df::axpy(x, D2{c4.x, c4.y}, T0);
+          x = df::axpy(x, D2{c4.z, c4.w}, T1);
+          if (CYC) {
+            const float4 c1 = ctb[j * K4 + 1], c5 = ctb[j * K4 + 5];
+            x = df::axpy(x, D2{c1.z, c1.w}, X0);
+            x = df::axpy(x, D2{c5.x, c5.y}, X1);
+          }
+          if constexpr (CN) x = df::add(D2{2.f * x.h, 2.f * x.l}, df::neg(df::from_double(cold[u])));
+          if (act && row0 + j < M) __stcs(p + j * ld, df::to_double(x));
+        }
       }
     }
   }
 }
 
-template <int L, int SB, int MAXT, bool CYC, bool CH = false>
+template <int L, int SB, int MAXT, bool CYC, int RHS = kRhsPlain>
 cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st, double k2 = 0.0) {
   const int P = p.sp_P;
   const size_t smem = split_smem_bytes(L, P, SB, CYC);
-  auto kern = k_split_df<L, SB, MAXT, CYC, CH>;
+  auto kern = k_split_df<L, SB, MAXT, CYC, RHS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nblk = (batch + SB - 1) / SB;
@@ -344,9 +370,15 @@ cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStre
 }
 
 cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st) {
-  if (p.sp_L == 16) return launch<16, 8, 512, true, true>(p, X, batch, st, k2);
-  return p.sp_P <= 32 ? launch<32, 16, 512, true, true>(p, X, batch, st, k2)
-                      : launch<32, 8, 512, true, true>(p, X, batch, st, k2);
+  if (p.sp_L == 16) return launch<16, 8, 512, true, kRhsCH>(p, X, batch, st, k2);
+  return p.sp_P <= 32 ? launch<32, 16, 512, true, kRhsCH>(p, X, batch, st, k2)
+                      : launch<32, 8, 512, true, kRhsCH>(p, X, batch, st, k2);
+}
+
+cudaError_t cn_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+  if (p.sp_L == 16) return launch<16, 8, 512, true, kRhsCN>(p, X, batch, st);
+  return p.sp_P <= 32 ? launch<32, 16, 512, true, kRhsCN>(p, X, batch, st)
+                      : launch<32, 8, 512, true, kRhsCN>(p, X, batch, st);
 }
 
 }  // namespace pent

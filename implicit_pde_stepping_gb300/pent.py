@@ -54,6 +54,7 @@ def lib():
             L.pent_factor_solve_noalloc.restype = i
             L.hyperdiffusion_step.argtypes = [vp, vp, i, i, vp]
             L.ch_step.argtypes = [vp, vp, i, d, i, vp]
+            L.cn_step.argtypes = [vp, vp, i, i, vp]
             L.pent_set_variant.argtypes = [vp, i]
             L.pent_get_variant.argtypes = [vp, i]
             L.pent_destroy.argtypes = [vp]
@@ -64,7 +65,7 @@ def lib():
             L.pent_launch_count.argtypes = []
             L.pent_launch_count.restype = ctypes.c_ulonglong
             for fn in ("pent_factor", "pent_solve", "pent_factor_solve", "hyperdiffusion_step",
-                       "ch_step", "pent_set_variant", "pent_get_variant", "pent_sync"):
+                       "ch_step", "cn_step", "pent_set_variant", "pent_get_variant", "pent_sync"):
                 getattr(L, fn).restype = i
             _lib = L
     return _lib
@@ -217,6 +218,12 @@ def ch_step(plan: Plan, C, dt_over_dx2: float, nsteps: int, stream=None) -> None
     p = _ptr(C, plan.N, plan.dtype, "C")
     _check(lib().ch_step(plan.handle, p, int(C.shape[1]), float(dt_over_dx2), int(nsteps),
                          _stream(stream)), "ch_step")
+
+
+def cn_step(plan: Plan, C, nsteps: int, stream=None) -> None:
+    """nsteps of Crank–Nicolson: C <- A^{-1} (2I - A) C for the plan's cyclic A."""
+    p = _ptr(C, plan.N, plan.dtype, "C")
+    _check(lib().cn_step(plan.handle, p, int(C.shape[1]), int(nsteps), _stream(stream)), "cn_step")
 
 
 def pent_sync(stream=None) -> None:

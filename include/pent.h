@@ -165,6 +165,25 @@ pent_status hyperdiffusion_step(pent_plan plan, void* C_inout, int batch, int ns
 pent_status ch_step(pent_plan plan, void* C_inout, int batch, double dt_over_dx2, int nsteps,
                     void* stream);
 
+/*
+ * cn_step — nsteps of the Crank–Nicolson scheme for hyperdiffusion (eqs. (5)
+ * and (6) of "cuPentBatch – A batched pentadiagonal solver for NVIDIA GPUs"),
+ * periodic on N points:
+ *   (I + sigma_x D4) C^{n+1} = (I - sigma_x D4) C^n,  sigma_x = dt / (2 dx^4).
+ * The plan must be cyclic, PENT_F64, built from the bands of
+ * A = I + sigma_x D4 ([sigma_x, -4 sigma_x, 1 + 6 sigma_x, -4 sigma_x, sigma_x]).
+ * The explicit half is taken as 2I - A, so for any cyclic plan
+ * A = I + (dt/2) L the call performs C <- A^{-1} (2I - A) C, the
+ * Crank–Nicolson step of dC/dt = -L C.  Explicit half and solve run in one
+ * kernel per step (no extra pass over memory).
+ *   C_inout : DEVICE, interleaved [N][batch] doubles, 16-byte aligned.
+ *   nsteps  : >= 0.
+ * Errors: PENT_ERR_INVALID_ARG for a null or non-cyclic or fp32 plan, a null
+ * or misaligned C_inout, batch < 1 or nsteps < 0 (nothing queued);
+ * PENT_ERR_CUDA if a launch fails (steps already queued stay queued).
+ */
+pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* stream);
+
 /* Select the kernel variant of a plan (PENT_VARIANT_AUTO restores the default).
  * PENT_ERR_UNSUPPORTED if the variant does not exist for this plan. */
 pent_status pent_set_variant(pent_plan plan, pent_variant variant);

@@ -33,7 +33,7 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     for fn in ("pent_factor", "pent_solve", "pent_factor_solve", "hyperdiffusion_step", "ch_step",
-               "pent_destroy", "pent_status_string", "pent_sync"):
+               "cn_step", "pent_destroy", "pent_status_string", "pent_sync"):
         assert fn in names
 
 
@@ -62,6 +62,7 @@ def test_argument_errors_before_any_device_work(L):
     assert L.pent_solve(None, ctypes.c_void_p(256), 1, None) == pent.ERR_INVALID_ARG
     assert L.hyperdiffusion_step(None, ctypes.c_void_p(256), 1, 1, None) == pent.ERR_INVALID_ARG
     assert L.ch_step(None, ctypes.c_void_p(256), 1, 0.1, 1, None) == pent.ERR_INVALID_ARG
+    assert L.cn_step(None, ctypes.c_void_p(256), 1, 1, None) == pent.ERR_INVALID_ARG
     z = ctypes.c_void_p(0)
     assert L.pent_factor_solve(z, z, z, z, z, z, 8, 1, 0, z, 0, z, z) == pent.ERR_INVALID_ARG
     assert L.pent_set_variant(None, 0) == pent.ERR_INVALID_ARG
