@@ -48,6 +48,15 @@ WORKLOADS = {
     "cn": dict(N=512, batch=4096, kind="cn", sigma=0.25, cyclic=True, dtype="f64",
                desc="periodic Crank-Nicolson hyperdiffusion step, (I+0.25*D4)C'=(I-0.25*D4)C, "
                     "N=512, batch=4096, fp64"),
+    "cyclic100": dict(N=512, batch=4096, kind="hyper", sigma=0.5, cyclic=True, dtype="f64", nsub=100,
+                      desc="periodic hyperdiffusion, 100 steps per call (persistent multi-step kernel), "
+                           "cyclic I+0.5*D4, N=512, batch=4096, fp64"),
+    "cn100": dict(N=512, batch=4096, kind="cn", sigma=0.25, cyclic=True, dtype="f64", nsub=100,
+                  desc="periodic Crank-Nicolson hyperdiffusion, 100 steps per call (persistent "
+                       "multi-step kernel), sigma_x=0.25, N=512, batch=4096, fp64"),
+    "ch100": dict(N=1024, batch=16384, kind="ch", cyclic=True, dtype="f64", nsub=100,
+                  desc="semi-implicit Cahn-Hilliard, 100 steps per call (persistent multi-step "
+                       "kernel), N=1024, batch=16384, fp64, gamma=1e-4, dt=0.1dx^2"),
     "ch": dict(N=1024, batch=16384, kind="ch", cyclic=True, dtype="f64",
                desc="semi-implicit Cahn-Hilliard step (fused RHS + cyclic solve), N=1024, "
                     "batch=16384, fp64, gamma=1e-4, dt=0.1dx^2"),
@@ -248,16 +257,18 @@ def run_ours(args, W: dict, dist: Dist):
     scratch = torch.empty(2 * l2_bytes // 4, dtype=torch.int32, device="cuda") if flush else None
     torch.cuda.synchronize()
 
+    nsub = W.get("nsub", 1)     # time steps per call (one launch for all of them)
+
     def step(k, X=None):
         X = bufs[k % 2] if X is None else X
         if kind == "shared":
             pent.pent_solve(plan, X, stream=stream)
         elif kind == "hyper":
-            pent.hyperdiffusion_step(plan, X, 1, stream=stream)
+            pent.hyperdiffusion_step(plan, X, nsub, stream=stream)
         elif kind == "ch":
-            pent.ch_step(plan, X, k2, 1, stream=stream)
+            pent.ch_step(plan, X, k2, nsub, stream=stream)
         elif kind == "cn":
-            pent.cn_step(plan, X, 1, stream=stream)
+            pent.cn_step(plan, X, nsub, stream=stream)
         else:
             pent.pent_factor_solve(*bands, X, work=work, stream=stream)
 
@@ -290,7 +301,7 @@ def run_ours(args, W: dict, dist: Dist):
     ms_local = sum(step_ms) if flush else t_start.elapsed_time(t_end)
     ms = dist.max(ms_local)
     kernel_ms = statistics.mean(step_ms)
-    total_units = batch * args.steps * dist.world
+    total_units = batch * nsub * args.steps * dist.world
     value = total_units / (ms / 1e3)
 
     # ---- end to end through the public API: pinned host in, host out, every step
@@ -331,7 +342,7 @@ def run_ours(args, W: dict, dist: Dist):
         ems = dist.max(e0.elapsed_time(e1))
         nbytes_out = host_in.numel() * host_in.element_size()
         nbytes = nbytes_out + sum(b.numel() * b.element_size() for b in host_bands)
-        e2e = {"value": batch * ke * dist.world / (ems / 1e3), "unit": "system-solves/s"
+        e2e = {"value": batch * nsub * ke * dist.world / (ems / 1e3), "unit": "system-solves/s"
                if kind in ("shared", "persys") else "system-steps/s",
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes_out, "steps": ke,
                "ms_per_step": ems / ke}
@@ -359,6 +370,8 @@ def run_ours(args, W: dict, dist: Dist):
         ("shared", pent.VARIANT_SPLIT): split, ("hyper", pent.VARIANT_SPLIT): split,
     }
     kname, kfile = kernel_names.get((kind, variant), ("?", "?"))
+    if nsub > 1 and variant in (pent.VARIANT_SPLIT, pent.VARIANT_THREAD_DF):
+        kname, kfile = "k_steps_df", "pent_steps_df.cu"
     traffic = ncu_traffic(kname, kfile, args.workload, batch)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
@@ -367,6 +380,21 @@ def run_ours(args, W: dict, dist: Dist):
                 "kernel": kname, "kernel_ms": round(kernel_ms, 4),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "bytes_per_unit": per_unit, "units_per_launch": batch}
+    if nsub > 1:
+        # many steps per launch: memory is touched once per launch, the bound is arithmetic.
+        # Algorithmic fp64 flops per point and step (cyclic sweep 9 + bordering 4 FMA = 17;
+        # Crank-Nicolson +2 for 2y - C; Cahn-Hilliard +8 for the explicit right-hand side),
+        # against GB300's nominal fp64 rate (the kernel computes them in double-float on the
+        # FP32 pipe, so a fraction above 1 is possible)
+        fpp = {"hyper": 17, "cn": 19, "ch": 25}[kind]
+        flops = fpp * N * batch * nsub
+        roofline = {"bound": "alu", "achieved": round(flops / (kernel_ms / 1e3) / 1e9, 1),
+                    "peak": 1250.0, "unit": "GFLOP/s", "frac": round(flops / (kernel_ms / 1e3) / 1.25e12, 4),
+                    "traffic": traffic, "peak_source": "nominal GB300 fp64 1.25 TFLOP/s",
+                    "kernel": kname, "kernel_ms": round(kernel_ms, 4),
+                    "algorithmic_flops_per_launch": flops, "flops_per_point_step": fpp,
+                    "steps_per_launch": nsub, "units_per_launch": batch * nsub,
+                    "hbm_bytes_per_launch": alg_bytes}
 
     unit = "system-solves/s" if kind in ("shared", "persys") else "system-steps/s"
     res = {
@@ -376,7 +404,8 @@ def run_ours(args, W: dict, dist: Dist):
         "scaling": "weak", "vs_baseline": None, "dtype": W["dtype"],
         "data": "synthetic (seeded SplitMix64 counter-based generator)",
         "config": {"workload": W["desc"], "N": N, "batch_per_gpu": batch,
-                   "global_batch": batch * dist.world, "parallelism": f"replicas x{dist.world} "
+                   "global_batch": batch * dist.world, "time_steps_per_call": nsub,
+                   "parallelism": f"replicas x{dist.world} "
                    "(batch split, no collective)", "variant": variant,
                    "l2": (f"L2 flushed between timed steps ({2 * l2_bytes >> 20} MB write outside the "
                           "per-step events); time = sum of per-step events") if flush else

@@ -64,6 +64,16 @@ int env_int(const char* name, int dflt) {
   return std::atoi(v);
 }
 
+// Whether nsteps of scheme `kind` run in the persistent multi-step kernel:
+// two or more steps, the default or partitioned variant, a plan it supports;
+// PENT_STEPS=0 keeps one launch per step.
+bool use_steps(const pent_plan_s& p, int nsteps, int kind) {
+  if (nsteps < 2) return false;
+  if (p.variant != PENT_VARIANT_AUTO && p.variant != PENT_VARIANT_SPLIT) return false;
+  if (env_int("PENT_STEPS", 1) == 0) return false;
+  return steps_supported(p, kind);
+}
+
 }  // namespace
 }  // namespace pent
 
@@ -224,6 +234,16 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
           return from_cuda(e);
         }
       }
+      if (p->split_ok) {
+        double Td = 0.0;
+        e = cudaMemcpy(&Td, p->spextra + 18, sizeof(double), cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          pent_destroy(p);
+          return from_cuda(e);
+        }
+        p->sp_T = (int)Td;
+      }
     }
   }
   *out = p;
@@ -288,6 +308,9 @@ pent_status pent_factor_solve(const void* a, const void* b, const void* c, const
 pent_status hyperdiffusion_step(pent_plan p, void* C, int batch, int nsteps, void* stream) {
   if (!p || !C || batch < 1 || nsteps < 0) return PENT_ERR_INVALID_ARG;
   if (!p->cyclic || p->dtype != PENT_F64) return PENT_ERR_INVALID_ARG;
+  if (!aligned(C, 16)) return PENT_ERR_INVALID_ARG;
+  if (use_steps(*p, nsteps, 0))
+    return from_cuda(steps_df(*p, static_cast<double*>(C), batch, nsteps, 0, 0.0, as_stream(stream)));
   for (int n = 0; n < nsteps; ++n) {
     const pent_status s = pent_solve(p, C, batch, stream);
     if (s != PENT_OK) return s;
@@ -303,6 +326,9 @@ pent_status ch_step(pent_plan p, void* C, int batch, double dt_over_dx2, int nst
   const bool use_split = p->split_ok && p->N >= 8 &&
                          (p->variant == PENT_VARIANT_AUTO || p->variant == PENT_VARIANT_SPLIT ||
                           p->variant == PENT_VARIANT_THREAD_DF);
+  if (use_steps(*p, nsteps, 1))
+    return from_cuda(steps_df(*p, static_cast<double*>(C), batch, nsteps, 1, dt_over_dx2,
+                              as_stream(stream)));
   for (int n = 0; n < nsteps; ++n) {
     const cudaError_t e =
         use_split ? ch_split_df(*p, static_cast<double*>(C), batch, dt_over_dx2, as_stream(stream))
@@ -320,6 +346,8 @@ pent_status cn_step(pent_plan p, void* C, int batch, int nsteps, void* stream) {
   const bool use_split = p->split_ok && (p->variant == PENT_VARIANT_AUTO ||
                                          p->variant == PENT_VARIANT_SPLIT ||
                                          p->variant == PENT_VARIANT_THREAD_DF);
+  if (use_steps(*p, nsteps, 2))
+    return from_cuda(steps_df(*p, static_cast<double*>(C), batch, nsteps, 2, 0.0, as_stream(stream)));
   for (int n = 0; n < nsteps; ++n) {
     const cudaError_t e = use_split ? cn_split_df(*p, static_cast<double*>(C), batch, as_stream(stream))
                                     : cn_thread_f64(*p, static_cast<double*>(C), batch, as_stream(stream));

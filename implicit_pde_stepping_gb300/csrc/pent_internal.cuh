@@ -51,6 +51,7 @@ struct pent_plan_s {
   // partitioned double-float variant (pent_factor_split.cu / pent_split_df.cu)
   int split_ok = 0;          // tables valid
   int sp_L = 0, sp_P = 0;    // chunk length, chunks per system (Mpad = sp_L * sp_P)
+  int sp_T = 0;              // chunk couplings kept by the parallel scan (0: exact serial scan)
   float4* sptab = nullptr;   // [Mpad][kSpK]
   double* spchunk = nullptr; // [sp_P][kSpChunk]
   double* spextra = nullptr; // [kSpExtra]
@@ -142,5 +143,12 @@ cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStre
 size_t split_smem_bytes(int L, int P, int SB, int cyclic);
 cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);
 cudaError_t cn_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
+
+// pent_steps_df.cu: nsteps of a periodic scheme in one launch, state in registers.
+// kind 0 = hyperdiffusion, 1 = Cahn–Hilliard (k2 = dt/dx^2), 2 = Crank–Nicolson.
+constexpr size_t kStepsSmemMax = 227 * 1024;
+bool steps_supported(const pent_plan_s& p, int kind);
+cudaError_t steps_df(const pent_plan_s& p, double* X, int batch, int nsteps, int kind, double k2,
+                     cudaStream_t st);
 
 }  // namespace pent

@@ -341,7 +341,12 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st, 
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   const int nblk = (batch + SB - 1) / SB;
-  const int per_sm = (MAXT <= 256 && smem <= 110 * 1024) ? 2 : 1;
+  // persistent grid: as many CTAs as fit on every SM at once (registers and
+  // shared memory of this instance), capped by the number of system blocks
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, SB * P, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
   int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
   if (grid > nblk) grid = nblk;
   kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch, k2);
@@ -357,28 +362,31 @@ size_t split_smem_bytes(int L, int P, int SB, int cyclic) {
          ((size_t)P * kSpChunk + 4 * (size_t)SB * P * 2 + (size_t)SB * 8) * sizeof(double);
 }
 
+// Cyclic plans with L = 32 and P <= 32 run 16 systems per CTA (one copy of the
+// tables in shared memory serves more systems) unless the batch is too small
+// to give every SM one such CTA; then 8, for twice as many CTAs.
+template <int RHS>
+cudaError_t launch_cyclic(const pent_plan_s& p, double* X, int batch, cudaStream_t st, double k2) {
+  if (p.sp_L == 16) return launch<16, 8, 512, true, RHS>(p, X, batch, st, k2);
+  const bool wide = p.sp_P <= 32 && batch > 16 * p.num_sms;
+  return wide ? launch<32, 16, 512, true, RHS>(p, X, batch, st, k2)
+              : launch<32, 8, 512, true, RHS>(p, X, batch, st, k2);
+}
+
 cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   // p.sp_L and p.sp_P were fixed at plan time (P % 4 == 0, SB * P threads)
-  if (p.sp_L == 16) {
-    if (p.cyclic) return launch<16, 8, 512, true>(p, X, batch, st);
-    return launch<16, 8, 512, false>(p, X, batch, st);
-  }
-  if (p.cyclic) return p.sp_P <= 32 ? launch<32, 16, 512, true>(p, X, batch, st)
-                                    : launch<32, 8, 512, true>(p, X, batch, st);
+  if (p.cyclic) return launch_cyclic<kRhsPlain>(p, X, batch, st, 0.0);
+  if (p.sp_L == 16) return launch<16, 8, 512, false>(p, X, batch, st);
   return p.sp_P <= 32 ? launch<32, 8, 256, false>(p, X, batch, st)
                       : launch<32, 8, 512, false>(p, X, batch, st);
 }
 
 cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st) {
-  if (p.sp_L == 16) return launch<16, 8, 512, true, kRhsCH>(p, X, batch, st, k2);
-  return p.sp_P <= 32 ? launch<32, 16, 512, true, kRhsCH>(p, X, batch, st, k2)
-                      : launch<32, 8, 512, true, kRhsCH>(p, X, batch, st, k2);
+  return launch_cyclic<kRhsCH>(p, X, batch, st, k2);
 }
 
 cudaError_t cn_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
-  if (p.sp_L == 16) return launch<16, 8, 512, true, kRhsCN>(p, X, batch, st);
-  return p.sp_P <= 32 ? launch<32, 16, 512, true, kRhsCN>(p, X, batch, st)
-                      : launch<32, 8, 512, true, kRhsCN>(p, X, batch, st);
+  return launch_cyclic<kRhsCN>(p, X, batch, st, 0.0);
 }
 
 }  // namespace pent

@@ -1,0 +1,352 @@
+// Persistent multi-step kernel: nsteps of a periodic time scheme in one launch,
+// the state of every system held in registers from the first step to the last.
+//
+// Each step is the partitioned double-float cyclic solve of pent_split_df.cu
+// (forward and back substitution of "cuPentBatch – A batched pentadiagonal
+// solver for NVIDIA GPUs" per chunk of L rows, chunk boundary states by the
+// truncated parallel scan, Navon's bordering, eqs. (8)–(12), for the two
+// periodic rows), but the right-hand side of step n+1 is taken from the
+// registers that hold the result of step n, so a system touches memory twice
+// in the whole launch: one load of C^0, one store of C^nsteps.  Schemes:
+//   hyperdiffusion (eq. (4)):      A C^{n+1} = C^n;
+//   Cahn–Hilliard (eq. (2)):       A C^{n+1} = C^n + k2 D2[(C^n)^3 - C^n];
+//   Crank–Nicolson (eqs. (5)–(6)): A C^{n+1} = (2I - A) C^n, i.e.
+//                                  C^{n+1} = 2 A^{-1} C^n - C^n.
+// Between steps the state stays a double-float (hi, lo) pair, renormalised
+// after every step; it is rounded to fp64 once, at the final store.
+//
+// Cross-chunk data per step: the Cahn–Hilliard right-hand side of a chunk's
+// first and last rows needs C of the neighbouring rows, exchanged through
+// shared memory (first and last value of every chunk); the two periodic rows
+// M = N-2 and M+1 = N-1 are kept by the system's chunk-0 thread in shared
+// memory.  Crank–Nicolson keeps C^n of every row in shared memory for the
+// final 2y - C.
+//
+// Launched only when the plan's chunk couplings are truncated (T > 0); the
+// exact serial chunk scan stays with the one-step kernel.
+#include "df64.cuh"
+#include "pent_internal.cuh"
+
+namespace pent {
+namespace {
+
+using df::D2;
+
+constexpr int kStepHyper = 0;
+constexpr int kStepCH = 1;
+constexpr int kStepCN = 2;
+
+// y += A x for a row-major 2x2 A
+__device__ __forceinline__ void mv2(const double* A, double x0, double x1, double& y0, double& y1) {
+  y0 = fma(A[0], x0, fma(A[1], x1, y0));
+  y1 = fma(A[2], x0, fma(A[3], x1, y1));
+}
+
+// u = c^3 - c
+__device__ __forceinline__ D2 cubic_minus(D2 c) { return df::add(df::mul(df::mul(c, c), c), df::neg(c)); }
+
+// C_i + k2 (u_{i-1} - 2 u_i + u_{i+1})
+__device__ __forceinline__ D2 ch_rhs(D2 c, D2 um, D2 u0, D2 up, D2 k2) {
+  const D2 lap = df::add(df::add(um, up), D2{-2.f * u0.h, -2.f * u0.l});
+  return df::add(c, df::mul(k2, lap));
+}
+
+__device__ __forceinline__ D2 pick(bool p, D2 a, D2 b) { return D2{p ? a.h : b.h, p ? a.l : b.l}; }
+__device__ __forceinline__ float2 pack(D2 a) { return make_float2(a.h, a.l); }
+__device__ __forceinline__ D2 unpack(float2 a) { return D2{a.x, a.y}; }
+
+// Shared memory of one CTA (bytes), in the order the kernel carves it.
+__host__ __device__ inline size_t steps_smem(int L, int P, int SB, int rhs) {
+  size_t b = (size_t)P * (L * kSpK + 1) * sizeof(float4);        // row tables
+  b += ((size_t)P * kSpChunk + 2 * (size_t)SB * P * 2 + (size_t)SB * 8) * sizeof(double);
+  if (rhs == kStepCH) b += ((size_t)SB * P * 2 + SB) * sizeof(float2);   // halo, C_{M-1}
+  if (rhs == kStepCN) b += (size_t)L * SB * P * sizeof(float2);          // C^n of every row
+  return b;
+}
+
+template <int L, int SB, int MAXT, int RHS>
+__global__ void __launch_bounds__(MAXT, 1)
+    k_steps_df(const float4* __restrict__ growtab, const double* __restrict__ gchunk,
+               const double* __restrict__ gextra, double* __restrict__ X, int M, int P, int batch,
+               int nsteps, double k2d) {
+  constexpr bool CH = RHS == kStepCH;
+  constexpr bool CN = RHS == kStepCN;
+  constexpr int K4 = kSpK;
+  constexpr int CS = L * K4 + 1;              // chunk stride (float4), padded
+  constexpr int SG = SB / 8;                  // system groups of 8 per CTA
+  constexpr int LG = 8;                       // rows per load group
+  extern __shared__ float4 smem4[];
+  float4* rtab = smem4;                                              // [P][CS]
+  double* ctab = reinterpret_cast<double*>(rtab + (size_t)P * CS);   // [P][kSpChunk]
+  double* sE = ctab + (size_t)P * kSpChunk;      // [SB][P][2] local forward end values
+  double* sW = sE + (size_t)SB * P * 2;          // [SB][P][2] w_c
+  double* sX = sW + (size_t)SB * P * 2;          // [SB][8] y at 4 rows, x_t, tail state
+  float2* sH = reinterpret_cast<float2*>(sX + (size_t)SB * 8);   // CH: [SB][P][2] first, last C
+  float2* sA = sH + (CH ? (size_t)SB * P * 2 : 0);               // CH: [SB] C_{M-1}
+  float2* sC = sA + (CH ? (size_t)SB : 0);                       // CN: [L][SB * P] C^n
+
+  for (int t = threadIdx.x; t < P * L * K4; t += blockDim.x) {
+    const int row = t / K4, k = t % K4;
+    rtab[(row / L) * CS + (row % L) * K4 + k] = growtab[(size_t)row * kSpK + k];
+  }
+  for (int t = threadIdx.x; t < P * kSpChunk; t += blockDim.x) ctab[t] = gchunk[t];
+  __syncthreads();
+  const int T = (int)gextra[18];
+
+  const int tid = threadIdx.x, nthr = SB * P;
+  const int lane = tid & 31, w = tid >> 5;
+  const int sys = (w % SG) * 8 + (lane & 7);
+  const int c = (w / SG) * 4 + (lane >> 3);
+  const int row0 = c * L;
+  const float4* ctb = rtab + (size_t)c * CS;
+  const double* ct = ctab + (size_t)c * kSpChunk;
+  const long long ld = batch;
+  const int nblk = (batch + SB - 1) / SB;
+  const bool ownM2 = row0 <= M - 2 && M - 2 < row0 + L;
+  const bool ownM1 = row0 <= M - 1 && M - 1 < row0 + L;
+  double* xc = sX + (size_t)sys * 8;
+
+  for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
+    const int s = blk * SB + sys;
+    const bool act = s < batch;
+    double* p = X + (long long)row0 * ld + (act ? s : 0);
+
+    // ---- C^0: rows of this chunk into registers (padding rows 0), tail into shared memory
+    D2 v[L];
+#pragma unroll
+    for (int j0 = 0; j0 < L; j0 += LG) {
+      double fv[LG];
+#pragma unroll
+      for (int u = 0; u < LG; ++u) fv[u] = (act && row0 + j0 + u < M) ? p[(j0 + u) * ld] : 0.0;
+#pragma unroll
+      for (int u = 0; u < LG; ++u) v[j0 + u] = df::from_double(fv[u]);
+    }
+    if (c == 0) {
+      xc[6] = act ? X[(long long)M * ld + s] : 0.0;
+      xc[7] = act ? X[(long long)(M + 1) * ld + s] : 0.0;
+    }
+    __syncthreads();
+
+    for (int n = 0; n < nsteps; ++n) {
+      const D2 ct0 = df::from_double(xc[6]), ct1 = df::from_double(xc[7]);   // C at rows M, M+1
+      double ft0 = xc[6], ft1 = xc[7];   // right-hand side of the two periodic rows
+
+      // ---- 1. forward substitution with this step's right-hand side (zero incoming state)
+      {
+        D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+        if constexpr (CH) {
+          float2* hs = sH + ((size_t)sys * P + c) * 2;
+          hs[0] = pack(v[0]);
+          hs[1] = pack(v[L - 1]);
+          if (ownM1) {
+            D2 cm1 = v[0];
+#pragma unroll
+            for (int j = 0; j < L; ++j) cm1 = pick(row0 + j == M - 1, v[j], cm1);
+            sA[sys] = pack(cm1);
+          }
+          __syncthreads();                                  // halos published
+          const D2 k2 = df::from_double(k2d);
+          if (c == 0) {                                     // rows M, M+1 need C_{M-1}, C_0
+            const D2 cA = unpack(sA[sys]);
+            const D2 uA = cubic_minus(cA), uB = cubic_minus(ct0), uC = cubic_minus(ct1);
+            const D2 uD = cubic_minus(v[0]);
+            ft0 = df::to_double(ch_rhs(ct0, uA, uB, uC, k2));
+            ft1 = df::to_double(ch_rhs(ct1, uB, uC, uD, k2));
+          }
+          const D2 lh = c == 0 ? ct1 : unpack(sH[((size_t)sys * P + c - 1) * 2 + 1]);
+          D2 rh = c + 1 < P ? unpack(sH[((size_t)sys * P + c + 1) * 2]) : D2{0.f, 0.f};
+          rh = pick(row0 + L == M, ct0, rh);
+          D2 cc = v[0];
+          D2 um = cubic_minus(lh), u0 = cubic_minus(cc);
+#pragma unroll
+          for (int j = 0; j < L; ++j) {
+            D2 cn = (j + 1 < L) ? v[j + 1 < L ? j + 1 : j] : rh;
+            cn = pick(row0 + j + 1 == M, ct0, cn);          // row M is periodic state
+            const D2 up = cubic_minus(cn);
+            D2 f = ch_rhs(cc, um, u0, up, k2);
+            if (row0 + j >= M) f = D2{0.f, 0.f};
+            const float4 c0 = ctb[j * K4];
+            const float4 c1 = ctb[j * K4 + 1];
+            const D2 g = df::sum3p(D2{c0.x, c0.y}, f, D2{c0.z, c0.w}, a2, D2{c1.x, c1.y}, a1);
+            v[j] = g;
+            a2 = a1;
+            a1 = g;
+            um = u0;
+            u0 = up;
+            cc = cn;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < L; ++j) {
+            const D2 f = v[j];                              // padding rows hold 0
+            if constexpr (CN) sC[(size_t)j * nthr + tid] = pack(f);
+            const float4 c0 = ctb[j * K4];
+            const float4 c1 = ctb[j * K4 + 1];
+            const D2 g = df::sum3p(D2{c0.x, c0.y}, f, D2{c0.z, c0.w}, a2, D2{c1.x, c1.y}, a1);
+            v[j] = g;
+            a2 = a1;
+            a1 = g;
+          }
+        }
+      }
+      double* eo = sE + ((size_t)sys * P + c) * 2;
+      eo[0] = df::to_double(v[L - 2]);
+      eo[1] = df::to_double(v[L - 1]);
+      {
+        D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+#pragma unroll
+        for (int j = L - 1; j >= 0; --j) {
+          const float4 c2 = ctb[j * K4 + 2];
+          const D2 y = df::sum3(v[j], D2{c2.x, c2.y}, a1, D2{c2.z, c2.w}, a2);
+          v[j] = y;
+          a2 = a1;
+          a1 = y;
+        }
+      }
+      const double xs0 = df::to_double(v[0]), xs1 = df::to_double(v[1]);
+      double xm2 = 0.0, xm1 = 0.0;
+      if (ownM2 || ownM1) {
+        D2 a = v[0], b = v[0];
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+          a = pick(row0 + j == M - 2, v[j], a);
+          b = pick(row0 + j == M - 1, v[j], b);
+        }
+        xm2 = df::to_double(a);
+        xm1 = df::to_double(b);
+      }
+
+      // ---- 2. chunk boundary states s_c, t_c (truncated parallel scan), fp64
+      double s0 = 0.0, s1 = 0.0, t0 = 0.0, t1 = 0.0;
+      __syncthreads();                                      // e_c published
+      {
+        const double* E = sE + (size_t)sys * P * 2;
+        for (int k = 1; k <= T && k <= c; ++k) {
+          const double ea = E[2 * (c - k)], eb = E[2 * (c - k) + 1];
+          if (k == 1) { s0 += ea; s1 += eb; }
+          else mv2(ct + 12 + 4 * (k - 2), ea, eb, s0, s1);
+        }
+      }
+      double w0 = xs0, w1 = xs1;
+      mv2(ct + 4, s0, s1, w0, w1);
+      double* wo = sW + ((size_t)sys * P + c) * 2;
+      wo[0] = w0;
+      wo[1] = w1;
+      __syncthreads();                                      // w_c published
+      {
+        const double* Wv = sW + (size_t)sys * P * 2;
+        for (int k = 0; k < T && c + 1 + k < P; ++k) {
+          const double wa = Wv[2 * (c + 1 + k)], wb = Wv[2 * (c + 1 + k) + 1];
+          if (k == 0) { t0 += wa; t1 += wb; }
+          else mv2(ct + 24 + 4 * (k - 1), wa, wb, t0, t1);
+        }
+      }
+      if (c == 0) {
+        double y0 = w0, y1 = w1;
+        mv2(ct + 8, t0, t1, y0, y1);
+        xc[2] = y0;
+        xc[3] = y1;
+      }
+      if (ownM2) xc[0] = xm2 + gextra[10] * s0 + gextra[11] * s1 + gextra[14] * t0 + gextra[15] * t1;
+      if (ownM1) xc[1] = xm1 + gextra[12] * s0 + gextra[13] * s1 + gextra[16] * t0 + gextra[17] * t1;
+      __syncthreads();                                      // y at rows M-2, M-1, 0, 1 published
+      // periodic rows: x_t = S^{-1}(f_t - H^T y)   (eq. (12)); then the next tail state
+      if (c == 0) {
+        const double r0 = gextra[4] * xc[0] + gextra[5] * xc[1] + gextra[6] * xc[2];
+        const double r1 = gextra[7] * xc[1] + gextra[8] * xc[2] + gextra[9] * xc[3];
+        const double u0 = gextra[0] * (ft0 - r0) + gextra[1] * (ft1 - r1);
+        const double u1 = gextra[2] * (ft0 - r0) + gextra[3] * (ft1 - r1);
+        xc[4] = u0;
+        xc[5] = u1;
+        xc[6] = CN ? 2.0 * u0 - xc[6] : u0;
+        xc[7] = CN ? 2.0 * u1 - xc[7] : u1;
+      }
+      __syncthreads();                                      // x_t published
+      const double xt0 = xc[4], xt1 = xc[5];
+
+      // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 - u0 x_t0 - u1 x_t1: the next state
+      {
+        const D2 S0 = df::from_double(s0), S1 = df::from_double(s1);
+        const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
+        const D2 X0 = df::from_double(-xt0), X1 = df::from_double(-xt1);
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+          const float4 c1 = ctb[j * K4 + 1], c3 = ctb[j * K4 + 3];
+          const float4 c4 = ctb[j * K4 + 4], c5 = ctb[j * K4 + 5];
+          D2 x = df::axpy(v[j], D2{c3.x, c3.y}, S0);
+          x = df::axpy(x, D2{c3.z, c3.w}, S1);
+          x = df::axpy(x, D2{c4.x, c4.y}, T0);
+          x = df::axpy(x, D2{c4.z, c4.w}, T1);
+          x = df::axpy(x, D2{c1.z, c1.w}, X0);
+          x = df::axpy(x, D2{c5.x, c5.y}, X1);
+          if constexpr (CN) x = df::add(D2{2.f * x.h, 2.f * x.l}, df::neg(unpack(sC[(size_t)j * nthr + tid])));
+          if (row0 + j >= M) x = D2{0.f, 0.f};
+          // renormalise (h, l) so that |l| <= ulp(h)/2: carried unnormalised from
+          // step to step, the low word grows and its own rounding error with it
+          float sh, sl;
+          df::two_sum(x.h, x.l, sh, sl);
+          v[j] = D2{sh, sl};
+        }
+      }
+    }
+
+    // ---- C^nsteps back to memory
+#pragma unroll
+    for (int j = 0; j < L; ++j)
+      if (act && row0 + j < M) __stcs(p + j * ld, df::to_double(v[j]));
+    if (c == 0 && act) {
+      X[(long long)M * ld + s] = xc[6];
+      X[(long long)(M + 1) * ld + s] = xc[7];
+    }
+    __syncthreads();                                        // shared state reused by the next block
+  }
+}
+
+template <int L, int SB, int RHS>
+cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, double k2,
+                   cudaStream_t st) {
+  const int P = p.sp_P;
+  const size_t smem = steps_smem(L, P, SB, RHS);
+  auto kern = k_steps_df<L, SB, 512, RHS>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, SB * P, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int nblk = (batch + SB - 1) / SB;
+  int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
+  if (grid > nblk) grid = nblk;
+  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch, nsteps, k2);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// 16 systems per CTA when they fit (one copy of the tables serves more
+// systems) and the batch still gives every SM a CTA; else 8.
+template <int RHS>
+cudaError_t launch_kind(const pent_plan_s& p, double* X, int batch, int nsteps, double k2,
+                        cudaStream_t st) {
+  if (p.sp_L == 16) return launch<16, 8, RHS>(p, X, batch, nsteps, k2, st);
+  const bool wide = p.sp_P <= 32 && batch > 16 * p.num_sms &&
+                    steps_smem(32, p.sp_P, 16, RHS) <= kStepsSmemMax;
+  return wide ? launch<32, 16, RHS>(p, X, batch, nsteps, k2, st)
+              : launch<32, 8, RHS>(p, X, batch, nsteps, k2, st);
+}
+
+}  // namespace
+
+bool steps_supported(const pent_plan_s& p, int kind) {
+  if (!p.cyclic || !p.split_ok || p.sp_T <= 0 || p.sp_P > kSpMaxChunks) return false;
+  const int rhs = kind == 1 ? kStepCH : kind == 2 ? kStepCN : kStepHyper;
+  return steps_smem(p.sp_L, p.sp_P, 8, rhs) <= kStepsSmemMax && 8 * p.sp_P <= 512;
+}
+
+cudaError_t steps_df(const pent_plan_s& p, double* X, int batch, int nsteps, int kind, double k2,
+                     cudaStream_t st) {
+  if (kind == 1) return launch_kind<kStepCH>(p, X, batch, nsteps, k2, st);
+  if (kind == 2) return launch_kind<kStepCN>(p, X, batch, nsteps, 0.0, st);
+  return launch_kind<kStepHyper>(p, X, batch, nsteps, 0.0, st);
+}
+
+}  // namespace pent

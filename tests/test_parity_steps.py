@@ -1,0 +1,132 @@
+"""GPU parity: the persistent multi-step kernel (nsteps >= 2 of hyperdiffusion,
+Cahn–Hilliard and Crank–Nicolson in one launch, state kept in registers) against
+the oracle, against one launch per step, and its launch count."""
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from implicit_pde_stepping_gb300 import inputs, pent
+from tests.gpu_util import TOL_F64, dev, host, max_rel_err
+
+pytestmark = pytest.mark.gpu
+
+SIGMA = {"hyper": 0.7, "ch": 3.0, "cn": 0.7}
+K2 = 0.2
+
+
+def run(kind, N, batch, steps, C0, per_step=False):
+    sigma = SIGMA[kind]
+    plan = pent.pent_factor(inputs.hyper_bands(N, sigma), batch, cyclic=True)
+    C = dev(C0)
+    old = os.environ.get("PENT_STEPS")
+    if per_step:
+        os.environ["PENT_STEPS"] = "0"
+    try:
+        l0 = pent.launch_count()
+        if kind == "hyper":
+            pent.hyperdiffusion_step(plan, C, steps)
+        elif kind == "ch":
+            pent.ch_step(plan, C, K2, steps)
+        else:
+            pent.cn_step(plan, C, steps)
+        pent.pent_sync()
+        launches = pent.launch_count() - l0
+    finally:
+        if per_step:
+            if old is None:
+                del os.environ["PENT_STEPS"]
+            else:
+                os.environ["PENT_STEPS"] = old
+    out = host(C)
+    plan.close()
+    return out, launches
+
+
+def ref(kind, C0, steps):
+    if kind == "hyper":
+        return oracle.batch_hyperdiffusion(C0, SIGMA[kind], steps)
+    if kind == "ch":
+        return oracle.batch_ch(C0, SIGMA[kind], K2, steps)
+    return oracle.batch_cn(C0, SIGMA[kind], steps)
+
+
+def initial(kind, N, batch, seed):
+    if kind == "ch":
+        return inputs.ch_initial(N, batch, seed=seed)
+    return inputs.rhs_uniform(N, batch, seed=seed)
+
+
+@pytest.mark.parametrize("kind", ["hyper", "ch", "cn"])
+@pytest.mark.parametrize("N", [18, 64, 130, 333, 512, 1000, 1024, 2000])
+@pytest.mark.parametrize("batch", [1, 33, 100])
+def test_multistep_matches_oracle(kind, N, batch):
+    steps = 7
+    C0 = initial(kind, N, batch, seed=N + batch)
+    out, launches = run(kind, N, batch, steps, C0)
+    assert max_rel_err(out, ref(kind, C0, steps)) < TOL_F64
+    # one launch for all steps where the plan keeps truncated chunk couplings;
+    # otherwise (N = 2000: 64 chunks of 32 rows, beyond the partitioned cyclic
+    # kernel; sigma = 3 with 16-row chunks: couplings decay too slowly to
+    # truncate) one launch per step
+    assert launches in (1, steps)
+    if kind != "ch" and N <= 1024:
+        assert launches == 1
+    if N == 2000:
+        assert launches == steps
+
+
+@pytest.mark.parametrize("kind", ["hyper", "ch", "cn"])
+def test_multistep_equals_one_launch_per_step(kind):
+    N, batch, steps = 512, 300, 20
+    C0 = initial(kind, N, batch, seed=5)
+    a, la = run(kind, N, batch, steps, C0)
+    b, lb = run(kind, N, batch, steps, C0, per_step=True)
+    assert la == 1 and lb == steps
+    assert max_rel_err(a, b) < TOL_F64
+
+
+@pytest.mark.parametrize("kind", ["hyper", "ch", "cn"])
+def test_multistep_more_blocks_than_grid(kind):
+    """20000 systems: more blocks of systems than resident CTAs, so the
+    persistent grid loops; 256 sampled systems against the oracle."""
+    N, batch, steps = 512, 20000, 3
+    C0 = initial(kind, N, batch, seed=9)
+    out, launches = run(kind, N, batch, steps, C0)
+    idx = inputs.sample_systems(batch, 256)
+    assert max_rel_err(out[:, idx], ref(kind, C0[:, idx], steps)) < TOL_F64
+    assert launches == 1
+
+
+def test_multistep_hyperdiffusion_closed_form():
+    """Config-2 shape: N=512, sigma=0.5, batch 4096, 100 steps in one launch,
+    against the discrete amplification factor of every Fourier mode."""
+    N, batch, sigma, steps = 512, 4096, 0.5, 100
+    C0 = inputs.fourier_initial(N, batch)
+    plan = pent.pent_factor(inputs.hyper_bands(N, sigma), batch, cyclic=True)
+    C = dev(C0)
+    l0 = pent.launch_count()
+    pent.hyperdiffusion_step(plan, C, steps)
+    pent.pent_sync()
+    assert pent.launch_count() - l0 == 1
+    out = host(C)
+    a, b = inputs.fourier_modes(N, batch)
+    k = np.arange(1, 9)
+    G = (1.0 / (1.0 + 16.0 * sigma * np.sin(np.pi * k / N) ** 4)) ** steps
+    x = np.arange(N) / N
+    ph = 2 * np.pi * k[:, None] * x[None, :]
+    exact = np.cos(ph).T @ (a * G[:, None]) + np.sin(ph).T @ (b * G[:, None])
+    assert max_rel_err(out, exact) < 1e-10
+    plan.close()
+
+
+def test_serial_scan_plans_step_one_launch_at_a_time(monkeypatch):
+    """With the exact serial chunk scan (PENT_SPLIT_T=0) the multi-step kernel is
+    not used: one launch per step, same results."""
+    monkeypatch.setenv("PENT_SPLIT_T", "0")
+    N, batch, steps = 333, 40, 4
+    C0 = inputs.rhs_uniform(N, batch, seed=2)
+    out, launches = run("hyper", N, batch, steps, C0)
+    assert launches == steps
+    assert max_rel_err(out, ref("hyper", C0, steps)) < TOL_F64
