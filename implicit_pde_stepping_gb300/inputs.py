@@ -141,6 +141,28 @@ def persys_bands(N: int, batch: int, seed: int = 0, systems=None, dtype=np.float
     return offs["a"], offs["b"], c, offs["d"], offs["e"]
 
 
+def tri_bands(N: int, batch: int, seed: int = 0, systems=None, dtype=np.float32):
+    """Strictly diagonally dominant per-system tridiagonal bands (a, b, c), interleaved [N][nsys].
+
+    a (column i-1) and c (column i+1) i.i.d. uniform[-1, 1], zero where the
+    column is outside the matrix, rounded to ``dtype``; diagonal b = 1 + |a| + |c|
+    + uniform[0, 1], rounded to ``dtype``.  The same draws as the lower and upper
+    neighbours of ``persys_bands``, so the two generators share one recipe.
+    """
+    s = _systems(batch, systems)
+    rows = np.arange(N)
+    offs = []
+    for field, off in ((F_B, -1), (F_D, 1)):
+        v = uniform(seed, field, N, s, -1.0, 1.0)
+        col = rows + off
+        v[(col < 0) | (col >= N), :] = 0.0
+        offs.append(v.astype(dtype))
+    diag = 1.0 + uniform01(seed, F_DIAG, N, s)
+    for v in offs:
+        diag += np.abs(v.astype(np.float64))
+    return offs[0], diag.astype(dtype), offs[1]
+
+
 def ch_initial(N: int, batch: int, seed: int = 0, systems=None) -> np.ndarray:
     """Cahn–Hilliard initial data C^0 i.i.d. uniform[-0.1, 0.1], interleaved [N][nsys]."""
     return uniform(seed, F_C0, N, _systems(batch, systems), -0.1, 0.1)

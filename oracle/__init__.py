@@ -66,9 +66,12 @@ def _load():
             lib.oracle_batch_hyperdiffusion.argtypes = [i, i, d, i, dp]
             lib.oracle_batch_ch.argtypes = [i, i, d, d, i, dp]
             lib.oracle_batch_cn.argtypes = [i, i, d, i, dp]
+            lib.oracle_tri_solve.argtypes = [i, dp, dp, dp, dp, dp]
+            lib.oracle_batch_tri.argtypes = [i, i, dp, dp, dp, dp, dp]
             for fn in ("oracle_pent_factor", "oracle_pent_solve", "oracle_cyclic_solve",
                        "oracle_batch_shared", "oracle_batch_persys",
-                       "oracle_batch_hyperdiffusion", "oracle_batch_ch", "oracle_batch_cn"):
+                       "oracle_batch_hyperdiffusion", "oracle_batch_ch", "oracle_batch_cn",
+                       "oracle_tri_solve", "oracle_batch_tri"):
                 getattr(lib, fn).restype = i
             _lib = lib
     return _lib
@@ -167,4 +170,22 @@ def batch_cn(C_il, sigma_x: float, nsteps: int) -> np.ndarray:
     batch, N = X.shape
     _check(_load().oracle_batch_cn(N, batch, float(sigma_x), int(nsteps), _p(X)), "batch_cn")
     return np.ascontiguousarray(X.T)
+
+
+def tri_solve(a, b, c, y) -> np.ndarray:
+    """One tridiagonal system by the Thomas algorithm (fp64)."""
+    a, b, c, y = (np.ascontiguousarray(v, dtype=np.float64) for v in (a, b, c, y))
+    u = np.empty_like(y)
+    _check(_load().oracle_tri_solve(len(y), _p(a), _p(b), _p(c), _p(y), _p(u)), "tri_solve")
+    return u
+
+
+def batch_tri(A_il, B_il, C_il, Y_il) -> np.ndarray:
+    """Per-system tridiagonal batch; every array interleaved [N][batch] (widened to fp64)."""
+    A, B, C = (_rows(v) for v in (A_il, B_il, C_il))
+    Y = _rows(Y_il)
+    batch, N = Y.shape
+    U = np.empty_like(Y)
+    _check(_load().oracle_batch_tri(N, batch, _p(A), _p(B), _p(C), _p(Y), _p(U)), "batch_tri")
+    return np.ascontiguousarray(U.T)
 

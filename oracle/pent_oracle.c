@@ -15,6 +15,12 @@
  *   - periodic (cyclic) matrix (7c) solved by Navon's bordering, eqs. (8)–(12);
  *   - hyperdiffusion / Cahn–Hilliard semi-implicit stepping, eqs. (1)–(2), (4);
  *   - Crank–Nicolson hyperdiffusion, eqs. (5)–(6), sigma_x = dt / (2 dx^4).
+ * And, from "Simulating the behavior of the human brain on GPUs" (Valero-Lara
+ * et al.), section 4.1 "Tridiagonal linear systems":
+ *   - the Thomas algorithm: forward elimination of the lower diagonal
+ *     (c'_i, y'_i), then backward substitution u_i = y'_i - c'_i u_{i+1}.
+ *     Its tridiagonal rows: a_i below the diagonal (column i-1), b_i on it,
+ *     c_i above it (column i+1); a_0 and c_{N-1} do not exist.
  *
  * Conventions (0-based; the page is 1-based).  Row i of the matrix holds
  *   a[i] at column i-2, b[i] at i-1, c[i] at i, d[i] at i+1, e[i] at i+2.
@@ -272,6 +278,38 @@ int oracle_cn_steps(int N, double sigma_x, int nsteps, double* C) {
   return rc;
 }
 
+/*
+ * Thomas algorithm (section 4.1 of the tridiagonal page), one system:
+ *   c'_0 = c_0 / b_0,   c'_i = c_i / (b_i - c'_{i-1} a_i),
+ *   y'_0 = y_0 / b_0,   y'_i = (y_i - y'_{i-1} a_i) / (b_i - c'_{i-1} a_i),
+ *   u_{N-1} = y'_{N-1}, u_i = y'_i - c'_i u_{i+1}.
+ * a[0] and c[N-1] are ignored.  A zero denominator is a zero pivot.
+ */
+int oracle_tri_solve(int N, const double* a, const double* b, const double* c, const double* y,
+                     double* u) {
+  if (N < 1) return OR_EINVAL;
+  double* cp = (double*)malloc(sizeof(double) * 2 * (size_t)N);
+  if (!cp) return OR_ENOMEM;
+  double* yp = cp + N;
+  for (int i = 0; i < N; ++i) {
+    const double ai = i > 0 ? a[i] : 0.0;
+    const double ci = i + 1 < N ? c[i] : 0.0;
+    const double cprev = i > 0 ? cp[i - 1] : 0.0;
+    const double yprev = i > 0 ? yp[i - 1] : 0.0;
+    const double den = b[i] - cprev * ai;
+    if (den == 0.0 || !isfinite(den)) {
+      free(cp);
+      return OR_ZERO_PIVOT;
+    }
+    cp[i] = ci / den;
+    yp[i] = (y[i] - yprev * ai) / den;
+  }
+  u[N - 1] = yp[N - 1];
+  for (int i = N - 2; i >= 0; --i) u[i] = yp[i] - cp[i] * u[i + 1];
+  free(cp);
+  return OR_OK;
+}
+
 /* ---------------------------------------------------------------------------
  * Batched drivers.  X and F are [batch][N] (one system per row); X may alias F.
  * Each returns the first nonzero per-system code, or 0.
@@ -374,6 +412,23 @@ int oracle_batch_cn(int N, int batch, double sigma_x, int nsteps, double* C) {
 #pragma omp parallel for schedule(static)
   for (long s = 0; s < batch; ++s) {
     int r = oracle_cn_steps(N, sigma_x, nsteps, C + s * (size_t)N);
+    if (r != OR_OK) {
+#pragma omp critical
+      if (rc == OR_OK) rc = r;
+    }
+  }
+  return rc;
+}
+
+/* Per-system tridiagonal bands, each array [batch][N]. */
+int oracle_batch_tri(int N, int batch, const double* A, const double* B, const double* Cd,
+                     const double* Y, double* U) {
+  if (N < 1 || batch < 0) return OR_EINVAL;
+  int rc = OR_OK;
+#pragma omp parallel for schedule(static)
+  for (long s = 0; s < batch; ++s) {
+    size_t o = s * (size_t)N;
+    int r = oracle_tri_solve(N, A + o, B + o, Cd + o, Y + o, U + o);
     if (r != OR_OK) {
 #pragma omp critical
       if (rc == OR_OK) rc = r;

@@ -289,3 +289,69 @@ def test_cn_exact_solution_second_order():
     et = [err(64, s, semi_discrete=True) for s in (10, 20, 40)]
     t_orders = [np.log2(et[i] / et[i + 1]) for i in range(2)]
     assert all(abs(o - 2.0) < 0.1 for o in t_orders), (et, t_orders)
+
+
+# ---------------------------------------------------------------------------
+# Thomas algorithm (tridiagonal page, section 4.1)
+# ---------------------------------------------------------------------------
+def tri_dense(a, b, c):
+    N = len(b)
+    A = np.diag(b).astype(np.float64)
+    for i in range(1, N):
+        A[i, i - 1] = a[i]
+    for i in range(N - 1):
+        A[i, i + 1] = c[i]
+    return A
+
+
+@pytest.mark.parametrize("N", list(range(1, 17)) + [33, 200])
+@pytest.mark.parametrize("kind", ["dd", "spd"])
+def test_thomas_matches_lapack(N, kind):
+    """Against LAPACK's banded solver (scipy solve_banded) on diagonally dominant and
+    SPD (second-difference) tridiagonal matrices."""
+    rng = np.random.default_rng(N)
+    if kind == "dd":
+        a, c = rng.uniform(-1, 1, N), rng.uniform(-1, 1, N)
+        b = 1.0 + np.abs(a) + np.abs(c) + rng.uniform(0, 1, N)
+    else:
+        a = c = np.full(N, -1.0)
+        b = np.full(N, 2.0 + 1e-3)
+    y = rng.uniform(-1, 1, N)
+    ab = np.zeros((3, N))
+    ab[0, 1:] = c[:-1]
+    ab[1] = b
+    ab[2, :-1] = a[1:]
+    ref = scipy.linalg.solve_banded((1, 1), ab, y)
+    u = oracle.tri_solve(a, b, c, y)
+    assert rel(u, ref) < 1e-11
+    # a[0] and c[N-1] are outside the matrix and must be ignored
+    a2, c2 = a.copy(), c.copy()
+    a2[0], c2[-1] = 123.0, -77.0
+    assert np.array_equal(oracle.tri_solve(a2, b, c2, y), u)
+
+
+def test_thomas_dirichlet_eigenmodes():
+    """[-r, 1 + 2r, -r] with the ends truncated has eigenvectors sin(pi j k/(N+1)) and
+    eigenvalues 1 + 4 r sin^2(pi k / (2 (N+1))): each mode is divided by its eigenvalue."""
+    N, r = 100, 2.5
+    j = np.arange(1, N + 1)
+    a = c = np.full(N, -r)
+    b = np.full(N, 1 + 2 * r)
+    for k in (1, 7, 50, 100):
+        y = np.sin(np.pi * j * k / (N + 1))
+        lam = 1 + 4 * r * np.sin(np.pi * k / (2 * (N + 1))) ** 2
+        assert rel(oracle.tri_solve(a, b, c, y), y / lam) < 1e-12
+
+
+def test_thomas_manufactured_batch_and_zero_pivot():
+    N, batch = 77, 9
+    a, b, c = inputs.tri_bands(N, batch, seed=4, dtype=np.float64)
+    U = inputs.rhs_uniform(N, batch, seed=5)
+    Y = np.empty_like(U)
+    for s in range(batch):
+        Y[:, s] = tri_dense(a[:, s], b[:, s], c[:, s]) @ U[:, s]
+    assert rel(oracle.batch_tri(a, b, c, Y), U) < 1e-12
+    bz = b.copy()
+    bz[0, 3] = 0.0
+    with pytest.raises(oracle.OracleError):
+        oracle.batch_tri(a, bz, c, Y)

@@ -42,6 +42,11 @@ MUTATIONS = [
     ("CN stencil index", "double d4 = C[im2] - 4.0 * C[im1] + 6.0 * C[i] - 4.0 * C[ip1] + C[ip2];",
      "double d4 = C[im2] - 4.0 * C[im1] + 6.0 * C[i] - 4.0 * C[ip1] + C[ip1];"),
     ("CN wrap", "int im2 = (i + N - 2) % N,", "int im2 = (i + N - 1) % N,"),
+    ("Thomas denominator sign", "const double den = b[i] - cprev * ai;",
+     "const double den = b[i] + cprev * ai;"),
+    ("Thomas y' operand", "yp[i] = (y[i] - yprev * ai) / den;", "yp[i] = (y[i] - yprev * ci) / den;"),
+    ("Thomas back index", "for (int i = N - 2; i >= 0; --i) u[i] = yp[i] - cp[i] * u[i + 1];",
+     "for (int i = N - 2; i >= 0; --i) u[i] = yp[i] - cp[i + 1] * u[i + 1];"),
 ]
 
 
@@ -58,6 +63,9 @@ def _pins():
     T.test_ch_linearised_single_mode()
     T.test_cn_discrete_amplification()
     T.test_cn_conserves_mean_and_matches_one_step_by_hand()
+    for N in (2, 5, 33):
+        T.test_thomas_matches_lapack(N, "dd")
+    T.test_thomas_dirichlet_eigenmodes()
     T.test_manufactured_solution_persys(False)
     T.test_manufactured_solution_persys(True)
 
