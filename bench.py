@@ -43,6 +43,9 @@ WORKLOADS = {
                   desc="shared-matrix pentadiagonal solve, N=128, batch=1024, fp64, sigma=1"),
     "cyclic": dict(N=512, batch=4096, kind="hyper", sigma=0.5, cyclic=True, dtype="f64",
                    desc="periodic hyperdiffusion step, cyclic I+0.5*D4, N=512, batch=4096, fp64"),
+    "tri": dict(N=256, batch=262144, kind="tri", dtype="f32",
+                desc="per-system tridiagonal factor+solve (Thomas), N=256, batch=262144, fp32, "
+                     "diagonally dominant"),
     "persys": dict(N=256, batch=262144, kind="persys", dtype="f32",
                    desc="per-system factor+solve, N=256, batch=262144, fp32, diagonally dominant"),
     "cn": dict(N=512, batch=4096, kind="cn", sigma=0.25, cyclic=True, dtype="f64",
@@ -240,6 +243,12 @@ def run_ours(args, W: dict, dist: Dist):
         plan = pent.pent_factor(inputs.hyper_bands(N, sigma), batch, cyclic=True)
         bufs = [torch.from_numpy(inputs.ch_initial(N, batch, seed=seed + r)).to("cuda")
                 for r in range(2)]
+    elif kind == "tri":
+        bands = [torch.from_numpy(v).to("cuda") for v in inputs.tri_bands(N, batch, seed=seed)]
+        bufs = [torch.from_numpy(inputs.rhs_uniform(N, batch, seed=seed + r).astype(np.float32))
+                .to("cuda") for r in range(2)]
+        work = torch.empty(pent.tri_factor_solve_work_bytes(N, batch, pent.F32),
+                           dtype=torch.uint8, device="cuda")
     else:  # persys
         bands = [torch.from_numpy(v).to("cuda") for v in inputs.persys_bands(N, batch, seed=seed)]
         bufs = [torch.from_numpy(inputs.rhs_uniform(N, batch, seed=seed + r).astype(np.float32))
@@ -249,6 +258,9 @@ def run_ours(args, W: dict, dist: Dist):
     if plan is not None and args.variant != "auto":
         plan.set_variant(args.variant)
     variant = plan.variant(batch) if plan is not None else pent.VARIANT_THREAD
+    tri_variant = args.variant if args.variant in ("thread", "split") else "auto"
+    if kind == "tri":
+        variant = pent.VARIANT_THREAD if tri_variant == "thread" else pent.VARIANT_SPLIT
     # inputs smaller than twice the L2: write a buffer larger than L2 between timed
     # steps, outside the per-step events, and time the steps by those events
     l2_bytes = getattr(torch.cuda.get_device_properties(dev_index), "L2_cache_size", 0) or (129 << 20)
@@ -269,6 +281,8 @@ def run_ours(args, W: dict, dist: Dist):
             pent.ch_step(plan, X, k2, nsub, stream=stream)
         elif kind == "cn":
             pent.cn_step(plan, X, nsub, stream=stream)
+        elif kind == "tri":
+            pent.tri_factor_solve(*bands, X, variant=tri_variant, work=work, stream=stream)
         else:
             pent.pent_factor_solve(*bands, X, work=work, stream=stream)
 
@@ -312,8 +326,8 @@ def run_ours(args, W: dict, dist: Dist):
         host_in = bufs[0].cpu().pin_memory()
         host_out = torch.empty_like(host_in).pin_memory()
         Xd = torch.empty_like(bufs[0])
-        host_bands = [b.cpu().pin_memory() for b in bands] if kind == "persys" else []
-        dev_bands = [torch.empty_like(b) for b in bands] if kind == "persys" else []
+        host_bands = [b.cpu().pin_memory() for b in bands] if kind in ("persys", "tri") else []
+        dev_bands = [torch.empty_like(b) for b in bands] if kind in ("persys", "tri") else []
 
         def e2e_step():
             for hb, db in zip(host_bands, dev_bands):
@@ -321,6 +335,8 @@ def run_ours(args, W: dict, dist: Dist):
             Xd.copy_(host_in, non_blocking=True)
             if kind == "persys":
                 pent.pent_factor_solve(*dev_bands, Xd, work=work, stream=stream)
+            elif kind == "tri":
+                pent.tri_factor_solve(*dev_bands, Xd, variant=tri_variant, work=work, stream=stream)
             else:
                 step(0, Xd)
             host_out.copy_(Xd, non_blocking=True)
@@ -343,13 +359,13 @@ def run_ours(args, W: dict, dist: Dist):
         nbytes_out = host_in.numel() * host_in.element_size()
         nbytes = nbytes_out + sum(b.numel() * b.element_size() for b in host_bands)
         e2e = {"value": batch * nsub * ke * dist.world / (ems / 1e3), "unit": "system-solves/s"
-               if kind in ("shared", "persys") else "system-steps/s",
+               if kind in ("shared", "persys", "tri") else "system-steps/s",
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes_out, "steps": ke,
                "ms_per_step": ems / ke}
 
     # ---- roofline of the dominant kernel (one kernel per step on every path)
     per_unit = {"shared": 2 * N * elem, "hyper": 2 * N * elem, "ch": 2 * N * elem,
-                "cn": 2 * N * elem, "persys": 7 * N * elem}[kind]
+                "cn": 2 * N * elem, "persys": 7 * N * elem, "tri": 5 * N * elem}[kind]
     alg_bytes = per_unit * batch
     achieved = alg_bytes / (kernel_ms / 1e3) / 1e9
     peak, peak_kind = hbm_peak()
@@ -363,6 +379,8 @@ def run_ours(args, W: dict, dist: Dist):
         ("ch", pent.VARIANT_THREAD): ("k_ch_thread_f64", "pent_ch.cu"),
         ("cn", pent.VARIANT_THREAD): ("k_cn_thread_f64", "pent_ch.cu"),
         ("persys", pent.VARIANT_THREAD): ("k_persys_thread", "pent_persys.cu"),
+        ("tri", pent.VARIANT_THREAD): ("k_tri_thread", "pent_tri.cu"),
+        ("tri", pent.VARIANT_SPLIT): ("k_tri_split", "pent_tri.cu"),
         ("shared", pent.VARIANT_THREAD_DF): (twisted, "pent_twisted_df.cu"),
         ("hyper", pent.VARIANT_THREAD_DF): (twisted, "pent_twisted_df.cu"),
         ("ch", pent.VARIANT_THREAD_DF): split, ("ch", pent.VARIANT_SPLIT): split,
@@ -396,7 +414,7 @@ def run_ours(args, W: dict, dist: Dist):
                     "steps_per_launch": nsub, "units_per_launch": batch * nsub,
                     "hbm_bytes_per_launch": alg_bytes}
 
-    unit = "system-solves/s" if kind in ("shared", "persys") else "system-steps/s"
+    unit = "system-solves/s" if kind in ("shared", "persys", "tri") else "system-steps/s"
     res = {
         "metric": METRIC if args.workload == "shared" else f"{W['desc']} throughput",
         "value": value, "unit": unit, "n_gpus": dist.world, "steps": args.steps,
@@ -442,6 +460,11 @@ def run_cpu_baseline(W: dict, seconds: float):
         S = 512
         F = inputs.fourier_initial(N, S)
         fn = lambda: oracle.batch_cn(F, W["sigma"], 1)  # noqa: E731
+    elif kind == "tri":
+        S = 32768
+        a, b, c = inputs.tri_bands(N, S)
+        F = inputs.rhs_uniform(N, S).astype(np.float32)
+        fn = lambda: oracle.batch_tri(a, b, c, F)  # noqa: E731
     else:
         S = 8192
         a, b, c, d, e = inputs.persys_bands(N, S)
@@ -455,7 +478,7 @@ def run_cpu_baseline(W: dict, seconds: float):
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    unit = "system-solves/s" if kind in ("shared", "persys") else "system-steps/s"
+    unit = "system-solves/s" if kind in ("shared", "persys", "tri") else "system-steps/s"
     return {"value": S * reps / el, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{S} systems of the workload (N={N}) x {reps} repetitions, {el:.1f} s"}
 
@@ -465,7 +488,7 @@ def run_reference(args, W: dict, dist: Dist):
     import oracle
     from implicit_pde_stepping_gb300 import inputs
     N, kind = W["N"], W["kind"]
-    S = {"shared": 1024, "hyper": 256, "cn": 256, "ch": 64, "persys": 2048}[kind]
+    S = {"shared": 1024, "hyper": 256, "cn": 256, "ch": 64, "persys": 2048, "tri": 8192}[kind]
     if kind == "shared":
         bands = inputs.hyper_bands(N, W["sigma"])
         F = inputs.rhs_uniform(N, S, seed=0)
@@ -480,6 +503,11 @@ def run_reference(args, W: dict, dist: Dist):
     elif kind == "cn":
         F = inputs.fourier_initial(N, S)
         fn = lambda: oracle.batch_cn(F, W["sigma"], 1)  # noqa: E731
+    elif kind == "tri":
+        import numpy as np
+        a, b, c = inputs.tri_bands(N, S)
+        F = inputs.rhs_uniform(N, S).astype(np.float32)
+        fn = lambda: oracle.batch_tri(a, b, c, F)  # noqa: E731
     else:
         import numpy as np
         a, b, c, d, e = inputs.persys_bands(N, S)
@@ -491,7 +519,7 @@ def run_reference(args, W: dict, dist: Dist):
     for _ in range(args.steps):
         fn()
     el = time.perf_counter() - t0
-    unit = "system-solves/s" if kind in ("shared", "persys") else "system-steps/s"
+    unit = "system-solves/s" if kind in ("shared", "persys", "tri") else "system-steps/s"
     value = S * args.steps / el
     sample = f"{S} systems of the workload (N={N}) per step"
     return {
@@ -514,7 +542,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="shared")
-    ap.add_argument("--variant", default="auto", choices=["auto", "thread", "thread_df", "split"])
+    ap.add_argument("--variant", default="auto", choices=sorted(__import__("implicit_pde_stepping_gb300.pent", fromlist=["VARIANTS"]).VARIANTS))
     ap.add_argument("--batch", type=int, default=0, help="override the per-GPU batch")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -305,6 +305,36 @@ pent_status pent_factor_solve(const void* a, const void* b, const void* c, const
   return from_cuda(persys_thread(a, b, c, d, e, rhs, N, batch, dtype, work, info, as_stream(stream)));
 }
 
+size_t tri_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {
+  if (N < 1 || batch < 1 || (dtype != PENT_F64 && dtype != PENT_F32)) return 0;
+  return tri_work_bytes(N, batch, dtype);
+}
+
+pent_status tri_factor_solve(const void* a, const void* b, const void* c, void* rhs, int N, int batch,
+                             pent_dtype dtype, pent_variant variant, void* work, size_t work_bytes,
+                             int* info, void* stream) {
+  if (!a || !b || !c || !rhs || N < 1 || batch < 1) return PENT_ERR_INVALID_ARG;
+  if (dtype != PENT_F64 && dtype != PENT_F32) return PENT_ERR_INVALID_ARG;
+  const size_t elem = dtype == PENT_F64 ? sizeof(double) : sizeof(float);
+  const void* ptrs[4] = {a, b, c, rhs};
+  for (const void* q : ptrs)
+    if (!aligned(q, elem)) return PENT_ERR_INVALID_ARG;
+  const bool split_ok = dtype == PENT_F32 && tri_split_chunks(N) > 0;
+  bool split;
+  switch (variant) {
+    case PENT_VARIANT_AUTO: split = split_ok; break;
+    case PENT_VARIANT_THREAD: split = false; break;
+    case PENT_VARIANT_SPLIT:
+      if (!split_ok) return PENT_ERR_UNSUPPORTED;
+      split = true;
+      break;
+    default: return PENT_ERR_INVALID_ARG;
+  }
+  if (!split && (!work || work_bytes < tri_work_bytes(N, batch, dtype) || !aligned(work, 256)))
+    return PENT_ERR_INVALID_ARG;
+  return from_cuda(tri_solve_batch(a, b, c, rhs, N, batch, dtype, split, work, info, as_stream(stream)));
+}
+
 pent_status hyperdiffusion_step(pent_plan p, void* C, int batch, int nsteps, void* stream) {
   if (!p || !C || batch < 1 || nsteps < 0) return PENT_ERR_INVALID_ARG;
   if (!p->cyclic || p->dtype != PENT_F64) return PENT_ERR_INVALID_ARG;

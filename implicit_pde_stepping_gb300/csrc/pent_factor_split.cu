@@ -19,14 +19,21 @@
 namespace pent {
 namespace {
 
+constexpr int kFactorThreads = 256;
+
+// One CTA.  The LR recurrences and the bordering sweeps are serial (thread 0,
+// or threads 0 and 1); the chunk responses, the row packing and the chunk
+// couplings run one thread per chunk or per row.
 // work (doubles): al be ga de ep (5 Mpad), g0 g1 h0 h1 (4 Mpad), u0 u1 (2 Mpad),
 // H1 H2 M1 M2 K1 K2 (6 Mpad)
-__global__ void k_factor_split(const double* __restrict__ bands, int N, int cyclic, int L, int Mpad,
-                               float4* __restrict__ rowtab, double* __restrict__ chunktab,
-                               double* __restrict__ extra, double* __restrict__ w,
-                               int* __restrict__ status) {
-  if (blockIdx.x != 0 || threadIdx.x != 0) return;
-  *status = 0;
+__global__ void __launch_bounds__(kFactorThreads)
+    k_factor_split(const double* __restrict__ bands, int N, int cyclic, int L, int Mpad,
+                   float4* __restrict__ rowtab, double* __restrict__ chunktab,
+                   double* __restrict__ extra, double* __restrict__ w, int* __restrict__ status) {
+  __shared__ int s_fail;
+  __shared__ double s_B[2][2];
+  __shared__ double s_tail[2][kSpMaxChunks][kSpTmax + 1];
+  const int tid = threadIdx.x, nt = blockDim.x;
   const int M = cyclic ? N - 2 : N;
   const int P = Mpad / L;
   double *al = w, *be = w + Mpad, *ga = w + 2 * Mpad, *de = w + 3 * Mpad, *ep = w + 4 * Mpad;
@@ -34,8 +41,13 @@ __global__ void k_factor_split(const double* __restrict__ bands, int N, int cycl
   double *u0 = w + 9 * Mpad, *u1 = w + 10 * Mpad;
   double *H1 = w + 11 * Mpad, *H2 = w + 12 * Mpad, *M1 = w + 13 * Mpad, *M2 = w + 14 * Mpad;
   double *K1 = w + 15 * Mpad, *K2 = w + 16 * Mpad;
-  if (!lr::factor_rows(bands, N, M, M, false, al, be, ga, de, ep)) {
-    *status = 1;
+  if (tid == 0) {
+    *status = 0;
+    s_fail = lr::factor_rows(bands, N, M, M, false, al, be, ga, de, ep) ? 0 : 1;
+  }
+  __syncthreads();
+  if (s_fail) {
+    if (tid == 0) *status = 1;
     return;
   }
   // recurrence coefficients, padding rows decoupled (g = r f, y = g)
@@ -44,9 +56,9 @@ __global__ void k_factor_split(const double* __restrict__ bands, int N, int cycl
   auto Q_ = [&](int i) { return i < M ? -be[i] / al[i] : 0.0; };
   auto C_ = [&](int i) { return i < M ? -ga[i] : 0.0; };
   auto D_ = [&](int i) { return i < M ? -de[i] : 0.0; };
-  for (int i = 0; i < Mpad; ++i) u0[i] = u1[i] = 0.0;
+  for (int i = tid; i < Mpad; i += nt) u0[i] = u1[i] = 0.0;
 
-  for (int c = 0; c < P; ++c) {
+  for (int c = tid; c < P; c += nt) {
     const int a = c * L, b = a + L;
     // forward responses to the incoming state (1,0) and (0,1)
     for (int k = 0; k < 2; ++k) {
@@ -79,13 +91,20 @@ __global__ void k_factor_split(const double* __restrict__ bands, int N, int cycl
     ct[4] = M1[a]; ct[5] = M2[a]; ct[6] = M1[a + 1]; ct[7] = M2[a + 1];
     ct[8] = K1[a]; ct[9] = K2[a]; ct[10] = K1[a + 1]; ct[11] = K2[a + 1];
   }
-  for (int k = 0; k < kSpExtra; ++k) extra[k] = 0.0;
+  __syncthreads();
+  if (tid == 0)
+    for (int k = 0; k < kSpExtra; ++k) extra[k] = 0.0;
 
   if (cyclic) {
-    double Bm[2][2];
-    lr::border(bands, N, g0, g1, h0, h1, Bm);
-    // u_k = E^{-1} G_k (eq. (11))
-    for (int k = 0; k < 2; ++k) {
+    if (tid == 0) {
+      double Bm[2][2];
+      lr::border(bands, N, g0, g1, h0, h1, Bm);
+      s_B[0][0] = Bm[0][0]; s_B[0][1] = Bm[0][1]; s_B[1][0] = Bm[1][0]; s_B[1][1] = Bm[1][1];
+    }
+    __syncthreads();
+    // u_k = E^{-1} G_k (eq. (11)), one thread per column
+    if (tid < 2) {
+      const int k = tid;
       const double* gc = k ? g1 : g0;
       double* u = k ? u1 : u0;
       double y1 = 0.0, y2 = 0.0;
@@ -101,26 +120,34 @@ __global__ void k_factor_split(const double* __restrict__ bands, int N, int cycl
         x2 = x1; x1 = x;
       }
     }
-    // S = B - H^T E^{-1} G (eq. (12))
-    double S00 = Bm[0][0], S01 = Bm[0][1], S10 = Bm[1][0], S11 = Bm[1][1];
-    for (int i = 0; i < M; ++i) {
-      S00 -= h0[i] * u0[i]; S01 -= h0[i] * u1[i];
-      S10 -= h1[i] * u0[i]; S11 -= h1[i] * u1[i];
+    __syncthreads();
+    if (tid == 0) {
+      // S = B - H^T E^{-1} G (eq. (12))
+      double S00 = s_B[0][0], S01 = s_B[0][1], S10 = s_B[1][0], S11 = s_B[1][1];
+      for (int i = 0; i < M; ++i) {
+        S00 -= h0[i] * u0[i]; S01 -= h0[i] * u1[i];
+        S10 -= h1[i] * u0[i]; S11 -= h1[i] * u1[i];
+      }
+      const double det = S00 * S11 - S01 * S10;
+      if (!(det != 0.0) || !isfinite(det)) {
+        s_fail = 3;
+      } else {
+        extra[0] = S11 / det; extra[1] = -S01 / det; extra[2] = -S10 / det; extra[3] = S00 / det;
+        // H^T y needs y at rows 0, 1, M-2, M-1 only (N >= 6 keeps them distinct)
+        extra[4] = h0[M - 2]; extra[5] = h0[M - 1]; extra[6] = h0[0];
+        extra[7] = h1[M - 1]; extra[8] = h1[0]; extra[9] = h1[1];
+        extra[10] = M1[M - 2]; extra[11] = M2[M - 2]; extra[12] = M1[M - 1]; extra[13] = M2[M - 1];
+        extra[14] = K1[M - 2]; extra[15] = K2[M - 2]; extra[16] = K1[M - 1]; extra[17] = K2[M - 1];
+      }
     }
-    const double det = S00 * S11 - S01 * S10;
-    if (!(det != 0.0) || !isfinite(det)) {
-      *status = 3;
+    __syncthreads();
+    if (s_fail) {
+      if (tid == 0) *status = s_fail;
       return;
     }
-    extra[0] = S11 / det; extra[1] = -S01 / det; extra[2] = -S10 / det; extra[3] = S00 / det;
-    // H^T y needs y at rows 0, 1, M-2, M-1 only (N >= 6 keeps them distinct)
-    extra[4] = h0[M - 2]; extra[5] = h0[M - 1]; extra[6] = h0[0];
-    extra[7] = h1[M - 1]; extra[8] = h1[0]; extra[9] = h1[1];
-    extra[10] = M1[M - 2]; extra[11] = M2[M - 2]; extra[12] = M1[M - 1]; extra[13] = M2[M - 1];
-    extra[14] = K1[M - 2]; extra[15] = K2[M - 2]; extra[16] = K1[M - 1]; extra[17] = K2[M - 1];
   }
 
-  for (int i = 0; i < Mpad; ++i) {
+  for (int i = tid; i < Mpad; i += nt) {
     const float2 r = lr::split(R_(i)), p = lr::split(P_(i)), q = lr::split(Q_(i));
     const float2 cc = lr::split(C_(i)), d = lr::split(D_(i));
     const float2 m1 = lr::split(M1[i]), m2 = lr::split(M2[i]);
@@ -147,10 +174,8 @@ __global__ void k_factor_split(const double* __restrict__ bands, int N, int cycl
   };
   auto nrm = [](const double* A) { return fmax(fabs(A[0]) + fabs(A[1]), fabs(A[2]) + fabs(A[3])); };
   const double tiny = ldexp(1.0, -64);
-  double tailA[kSpTmax + 1], tailB[kSpTmax + 1];
-  for (int t = 0; t <= kSpTmax; ++t) tailA[t] = tailB[t] = 0.0;
   double nA[kSpMaxChunks + 1], nB[kSpMaxChunks + 1];
-  for (int c = 0; c < P; ++c) {
+  for (int c = tid; c < P; c += nt) {
     double* ct = chunktab + (size_t)c * kSpChunk;
     for (int k = 12; k < kSpChunk; ++k) ct[k] = 0.0;
     // forward: A_{c,k} = Phi_{c-1}..Phi_{c-k+1}, k = 2..c (A_{c,1} = I)
@@ -174,14 +199,23 @@ __global__ void k_factor_split(const double* __restrict__ bands, int N, int cycl
       double sa = 0.0, sb = 0.0;
       for (int k = t + 1; k <= c; ++k) sa += nA[k];
       for (int k = t; k <= P - 2 - c; ++k) sb += nB[k];
-      tailA[t] = fmax(tailA[t], sa);
-      tailB[t] = fmax(tailB[t], sb);
+      s_tail[0][c][t] = sa;
+      s_tail[1][c][t] = sb;
     }
   }
-  int T = 0;
-  for (int t = 1; t <= kSpTmax && T == 0; ++t)
-    if (tailA[t] <= tiny && tailB[t] <= tiny) T = t;
-  extra[18] = (double)T;
+  __syncthreads();
+  if (tid == 0) {
+    int T = 0;
+    for (int t = 1; t <= kSpTmax && T == 0; ++t) {
+      double ta = 0.0, tb = 0.0;
+      for (int c = 0; c < P; ++c) {
+        ta = fmax(ta, s_tail[0][c][t]);
+        tb = fmax(tb, s_tail[1][c][t]);
+      }
+      if (ta <= tiny && tb <= tiny) T = t;
+    }
+    extra[18] = (double)T;
+  }
 }
 
 }  // namespace
@@ -189,8 +223,8 @@ __global__ void k_factor_split(const double* __restrict__ bands, int N, int cycl
 cudaError_t factor_split(const double* d_bands, int N, int cyclic, int L, int Mpad, float4* rowtab,
                          double* chunktab, double* extra, double* d_work, int* d_status,
                          cudaStream_t st) {
-  k_factor_split<<<1, 1, 0, st>>>(d_bands, N, cyclic, L, Mpad, rowtab, chunktab, extra, d_work,
-                                  d_status);
+  k_factor_split<<<1, kFactorThreads, 0, st>>>(d_bands, N, cyclic, L, Mpad, rowtab, chunktab, extra,
+                                               d_work, d_status);
   note_launch();
   return cudaGetLastError();
 }

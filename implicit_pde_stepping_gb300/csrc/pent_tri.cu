@@ -1,0 +1,318 @@
+// Batched tridiagonal solves with per-system matrices.
+//
+// "Simulating the behavior of the human brain on GPUs" (Valero-Lara et al.),
+// section 4.1 "Tridiagonal linear systems" and 4.1.1 (cuThomasBatch): the
+// Thomas algorithm, one system per thread, systems interleaved in memory so
+// that a warp's loads of one row are contiguous.  Rows: a_i below the
+// diagonal (column i-1), b_i on it, c_i above it (column i+1).
+//
+// Two kernels:
+//   k_tri_thread<T>  the page's mapping: forward elimination writes c'_i to a
+//                    scratch array and y'_i over the right-hand side, the
+//                    backward substitution reads both back.  Any N, fp32/fp64.
+//   k_tri_split      fp32, N <= 512: each system is cut into P = 2^k chunks of
+//                    L = 8 (N <= 256) or 16 rows, one thread per chunk, and never leaves
+//                    registers, so memory sees the minimum (a, b, c, y read
+//                    once, u written once).  Per chunk [s, e] a downward and an
+//                    upward elimination give
+//                        x_i = y''_i - l_i x_{s-1} - r_i x_{e+1},
+//                    eliminating x_{s+1} ... leaves one equation per chunk in
+//                    the chunk-end unknowns t_c = x_{e_c}:
+//                        l_e t_{c-1} + (1 - r_e l_s') t_c - r_e r_s' t_{c+1}
+//                            = y''_e - r_e y''_s'
+//                    (primes: the next chunk's first row), a P-unknown
+//                    tridiagonal system solved by parallel cyclic reduction
+//                    across P lanes with warp shuffles.  Then every row follows
+//                    from t_{c-1} and x_{s_{c+1}}.
+//   The partition trades the page's 8n operations for about twice as many,
+//   which fp32 affords: the kernel is bound by memory, not arithmetic.
+#include "pent_internal.cuh"
+
+namespace pent {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kUnroll = 4;
+
+template <typename T>
+__device__ __forceinline__ bool bad_pivot(T d) {
+  return !(d != T(0)) || !isfinite(d);
+}
+
+// 1/x: the fast hardware reciprocal in fp32 (about 1 ulp, well inside the fp32
+// tolerance of the solve); IEEE division in fp64
+__device__ __forceinline__ float recip(float x) { return __fdividef(1.f, x); }
+__device__ __forceinline__ double recip(double x) { return 1.0 / x; }
+
+// ---------------------------------------------------------------------------
+// one thread per system (cuThomasBatch mapping)
+// ---------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+    k_tri_thread(const T* __restrict__ A, const T* __restrict__ B, const T* __restrict__ C,
+                 T* __restrict__ X, T* __restrict__ Wc, int N, int batch, int* __restrict__ info) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= batch) return;
+  const size_t ld = (size_t)batch;
+  T cp = T(0), yp = T(0);
+  int bad = 0;
+  for (int i0 = 0; i0 < N; i0 += kUnroll) {
+    T a[kUnroll], b[kUnroll], c[kUnroll], y[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u;
+      const size_t o = (size_t)i * ld + s;
+      const bool in = i < N;
+      a[u] = (in && i >= 1) ? A[o] : T(0);
+      b[u] = in ? B[o] : T(1);
+      c[u] = (in && i + 1 < N) ? C[o] : T(0);
+      y[u] = in ? X[o] : T(0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u;
+      if (i < N) {
+        const size_t o = (size_t)i * ld + s;
+        const T den = b[u] - cp * a[u];
+        if (bad == 0 && bad_pivot(den)) bad = i + 1;
+        const T rd = recip(den);
+        cp = c[u] * rd;
+        yp = (y[u] - yp * a[u]) * rd;
+        Wc[o] = cp;
+        X[o] = yp;
+      }
+    }
+  }
+  T x1 = T(0);
+  for (int i0 = N - 1; i0 >= 0; i0 -= kUnroll) {
+    T yv[kUnroll], cv[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 - u;
+      const size_t o = (size_t)(i >= 0 ? i : 0) * ld + s;
+      yv[u] = (i >= 0) ? X[o] : T(0);
+      cv[u] = (i >= 0) ? Wc[o] : T(0);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 - u;
+      if (i >= 0) {
+        const T x = yv[u] - cv[u] * x1;
+        X[(size_t)i * ld + s] = x;
+        x1 = x;
+      }
+    }
+  }
+  if (info) info[s] = bad;
+}
+
+// ---------------------------------------------------------------------------
+// partitioned fp32 kernel: 16 systems x P chunks of L rows per CTA (2 CTAs/SM for L = 8,
+// so that one CTA's loads overlap the other's arithmetic and barriers)
+// ---------------------------------------------------------------------------
+constexpr int kTriSB = 16;    // systems per CTA
+
+// 4-byte asynchronous global -> shared copy (all of a thread's rows are put in
+// flight at once, without holding registers)
+__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_commit_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+template <int L, int P>
+__global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
+    k_tri_split(const float* __restrict__ A, const float* __restrict__ B, const float* __restrict__ C,
+                float* __restrict__ X, int N, int batch, int* __restrict__ info) {
+  constexpr int SB = kTriSB;
+  // Per chunk: first row (l', r, y''), last row (l', r, y''); t_c = x at the last row.
+  // Stored [quantity][chunk][system] with rows of SB + 1 so that both thread
+  // mappings (threads over systems; threads over chunks) spread over the banks.
+  __shared__ float sB[6][P][SB + 1];
+  __shared__ float sT[P][SB + 1];
+  __shared__ int sBad[SB];
+  constexpr int NT = SB * P;
+  extern __shared__ float stage[];           // [4][L][NT]: a, b, c, y of every row
+  const int tid = threadIdx.x;
+  const int lane = threadIdx.x % SB;         // phases 1, 3: system of this thread
+  const int c = threadIdx.x / SB;            //              its chunk
+  const int s = blockIdx.x * SB + lane;
+  const bool act = s < batch;
+  const size_t ld = (size_t)batch;
+  const int row0 = c * L;
+  if (threadIdx.x < SB) sBad[threadIdx.x] = 0;
+
+  // ---- 0. every row of this chunk in flight at once (cp.async into shared memory)
+#pragma unroll
+  for (int j = 0; j < L; ++j) {
+    const int i = row0 + j;
+    if (act && i < N) {
+      const size_t o = (size_t)i * ld + s;
+      cp_async4(&stage[(0 * L + j) * NT + tid], A + o);
+      cp_async4(&stage[(1 * L + j) * NT + tid], B + o);
+      cp_async4(&stage[(2 * L + j) * NT + tid], C + o);
+      cp_async4(&stage[(3 * L + j) * NT + tid], X + o);
+    }
+  }
+  cp_commit_wait_all();
+
+  // ---- 1. downward elimination: x_i + c'_i x_{i+1} + l_i x_{s-1} = y'_i
+  float cp[L], lv[L], yv[L];
+  int bad = 0;
+  {
+    float cprev = 0.f, lprev = 0.f, yprev = 0.f;
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+      const int i = row0 + j;
+      const bool in = act && i < N;
+      const float a = (in && i >= 1) ? stage[(0 * L + j) * NT + tid] : 0.f;
+      const float b = in ? stage[(1 * L + j) * NT + tid] : 1.f;
+      const float cc = (in && i + 1 < N) ? stage[(2 * L + j) * NT + tid] : 0.f;
+      const float y = in ? stage[(3 * L + j) * NT + tid] : 0.f;
+      const float den = (j == 0) ? b : fmaf(-a, cprev, b);
+      if (bad == 0 && bad_pivot(den)) bad = i + 1;
+      const float rd = recip(den);
+      cp[j] = cc * rd;
+      lv[j] = (j == 0) ? a * rd : -a * lprev * rd;
+      yv[j] = (j == 0) ? y * rd : fmaf(-a, yprev, y) * rd;
+      cprev = cp[j];
+      lprev = lv[j];
+      yprev = yv[j];
+    }
+  }
+  // ---- upward elimination: x_i = y''_i - l'_i x_{s-1} - r_i x_{e+1}
+  //      (in place: yv <- y'', lv <- l', cp <- r)
+#pragma unroll
+  for (int j = L - 2; j >= 0; --j) {
+    const float cj = cp[j];
+    yv[j] = fmaf(-cj, yv[j + 1], yv[j]);
+    lv[j] = fmaf(-cj, lv[j + 1], lv[j]);
+    cp[j] = -cj * cp[j + 1];
+  }
+  sB[0][c][lane] = lv[0];
+  sB[1][c][lane] = cp[0];
+  sB[2][c][lane] = yv[0];
+  sB[3][c][lane] = lv[L - 1];
+  sB[4][c][lane] = cp[L - 1];
+  sB[5][c][lane] = yv[L - 1];
+  __syncthreads();
+  if (bad) atomicCAS(&sBad[lane], 0, bad);
+
+  // ---- 2. chunk-end unknowns: P-row tridiagonal system per system, PCR over P lanes
+  {
+    const int q = threadIdx.x / P;           // system of this lane group (P lanes of a warp)
+    const int k = threadIdx.x % P;           // its chunk
+    const float le = sB[3][k][q], re = sB[4][k][q], ye = sB[5][k][q];
+    const bool last = k == P - 1;
+    const float ln = last ? 0.f : sB[0][k + 1][q];
+    const float rn = last ? 0.f : sB[1][k + 1][q];
+    const float yn = last ? 0.f : sB[2][k + 1][q];
+    float sub = k > 0 ? le : 0.f;
+    float dia = fmaf(-re, ln, 1.f);
+    float sup = last ? 0.f : -re * rn;
+    float rhs = fmaf(-re, yn, ye);
+#pragma unroll
+    for (int d = 1; d < P; d *= 2) {
+      const float subm = __shfl_up_sync(0xffffffffu, sub, d, P);
+      const float diam = __shfl_up_sync(0xffffffffu, dia, d, P);
+      const float supm = __shfl_up_sync(0xffffffffu, sup, d, P);
+      const float rhsm = __shfl_up_sync(0xffffffffu, rhs, d, P);
+      const float subp = __shfl_down_sync(0xffffffffu, sub, d, P);
+      const float diap = __shfl_down_sync(0xffffffffu, dia, d, P);
+      const float supp = __shfl_down_sync(0xffffffffu, sup, d, P);
+      const float rhsp = __shfl_down_sync(0xffffffffu, rhs, d, P);
+      const bool hasm = k >= d, hasp = k + d < P;
+      const float al = hasm ? -sub * recip(diam) : 0.f;
+      const float be = hasp ? -sup * recip(diap) : 0.f;
+      const float nsub = hasm ? al * subm : 0.f;
+      const float nsup = hasp ? be * supp : 0.f;
+      dia = dia + (hasm ? al * supm : 0.f) + (hasp ? be * subp : 0.f);
+      rhs = rhs + (hasm ? al * rhsm : 0.f) + (hasp ? be * rhsp : 0.f);
+      sub = nsub;
+      sup = nsup;
+    }
+    if (bad_pivot(dia)) atomicCAS(&sBad[q], 0, min(N, (k + 1) * L));
+    sT[k][q] = rhs * recip(dia);
+  }
+  __syncthreads();
+
+  // ---- 3. every row from t_{c-1} and x at the next chunk's first row
+  const float tprev = c > 0 ? sT[c - 1][lane] : 0.f;
+  float xnext = 0.f;
+  if (c < P - 1) {
+    const float tnext = sT[c + 1][lane];
+    xnext = sB[2][c + 1][lane] - sB[0][c + 1][lane] * sT[c][lane] - sB[1][c + 1][lane] * tnext;
+  }
+#pragma unroll
+  for (int j = 0; j < L; ++j) {
+    const int i = row0 + j;
+    const float x = yv[j] - lv[j] * tprev - cp[j] * xnext;
+    if (act && i < N) X[(size_t)i * ld + s] = x;
+  }
+  if (c == 0 && act && info) info[s] = sBad[lane];
+}
+
+template <typename T>
+cudaError_t launch_thread(const void* a, const void* b, const void* c, void* X, int N, int batch,
+                          void* work, int* info, cudaStream_t st) {
+  const int grid = (batch + kThreads - 1) / kThreads;
+  k_tri_thread<T><<<grid, kThreads, 0, st>>>(static_cast<const T*>(a), static_cast<const T*>(b),
+                                             static_cast<const T*>(c), static_cast<T*>(X),
+                                             static_cast<T*>(work), N, batch, info);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <int L, int P>
+cudaError_t launch_split(const void* a, const void* b, const void* c, void* X, int N, int batch,
+                         int* info, cudaStream_t st) {
+  const int grid = (batch + kTriSB - 1) / kTriSB;
+  const size_t smem = (size_t)4 * L * kTriSB * P * sizeof(float);
+  auto kern = k_tri_split<L, P>;
+  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kTriSB * P, smem, st>>>(static_cast<const float*>(a), static_cast<const float*>(b),
+                                          static_cast<const float*>(c), static_cast<float*>(X), N,
+                                          batch, info);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+// rows per chunk of the partitioned kernel: 8 up to N = 256, else 16
+static int tri_split_rows(int N) { return N <= 256 ? 8 : 16; }
+
+int tri_split_chunks(int N) {
+  const int L = tri_split_rows(N);
+  const int need = (N + L - 1) / L;
+  int P = 2;
+  while (P < need) P *= 2;
+  return P <= 32 ? P : 0;
+}
+
+size_t tri_work_bytes(int N, int batch, pent_dtype dt) {
+  const size_t elem = dt == PENT_F64 ? sizeof(double) : sizeof(float);
+  return (size_t)N * (size_t)batch * elem;
+}
+
+cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch,
+                            pent_dtype dt, bool split, void* work, int* info, cudaStream_t st) {
+  if (split) {
+    if (tri_split_rows(N) == 16) return launch_split<16, 32>(a, b, c, X, N, batch, info, st);
+    switch (tri_split_chunks(N)) {
+      case 2: return launch_split<8, 2>(a, b, c, X, N, batch, info, st);
+      case 4: return launch_split<8, 4>(a, b, c, X, N, batch, info, st);
+      case 8: return launch_split<8, 8>(a, b, c, X, N, batch, info, st);
+      case 16: return launch_split<8, 16>(a, b, c, X, N, batch, info, st);
+      case 32: return launch_split<8, 32>(a, b, c, X, N, batch, info, st);
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  if (dt == PENT_F64) return launch_thread<double>(a, b, c, X, N, batch, work, info, st);
+  return launch_thread<float>(a, b, c, X, N, batch, work, info, st);
+}
+
+}  // namespace pent

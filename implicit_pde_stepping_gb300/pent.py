@@ -55,6 +55,9 @@ def lib():
             L.hyperdiffusion_step.argtypes = [vp, vp, i, i, vp]
             L.ch_step.argtypes = [vp, vp, i, d, i, vp]
             L.cn_step.argtypes = [vp, vp, i, i, vp]
+            L.tri_factor_solve_work_bytes.argtypes = [i, i, i]
+            L.tri_factor_solve_work_bytes.restype = sz
+            L.tri_factor_solve.argtypes = [vp] * 4 + [i, i, i, i, vp, sz, vp, vp]
             L.pent_set_variant.argtypes = [vp, i]
             L.pent_get_variant.argtypes = [vp, i]
             L.pent_destroy.argtypes = [vp]
@@ -65,7 +68,7 @@ def lib():
             L.pent_launch_count.argtypes = []
             L.pent_launch_count.restype = ctypes.c_ulonglong
             for fn in ("pent_factor", "pent_solve", "pent_factor_solve", "hyperdiffusion_step",
-                       "ch_step", "cn_step", "pent_set_variant", "pent_get_variant", "pent_sync"):
+                       "ch_step", "cn_step", "tri_factor_solve", "pent_set_variant", "pent_get_variant", "pent_sync"):
                 getattr(L, fn).restype = i
             _lib = L
     return _lib
@@ -206,6 +209,33 @@ def pent_factor_solve_noalloc(a, b, c, d, e, rhs, info=None, stream=None) -> Non
         ip = ctypes.c_void_p(info.data_ptr())
     _check(lib().pent_factor_solve_noalloc(*ptrs, _ptr(rhs, N, code, "rhs"), N, batch, code, ip,
                                            _stream(stream)), "pent_factor_solve_noalloc")
+
+
+def tri_factor_solve_work_bytes(N: int, batch: int, dtype) -> int:
+    code = dtype if isinstance(dtype, int) else (F64 if str(dtype).endswith("64") else F32)
+    return int(lib().tri_factor_solve_work_bytes(int(N), int(batch), code))
+
+
+def tri_factor_solve(a, b, c, rhs, variant: str = "auto", work=None, info=None, stream=None):
+    """Per-system tridiagonal solve in place in rhs (Thomas algorithm).  variant: "auto",
+    "thread" or "split".  work: CUDA uint8 tensor of tri_factor_solve_work_bytes() bytes
+    (allocated here if None; unused by the split kernel).  info: CUDA int32 [batch]."""
+    import torch
+    N, batch = rhs.shape
+    code = _dtype_code(rhs)
+    ptrs = [_ptr(t, N, code, n) for t, n in zip((a, b, c), "abc")]
+    need = tri_factor_solve_work_bytes(N, batch, code)
+    if work is None:
+        work = torch.empty(need, dtype=torch.uint8, device=rhs.device)
+    ip = None
+    if info is not None:
+        if info.dtype != torch.int32 or info.numel() < batch or not info.is_cuda:
+            raise ValueError("info must be a CUDA int32 tensor of >= batch elements")
+        ip = ctypes.c_void_p(info.data_ptr())
+    _check(lib().tri_factor_solve(*ptrs, _ptr(rhs, N, code, "rhs"), N, batch, code, VARIANTS[variant],
+                                  ctypes.c_void_p(work.data_ptr()), work.numel() * work.element_size(),
+                                  ip, _stream(stream)), "tri_factor_solve")
+    return work
 
 
 def hyperdiffusion_step(plan: Plan, C, nsteps: int, stream=None) -> None:

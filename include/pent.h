@@ -184,6 +184,41 @@ pent_status ch_step(pent_plan plan, void* C_inout, int batch, double dt_over_dx2
  */
 pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* stream);
 
+/*
+ * tri_factor_solve — batched tridiagonal systems with per-system matrices,
+ * factor + solve in one call: the Thomas algorithm of "Simulating the
+ * behavior of the human brain on GPUs" (Valero-Lara et al.), section 4.1,
+ * in the interleaved one-thread-per-system layout of its section 4.1.1
+ * (cuThomasBatch).  Row i of system s:
+ *   a_i x_{i-1} + b_i x_i + c_i x_{i+1} = y_i   (a_0 and c_{N-1} are ignored).
+ *   a, b, c   : DEVICE, interleaved [N][batch] each, dtype elements; not modified.
+ *   rhs_inout : DEVICE, interleaved [N][batch]; y in, x out.
+ *   N, batch  : >= 1.
+ *   variant   : PENT_VARIANT_THREAD — one thread per system, c'_i kept in `work`
+ *               and y'_i written over the right-hand side (the page's scheme);
+ *               PENT_VARIANT_SPLIT — fp32 and N <= 512 only: each system held
+ *               in registers across a group of threads (chunks of 16 rows,
+ *               partitioned elimination, chunk-end unknowns by parallel cyclic
+ *               reduction), so memory sees a, b, c, y once and x once;
+ *               PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD.
+ *               PENT_VARIANT_THREAD_DF is not a tridiagonal variant.
+ *   work      : DEVICE scratch of tri_factor_solve_work_bytes() bytes,
+ *               256-byte aligned (may be NULL with work_bytes 0 when the SPLIT
+ *               kernel runs); contents undefined afterwards.
+ *   info      : DEVICE int[batch] or NULL.  info[s] = 0, or the 1-based row of a
+ *               zero or non-finite pivot met by the kernel's elimination (the
+ *               row may differ between variants); x of that system is then
+ *               undefined.  No pivoting is done: use diagonally dominant or SPD
+ *               matrices, as the page does.
+ * Errors: PENT_ERR_INVALID_ARG for null or misaligned pointers, N or batch < 1,
+ * a bad dtype or variant, or a short work buffer; PENT_ERR_UNSUPPORTED for
+ * SPLIT outside fp32 / N <= 512.  Nothing is queued on an error.
+ */
+size_t tri_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);
+pent_status tri_factor_solve(const void* a, const void* b, const void* c, void* rhs_inout, int N,
+                             int batch, pent_dtype dtype, pent_variant variant, void* work,
+                             size_t work_bytes, int* info, void* stream);
+
 /* Select the kernel variant of a plan (PENT_VARIANT_AUTO restores the default).
  * PENT_ERR_UNSUPPORTED if the variant does not exist for this plan. */
 pent_status pent_set_variant(pent_plan plan, pent_variant variant);
