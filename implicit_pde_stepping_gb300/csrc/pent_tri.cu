@@ -26,7 +26,14 @@
 //                    from t_{c-1} and x_{s_{c+1}}.
 //   The partition trades the page's 8n operations for about twice as many,
 //   which fp32 affords: the kernel is bound by memory, not arithmetic.
+//   A CTA's tile of a, b, c and y (16 systems x all rows) reaches shared memory
+//   by TMA: one thread issues four box copies per 256 rows and the CTA waits
+//   on an mbarrier, so the whole tile is in flight without holding registers.
+//   Where a tensor map cannot describe the arrays (base or row pitch not a
+//   multiple of 16 bytes) every thread stages its own rows with 4-byte
+//   cp.async instead.
 #include "pent_internal.cuh"
+#include "tma.cuh"
 
 namespace pent {
 namespace {
@@ -122,10 +129,17 @@ __device__ __forceinline__ void cp_commit_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-template <int L, int P>
+struct TriMaps {
+  CUtensorMap m[4];   // a, b, c, y
+};
+
+// Staged tile: TMA layout [array][RS rows][SB systems]; cp.async layout
+// [array][L rows][SB * P threads].
+template <int L, int P, bool TMA>
 __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
-    k_tri_split(const float* __restrict__ A, const float* __restrict__ B, const float* __restrict__ C,
-                float* __restrict__ X, int N, int batch, int* __restrict__ info) {
+    k_tri_split(const __grid_constant__ TriMaps maps, const float* __restrict__ A,
+                const float* __restrict__ B, const float* __restrict__ C, float* __restrict__ X, int N,
+                int batch, int RS, int BR, int* __restrict__ info) {
   constexpr int SB = kTriSB;
   // Per chunk: first row (l', r, y''), last row (l', r, y''); t_c = x at the last row.
   // Stored [quantity][chunk][system] with rows of SB + 1 so that both thread
@@ -134,7 +148,8 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
   __shared__ float sT[P][SB + 1];
   __shared__ int sBad[SB];
   constexpr int NT = SB * P;
-  extern __shared__ float stage[];           // [4][L][NT]: a, b, c, y of every row
+  extern __shared__ __align__(128) float stage[];
+  __shared__ uint64_t bar;
   const int tid = threadIdx.x;
   const int lane = threadIdx.x % SB;         // phases 1, 3: system of this thread
   const int c = threadIdx.x / SB;            //              its chunk
@@ -144,33 +159,48 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
   const int row0 = c * L;
   if (threadIdx.x < SB) sBad[threadIdx.x] = 0;
 
-  // ---- 0. every row of this chunk in flight at once (cp.async into shared memory)
-#pragma unroll
-  for (int j = 0; j < L; ++j) {
-    const int i = row0 + j;
-    if (act && i < N) {
-      const size_t o = (size_t)i * ld + s;
-      cp_async4(&stage[(0 * L + j) * NT + tid], A + o);
-      cp_async4(&stage[(1 * L + j) * NT + tid], B + o);
-      cp_async4(&stage[(2 * L + j) * NT + tid], C + o);
-      cp_async4(&stage[(3 * L + j) * NT + tid], X + o);
+  int bad = 0;
+  // ---- 0. the tile into shared memory, all of it in flight at once
+  if constexpr (TMA) {
+    if (tid == 0) tma::mbar_init(&bar, 1);
+    __syncthreads();
+    if (tid == 0) {
+      tma::mbar_expect_tx(&bar, (unsigned)(4 * RS * SB * sizeof(float)));
+      for (int arr = 0; arr < 4; ++arr)
+        for (int y0 = 0; y0 < RS; y0 += BR)
+          tma::load_2d(stage + ((size_t)arr * RS + y0) * SB, &maps.m[arr], blockIdx.x * SB, y0, &bar);
     }
+    if (!tma::mbar_wait(&bar, 0, 2000000000ull)) bad = -1;   // 2 s: the copy never arrived
+  } else {
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+      const int i = row0 + j;
+      if (act && i < N) {
+        const size_t o = (size_t)i * ld + s;
+        cp_async4(&stage[(0 * L + j) * NT + tid], A + o);
+        cp_async4(&stage[(1 * L + j) * NT + tid], B + o);
+        cp_async4(&stage[(2 * L + j) * NT + tid], C + o);
+        cp_async4(&stage[(3 * L + j) * NT + tid], X + o);
+      }
+    }
+    cp_commit_wait_all();
   }
-  cp_commit_wait_all();
+  auto staged = [&](int arr, int j) -> float {
+    return TMA ? stage[((size_t)arr * RS + row0 + j) * SB + lane] : stage[(arr * L + j) * NT + tid];
+  };
 
   // ---- 1. downward elimination: x_i + c'_i x_{i+1} + l_i x_{s-1} = y'_i
   float cp[L], lv[L], yv[L];
-  int bad = 0;
   {
     float cprev = 0.f, lprev = 0.f, yprev = 0.f;
 #pragma unroll
     for (int j = 0; j < L; ++j) {
       const int i = row0 + j;
       const bool in = act && i < N;
-      const float a = (in && i >= 1) ? stage[(0 * L + j) * NT + tid] : 0.f;
-      const float b = in ? stage[(1 * L + j) * NT + tid] : 1.f;
-      const float cc = (in && i + 1 < N) ? stage[(2 * L + j) * NT + tid] : 0.f;
-      const float y = in ? stage[(3 * L + j) * NT + tid] : 0.f;
+      const float a = (in && i >= 1) ? staged(0, j) : 0.f;
+      const float b = in ? staged(1, j) : 1.f;
+      const float cc = (in && i + 1 < N) ? staged(2, j) : 0.f;
+      const float y = in ? staged(3, j) : 0.f;
       const float den = (j == 0) ? b : fmaf(-a, cprev, b);
       if (bad == 0 && bad_pivot(den)) bad = i + 1;
       const float rd = recip(den);
@@ -269,13 +299,23 @@ template <int L, int P>
 cudaError_t launch_split(const void* a, const void* b, const void* c, void* X, int N, int batch,
                          int* info, cudaStream_t st) {
   const int grid = (batch + kTriSB - 1) / kTriSB;
-  const size_t smem = (size_t)4 * L * kTriSB * P * sizeof(float);
-  auto kern = k_tri_split<L, P>;
+  // TMA boxes of BR rows (even, <= 256) covering RS >= N rows
+  const int BR = N <= 256 ? ((N + 1) & ~1) : 256;
+  const int RS = (N + BR - 1) / BR * BR;
+  TriMaps maps;
+  const void* ptr[4] = {a, b, c, X};
+  bool tma_ok = true;
+  for (int k = 0; k < 4 && tma_ok; ++k)
+    tma_ok = tma::encode_2d(&maps.m[k], ptr[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float), batch, N,
+                            kTriSB, (unsigned)BR);
+  const size_t smem = tma_ok ? (size_t)4 * RS * kTriSB * sizeof(float)
+                             : (size_t)4 * L * kTriSB * P * sizeof(float);
+  auto kern = tma_ok ? k_tri_split<L, P, true> : k_tri_split<L, P, false>;
   const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kTriSB * P, smem, st>>>(static_cast<const float*>(a), static_cast<const float*>(b),
+  kern<<<grid, kTriSB * P, smem, st>>>(maps, static_cast<const float*>(a), static_cast<const float*>(b),
                                           static_cast<const float*>(c), static_cast<float*>(X), N,
-                                          batch, info);
+                                          batch, RS, BR, info);
   note_launch();
   return cudaGetLastError();
 }
