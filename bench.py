@@ -46,6 +46,9 @@ WORKLOADS = {
     "tri": dict(N=256, batch=262144, kind="tri", dtype="f32",
                 desc="per-system tridiagonal factor+solve (Thomas), N=256, batch=262144, fp32, "
                      "diagonally dominant"),
+    "tri_bi16": dict(N=256, batch=262144, kind="tri", dtype="f32", bs=16,
+                     desc="per-system tridiagonal factor+solve, block-interleaved layout (blocks of 16 "
+                          "systems), N=256, batch=262144, fp32, diagonally dominant"),
     "persys": dict(N=256, batch=262144, kind="persys", dtype="f32",
                    desc="per-system factor+solve, N=256, batch=262144, fp32, diagonally dominant"),
     "cn": dict(N=512, batch=4096, kind="cn", sigma=0.25, cyclic=True, dtype="f64",
@@ -244,8 +247,14 @@ def run_ours(args, W: dict, dist: Dist):
         bufs = [torch.from_numpy(inputs.ch_initial(N, batch, seed=seed + r)).to("cuda")
                 for r in range(2)]
     elif kind == "tri":
-        bands = [torch.from_numpy(v).to("cuda") for v in inputs.tri_bands(N, batch, seed=seed)]
-        bufs = [torch.from_numpy(inputs.rhs_uniform(N, batch, seed=seed + r).astype(np.float32))
+        bs = W.get("bs", 0)
+
+        def lay(x):   # interleaved [N][batch] -> the workload's layout
+            if not bs:
+                return np.ascontiguousarray(x)
+            return np.ascontiguousarray(x.reshape(N, batch // bs, bs).transpose(1, 0, 2))
+        bands = [torch.from_numpy(lay(v)).to("cuda") for v in inputs.tri_bands(N, batch, seed=seed)]
+        bufs = [torch.from_numpy(lay(inputs.rhs_uniform(N, batch, seed=seed + r).astype(np.float32)))
                 .to("cuda") for r in range(2)]
         work = torch.empty(pent.tri_factor_solve_work_bytes(N, batch, pent.F32),
                            dtype=torch.uint8, device="cuda")
@@ -282,7 +291,8 @@ def run_ours(args, W: dict, dist: Dist):
         elif kind == "cn":
             pent.cn_step(plan, X, nsub, stream=stream)
         elif kind == "tri":
-            pent.tri_factor_solve(*bands, X, variant=tri_variant, work=work, stream=stream)
+            pent.tri_factor_solve(*bands, X, variant=tri_variant, work=work, stream=stream,
+                                  block_size=W.get("bs", 0))
         else:
             pent.pent_factor_solve(*bands, X, work=work, stream=stream)
 
@@ -336,7 +346,8 @@ def run_ours(args, W: dict, dist: Dist):
             if kind == "persys":
                 pent.pent_factor_solve(*dev_bands, Xd, work=work, stream=stream)
             elif kind == "tri":
-                pent.tri_factor_solve(*dev_bands, Xd, variant=tri_variant, work=work, stream=stream)
+                pent.tri_factor_solve(*dev_bands, Xd, variant=tri_variant, work=work, stream=stream,
+                                      block_size=W.get("bs", 0))
             else:
                 step(0, Xd)
             host_out.copy_(Xd, non_blocking=True)

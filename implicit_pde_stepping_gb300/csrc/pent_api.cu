@@ -311,9 +311,10 @@ size_t tri_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {
 }
 
 pent_status tri_factor_solve(const void* a, const void* b, const void* c, void* rhs, int N, int batch,
-                             pent_dtype dtype, pent_variant variant, void* work, size_t work_bytes,
-                             int* info, void* stream) {
+                             pent_dtype dtype, pent_variant variant, int block_size, void* work,
+                             size_t work_bytes, int* info, void* stream) {
   if (!a || !b || !c || !rhs || N < 1 || batch < 1) return PENT_ERR_INVALID_ARG;
+  if (block_size < 0 || (block_size > 0 && batch % block_size != 0)) return PENT_ERR_INVALID_ARG;
   if (dtype != PENT_F64 && dtype != PENT_F32) return PENT_ERR_INVALID_ARG;
   const size_t elem = dtype == PENT_F64 ? sizeof(double) : sizeof(float);
   const void* ptrs[4] = {a, b, c, rhs};
@@ -332,7 +333,8 @@ pent_status tri_factor_solve(const void* a, const void* b, const void* c, void* 
   }
   if (!split && (!work || work_bytes < tri_work_bytes(N, batch, dtype) || !aligned(work, 256)))
     return PENT_ERR_INVALID_ARG;
-  return from_cuda(tri_solve_batch(a, b, c, rhs, N, batch, dtype, split, work, info, as_stream(stream)));
+  return from_cuda(
+      tri_solve_batch(a, b, c, rhs, N, batch, block_size, dtype, split, work, info, as_stream(stream)));
 }
 
 pent_status hyperdiffusion_step(pent_plan p, void* C, int batch, int nsteps, void* stream) {

@@ -82,7 +82,8 @@ size_t persys_work_bytes(int N, int batch, pent_dtype dt);
 // tri.cu: per-system tridiagonal solves (Thomas algorithm; partitioned fp32 kernel)
 int tri_split_chunks(int N);   // chunks of the partitioned kernel for N rows, 0 if too large
 size_t tri_work_bytes(int N, int batch, pent_dtype dt);
-cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch,
+// bs = 0: interleaved [N][batch]; bs > 0: block-interleaved, blocks of bs systems
+cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
                             pent_dtype dt, bool split, void* work, int* info, cudaStream_t st);
 
 // ch.cu: fused explicit right-hand side + cyclic solve, one thread per system

@@ -6,6 +6,11 @@
 // that a warp's loads of one row are contiguous.  Rows: a_i below the
 // diagonal (column i-1), b_i on it, c_i above it (column i+1).
 //
+// Layouts: interleaved [N][batch] (element (i, s) at i * batch + s), or the
+// page's block-interleaved layout (section 4.1.1) with blocks of bs systems,
+// each block an interleaved [N][bs] array: (i, s) at (s / bs) N bs + i bs + s % bs.
+// Either way a system's rows are a fixed stride apart from its own base.
+//
 // Two kernels:
 //   k_tri_thread<T>  the page's mapping: forward elimination writes c'_i to a
 //                    scratch array and y'_i over the right-hand side, the
@@ -57,10 +62,11 @@ __device__ __forceinline__ double recip(double x) { return 1.0 / x; }
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
     k_tri_thread(const T* __restrict__ A, const T* __restrict__ B, const T* __restrict__ C,
-                 T* __restrict__ X, T* __restrict__ Wc, int N, int batch, int* __restrict__ info) {
+                 T* __restrict__ X, T* __restrict__ Wc, int N, int batch, int bs, int* __restrict__ info) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
-  const size_t ld = (size_t)batch;
+  const size_t ld = bs ? (size_t)bs : (size_t)batch;                          // row stride
+  const size_t sb = bs ? (size_t)(s / bs) * N * bs + s % bs : (size_t)s;     // row 0 of system s
   T cp = T(0), yp = T(0);
   int bad = 0;
   for (int i0 = 0; i0 < N; i0 += kUnroll) {
@@ -68,7 +74,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 + u;
-      const size_t o = (size_t)i * ld + s;
+      const size_t o = (size_t)i * ld + sb;
       const bool in = i < N;
       a[u] = (in && i >= 1) ? A[o] : T(0);
       b[u] = in ? B[o] : T(1);
@@ -79,7 +85,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 + u;
       if (i < N) {
-        const size_t o = (size_t)i * ld + s;
+        const size_t o = (size_t)i * ld + sb;
         const T den = b[u] - cp * a[u];
         if (bad == 0 && bad_pivot(den)) bad = i + 1;
         const T rd = recip(den);
@@ -96,7 +102,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 - u;
-      const size_t o = (size_t)(i >= 0 ? i : 0) * ld + s;
+      const size_t o = (size_t)(i >= 0 ? i : 0) * ld + sb;
       yv[u] = (i >= 0) ? X[o] : T(0);
       cv[u] = (i >= 0) ? Wc[o] : T(0);
     }
@@ -105,7 +111,7 @@ __global__ void __launch_bounds__(kThreads)
       const int i = i0 - u;
       if (i >= 0) {
         const T x = yv[u] - cv[u] * x1;
-        X[(size_t)i * ld + s] = x;
+        X[(size_t)i * ld + sb] = x;
         x1 = x;
       }
     }
@@ -139,7 +145,7 @@ template <int L, int P, bool TMA>
 __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
     k_tri_split(const __grid_constant__ TriMaps maps, const float* __restrict__ A,
                 const float* __restrict__ B, const float* __restrict__ C, float* __restrict__ X, int N,
-                int batch, int RS, int BR, int* __restrict__ info) {
+                int batch, int bs, int RS, int BR, int* __restrict__ info) {
   constexpr int SB = kTriSB;
   // Per chunk: first row (l', r, y''), last row (l', r, y''); t_c = x at the last row.
   // Stored [quantity][chunk][system] with rows of SB + 1 so that both thread
@@ -155,7 +161,8 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
   const int c = threadIdx.x / SB;            //              its chunk
   const int s = blockIdx.x * SB + lane;
   const bool act = s < batch;
-  const size_t ld = (size_t)batch;
+  const size_t ld = bs ? (size_t)bs : (size_t)batch;                          // row stride
+  const size_t sb = bs ? (size_t)(s / bs) * N * bs + s % bs : (size_t)s;     // row 0 of system s
   const int row0 = c * L;
   if (threadIdx.x < SB) sBad[threadIdx.x] = 0;
 
@@ -167,8 +174,11 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
     if (tid == 0) {
       tma::mbar_expect_tx(&bar, (unsigned)(4 * RS * SB * sizeof(float)));
       for (int arr = 0; arr < 4; ++arr)
-        for (int y0 = 0; y0 < RS; y0 += BR)
-          tma::load_2d(stage + ((size_t)arr * RS + y0) * SB, &maps.m[arr], blockIdx.x * SB, y0, &bar);
+        for (int y0 = 0; y0 < RS; y0 += BR) {
+          float* dst = stage + ((size_t)arr * RS + y0) * SB;
+          if (bs) tma::load_3d(dst, &maps.m[arr], (blockIdx.x * SB) % bs, y0, (blockIdx.x * SB) / bs, &bar);
+          else tma::load_2d(dst, &maps.m[arr], blockIdx.x * SB, y0, &bar);
+        }
     }
     if (!tma::mbar_wait(&bar, 0, 2000000000ull)) bad = -1;   // 2 s: the copy never arrived
   } else {
@@ -176,7 +186,7 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
     for (int j = 0; j < L; ++j) {
       const int i = row0 + j;
       if (act && i < N) {
-        const size_t o = (size_t)i * ld + s;
+        const size_t o = (size_t)i * ld + sb;
         cp_async4(&stage[(0 * L + j) * NT + tid], A + o);
         cp_async4(&stage[(1 * L + j) * NT + tid], B + o);
         cp_async4(&stage[(2 * L + j) * NT + tid], C + o);
@@ -279,24 +289,24 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
   for (int j = 0; j < L; ++j) {
     const int i = row0 + j;
     const float x = yv[j] - lv[j] * tprev - cp[j] * xnext;
-    if (act && i < N) X[(size_t)i * ld + s] = x;
+    if (act && i < N) X[(size_t)i * ld + sb] = x;
   }
   if (c == 0 && act && info) info[s] = sBad[lane];
 }
 
 template <typename T>
-cudaError_t launch_thread(const void* a, const void* b, const void* c, void* X, int N, int batch,
+cudaError_t launch_thread(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
                           void* work, int* info, cudaStream_t st) {
   const int grid = (batch + kThreads - 1) / kThreads;
   k_tri_thread<T><<<grid, kThreads, 0, st>>>(static_cast<const T*>(a), static_cast<const T*>(b),
                                              static_cast<const T*>(c), static_cast<T*>(X),
-                                             static_cast<T*>(work), N, batch, info);
+                                             static_cast<T*>(work), N, batch, bs, info);
   note_launch();
   return cudaGetLastError();
 }
 
 template <int L, int P>
-cudaError_t launch_split(const void* a, const void* b, const void* c, void* X, int N, int batch,
+cudaError_t launch_split(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
                          int* info, cudaStream_t st) {
   const int grid = (batch + kTriSB - 1) / kTriSB;
   // TMA boxes of BR rows (even, <= 256) covering RS >= N rows
@@ -304,10 +314,13 @@ cudaError_t launch_split(const void* a, const void* b, const void* c, void* X, i
   const int RS = (N + BR - 1) / BR * BR;
   TriMaps maps;
   const void* ptr[4] = {a, b, c, X};
-  bool tma_ok = true;
+  // a CTA's 16 systems must lie in one block of a block-interleaved array
+  bool tma_ok = bs == 0 || bs % kTriSB == 0;
   for (int k = 0; k < 4 && tma_ok; ++k)
-    tma_ok = tma::encode_2d(&maps.m[k], ptr[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float), batch, N,
-                            kTriSB, (unsigned)BR);
+    tma_ok = bs ? tma::encode_3d_blocked(&maps.m[k], ptr[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float),
+                                         bs, N, batch / bs, kTriSB, (unsigned)BR)
+                : tma::encode_2d(&maps.m[k], ptr[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float), batch,
+                                 N, kTriSB, (unsigned)BR);
   const size_t smem = tma_ok ? (size_t)4 * RS * kTriSB * sizeof(float)
                              : (size_t)4 * L * kTriSB * P * sizeof(float);
   auto kern = tma_ok ? k_tri_split<L, P, true> : k_tri_split<L, P, false>;
@@ -315,7 +328,7 @@ cudaError_t launch_split(const void* a, const void* b, const void* c, void* X, i
   if (e != cudaSuccess) return e;
   kern<<<grid, kTriSB * P, smem, st>>>(maps, static_cast<const float*>(a), static_cast<const float*>(b),
                                           static_cast<const float*>(c), static_cast<float*>(X), N,
-                                          batch, RS, BR, info);
+                                          batch, bs, RS, BR, info);
   note_launch();
   return cudaGetLastError();
 }
@@ -338,21 +351,21 @@ size_t tri_work_bytes(int N, int batch, pent_dtype dt) {
   return (size_t)N * (size_t)batch * elem;
 }
 
-cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch,
+cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
                             pent_dtype dt, bool split, void* work, int* info, cudaStream_t st) {
   if (split) {
-    if (tri_split_rows(N) == 16) return launch_split<16, 32>(a, b, c, X, N, batch, info, st);
+    if (tri_split_rows(N) == 16) return launch_split<16, 32>(a, b, c, X, N, batch, bs, info, st);
     switch (tri_split_chunks(N)) {
-      case 2: return launch_split<8, 2>(a, b, c, X, N, batch, info, st);
-      case 4: return launch_split<8, 4>(a, b, c, X, N, batch, info, st);
-      case 8: return launch_split<8, 8>(a, b, c, X, N, batch, info, st);
-      case 16: return launch_split<8, 16>(a, b, c, X, N, batch, info, st);
-      case 32: return launch_split<8, 32>(a, b, c, X, N, batch, info, st);
+      case 2: return launch_split<8, 2>(a, b, c, X, N, batch, bs, info, st);
+      case 4: return launch_split<8, 4>(a, b, c, X, N, batch, bs, info, st);
+      case 8: return launch_split<8, 8>(a, b, c, X, N, batch, bs, info, st);
+      case 16: return launch_split<8, 16>(a, b, c, X, N, batch, bs, info, st);
+      case 32: return launch_split<8, 32>(a, b, c, X, N, batch, bs, info, st);
       default: return cudaErrorInvalidValue;
     }
   }
-  if (dt == PENT_F64) return launch_thread<double>(a, b, c, X, N, batch, work, info, st);
-  return launch_thread<float>(a, b, c, X, N, batch, work, info, st);
+  if (dt == PENT_F64) return launch_thread<double>(a, b, c, X, N, batch, bs, work, info, st);
+  return launch_thread<float>(a, b, c, X, N, batch, bs, work, info, st);
 }
 
 }  // namespace pent

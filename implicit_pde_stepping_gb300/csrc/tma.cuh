@@ -53,6 +53,24 @@ inline bool encode_2d(CUtensorMap* map, const void* base, CUtensorMapDataType ty
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map of a block-interleaved array: blocks of `bs` systems, each block an
+// interleaved [rows][bs] array, blocks one after another (dims: system within
+// the block, row, block).  Boxes of box_x systems x box_y rows of one block.
+inline bool encode_3d_blocked(CUtensorMap* map, const void* base, CUtensorMapDataType type, size_t elem,
+                              long long bs, long long rows, long long nblocks, unsigned box_x,
+                              unsigned box_y) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encoder();
+  if (!fn) return false;
+  if ((reinterpret_cast<uintptr_t>(base) % 16) != 0 || ((size_t)bs * elem) % 16 != 0) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)bs, (cuuint64_t)rows, (cuuint64_t)nblocks};
+  const cuuint64_t strides[2] = {(cuuint64_t)bs * elem, (cuuint64_t)bs * rows * elem};
+  const cuuint32_t box[3] = {box_x, box_y, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ---------------------------------------------------------------------------
 // device
 // ---------------------------------------------------------------------------
@@ -103,6 +121,15 @@ __device__ __forceinline__ void load_2d(void* dst, const CUtensorMap* map, int x
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
       "[%4];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void load_3d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                        uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
 }
 

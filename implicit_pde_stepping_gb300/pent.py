@@ -57,7 +57,7 @@ def lib():
             L.cn_step.argtypes = [vp, vp, i, i, vp]
             L.tri_factor_solve_work_bytes.argtypes = [i, i, i]
             L.tri_factor_solve_work_bytes.restype = sz
-            L.tri_factor_solve.argtypes = [vp] * 4 + [i, i, i, i, vp, sz, vp, vp]
+            L.tri_factor_solve.argtypes = [vp] * 4 + [i, i, i, i, i, vp, sz, vp, vp]
             L.pent_set_variant.argtypes = [vp, i]
             L.pent_get_variant.argtypes = [vp, i]
             L.pent_destroy.argtypes = [vp]
@@ -68,7 +68,8 @@ def lib():
             L.pent_launch_count.argtypes = []
             L.pent_launch_count.restype = ctypes.c_ulonglong
             for fn in ("pent_factor", "pent_solve", "pent_factor_solve", "hyperdiffusion_step",
-                       "ch_step", "cn_step", "tri_factor_solve", "pent_set_variant", "pent_get_variant", "pent_sync"):
+                       "ch_step", "cn_step", "tri_factor_solve", "pent_set_variant",
+                       "pent_get_variant", "pent_sync"):
                 getattr(L, fn).restype = i
             _lib = L
     return _lib
@@ -216,14 +217,30 @@ def tri_factor_solve_work_bytes(N: int, batch: int, dtype) -> int:
     return int(lib().tri_factor_solve_work_bytes(int(N), int(batch), code))
 
 
-def tri_factor_solve(a, b, c, rhs, variant: str = "auto", work=None, info=None, stream=None):
+def tri_factor_solve(a, b, c, rhs, variant: str = "auto", work=None, info=None, stream=None,
+                     block_size: int = 0):
     """Per-system tridiagonal solve in place in rhs (Thomas algorithm).  variant: "auto",
     "thread" or "split".  work: CUDA uint8 tensor of tri_factor_solve_work_bytes() bytes
-    (allocated here if None; unused by the split kernel).  info: CUDA int32 [batch]."""
+    (allocated here if None; unused by the split kernel).  info: CUDA int32 [batch].
+    block_size 0: arrays interleaved [N][batch]; block_size bs > 0: block-interleaved,
+    arrays shaped [batch / bs][N][bs]."""
     import torch
-    N, batch = rhs.shape
-    code = _dtype_code(rhs)
-    ptrs = [_ptr(t, N, code, n) for t, n in zip((a, b, c), "abc")]
+    if block_size:
+        nb, N, bs = rhs.shape
+        if bs != block_size:
+            raise ValueError("block-interleaved arrays must be [batch / bs][N][bs]")
+        batch = nb * bs
+        for t, n in zip((a, b, c, rhs), "abcr"):
+            if t.shape != rhs.shape or not t.is_cuda or not t.is_contiguous() or t.dtype != rhs.dtype:
+                raise ValueError(f"{n} must match rhs: contiguous CUDA [batch / bs][N][bs]")
+        code = _dtype_code(rhs)
+        ptrs = [ctypes.c_void_p(t.data_ptr()) for t in (a, b, c)]
+        rp = ctypes.c_void_p(rhs.data_ptr())
+    else:
+        N, batch = rhs.shape
+        code = _dtype_code(rhs)
+        ptrs = [_ptr(t, N, code, n) for t, n in zip((a, b, c), "abc")]
+        rp = _ptr(rhs, N, code, "rhs")
     need = tri_factor_solve_work_bytes(N, batch, code)
     if work is None:
         work = torch.empty(need, dtype=torch.uint8, device=rhs.device)
@@ -232,7 +249,7 @@ def tri_factor_solve(a, b, c, rhs, variant: str = "auto", work=None, info=None, 
         if info.dtype != torch.int32 or info.numel() < batch or not info.is_cuda:
             raise ValueError("info must be a CUDA int32 tensor of >= batch elements")
         ip = ctypes.c_void_p(info.data_ptr())
-    _check(lib().tri_factor_solve(*ptrs, _ptr(rhs, N, code, "rhs"), N, batch, code, VARIANTS[variant],
+    _check(lib().tri_factor_solve(*ptrs, rp, N, batch, code, VARIANTS[variant], int(block_size),
                                   ctypes.c_void_p(work.data_ptr()), work.numel() * work.element_size(),
                                   ip, _stream(stream)), "tri_factor_solve")
     return work

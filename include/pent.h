@@ -191,9 +191,16 @@ pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* 
  * in the interleaved one-thread-per-system layout of its section 4.1.1
  * (cuThomasBatch).  Row i of system s:
  *   a_i x_{i-1} + b_i x_i + c_i x_{i+1} = y_i   (a_0 and c_{N-1} are ignored).
- *   a, b, c   : DEVICE, interleaved [N][batch] each, dtype elements; not modified.
- *   rhs_inout : DEVICE, interleaved [N][batch]; y in, x out.
+ *   a, b, c   : DEVICE, dtype elements, layout given by block_size; not modified.
+ *   rhs_inout : DEVICE, same layout; y in, x out.
  *   N, batch  : >= 1.
+ *   block_size: 0 — interleaved [N][batch]: element (i, s) at i * batch + s.
+ *               bs > 0 — the page's block-interleaved layout (section 4.1.1):
+ *               blocks of bs systems, each block an interleaved [N][bs] array,
+ *               blocks one after another: (i, s) at (s / bs) * N * bs + i * bs
+ *               + s % bs.  batch must be a multiple of bs.  The SPLIT kernel
+ *               loads a block-interleaved tile with one contiguous box per array
+ *               when bs is a multiple of 16.
  *   variant   : PENT_VARIANT_THREAD — one thread per system, c'_i kept in `work`
  *               and y'_i written over the right-hand side (the page's scheme);
  *               PENT_VARIANT_SPLIT — fp32 and N <= 512 only: each system held
@@ -211,13 +218,13 @@ pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* 
  *               undefined.  No pivoting is done: use diagonally dominant or SPD
  *               matrices, as the page does.
  * Errors: PENT_ERR_INVALID_ARG for null or misaligned pointers, N or batch < 1,
- * a bad dtype or variant, or a short work buffer; PENT_ERR_UNSUPPORTED for
+ * a bad dtype, variant or block_size, or a short work buffer; PENT_ERR_UNSUPPORTED for
  * SPLIT outside fp32 / N <= 512.  Nothing is queued on an error.
  */
 size_t tri_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);
 pent_status tri_factor_solve(const void* a, const void* b, const void* c, void* rhs_inout, int N,
-                             int batch, pent_dtype dtype, pent_variant variant, void* work,
-                             size_t work_bytes, int* info, void* stream);
+                             int batch, pent_dtype dtype, pent_variant variant, int block_size,
+                             void* work, size_t work_bytes, int* info, void* stream);
 
 /* Select the kernel variant of a plan (PENT_VARIANT_AUTO restores the default).
  * PENT_ERR_UNSUPPORTED if the variant does not exist for this plan. */

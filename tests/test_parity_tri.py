@@ -102,3 +102,50 @@ def test_periodic_implicit_diffusion_through_pentadiagonal_plan():
     ph = 2 * np.pi * k[:, None] * x[None, :]
     exact = np.cos(ph).T @ (a * G[:, None]) + np.sin(ph).T @ (b * G[:, None])
     assert max_rel_err(out, exact) < 1e-10
+
+
+def to_blocked(x, bs):
+    """Interleaved [N][batch] -> block-interleaved [batch / bs][N][bs]."""
+    N, batch = x.shape
+    return np.ascontiguousarray(x.reshape(N, batch // bs, bs).transpose(1, 0, 2))
+
+
+def from_blocked(x):
+    nb, N, bs = x.shape
+    return np.ascontiguousarray(x.transpose(1, 0, 2).reshape(N, nb * bs))
+
+
+@pytest.mark.parametrize("variant,dtype,tol", CASES[:3], ids=[f"{v}-{d.__name__}" for v, d, _ in CASES[:3]])
+@pytest.mark.parametrize("bs", [16, 32, 8, 48])
+@pytest.mark.parametrize("N", [7, 256, 300])
+def test_tri_block_interleaved(variant, dtype, tol, bs, N):
+    """The page's block-interleaved layout (blocks of bs systems, each an interleaved
+    [N][bs] array): same solutions as the oracle.  bs = 8 is not a multiple of 16, so
+    the partitioned kernel stages rows with cp.async instead of tensor maps."""
+    import torch
+    batch = bs * 9
+    a, b, c = inputs.tri_bands(N, batch, seed=N + bs, dtype=dtype)
+    y = inputs.rhs_uniform(N, batch, seed=N + bs + 1).astype(dtype)
+    ref = oracle.batch_tri(a, b, c, y)
+    X = dev(to_blocked(y, bs))
+    info = torch.zeros(batch, dtype=torch.int32, device="cuda")
+    pent.tri_factor_solve(dev(to_blocked(a, bs)), dev(to_blocked(b, bs)), dev(to_blocked(c, bs)), X,
+                          variant=variant, info=info, block_size=bs)
+    pent.pent_sync()
+    assert not host(info).any()
+    assert max_rel_err(from_blocked(host(X)), ref) < tol
+
+
+def test_tri_block_size_must_divide_batch():
+    import torch
+    z = torch.zeros((16, 4), dtype=torch.float32, device="cuda")
+    work = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
+    L = pent.lib()
+    p = [ctypes_ptr(z) for _ in range(4)]
+    assert L.tri_factor_solve(*p, 4, 16, pent.F32, pent.VARIANT_THREAD, 3, ctypes_ptr(work), 1 << 16, None,
+                              None) == pent.ERR_INVALID_ARG
+
+
+def ctypes_ptr(t):
+    import ctypes
+    return ctypes.c_void_p(t.data_ptr())
