@@ -190,8 +190,10 @@ def hbm_peak():
 
 
 def source_digest(kernel_file: str) -> str:
+    """Digest of a kernel's source and the device headers it is built from (the
+    plan/launcher declarations are left out: they do not change the kernel)."""
     h = hashlib.sha256()
-    for name in (kernel_file, "pent_internal.cuh", "df64.cuh"):
+    for name in (kernel_file, "df64.cuh", "tma.cuh"):
         path = os.path.join(ROOT, "implicit_pde_stepping_gb300", "csrc", name)
         if os.path.exists(path):
             with open(path, "rb") as fh:
