@@ -342,6 +342,10 @@ def run_ours(args, W: dict, dist: Dist):
         dev_bands = [torch.empty_like(b) for b in bands] if kind in ("persys", "tri") else []
 
         def e2e_step():
+            if kind == "shared":
+                # the library's host-buffer call: copy in, solve, copy out, overlapped
+                pent.pent_solve_host(plan, host_in, host_out, chunks=args.e2e_chunks, stream=stream)
+                return
             for hb, db in zip(host_bands, dev_bands):
                 db.copy_(hb, non_blocking=True)
             Xd.copy_(host_in, non_blocking=True)
@@ -374,7 +378,9 @@ def run_ours(args, W: dict, dist: Dist):
         e2e = {"value": batch * nsub * ke * dist.world / (ems / 1e3), "unit": "system-solves/s"
                if kind in ("shared", "persys", "tri") else "system-steps/s",
                "h2d_bytes_per_step": nbytes, "d2h_bytes_per_step": nbytes_out, "steps": ke,
-               "ms_per_step": ems / ke}
+               "ms_per_step": ems / ke,
+               "api": ("pent_solve_host (pinned host in/out, chunks=%s)" % (args.e2e_chunks or "auto")
+                       if kind == "shared" else "pinned host copies + the device-buffer call")}
 
     # ---- roofline of the dominant kernel (one kernel per step on every path)
     per_unit = {"shared": 2 * N * elem, "hyper": 2 * N * elem, "ch": 2 * N * elem,
@@ -555,11 +561,15 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="shared")
-    ap.add_argument("--variant", default="auto", choices=sorted(__import__("implicit_pde_stepping_gb300.pent", fromlist=["VARIANTS"]).VARIANTS))
+    from implicit_pde_stepping_gb300.pent import VARIANTS
+    ap.add_argument("--variant", default="auto", choices=sorted(VARIANTS))
     ap.add_argument("--batch", type=int, default=0, help="override the per-GPU batch")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=0,
+                    help="blocks of systems the host-buffer solve pipelines (shared workloads; 0: "
+                         "the library's choice)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -75,6 +75,20 @@ bool use_steps(const pent_plan_s& p, int nsteps, int kind) {
 }
 
 }  // namespace
+
+// The solve kernel of the plan's variant for `batch` systems, in place on a
+// device array with leading dimension batch.
+cudaError_t solve_device(pent_plan_s& p, void* rhs, int batch, cudaStream_t st) {
+  const pent_variant v = resolve(p, batch);
+  if (p.dtype == PENT_F32) return shared_thread_f32(p, static_cast<float*>(rhs), batch, st);
+  switch (v) {
+    case PENT_VARIANT_THREAD: return shared_thread_f64(p, static_cast<double*>(rhs), batch, st);
+    case PENT_VARIANT_THREAD_DF: return shared_twisted_df(p, static_cast<double*>(rhs), batch, st);
+    case PENT_VARIANT_SPLIT: return shared_split_df(p, static_cast<double*>(rhs), batch, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 }  // namespace pent
 
 using namespace pent;
@@ -103,6 +117,7 @@ pent_status pent_sync(void* stream) {
 
 void pent_destroy(pent_plan p) {
   if (!p) return;
+  host_pipeline_release(*p);
   if (p->arena) cudaFree(p->arena);
   delete p;
 }
@@ -265,27 +280,23 @@ pent_variant pent_get_variant(pent_plan p, int batch) {
 pent_status pent_solve(pent_plan p, void* rhs, int batch, void* stream) {
   if (!p || !rhs || batch < 1) return PENT_ERR_INVALID_ARG;
   if (!aligned(rhs, 16)) return PENT_ERR_INVALID_ARG;
-  const pent_variant v = resolve(*p, batch);
-  cudaError_t e;
-  if (p->dtype == PENT_F32) {
-    if (v != PENT_VARIANT_THREAD) return PENT_ERR_UNSUPPORTED;
-    e = shared_thread_f32(*p, static_cast<float*>(rhs), batch, as_stream(stream));
-  } else {
-    switch (v) {
-      case PENT_VARIANT_THREAD:
-        e = shared_thread_f64(*p, static_cast<double*>(rhs), batch, as_stream(stream));
-        break;
-      case PENT_VARIANT_THREAD_DF:
-        e = shared_twisted_df(*p, static_cast<double*>(rhs), batch, as_stream(stream));
-        break;
-      case PENT_VARIANT_SPLIT:
-        e = shared_split_df(*p, static_cast<double*>(rhs), batch, as_stream(stream));
-        break;
-      default:
-        return PENT_ERR_UNSUPPORTED;
-    }
+  if (p->dtype == PENT_F32 && resolve(*p, batch) != PENT_VARIANT_THREAD) return PENT_ERR_UNSUPPORTED;
+  return from_cuda(solve_device(*p, rhs, batch, as_stream(stream)));
+}
+
+pent_status pent_solve_host(pent_plan p, const void* rhs_host, void* x_host, int batch, int chunks,
+                            void* stream) {
+  if (!p || !rhs_host || !x_host || batch < 1 || chunks < 0) return PENT_ERR_INVALID_ARG;
+  if (p->dtype == PENT_F32 && resolve(*p, batch) != PENT_VARIANT_THREAD) return PENT_ERR_UNSUPPORTED;
+  if (chunks == 0) {
+    // 2-D copies keep the copy engines at full rate for rows of >= 128 KB, so
+    // blocks are at least that wide; at most 8 blocks
+    const size_t elem = p->dtype == PENT_F64 ? sizeof(double) : sizeof(float);
+    const size_t row_bytes = (size_t)batch * elem;
+    chunks = (int)(row_bytes / (128 * 1024));
+    chunks = chunks < 1 ? 1 : chunks > 8 ? 8 : chunks;
   }
-  return from_cuda(e);
+  return from_cuda(solve_host(*p, rhs_host, x_host, batch, chunks, as_stream(stream), solve_device));
 }
 
 size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {

@@ -55,6 +55,13 @@ struct pent_plan_s {
   float4* sptab = nullptr;   // [Mpad][kSpK]
   double* spchunk = nullptr; // [sp_P][kSpChunk]
   double* spextra = nullptr; // [kSpExtra]
+  // host-buffer pipeline (pent_host.cu), created on first use
+  static constexpr int kHostRing = 3;
+  cudaStream_t hs[3] = {nullptr, nullptr, nullptr};   // copy in, solve, copy out
+  cudaEvent_t hev_in[kHostRing] = {}, hev_solved[kHostRing] = {}, hev_out[kHostRing] = {};
+  cudaEvent_t hev_fork = nullptr;
+  void* hbuf = nullptr;       // kHostRing staging buffers of hbuf_bytes each
+  size_t hbuf_bytes = 0;
 };
 
 namespace pent {
@@ -85,6 +92,13 @@ size_t tri_work_bytes(int N, int batch, pent_dtype dt);
 // bs = 0: interleaved [N][batch]; bs > 0: block-interleaved, blocks of bs systems
 cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
                             pent_dtype dt, bool split, void* work, int* info, cudaStream_t st);
+
+// host.cu: shared-matrix solve of host arrays, transfers overlapped with the solves
+void host_pipeline_release(pent_plan_s& p);
+cudaError_t solve_host(pent_plan_s& p, const void* in, void* out, int batch, int chunks, cudaStream_t st,
+                       cudaError_t (*solve)(pent_plan_s&, void*, int, cudaStream_t));
+// api.cu: the plan's solve kernel, in place on a device array (leading dimension batch)
+cudaError_t solve_device(pent_plan_s& p, void* rhs, int batch, cudaStream_t st);
 
 // ch.cu: fused explicit right-hand side + cyclic solve, one thread per system
 cudaError_t ch_thread_f64(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);

@@ -47,6 +47,7 @@ def lib():
             L.pent_factor.argtypes = [ctypes.POINTER(ctypes.c_double), i, i, i, i,
                                       ctypes.POINTER(vp)]
             L.pent_solve.argtypes = [vp, vp, i, vp]
+            L.pent_solve_host.argtypes = [vp, vp, vp, i, i, vp]
             L.pent_factor_solve.argtypes = [vp] * 6 + [i, i, i, vp, sz, vp, vp]
             L.pent_factor_solve_work_bytes.argtypes = [i, i, i]
             L.pent_factor_solve_work_bytes.restype = sz
@@ -67,7 +68,8 @@ def lib():
             L.pent_status_string.restype = ctypes.c_char_p
             L.pent_launch_count.argtypes = []
             L.pent_launch_count.restype = ctypes.c_ulonglong
-            for fn in ("pent_factor", "pent_solve", "pent_factor_solve", "hyperdiffusion_step",
+            for fn in ("pent_factor", "pent_solve", "pent_solve_host", "pent_factor_solve",
+                       "hyperdiffusion_step",
                        "ch_step", "cn_step", "tri_factor_solve", "pent_set_variant",
                        "pent_get_variant", "pent_sync"):
                 getattr(L, fn).restype = i
@@ -165,6 +167,27 @@ def pent_solve(plan: Plan, rhs, stream=None) -> None:
     """In-place shared-matrix solve of rhs ([N][batch] CUDA tensor)."""
     p = _ptr(rhs, plan.N, plan.dtype, "rhs")
     _check(lib().pent_solve(plan.handle, p, int(rhs.shape[1]), _stream(stream)), "pent_solve")
+
+
+def pent_solve_host(plan: Plan, rhs_host, x_host=None, chunks: int = 0, stream=None):
+    """Shared-matrix solve of a HOST tensor ([N][batch], pinned for asynchronous copies):
+    copy in, solve and copy out overlapped in blocks of systems.  Returns x_host (a new
+    pinned tensor if None); valid once the stream reaches this call (e.g. pent_sync)."""
+    import torch
+    if rhs_host.is_cuda or (x_host is not None and x_host.is_cuda):
+        raise ValueError("pent_solve_host takes host tensors")
+    if rhs_host.dim() != 2 or rhs_host.shape[0] != plan.N or not rhs_host.is_contiguous():
+        raise ValueError("rhs_host must be a contiguous [N][batch] host tensor")
+    if _dtype_code(rhs_host) != plan.dtype:
+        raise TypeError("rhs_host dtype does not match the plan")
+    if x_host is None:
+        x_host = torch.empty_like(rhs_host).pin_memory()
+    if x_host.shape != rhs_host.shape or x_host.dtype != rhs_host.dtype or not x_host.is_contiguous():
+        raise ValueError("x_host must match rhs_host")
+    _check(lib().pent_solve_host(plan.handle, ctypes.c_void_p(rhs_host.data_ptr()),
+                                 ctypes.c_void_p(x_host.data_ptr()), int(rhs_host.shape[1]), int(chunks),
+                                 _stream(stream)), "pent_solve_host")
+    return x_host
 
 
 def pent_factor_solve_work_bytes(N: int, batch: int, dtype) -> int:

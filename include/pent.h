@@ -93,6 +93,30 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
 pent_status pent_solve(pent_plan plan, void* rhs_inout, int batch, void* stream);
 
 /*
+ * pent_solve_host — pent_solve for right-hand sides held in HOST memory: the
+ * call copies them to the device, solves and copies the solutions back, with
+ * the transfers overlapped with the solves.  A library service around
+ * pent_solve (the page solves device-resident batches).
+ *   rhs_host : HOST, interleaved [N][batch] of the plan dtype (f in); pinned
+ *              (page-locked) memory for the copies to run asynchronously.
+ *   x_host   : HOST, same shape (x out); may equal rhs_host.
+ *   chunks   : number of column blocks of systems the batch is cut into for the
+ *              copy-in / solve / copy-out pipeline.  0 picks blocks whose rows
+ *              are at least 128 KB (narrower 2-D copies run below the copy
+ *              engines' rate on GB300), at most 8.  Each block is a multiple of
+ *              64 systems except possibly the last.
+ * The plan allocates, on first use, three device staging buffers of one block
+ * each and three streams; they live until pent_destroy.  The call is ordered on
+ * `stream` like pent_solve (it forks from and joins back into it) and returns
+ * before the work completes; the host arrays must stay valid and unmodified until
+ * the stream reaches this point.  Calls on one plan must be ordered (for example
+ * issued on one stream): they share the staging buffers.
+ * Errors: as pent_solve; PENT_ERR_ALLOC if the staging buffers cannot be made.
+ */
+pent_status pent_solve_host(pent_plan plan, const void* rhs_host, void* x_host, int batch, int chunks,
+                            void* stream);
+
+/*
  * pent_factor_solve — per-system matrices, factor + solve in one call
  * ("cuPentBatchRewrite": a new matrix every call).  Unlike the page, the
  * bands are left unchanged; the factor coefficients go to `work`.
