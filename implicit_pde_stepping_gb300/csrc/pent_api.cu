@@ -31,13 +31,14 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 constexpr int kMaxTwistedRows = 2560;
 
 // The kernel variant a plan uses for `batch` systems.  fp64 plans run in
-// double-float: the twisted kernel when the batch alone fills every SM with
-// a CTA of 256 systems, else the partitioned kernel (fine-grained, so small
+// double-float: the twisted kernel from about 160 systems per SM on (measured
+// crossover at N = 1024: the partitioned kernel wins at 16384 systems, the
+// twisted one at 32768), else the partitioned kernel (fine-grained, so small
 // batches still spread over the GPU); the native kernel when neither exists.
 pent_variant resolve(const pent_plan_s& p, int batch) {
   if (p.variant != PENT_VARIANT_AUTO) return p.variant;
   if (p.dtype != PENT_F64) return PENT_VARIANT_THREAD;
-  const long long fill = 256LL * (p.num_sms > 0 ? p.num_sms : 1);
+  const long long fill = 160LL * (p.num_sms > 0 ? p.num_sms : 1);
   if (p.twist_ok && batch % 2 == 0 && batch >= fill) return PENT_VARIANT_THREAD_DF;
   if (p.split_ok) return PENT_VARIANT_SPLIT;
   if (p.twist_ok) return PENT_VARIANT_THREAD_DF;
