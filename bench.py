@@ -190,14 +190,23 @@ def hbm_peak():
 
 
 def source_digest(kernel_file: str) -> str:
-    """Digest of a kernel's source and the device headers it is built from (the
-    plan/launcher declarations are left out: they do not change the kernel)."""
+    """Digest of a kernel's source file and the local headers it includes (the
+    plan/launcher declarations in pent_internal.cuh are left out: they do not change
+    the kernel's code)."""
+    csrc = os.path.join(ROOT, "implicit_pde_stepping_gb300", "csrc")
     h = hashlib.sha256()
-    for name in (kernel_file, "df64.cuh", "tma.cuh"):
-        path = os.path.join(ROOT, "implicit_pde_stepping_gb300", "csrc", name)
-        if os.path.exists(path):
-            with open(path, "rb") as fh:
-                h.update(fh.read())
+    path = os.path.join(csrc, kernel_file)
+    if not os.path.exists(path):
+        return ""
+    text = open(path, "rb").read()
+    h.update(text)
+    for line in text.decode(errors="replace").splitlines():
+        line = line.strip()
+        if line.startswith('#include "') and "pent_internal.cuh" not in line:
+            inc = os.path.join(csrc, line.split('"')[1])
+            if os.path.exists(inc):
+                with open(inc, "rb") as fh:
+                    h.update(fh.read())
     return h.hexdigest()[:16]
 
 
