@@ -353,7 +353,10 @@ pent_status hyperdiffusion_step(pent_plan p, void* C, int batch, int nsteps, voi
   if (!p || !C || batch < 1 || nsteps < 0) return PENT_ERR_INVALID_ARG;
   if (!p->cyclic || p->dtype != PENT_F64) return PENT_ERR_INVALID_ARG;
   if (!aligned(C, 16)) return PENT_ERR_INVALID_ARG;
-  if (use_steps(*p, nsteps, 0))
+  // the multi-step kernel is arithmetic-bound (~250 instructions per point and
+  // step); where the twisted kernel runs the single step it is memory-bound and
+  // about twice as fast per step, so many steps use it one launch at a time
+  if (resolve(*p, batch) != PENT_VARIANT_THREAD_DF && use_steps(*p, nsteps, 0))
     return from_cuda(steps_df(*p, static_cast<double*>(C), batch, nsteps, 0, 0.0, as_stream(stream)));
   for (int n = 0; n < nsteps; ++n) {
     const pent_status s = pent_solve(p, C, batch, stream);
