@@ -250,6 +250,16 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
           return from_cuda(e);
         }
       }
+      // PENT_BORDER_ALL=1 applies the x_t correction in every chunk (testing)
+      if (p->split_ok && cyclic && env_int("PENT_BORDER_ALL", 0) == 1) {
+        const double all = (double)spP;
+        e = cudaMemcpy(p->spextra + 19, &all, sizeof(double), cudaMemcpyHostToDevice);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          pent_destroy(p);
+          return from_cuda(e);
+        }
+      }
       if (p->split_ok) {
         double Td = 0.0;
         e = cudaMemcpy(&Td, p->spextra + 18, sizeof(double), cudaMemcpyDeviceToHost);

@@ -215,6 +215,23 @@ __global__ void __launch_bounds__(kFactorThreads)
       if (ta <= tiny && tb <= tiny) T = t;
     }
     extra[18] = (double)T;
+    // Border reach: U = E^{-1} G decays away from the two ends of the block;
+    // chunks farther than extra[19] chunks from the first (chunk 0) and the last
+    // real chunk have every |U| entry below 2^-60 and skip the x_t correction.
+    extra[19] = 0.0;
+    if (cyclic) {
+      const int clast = (M - 1) / L;
+      int reach = 0;
+      for (int c = 0; c <= clast; ++c) {
+        double um = 0.0;
+        for (int i = c * L; i < c * L + L && i < M; ++i) um = fmax(um, fmax(fabs(u0[i]), fabs(u1[i])));
+        if (!(um < ldexp(1.0, -60))) {
+          const int d = min(c, clast - c) + 1;
+          reach = max(reach, d);
+        }
+      }
+      extra[19] = (double)reach;
+    }
   }
 }
 

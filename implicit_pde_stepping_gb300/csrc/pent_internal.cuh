@@ -154,7 +154,9 @@ constexpr int kSpMaxChunks = 64;   // chunks per system the split kernel support
 constexpr int kSpChunk = 36;
 // Extras: [0..3] S^{-1} (cyclic); [4..6] h0 at rows M-2, M-1, 0; [7..9] h1 at rows
 // M-1, 0, 1; [10..13] M1,M2 at rows M-2 then M-1; [14..17] K1,K2 at rows M-2 then
-// M-1; [18] T, the number of chunk couplings kept (0: exact serial scan).
+// M-1; [18] T, the number of chunk couplings kept (0: exact serial scan); [19] the
+// border reach R (cyclic): only chunks c < R or c > (M-1)/L - R carry a
+// non-negligible E^{-1} G and apply the x_t correction.
 constexpr int kSpExtra = 20;
 
 cudaError_t factor_split(const double* d_bands, int N, int cyclic, int L, int Mpad, float4* rowtab,

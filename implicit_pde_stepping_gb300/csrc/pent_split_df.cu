@@ -93,6 +93,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   const int c = (w / SG) * 4 + (lane >> 3);
   const int row0 = c * L;
   const float4* ctb = rtab + (size_t)c * CS;     // this chunk's rows
+  const int reach = CYC ? (int)gextra[19] : 0;
+  const bool needU = CYC && (c < reach || c > (M - 1) / L - reach);   // x_t correction not negligible
   const double* ct = ctab + (size_t)c * kSpChunk;
   const long long ld = batch;
   const int nblk = (batch + SB - 1) / SB;
@@ -304,6 +306,14 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
       const D2 S0 = df::from_double(s0), S1 = df::from_double(s1);
       const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
       const D2 X0 = df::from_double(-xt0), X1 = df::from_double(-xt1);
+      if (CYC && needU) {
+#pragma unroll
+        for (int j = 0; j < L; ++j) {
+          const float4 c1 = ctb[j * K4 + 1], c5 = ctb[j * K4 + 5];
+          const D2 x = df::axpy(v[j], D2{c1.z, c1.w}, X0);
+          v[j] = df::axpy(x, D2{c5.x, c5.y}, X1);
+        }
+      }
       constexpr int G = CN ? 8 : L;                    // rows per group (CN re-reads C)
 #pragma unroll
       for (int j0 = 0; j0 < L; j0 += G) {
@@ -320,11 +330,6 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
           x = df::axpy(x, D2{c3.z, c3.w}, S1);
           x = df::axpy(x, D2{c4.x, c4.y}, T0);
           x = df::axpy(x, D2{c4.z, c4.w}, T1);
-          if (CYC) {
-            const float4 c1 = ctb[j * K4 + 1], c5 = ctb[j * K4 + 5];
-            x = df::axpy(x, D2{c1.z, c1.w}, X0);
-            x = df::axpy(x, D2{c5.x, c5.y}, X1);
-          }
           if constexpr (CN) x = df::add(D2{2.f * x.h, 2.f * x.l}, df::neg(df::from_double(cold[u])));
           if (act && row0 + j < M) __stcs(p + j * ld, df::to_double(x));
         }

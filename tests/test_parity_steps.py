@@ -130,3 +130,18 @@ def test_serial_scan_plans_step_one_launch_at_a_time(monkeypatch):
     out, launches = run("hyper", N, batch, steps, C0)
     assert launches == steps
     assert max_rel_err(out, ref("hyper", C0, steps)) < TOL_F64
+
+
+@pytest.mark.parametrize("kind", ["ch", "cn", "hyper"])
+@pytest.mark.parametrize("steps", [1, 9])
+def test_border_correction_skipped_only_where_negligible(kind, steps, monkeypatch):
+    """Chunks far from the periodic border skip the x_t correction (its E^{-1} G
+    entries are below 2^-60 there); the results match plans that apply it in
+    every chunk (PENT_BORDER_ALL=1) and the oracle."""
+    N, batch = 1024, 64
+    C0 = initial(kind, N, batch, seed=21)
+    a, _ = run(kind, N, batch, steps, C0)
+    monkeypatch.setenv("PENT_BORDER_ALL", "1")
+    b, _ = run(kind, N, batch, steps, C0)
+    assert max_rel_err(a, b) < 1e-13
+    assert max_rel_err(a, ref(kind, C0, steps)) < TOL_F64
