@@ -109,7 +109,7 @@ __global__ void k_factor_twisted(const double* __restrict__ bands, int N, int cy
   }
   for (int i = 0; i < 4; ++i)
     for (int j = 0; j < 4; ++j) twist[4 * i + j] = Ti[i][j];
-  twist[16] = twist[17] = twist[18] = twist[19] = 0.0;
+  twist[16] = twist[17] = twist[18] = twist[19] = twist[20] = 0.0;
 
   if (cyclic) {
     const double* A = bands;
@@ -172,6 +172,7 @@ __global__ void k_factor_twisted(const double* __restrict__ bands, int N, int cy
   }
 
   // pack: top rows j = 0..m-1 (global j), bottom rows j = 0..Mb-1 (global M-1-j)
+  int reach = 0;
   for (int dir = 0; dir < 2; ++dir) {
     const int R = dir ? Mb : m;
     const double* A_ = dir ? bal : al;
@@ -192,8 +193,13 @@ __global__ void k_factor_twisted(const double* __restrict__ bands, int N, int cy
       row[2] = make_float4(sD.x, sD.y, sq0.x, sq0.y);
       row[3] = make_float4(sq1.x, sq1.y, su0.x, su0.y);
       row[4] = make_float4(su1.x, su1.y, 0.f, 0.f);
+      if (cyclic) {
+        const double mag = fmax(fmax(fabs(q0[gi]), fabs(q1[gi])), fmax(fabs(u0[gi]), fabs(u1[gi])));
+        if (!(mag < ldexp(1.0, -60))) reach = max(reach, j + 1);
+      }
     }
   }
+  twist[20] = (double)reach;
 }
 
 }  // namespace

@@ -122,8 +122,10 @@ namespace pent {
 // (local row j at table row m + j, global row M-1-j).
 constexpr int kTwK = 5;
 // twist[0..15] = T^{-1} (row-major, unknowns x_{m-2}, x_{m-1}, x_m, x_{m+1});
-// twist[16..19] = S^{-1} of the border (cyclic plans).
-constexpr int kTwistCount = 20;
+// twist[16..19] = S^{-1} of the border (cyclic plans); twist[20] = border reach W
+// (cyclic): only local rows j < W of either direction carry a q or u entry of
+// magnitude >= 2^-60, so the others skip the border terms.
+constexpr int kTwistCount = 21;
 
 cudaError_t factor_twisted(const double* d_bands, int N, int cyclic, int m, float4* tab,
                            double* twist, double* d_work, int* d_status, cudaStream_t st);

@@ -22,6 +22,8 @@
 //    read back by the outward sweep, mostly from L2;
 //  * register ring of two blocks of kU rows, loads issued one block ahead;
 //    full blocks run without per-row guards, a ragged last block with them.
+#include <type_traits>
+
 #include "df64.cuh"
 #include "pent_internal.cuh"
 
@@ -382,6 +384,9 @@ __global__ void __launch_bounds__(SPB, 2)
   const int nblk = (batch + SPB - 1) / SPB;
   const int jtop = rows - 3;
   uint4* myring = ring + tid;
+  // cyclic: the border terms (q . f inward, u x_t outward) only in local rows
+  // j < W, the rest of the row entries being below 2^-60
+  const int W = CYC ? (int)sT[20] : 0;
 
   for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
     const int s0 = blk * SPB + tl * SPT;
@@ -403,19 +408,42 @@ __global__ void __launch_bounds__(SPB, 2)
       char* q = p0;
       const long long pf = (long long)D * stepB;
       const float4* row = tab;
-      for (int b = 0; b < nmain; ++b) {
+      auto block = [&](auto border) {
+        constexpr bool B = decltype(border)::value;
 #pragma unroll
         for (int u = 0; u < D; ++u) {
           cp_wait<D - 1>();
           double f[SPT];
           unpack2(myring[u * NT], f);
           D2 g[SPT];
-          inward_row<SPT, CYC>(row, f, st, g);
+          inward_row<SPT, B>(row, f, st, g);
           if (act) st_g<SPT>(q, g);
           cp_async16(myring + u * NT, q + pf);
           cp_commit();
           q += stepB;
           row += KT;
+        }
+      };
+      if constexpr (CYC) {
+        const int nb = min(nmain, (W + D - 1) / D);   // blocks that hold border rows
+        int b = 0;
+        for (; b < nb; ++b) block(std::true_type{});
+        for (; b < nmain; ++b) block(std::false_type{});
+      } else {
+        for (int b = 0; b < nmain; ++b) {
+#pragma unroll
+          for (int u = 0; u < D; ++u) {
+            cp_wait<D - 1>();
+            double f[SPT];
+            unpack2(myring[u * NT], f);
+            D2 g[SPT];
+            inward_row<SPT, false>(row, f, st, g);
+            if (act) st_g<SPT>(q, g);
+            cp_async16(myring + u * NT, q + pf);
+            cp_commit();
+            q += stepB;
+            row += KT;
+          }
         }
       }
       for (int j0 = nmain * D; j0 < rows; j0 += D) {
@@ -427,7 +455,8 @@ __global__ void __launch_bounds__(SPB, 2)
             double f[SPT];
             unpack2(myring[u * NT], f);
             D2 g[SPT];
-            inward_row<SPT, CYC>(tab + j * KT, f, st, g);
+            if (CYC && j < W) inward_row<SPT, CYC>(tab + j * KT, f, st, g);
+            else inward_row<SPT, false>(tab + j * KT, f, st, g);
             char* qq = p0 + (long long)j * stepB;
             if (act) st_g<SPT>(qq, g);
             if (j + D < rows) cp_async16(myring + u * NT, qq + pf);
@@ -520,7 +549,8 @@ __global__ void __launch_bounds__(SPB, 2)
       char* q = p0 + (long long)jtop * stepB;
       const long long pf = (long long)D * stepB;
       const float4* row = tab + jtop * KT;
-      for (int b = 0; b < nmain; ++b) {
+      auto block = [&](auto border) {
+        constexpr bool B = decltype(border)::value;
 #pragma unroll
         for (int u = 0; u < D; ++u) {
           cp_wait<D - 1>();
@@ -528,12 +558,39 @@ __global__ void __launch_bounds__(SPB, 2)
           D2 g[SPT] = {D2{__uint_as_float(r.x), __uint_as_float(r.y)},
                        D2{__uint_as_float(r.z), __uint_as_float(r.w)}};
           double x[SPT];
-          outward_row<SPT, CYC>(row, g, st, nx0, nx1, x);
+          outward_row<SPT, B>(row, g, st, nx0, nx1, x);
           if (act) st_x<SPT>(q, x);
           cp_async16(myring + u * NT, q - pf);
           cp_commit();
           q -= stepB;
           row -= KT;
+        }
+      };
+      // blocks b cover local rows jtop - b D .. jtop - b D - (D - 1); those wholly at
+      // rows >= W skip the border term
+      if constexpr (CYC) {
+        const int lowest0 = jtop - (D - 1) - W;   // >= 0: block 0 is border-free
+        int nfree = lowest0 < 0 ? 0 : lowest0 / D + 1;
+        nfree = nfree > nmain ? nmain : nfree;
+        int b = 0;
+        for (; b < nfree; ++b) block(std::false_type{});
+        for (; b < nmain; ++b) block(std::true_type{});
+      } else {
+        for (int b = 0; b < nmain; ++b) {
+#pragma unroll
+          for (int u = 0; u < D; ++u) {
+            cp_wait<D - 1>();
+            const uint4 r = myring[u * NT];
+            D2 g[SPT] = {D2{__uint_as_float(r.x), __uint_as_float(r.y)},
+                         D2{__uint_as_float(r.z), __uint_as_float(r.w)}};
+            double x[SPT];
+            outward_row<SPT, false>(row, g, st, nx0, nx1, x);
+            if (act) st_x<SPT>(q, x);
+            cp_async16(myring + u * NT, q - pf);
+            cp_commit();
+            q -= stepB;
+            row -= KT;
+          }
         }
       }
       for (int j0 = jtop - nmain * D; j0 >= 0; j0 -= D) {
@@ -546,7 +603,8 @@ __global__ void __launch_bounds__(SPB, 2)
             D2 g[SPT] = {D2{__uint_as_float(r.x), __uint_as_float(r.y)},
                          D2{__uint_as_float(r.z), __uint_as_float(r.w)}};
             double x[SPT];
-            outward_row<SPT, CYC>(tab + j * KT, g, st, nx0, nx1, x);
+            if (CYC && j < W) outward_row<SPT, CYC>(tab + j * KT, g, st, nx0, nx1, x);
+            else outward_row<SPT, false>(tab + j * KT, g, st, nx0, nx1, x);
             char* qq = p0 + (long long)j * stepB;
             if (act) st_x<SPT>(qq, x);
             if (j - D >= 0) cp_async16(myring + u * NT, qq - pf);

@@ -181,3 +181,21 @@ def test_batch_smaller_than_plan_and_stream_order():
     s.synchronize()
     ref = oracle.batch_shared(bands, oracle.batch_shared(bands, F), cyclic=False)
     assert max_rel_err(host(X), ref) < TOL_F64
+
+
+@pytest.mark.parametrize("sigma", [0.05, 1.0, 50.0])
+@pytest.mark.parametrize("N", [64, 1000, 2051])
+def test_cyclic_twisted_border_reach(sigma, N, monkeypatch):
+    """The twisted kernel applies the periodic-border terms only in the rows near the
+    two ends where they exceed 2^-60 (few rows for small sigma, all rows for large):
+    parity with the oracle on random right-hand sides."""
+    batch = 512
+    bands = inputs.hyper_bands(N, sigma)
+    F = inputs.rhs_uniform(N, batch, seed=N)
+    ref = oracle.batch_shared(bands, F, cyclic=True)
+    plan = pent.pent_factor(bands, batch, cyclic=True)
+    plan.set_variant("thread_df")
+    X = dev(F)
+    pent.pent_solve(plan, X)
+    assert max_rel_err(host(X), ref) < TOL_F64
+    plan.close()
