@@ -109,7 +109,7 @@ __global__ void k_factor_twisted(const double* __restrict__ bands, int N, int cy
   }
   for (int i = 0; i < 4; ++i)
     for (int j = 0; j < 4; ++j) twist[4 * i + j] = Ti[i][j];
-  twist[16] = twist[17] = twist[18] = twist[19] = twist[20] = 0.0;
+  for (int k = 16; k < kTwistCount; ++k) twist[k] = 0.0;
 
   if (cyclic) {
     const double* A = bands;

@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(SPB, 2)
   constexpr int NT = 2 * TPD;               // threads per CTA
   constexpr int KT = CYC ? kTwK : 3;        // float4 per table row kept in shared memory
   constexpr int NX = CYC ? 8 : 4;
-  extern __shared__ float4 sm_tw[];
+  extern __shared__ __align__(128) float4 sm_tw[];
   float4* stab = sm_tw;                                          // [M][KT]
   uint4* ring = reinterpret_cast<uint4*>(stab + (size_t)M * KT);  // [D][NT]
   __shared__ double sx[TPD][SPT][NX];

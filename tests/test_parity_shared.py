@@ -199,3 +199,16 @@ def test_cyclic_twisted_border_reach(sigma, N, monkeypatch):
     pent.pent_solve(plan, X)
     assert max_rel_err(host(X), ref) < TOL_F64
     plan.close()
+
+
+@pytest.mark.parametrize("depth", ["0", "4", "8", "12"])
+@pytest.mark.parametrize("cyclic", [False, True])
+def test_twisted_prefetch_depths(depth, cyclic, monkeypatch):
+    """The twisted kernel's cp.async ring depths other than the default 6, and the
+    register-ring kernel (PENT_DF_ASYNC=0), against the oracle."""
+    monkeypatch.setenv("PENT_DF_ASYNC", depth)
+    N, batch = 700, 1024
+    bands = inputs.hyper_bands(N, 0.9)
+    F = inputs.rhs_uniform(N, batch, seed=int(depth) + 1)
+    ref = oracle.batch_shared(bands, F, cyclic=cyclic)
+    assert max_rel_err(solve_gpu(bands, F, cyclic, "thread_df"), ref) < TOL_F64
