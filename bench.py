@@ -41,6 +41,9 @@ WORKLOADS = {
                         "bands [1,-4,7,-4,1] (sigma=1), non-cyclic, factor once"),
     "small": dict(N=128, batch=1024, kind="shared", sigma=1.0, cyclic=False, dtype="f64",
                   desc="shared-matrix pentadiagonal solve, N=128, batch=1024, fp64, sigma=1"),
+    "long": dict(N=1 << 20, batch=16, kind="shared", sigma=1.0, cyclic=False, dtype="f64",
+                 desc="shared-matrix pentadiagonal solve of few long systems, N=1048576, batch=16, "
+                      "fp64, sigma=1 (partitioned solve across CTAs)"),
     "cyclic": dict(N=512, batch=4096, kind="hyper", sigma=0.5, cyclic=True, dtype="f64",
                    desc="periodic hyperdiffusion step, cyclic I+0.5*D4, N=512, batch=4096, fp64"),
     "tri": dict(N=256, batch=262144, kind="tri", dtype="f32",
@@ -471,7 +474,7 @@ def run_cpu_baseline(W: dict, seconds: float):
     from implicit_pde_stepping_gb300 import inputs
     N, kind = W["N"], W["kind"]
     if kind == "shared":
-        S = 4096
+        S = max(1, min(4096, (4096 * 1024) // N))   # about 4M rows of work per call
         bands = inputs.hyper_bands(N, W["sigma"])
         F = inputs.rhs_uniform(N, S, seed=0)
         fn = lambda: oracle.batch_shared(bands, F, cyclic=W["cyclic"])  # noqa: E731
@@ -517,6 +520,7 @@ def run_reference(args, W: dict, dist: Dist):
     from implicit_pde_stepping_gb300 import inputs
     N, kind = W["N"], W["kind"]
     S = {"shared": 1024, "hyper": 256, "cn": 256, "ch": 64, "persys": 2048, "tri": 8192}[kind]
+    S = max(1, min(S, (S * 1024) // N))   # long systems: about the same rows per step
     if kind == "shared":
         bands = inputs.hyper_bands(N, W["sigma"])
         F = inputs.rhs_uniform(N, S, seed=0)

@@ -40,7 +40,7 @@ pent_variant resolve(const pent_plan_s& p, int batch) {
   if (p.dtype != PENT_F64) return PENT_VARIANT_THREAD;
   const long long fill = 160LL * (p.num_sms > 0 ? p.num_sms : 1);
   if (p.twist_ok && batch % 2 == 0 && batch >= fill) return PENT_VARIANT_THREAD_DF;
-  if (p.split_ok) return PENT_VARIANT_SPLIT;
+  if (p.split_ok || p.split_big) return PENT_VARIANT_SPLIT;   // long systems: two-kernel form
   if (p.twist_ok) return PENT_VARIANT_THREAD_DF;
   return PENT_VARIANT_THREAD;
 }
@@ -53,7 +53,7 @@ bool variant_exists(const pent_plan_s& p, pent_variant v) {
     case PENT_VARIANT_THREAD_DF:
       return p.dtype == PENT_F64 && p.twist_ok;
     case PENT_VARIANT_SPLIT:
-      return p.dtype == PENT_F64 && p.split_ok;
+      return p.dtype == PENT_F64 && (p.split_ok || p.split_big);
     default:
       return false;
   }
@@ -85,7 +85,9 @@ cudaError_t solve_device(pent_plan_s& p, void* rhs, int batch, cudaStream_t st) 
   switch (v) {
     case PENT_VARIANT_THREAD: return shared_thread_f64(p, static_cast<double*>(rhs), batch, st);
     case PENT_VARIANT_THREAD_DF: return shared_twisted_df(p, static_cast<double*>(rhs), batch, st);
-    case PENT_VARIANT_SPLIT: return shared_split_df(p, static_cast<double*>(rhs), batch, st);
+    case PENT_VARIANT_SPLIT:
+      return p.split_ok ? shared_split_df(p, static_cast<double*>(rhs), batch, st)
+                        : shared_split_big(p, static_cast<double*>(rhs), batch, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -119,6 +121,7 @@ pent_status pent_sync(void* stream) {
 void pent_destroy(pent_plan p) {
   if (!p) return;
   host_pipeline_release(*p);
+  if (p->spsum) cudaFree(p->spsum);
   if (p->arena) cudaFree(p->arena);
   delete p;
 }
@@ -227,7 +230,9 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
     const int SB = (cyclic && spL == 32 && spP <= 32) ? 16 : 8;
     const bool fits = split_smem_bytes(spL, spP, SB, cyclic) <= 200 * 1024 && SB * spP <= 1024 && spP <= kSpMaxChunks &&
                       !(cyclic && spL == 32 && spP > 32);
-    if (dtype == PENT_F64 && p->M >= 16 && fits) {
+    // tables for every fp64 plan of 16 rows or more: one kernel (tables in shared
+    // memory) where they fit, else the two-kernel form for long systems
+    if (dtype == PENT_F64 && p->M >= 16) {
       p->sp_L = spL;
       p->sp_P = spP;
       int sstatus = 0;
@@ -239,7 +244,8 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
         pent_destroy(p);
         return from_cuda(e);
       }
-      p->split_ok = (sstatus == 0);
+      const bool tables = (sstatus == 0);
+      p->split_ok = tables && fits;
       // PENT_SPLIT_T=0 forces the exact serial chunk scan (testing)
       if (p->split_ok && std::getenv("PENT_SPLIT_T") && env_int("PENT_SPLIT_T", -1) == 0) {
         const double zero = 0.0;
@@ -251,7 +257,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
         }
       }
       // PENT_BORDER_ALL=1 applies the x_t correction in every chunk (testing)
-      if (p->split_ok && cyclic && env_int("PENT_BORDER_ALL", 0) == 1) {
+      if (tables && cyclic && env_int("PENT_BORDER_ALL", 0) == 1) {
         const double all = (double)spP;
         e = cudaMemcpy(p->spextra + 19, &all, sizeof(double), cudaMemcpyHostToDevice);
         if (e != cudaSuccess) {
@@ -260,7 +266,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
           return from_cuda(e);
         }
       }
-      if (p->split_ok) {
+      if (tables) {
         double Td = 0.0;
         e = cudaMemcpy(&Td, p->spextra + 18, sizeof(double), cudaMemcpyDeviceToHost);
         if (e != cudaSuccess) {
@@ -269,6 +275,8 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
           return from_cuda(e);
         }
         p->sp_T = (int)Td;
+        // the two-kernel form needs the truncated chunk couplings
+        p->split_big = !fits && p->sp_T > 0;
       }
     }
   }

@@ -6,13 +6,17 @@
 //   - Navon's bordering of the cyclic matrix (7c), eqs. (8)–(12): the page
 //     stores the 2x2 inverse of eq. (12) and h^T E^{-1} once at start-up.
 //
-// The work is O(N) and serial, done once per plan, so one thread runs it.
+// The work is O(N) and serial, done once per plan, so one thread runs it.  The
+// sweeps go in blocks of kPre rows whose inputs are loaded before the block is
+// computed, so the thread waits for memory once per block, not once per row.
 #include <cmath>
 
 #include "pent_internal.cuh"
 
 namespace pent {
 namespace {
+
+constexpr int kPre = 8;
 
 __global__ void k_factor_shared(const double* __restrict__ bands, int N, int cyclic,
                                 double* __restrict__ coef, double* __restrict__ tail,
@@ -38,27 +42,42 @@ __global__ void k_factor_shared(const double* __restrict__ bands, int N, int cyc
   // Leading M x M block (the whole matrix when non-cyclic): entries whose
   // column leaves 0..M-1 belong to the border (cyclic) or do not exist.
   double gm1 = 0.0, gm2 = 0.0, dm1 = 0.0, dm2 = 0.0;
-  for (int i = 0; i < M; ++i) {
-    const double ai = (i >= 2) ? A[i] : 0.0;
-    const double bi = (i >= 1) ? B[i] : 0.0;
-    const double di = (i + 1 < M) ? D[i] : 0.0;
-    const double ei = (i + 2 < M) ? E[i] : 0.0;
-    const double beta = bi - ai * gm2;                       // step 8.1
-    const double alpha = C[i] - ai * dm2 - beta * gm1;       // step 8.2
-    if (!(alpha != 0.0) || !isfinite(alpha)) {
-      *status = i + 1;
-      return;
+  for (int i0 = 0; i0 < M; i0 += kPre) {
+    double av[kPre], bv[kPre], cv[kPre], dv[kPre], ev[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int i = i0 + u;
+      av[u] = (i >= 2 && i < M) ? A[i] : 0.0;
+      bv[u] = (i >= 1 && i < M) ? B[i] : 0.0;
+      cv[u] = (i < M) ? C[i] : 1.0;
+      dv[u] = (i + 1 < M) ? D[i] : 0.0;
+      ev[u] = (i + 2 < M) ? E[i] : 0.0;
     }
-    const double g = (di - beta * dm1) / alpha;              // step 8.3
-    const double dd = ei / alpha;                            // step 8.4
-    r[i] = 1.0 / alpha;
-    p[i] = ai / alpha;                                       // eps_i = a_i (step 14)
-    q[i] = beta / alpha;
-    gam[i] = g;
-    del[i] = dd;
-    w0[i] = w1[i] = u0[i] = u1[i] = 0.0;
-    gm2 = gm1; gm1 = g;
-    dm2 = dm1; dm1 = dd;
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int i = i0 + u;
+      if (i >= M) break;
+      const double ai = av[u], bi = bv[u], di = dv[u], ei = ev[u];
+      const double beta = bi - ai * gm2;                       // step 8.1
+      const double alpha = cv[u] - ai * dm2 - beta * gm1;      // step 8.2
+      if (!(alpha != 0.0) || !isfinite(alpha)) {
+        *status = i + 1;
+        return;
+      }
+      // one division per row (the fp64 division is the slow step of this
+      // serial sweep); the page's quotients become products with 1/alpha
+      const double ra = 1.0 / alpha;
+      const double g = (di - beta * dm1) * ra;                 // step 8.3
+      const double dd = ei * ra;                               // step 8.4
+      r[i] = ra;
+      p[i] = ai * ra;                                          // eps_i = a_i (step 14)
+      q[i] = beta * ra;
+      gam[i] = g;
+      del[i] = dd;
+      w0[i] = w1[i] = u0[i] = u1[i] = 0.0;
+      gm2 = gm1; gm1 = g;
+      dm2 = dm1; dm1 = dd;
+    }
   }
   if (!cyclic) return;
 
@@ -90,12 +109,23 @@ __global__ void k_factor_shared(const double* __restrict__ bands, int N, int cyc
     const double* h = k ? h1 : h0;
     double* w = k ? w1 : w0;
     double wm1 = 0.0, wm2 = 0.0;
-    for (int i = 0; i < M; ++i) {
-      const double gi1 = (i >= 1) ? gam[i - 1] : 0.0;
-      const double di2 = (i >= 2) ? del[i - 2] : 0.0;
-      const double wi = h[i] - gi1 * wm1 - di2 * wm2;
-      w[i] = wi;
-      wm2 = wm1; wm1 = wi;
+    for (int i0 = 0; i0 < M; i0 += kPre) {
+      double hv[kPre], gv[kPre], dv[kPre];
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        const int i = i0 + u;
+        hv[u] = (i < M) ? h[i] : 0.0;
+        gv[u] = (i >= 1 && i < M) ? gam[i - 1] : 0.0;
+        dv[u] = (i >= 2 && i < M) ? del[i - 2] : 0.0;
+      }
+#pragma unroll
+      for (int u = 0; u < kPre; ++u) {
+        const int i = i0 + u;
+        if (i >= M) break;
+        const double wi = hv[u] - gv[u] * wm1 - dv[u] * wm2;
+        w[i] = wi;
+        wm2 = wm1; wm1 = wi;
+      }
     }
   }
   // u_k = E^{-1} G_k (eq. (11)): forward then back substitution with E's factors.
@@ -103,20 +133,50 @@ __global__ void k_factor_shared(const double* __restrict__ bands, int N, int cyc
     const double* gcol = k ? g1 : g0;
     double* u = k ? u1 : u0;
     double y1 = 0.0, y2 = 0.0;
-    for (int i = 0; i < M; ++i) {
-      const double y = r[i] * gcol[i] - p[i] * y2 - q[i] * y1;
-      u[i] = y;
-      y2 = y1; y1 = y;
+    for (int i0 = 0; i0 < M; i0 += kPre) {
+      double rv[kPre], fv[kPre], pv[kPre], qv[kPre];
+#pragma unroll
+      for (int u2 = 0; u2 < kPre; ++u2) {
+        const int i = i0 + u2;
+        const bool in = i < M;
+        rv[u2] = in ? r[i] : 0.0;
+        fv[u2] = in ? gcol[i] : 0.0;
+        pv[u2] = in ? p[i] : 0.0;
+        qv[u2] = in ? q[i] : 0.0;
+      }
+#pragma unroll
+      for (int u2 = 0; u2 < kPre; ++u2) {
+        const int i = i0 + u2;
+        if (i >= M) break;
+        const double y = rv[u2] * fv[u2] - pv[u2] * y2 - qv[u2] * y1;
+        u[i] = y;
+        y2 = y1; y1 = y;
+      }
     }
     double x1 = 0.0, x2 = 0.0;
-    for (int i = M - 1; i >= 0; --i) {
-      const double x = u[i] - gam[i] * x1 - del[i] * x2;
-      u[i] = x;
-      x2 = x1; x1 = x;
+    for (int i0 = M - 1; i0 >= 0; i0 -= kPre) {
+      double yv[kPre], gv[kPre], dv[kPre];
+#pragma unroll
+      for (int u2 = 0; u2 < kPre; ++u2) {
+        const int i = i0 - u2;
+        const bool in = i >= 0;
+        yv[u2] = in ? u[i] : 0.0;
+        gv[u2] = in ? gam[i] : 0.0;
+        dv[u2] = in ? del[i] : 0.0;
+      }
+#pragma unroll
+      for (int u2 = 0; u2 < kPre; ++u2) {
+        const int i = i0 - u2;
+        if (i < 0) break;
+        const double x = yv[u2] - gv[u2] * x1 - dv[u2] * x2;
+        u[i] = x;
+        x2 = x1; x1 = x;
+      }
     }
   }
   // S = B - H^T E^{-1} G (eq. (12)) and its inverse.
   double S00 = B00, S01 = B01, S10 = B10, S11 = B11;
+#pragma unroll 8
   for (int i = 0; i < M; ++i) {
     S00 -= h0[i] * u0[i];
     S01 -= h0[i] * u1[i];

@@ -32,7 +32,8 @@ __global__ void __launch_bounds__(kFactorThreads)
                    double* __restrict__ extra, double* __restrict__ w, int* __restrict__ status) {
   __shared__ int s_fail;
   __shared__ double s_B[2][2];
-  __shared__ double s_tail[2][kSpMaxChunks][kSpTmax + 1];
+  __shared__ double s_red[kFactorThreads][2 * kSpTmax];
+  __shared__ double s_q[2];
   const int tid = threadIdx.x, nt = blockDim.x;
   const int M = cyclic ? N - 2 : N;
   const int P = Mpad / L;
@@ -107,23 +108,55 @@ __global__ void __launch_bounds__(kFactorThreads)
       const int k = tid;
       const double* gc = k ? g1 : g0;
       double* u = k ? u1 : u0;
+      // blocks of 8 rows, inputs loaded ahead (one memory wait per block)
+      constexpr int kPre = 8;
       double y1 = 0.0, y2 = 0.0;
-      for (int i = 0; i < M; ++i) {
-        const double y = (gc[i] - ep[i] * y2 - be[i] * y1) / al[i];
-        u[i] = y;
-        y2 = y1; y1 = y;
+      for (int i0 = 0; i0 < M; i0 += kPre) {
+        double fv[kPre], ev[kPre], bv[kPre], av[kPre];
+#pragma unroll
+        for (int q2 = 0; q2 < kPre; ++q2) {
+          const int i = i0 + q2;
+          const bool in = i < M;
+          fv[q2] = in ? gc[i] : 0.0;
+          ev[q2] = in ? ep[i] : 0.0;
+          bv[q2] = in ? be[i] : 0.0;
+          av[q2] = in ? 1.0 / al[i] : 1.0;         // off the recurrence's chain
+        }
+#pragma unroll
+        for (int q2 = 0; q2 < kPre; ++q2) {
+          const int i = i0 + q2;
+          if (i >= M) break;
+          const double y = (fv[q2] - ev[q2] * y2 - bv[q2] * y1) * av[q2];
+          u[i] = y;
+          y2 = y1; y1 = y;
+        }
       }
       double x1 = 0.0, x2 = 0.0;
-      for (int i = M - 1; i >= 0; --i) {
-        const double x = u[i] - ga[i] * x1 - de[i] * x2;
-        u[i] = x;
-        x2 = x1; x1 = x;
+      for (int i0 = M - 1; i0 >= 0; i0 -= kPre) {
+        double yv[kPre], gv[kPre], dv[kPre];
+#pragma unroll
+        for (int q2 = 0; q2 < kPre; ++q2) {
+          const int i = i0 - q2;
+          const bool in = i >= 0;
+          yv[q2] = in ? u[i] : 0.0;
+          gv[q2] = in ? ga[i] : 0.0;
+          dv[q2] = in ? de[i] : 0.0;
+        }
+#pragma unroll
+        for (int q2 = 0; q2 < kPre; ++q2) {
+          const int i = i0 - q2;
+          if (i < 0) break;
+          const double x = yv[q2] - gv[q2] * x1 - dv[q2] * x2;
+          u[i] = x;
+          x2 = x1; x1 = x;
+        }
       }
     }
     __syncthreads();
     if (tid == 0) {
       // S = B - H^T E^{-1} G (eq. (12))
       double S00 = s_B[0][0], S01 = s_B[0][1], S10 = s_B[1][0], S11 = s_B[1][1];
+#pragma unroll 8
       for (int i = 0; i < M; ++i) {
         S00 -= h0[i] * u0[i]; S01 -= h0[i] * u1[i];
         S10 -= h1[i] * u0[i]; S11 -= h1[i] * u1[i];
@@ -174,45 +207,91 @@ __global__ void __launch_bounds__(kFactorThreads)
   };
   auto nrm = [](const double* A) { return fmax(fabs(A[0]) + fabs(A[1]), fabs(A[2]) + fabs(A[3])); };
   const double tiny = ldexp(1.0, -64);
-  double nA[kSpMaxChunks + 1], nB[kSpMaxChunks + 1];
+  // Products are formed explicitly up to kCap maps; beyond that the remaining
+  // terms are bounded geometrically by the largest map norm q (< 1 needed).
+  constexpr int kCap = 64;
+  double qa = 0.0, qb = 0.0;
+  for (int c = tid; c < P; c += nt) {
+    qa = fmax(qa, nrm(chunktab + (size_t)c * kSpChunk));
+    qb = fmax(qb, nrm(chunktab + (size_t)c * kSpChunk + 8));
+  }
+  s_red[tid][0] = qa;
+  s_red[tid][1] = qb;
+  __syncthreads();
+  if (tid == 0) {
+    for (int k = 1; k < nt; ++k) {
+      qa = fmax(qa, s_red[k][0]);
+      qb = fmax(qb, s_red[k][1]);
+    }
+    s_q[0] = qa;
+    s_q[1] = qb;
+  }
+  __syncthreads();
+  qa = s_q[0];
+  qb = s_q[1];
+  const double inf = (double)INFINITY;
+  double ta[kSpTmax + 1], tb[kSpTmax + 1];
+  for (int t = 0; t <= kSpTmax; ++t) ta[t] = tb[t] = 0.0;
   for (int c = tid; c < P; c += nt) {
     double* ct = chunktab + (size_t)c * kSpChunk;
     for (int k = 12; k < kSpChunk; ++k) ct[k] = 0.0;
-    // forward: A_{c,k} = Phi_{c-1}..Phi_{c-k+1}, k = 2..c (A_{c,1} = I)
+    double sa[kSpTmax + 1], sb[kSpTmax + 1];
+    for (int t = 0; t <= kSpTmax; ++t) sa[t] = sb[t] = 0.0;
+    // forward: A_{c,k} = Phi_{c-1}..Phi_{c-k+1}, k = 2..c (A_{c,1} = I); the
+    // scan keeping T couplings drops sum_{k > T} ||A_{c,k}||
     double Acc[4] = {1.0, 0.0, 0.0, 1.0};
-    for (int k = 2; k <= c; ++k) {
+    double n = 1.0;
+    const int ka = c < kCap ? c : kCap;
+    for (int k = 2; k <= ka; ++k) {
       mul(Acc, chunktab + (size_t)(c - k + 1) * kSpChunk, Acc);
       if (k <= kSpTmax)
         for (int q2 = 0; q2 < 4; ++q2) ct[12 + 4 * (k - 2) + q2] = Acc[q2];
-      nA[k] = nrm(Acc);
+      n = nrm(Acc);
+      for (int t = 1; t <= kSpTmax; ++t)
+        if (k >= t + 1) sa[t] += n;
     }
-    // backward: B_{c,k} = Kst_{c+1}..Kst_{c+k}, k = 1..P-2-c (B_{c,0} = I)
+    if (c > ka) {                                   // terms k = ka+1..c
+      const double rest = qa < 1.0 ? n * qa / (1.0 - qa) : inf;
+      for (int t = 1; t <= kSpTmax; ++t) sa[t] += rest;
+    }
+    // backward: B_{c,k} = Kst_{c+1}..Kst_{c+k}, k = 1..P-2-c (B_{c,0} = I);
+    // dropped: sum_{k >= T} ||B_{c,k}||
     double Bcc[4] = {1.0, 0.0, 0.0, 1.0};
-    for (int k = 1; k <= P - 2 - c; ++k) {
+    n = 1.0;
+    const int kbmax = P - 2 - c;
+    const int kb = kbmax < kCap ? kbmax : kCap;
+    for (int k = 1; k <= kb; ++k) {
       mul(Bcc, chunktab + (size_t)(c + k) * kSpChunk + 8, Bcc);
       if (k <= kSpTmax - 1)
         for (int q2 = 0; q2 < 4; ++q2) ct[24 + 4 * (k - 1) + q2] = Bcc[q2];
-      nB[k] = nrm(Bcc);
+      n = nrm(Bcc);
+      for (int t = 1; t <= kSpTmax; ++t)
+        if (k >= t) sb[t] += n;
     }
-    // summed norms of the terms a scan keeping T couplings drops
+    if (kbmax > kb) {
+      const double rest = qb < 1.0 ? n * qb / (1.0 - qb) : inf;
+      for (int t = 1; t <= kSpTmax; ++t) sb[t] += rest;
+    }
     for (int t = 1; t <= kSpTmax; ++t) {
-      double sa = 0.0, sb = 0.0;
-      for (int k = t + 1; k <= c; ++k) sa += nA[k];
-      for (int k = t; k <= P - 2 - c; ++k) sb += nB[k];
-      s_tail[0][c][t] = sa;
-      s_tail[1][c][t] = sb;
+      ta[t] = fmax(ta[t], sa[t]);
+      tb[t] = fmax(tb[t], sb[t]);
     }
+  }
+  __syncthreads();
+  for (int t = 1; t <= kSpTmax; ++t) {
+    s_red[tid][2 * (t - 1)] = ta[t];
+    s_red[tid][2 * (t - 1) + 1] = tb[t];
   }
   __syncthreads();
   if (tid == 0) {
     int T = 0;
     for (int t = 1; t <= kSpTmax && T == 0; ++t) {
-      double ta = 0.0, tb = 0.0;
-      for (int c = 0; c < P; ++c) {
-        ta = fmax(ta, s_tail[0][c][t]);
-        tb = fmax(tb, s_tail[1][c][t]);
+      double a = 0.0, b = 0.0;
+      for (int k = 0; k < nt; ++k) {
+        a = fmax(a, s_red[k][2 * (t - 1)]);
+        b = fmax(b, s_red[k][2 * (t - 1) + 1]);
       }
-      if (ta <= tiny && tb <= tiny) T = t;
+      if (a <= tiny && b <= tiny) T = t;
     }
     extra[18] = (double)T;
     // Border reach: U = E^{-1} G decays away from the two ends of the block;

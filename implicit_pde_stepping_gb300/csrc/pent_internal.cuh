@@ -52,6 +52,9 @@ struct pent_plan_s {
   int split_ok = 0;          // tables valid
   int sp_L = 0, sp_P = 0;    // chunk length, chunks per system (Mpad = sp_L * sp_P)
   int sp_T = 0;              // chunk couplings kept by the parallel scan (0: exact serial scan)
+  int split_big = 0;         // tables valid for the two-kernel form (systems too long for one CTA)
+  double* spsum = nullptr;   // two-kernel form: per system and chunk summaries, grown on use
+  size_t spsum_bytes = 0;
   float4* sptab = nullptr;   // [Mpad][kSpK]
   double* spchunk = nullptr; // [sp_P][kSpChunk]
   double* spextra = nullptr; // [kSpExtra]
@@ -168,6 +171,8 @@ cudaError_t factor_split(const double* d_bands, int N, int cyclic, int L, int Mp
                          double* chunktab, double* extra, double* d_work, int* d_status,
                          cudaStream_t st);
 cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
+// pent_split_big.cu: the same solve for systems too long for one CTA (two kernels)
+cudaError_t shared_split_big(pent_plan_s& p, double* X, int batch, cudaStream_t st);
 size_t split_smem_bytes(int L, int P, int SB, int cyclic);
 cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);
 cudaError_t cn_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);

@@ -24,19 +24,31 @@ __device__ inline double band(const double* bands, int N, int M, int k, int j, b
 // rows 0..R-1: alpha, beta, gamma, delta, eps (= a).  false on a zero pivot.
 __device__ inline bool factor_rows(const double* bands, int N, int M, int R, bool rev, double* al,
                                    double* be, double* ga, double* de, double* ep) {
+  // blocks of 8 rows whose bands are loaded before they are used, so the
+  // thread waits for memory once per block
+  constexpr int kPre = 8;
   double gm1 = 0.0, gm2 = 0.0, dm1 = 0.0, dm2 = 0.0;
-  for (int j = 0; j < R; ++j) {
-    const double a = band(bands, N, M, 0, j, rev), b = band(bands, N, M, 1, j, rev);
-    const double c = band(bands, N, M, 2, j, rev), d = band(bands, N, M, 3, j, rev);
-    const double e = band(bands, N, M, 4, j, rev);
-    const double beta = b - a * gm2;                 // step 8.1
-    const double alpha = c - a * dm2 - beta * gm1;   // step 8.2
-    if (!(alpha != 0.0) || !isfinite(alpha)) return false;
-    const double g = (d - beta * dm1) / alpha;       // step 8.3
-    const double dd = e / alpha;                     // step 8.4
-    al[j] = alpha; be[j] = beta; ga[j] = g; de[j] = dd; ep[j] = a;
-    gm2 = gm1; gm1 = g;
-    dm2 = dm1; dm1 = dd;
+  for (int j0 = 0; j0 < R; j0 += kPre) {
+    double bv[5][kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u)
+#pragma unroll
+      for (int k = 0; k < 5; ++k) bv[k][u] = (j0 + u < R) ? band(bands, N, M, k, j0 + u, rev) : 0.0;
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int j = j0 + u;
+      if (j >= R) break;
+      const double a = bv[0][u], b = bv[1][u], c = bv[2][u], d = bv[3][u], e = bv[4][u];
+      const double beta = b - a * gm2;                 // step 8.1
+      const double alpha = c - a * dm2 - beta * gm1;   // step 8.2
+      if (!(alpha != 0.0) || !isfinite(alpha)) return false;
+      const double ra = 1.0 / alpha;                   // one division per row
+      const double g = (d - beta * dm1) * ra;          // step 8.3
+      const double dd = e * ra;                        // step 8.4
+      al[j] = alpha; be[j] = beta; ga[j] = g; de[j] = dd; ep[j] = a;
+      gm2 = gm1; gm1 = g;
+      dm2 = dm1; dm1 = dd;
+    }
   }
   return true;
 }

@@ -1,0 +1,285 @@
+// Partitioned double-float solve for systems too long for one CTA.
+//
+// The mathematics of pent_split_df.cu (cuPentBatch's forward substitution
+// L g = f and back substitution R x = g per chunk of L rows, chunk boundary
+// states s_c, t_c by the truncated chunk-coupling scan, Navon's bordering,
+// eqs. (8)–(12), for periodic plans), split over kernels because a system's
+// P chunks no longer fit in one CTA:
+//   k_big_local   one thread per (system, chunk): load f, local forward and back
+//                 substitution with zero boundary states; x' (double-float pair,
+//                 8 bytes) goes back in place of f; summaries e_c (local forward
+//                 end values) and x'_start(c) go to a small array;
+//   k_big_states  one thread per (system, chunk): s_c = sum_k A_{c,k} e_{c-k},
+//                 w_c = x'_start(c) + Mst_c s_c;
+//   k_big_border  periodic plans, one thread per system: t at chunk 0 and at the
+//                 chunks holding rows M-2, M-1, y at rows 0, 1, M-2, M-1 and
+//                 x_t = S^{-1}(f_t - H^T y), written to rows M, M+1;
+//   k_big_fix     one thread per (system, chunk): t_c = sum_k B_{c,k} w_{c+1+k},
+//                 x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 (- U x_t), stored in fp64.
+// Memory traffic: f read, x' written and read, x written (four arrays, as the
+// twisted kernel), plus summaries of 64 bytes per chunk.  The parallelism is
+// batch x P threads, so a handful of very long systems still fills the GPU.
+#include "df64.cuh"
+#include "pent_internal.cuh"
+
+namespace pent {
+namespace {
+
+using df::D2;
+
+constexpr int kBigL = 32;       // rows per chunk (the plan's sp_L for long systems)
+constexpr int kBigThreads = 256;
+constexpr int kSum = 8;         // doubles per (chunk, system): e(2) x'start(2) s(2) w(2)
+
+__device__ __forceinline__ void mv2(const double* A, double x0, double x1, double& y0, double& y1) {
+  y0 = fma(A[0], x0, fma(A[1], x1, y0));
+  y1 = fma(A[2], x0, fma(A[3], x1, y1));
+}
+
+// (system, chunk) of this thread: SPW consecutive systems per warp row, so a
+// load instruction covers SPW * 8 bytes of each of 32 / SPW rows
+template <int SPW>
+__device__ __forceinline__ void place(int& s, int& c) {
+  constexpr int CPW = 32 / SPW;                      // chunks per warp
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  s = blockIdx.y * SPW + lane % SPW;
+  c = (blockIdx.x * (kBigThreads / 32) + w) * CPW + lane / SPW;
+}
+
+template <int SPW, bool CYC>
+__global__ void __launch_bounds__(kBigThreads)
+    k_big_local(const float4* __restrict__ tab, double* __restrict__ X, double* __restrict__ sum,
+                double* __restrict__ xm, int M, int P, int batch) {
+  constexpr int L = kBigL;
+  int s, c;
+  place<SPW>(s, c);
+  if (s >= batch || c >= P) return;
+  const long long ld = batch;
+  const int row0 = c * L;
+  double* p = X + (long long)row0 * ld + s;
+  const float4* t = tab + (size_t)row0 * kSpK;
+  D2 v[L];
+  {
+    double fv[L];
+#pragma unroll
+    for (int j = 0; j < L; ++j) fv[j] = (row0 + j < M) ? p[j * ld] : 0.0;
+    D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+      const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
+      const D2 g = df::sum3p(D2{c0.x, c0.y}, df::from_double(fv[j]), D2{c0.z, c0.w}, a2,
+                             D2{c1.x, c1.y}, a1);
+      v[j] = g;
+      a2 = a1;
+      a1 = g;
+    }
+  }
+  double* o = sum + ((size_t)c * batch + s) * kSum;
+  o[0] = df::to_double(v[L - 2]);
+  o[1] = df::to_double(v[L - 1]);
+  {
+    D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+#pragma unroll
+    for (int j = L - 1; j >= 0; --j) {
+      const float4 c2 = __ldg(t + j * kSpK + 2);
+      const D2 y = df::sum3(v[j], D2{c2.x, c2.y}, a1, D2{c2.z, c2.w}, a2);
+      v[j] = y;
+      a2 = a1;
+      a1 = y;
+    }
+  }
+  o[2] = df::to_double(v[0]);
+  o[3] = df::to_double(v[1]);
+  if (CYC) {                                      // x' at rows M-2, M-1 for the border
+#pragma unroll
+    for (int j = 0; j < L; ++j) {
+      if (row0 + j == M - 2) xm[(size_t)s * 2] = df::to_double(v[j]);
+      if (row0 + j == M - 1) xm[(size_t)s * 2 + 1] = df::to_double(v[j]);
+    }
+  }
+  float2* q = reinterpret_cast<float2*>(p);       // x' in place of f, as (hi, lo)
+#pragma unroll
+  for (int j = 0; j < L; ++j)
+    if (row0 + j < M) q[j * ld] = make_float2(v[j].h, v[j].l);
+}
+
+// s_c from the local end values of the T chunks before c
+__device__ __forceinline__ void state_s(const double* __restrict__ ctab, const double* __restrict__ sum,
+                                        int c, int s, int batch, int T, double& s0, double& s1) {
+  const double* ct = ctab + (size_t)c * kSpChunk;
+  s0 = s1 = 0.0;
+  for (int k = 1; k <= T && k <= c; ++k) {
+    const double* e = sum + ((size_t)(c - k) * batch + s) * kSum;
+    if (k == 1) { s0 += e[0]; s1 += e[1]; }
+    else mv2(ct + 12 + 4 * (k - 2), e[0], e[1], s0, s1);
+  }
+}
+
+// t_c from w of the T chunks after c
+__device__ __forceinline__ void state_t(const double* __restrict__ ctab, const double* __restrict__ sum,
+                                        int c, int s, int P, int batch, int T, double& t0, double& t1) {
+  const double* ct = ctab + (size_t)c * kSpChunk;
+  t0 = t1 = 0.0;
+  for (int k = 0; k < T && c + 1 + k < P; ++k) {
+    const double* w = sum + ((size_t)(c + 1 + k) * batch + s) * kSum + 6;
+    if (k == 0) { t0 += w[0]; t1 += w[1]; }
+    else mv2(ct + 24 + 4 * (k - 1), w[0], w[1], t0, t1);
+  }
+}
+
+__global__ void __launch_bounds__(kBigThreads)
+    k_big_states(const double* __restrict__ ctab, const double* __restrict__ extra, double* __restrict__ sum,
+                 int P, int batch) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)P * batch) return;
+  const int c = (int)(i / batch), s = (int)(i % batch);
+  const int T = (int)extra[18];
+  double s0, s1;
+  state_s(ctab, sum, c, s, batch, T, s0, s1);
+  double* o = sum + (size_t)i * kSum;
+  double w0 = o[2], w1 = o[3];
+  mv2(ctab + (size_t)c * kSpChunk + 4, s0, s1, w0, w1);   // w_c = x'_start + Mst_c s_c
+  o[4] = s0;
+  o[5] = s1;
+  o[6] = w0;
+  o[7] = w1;
+}
+
+__global__ void __launch_bounds__(kBigThreads)
+    k_big_border(const double* __restrict__ ctab, const double* __restrict__ extra,
+                 const double* __restrict__ sum, const double* __restrict__ xm, double* __restrict__ X,
+                 int M, int P, int batch) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= batch) return;
+  const long long ld = batch;
+  const int T = (int)extra[18];
+  // y at rows 0, 1: chunk 0 has s_0 = 0, so y = w_0 + Kst_0 t_0
+  double t0, t1;
+  state_t(ctab, sum, 0, s, P, batch, T, t0, t1);
+  const double* o0 = sum + (size_t)s * kSum;
+  double y0 = o0[6], y1 = o0[7];
+  mv2(ctab + 8, t0, t1, y0, y1);
+  // y at rows M-2, M-1 from their chunks' s and t
+  double yv[2];
+  for (int r = 0; r < 2; ++r) {
+    const int row = M - 2 + r, c = row / kBigL;
+    const double* oc = sum + ((size_t)c * batch + s) * kSum;
+    double u0, u1;
+    state_t(ctab, sum, c, s, P, batch, T, u0, u1);
+    const double* mk = extra + 10 + 2 * r;   // M1, M2 at the row; K1, K2 four slots on
+    yv[r] = xm[(size_t)s * 2 + r] + mk[0] * oc[4] + mk[1] * oc[5] + mk[4] * u0 + mk[5] * u1;
+  }
+  const double r0 = extra[4] * yv[0] + extra[5] * yv[1] + extra[6] * y0;
+  const double r1 = extra[7] * yv[1] + extra[8] * y0 + extra[9] * y1;
+  const double f0 = X[(long long)M * ld + s], f1 = X[(long long)(M + 1) * ld + s];
+  X[(long long)M * ld + s] = extra[0] * (f0 - r0) + extra[1] * (f1 - r1);
+  X[(long long)(M + 1) * ld + s] = extra[2] * (f0 - r0) + extra[3] * (f1 - r1);
+}
+
+template <int SPW, bool CYC>
+__global__ void __launch_bounds__(kBigThreads)
+    k_big_fix(const float4* __restrict__ tab, const double* __restrict__ ctab,
+              const double* __restrict__ extra, const double* __restrict__ sum, double* __restrict__ X,
+              int M, int P, int batch) {
+  constexpr int L = kBigL;
+  int s, c;
+  place<SPW>(s, c);
+  if (s >= batch || c >= P) return;
+  const long long ld = batch;
+  const int row0 = c * L;
+  if (row0 >= M) return;
+  const int T = (int)extra[18];
+  const double* o = sum + ((size_t)c * batch + s) * kSum;
+  double t0, t1;
+  state_t(ctab, sum, c, s, P, batch, T, t0, t1);
+  const D2 S0 = df::from_double(o[4]), S1 = df::from_double(o[5]);
+  const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
+  bool needU = false;
+  D2 X0{0.f, 0.f}, X1{0.f, 0.f};
+  if (CYC) {
+    const int reach = (int)extra[19];
+    needU = c < reach || c > (M - 1) / L - reach;
+    X0 = df::from_double(-X[(long long)M * ld + s]);
+    X1 = df::from_double(-X[(long long)(M + 1) * ld + s]);
+  }
+  double* p = X + (long long)row0 * ld + s;
+  const float2* q = reinterpret_cast<const float2*>(p);
+  const float4* t = tab + (size_t)row0 * kSpK;
+  constexpr int G = 8;
+#pragma unroll
+  for (int j0 = 0; j0 < L; j0 += G) {
+    float2 xv[G];
+#pragma unroll
+    for (int u = 0; u < G; ++u) xv[u] = (row0 + j0 + u < M) ? q[(j0 + u) * ld] : make_float2(0.f, 0.f);
+#pragma unroll
+    for (int u = 0; u < G; ++u) {
+      const int j = j0 + u;
+      const float4 c3 = __ldg(t + j * kSpK + 3), c4 = __ldg(t + j * kSpK + 4);
+      D2 x = df::axpy(D2{xv[u].x, xv[u].y}, D2{c3.x, c3.y}, S0);
+      x = df::axpy(x, D2{c3.z, c3.w}, S1);
+      x = df::axpy(x, D2{c4.x, c4.y}, T0);
+      x = df::axpy(x, D2{c4.z, c4.w}, T1);
+      if (CYC && needU) {
+        const float4 c1 = __ldg(t + j * kSpK + 1), c5 = __ldg(t + j * kSpK + 5);
+        x = df::axpy(x, D2{c1.z, c1.w}, X0);
+        x = df::axpy(x, D2{c5.x, c5.y}, X1);
+      }
+      if (row0 + j < M) __stcs(p + j * ld, df::to_double(x));
+    }
+  }
+}
+
+template <int SPW, bool CYC>
+cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+  const int P = p.sp_P;
+  constexpr int CPB = (kBigThreads / 32) * (32 / SPW);     // chunks per CTA
+  const dim3 grid((P + CPB - 1) / CPB, (batch + SPW - 1) / SPW);
+  double* xm = p.spsum + (size_t)P * batch * kSum;
+  k_big_local<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, X, p.spsum, xm, p.M, P, batch);
+  note_launch();
+  const long long n = (long long)P * batch;
+  k_big_states<<<(unsigned)((n + kBigThreads - 1) / kBigThreads), kBigThreads, 0, st>>>(
+      p.spchunk, p.spextra, p.spsum, P, batch);
+  note_launch();
+  if (CYC) {
+    k_big_border<<<(batch + kBigThreads - 1) / kBigThreads, kBigThreads, 0, st>>>(
+        p.spchunk, p.spextra, p.spsum, xm, X, p.M, P, batch);
+    note_launch();
+  }
+  k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk, p.spextra, p.spsum, X, p.M, P,
+                                                   batch);
+  note_launch();
+  return cudaGetLastError();
+}
+
+template <bool CYC>
+cudaError_t run_cyc(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+  if (batch >= 8) return run<8, CYC>(p, X, batch, st);
+  if (batch >= 4) return run<4, CYC>(p, X, batch, st);
+  if (batch >= 2) return run<2, CYC>(p, X, batch, st);
+  return run<1, CYC>(p, X, batch, st);
+}
+
+}  // namespace
+
+cudaError_t shared_split_big(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
+  if (p.sp_L != kBigL || p.sp_T <= 0) return cudaErrorInvalidValue;
+  if ((batch + 7) / 8 > 65535) return cudaErrorInvalidConfiguration;   // grid y limit
+  // summaries: kSum doubles per (chunk, system), then x' at rows M-2, M-1 per system
+  const size_t need = ((size_t)p.sp_P * batch * kSum + 2 * (size_t)batch) * sizeof(double);
+  if (p.spsum_bytes < need) {
+    if (p.spsum) {
+      cudaError_t e = cudaStreamSynchronize(st);   // earlier solves may still read it
+      if (e != cudaSuccess) return e;
+      cudaFree(p.spsum);
+      p.spsum = nullptr;
+      p.spsum_bytes = 0;
+    }
+    cudaError_t e = cudaMalloc(&p.spsum, need);
+    if (e != cudaSuccess) return e;
+    p.spsum_bytes = need;
+  }
+  return p.cyclic ? run_cyc<true>(p, X, batch, st) : run_cyc<false>(p, X, batch, st);
+}
+
+}  // namespace pent
