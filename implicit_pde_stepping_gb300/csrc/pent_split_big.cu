@@ -37,17 +37,20 @@ __device__ __forceinline__ void mv2(const double* A, double x0, double x1, doubl
 }
 
 // (system, chunk) of this thread: SPW consecutive systems per warp row, so a
-// load instruction covers SPW * 8 bytes of each of 32 / SPW rows
+// load instruction covers SPW * 8 bytes of each of 32 / SPW rows.  The grid's x
+// runs over groups of systems and y over groups of chunks, so the CTAs that
+// read the same table rows for different systems are scheduled together and
+// share them through L2.
 template <int SPW>
 __device__ __forceinline__ void place(int& s, int& c) {
   constexpr int CPW = 32 / SPW;                      // chunks per warp
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  s = blockIdx.y * SPW + lane % SPW;
-  c = (blockIdx.x * (kBigThreads / 32) + w) * CPW + lane / SPW;
+  s = blockIdx.x * SPW + lane % SPW;
+  c = (blockIdx.y * (kBigThreads / 32) + w) * CPW + lane / SPW;
 }
 
 template <int SPW, bool CYC>
-__global__ void __launch_bounds__(kBigThreads)
+__global__ void __launch_bounds__(kBigThreads, 2)
     k_big_local(const float4* __restrict__ tab, double* __restrict__ X, double* __restrict__ sum,
                 double* __restrict__ xm, int M, int P, int batch) {
   constexpr int L = kBigL;
@@ -60,18 +63,23 @@ __global__ void __launch_bounds__(kBigThreads)
   const float4* t = tab + (size_t)row0 * kSpK;
   D2 v[L];
   {
-    double fv[L];
-#pragma unroll
-    for (int j = 0; j < L; ++j) fv[j] = (row0 + j < M) ? p[j * ld] : 0.0;
+    constexpr int G = 16;                         // rows loaded ahead at a time
     D2 a1{0.f, 0.f}, a2{0.f, 0.f};
 #pragma unroll
-    for (int j = 0; j < L; ++j) {
-      const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
-      const D2 g = df::sum3p(D2{c0.x, c0.y}, df::from_double(fv[j]), D2{c0.z, c0.w}, a2,
-                             D2{c1.x, c1.y}, a1);
-      v[j] = g;
-      a2 = a1;
-      a1 = g;
+    for (int j0 = 0; j0 < L; j0 += G) {
+      double fv[G];
+#pragma unroll
+      for (int u = 0; u < G; ++u) fv[u] = (row0 + j0 + u < M) ? p[(j0 + u) * ld] : 0.0;
+#pragma unroll
+      for (int u = 0; u < G; ++u) {
+        const int j = j0 + u;
+        const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
+        const D2 g = df::sum3p(D2{c0.x, c0.y}, df::from_double(fv[u]), D2{c0.z, c0.w}, a2,
+                               D2{c1.x, c1.y}, a1);
+        v[j] = g;
+        a2 = a1;
+        a1 = g;
+      }
     }
   }
   double* o = sum + ((size_t)c * batch + s) * kSum;
@@ -233,7 +241,8 @@ template <int SPW, bool CYC>
 cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   const int P = p.sp_P;
   constexpr int CPB = (kBigThreads / 32) * (32 / SPW);     // chunks per CTA
-  const dim3 grid((P + CPB - 1) / CPB, (batch + SPW - 1) / SPW);
+  const dim3 grid((batch + SPW - 1) / SPW, (P + CPB - 1) / CPB);
+  if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   double* xm = p.spsum + (size_t)P * batch * kSum;
   k_big_local<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, X, p.spsum, xm, p.M, P, batch);
   note_launch();
@@ -264,7 +273,6 @@ cudaError_t run_cyc(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
 
 cudaError_t shared_split_big(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   if (p.sp_L != kBigL || p.sp_T <= 0) return cudaErrorInvalidValue;
-  if ((batch + 7) / 8 > 65535) return cudaErrorInvalidConfiguration;   // grid y limit
   // summaries: kSum doubles per (chunk, system), then x' at rows M-2, M-1 per system
   const size_t need = ((size_t)p.sp_P * batch * kSum + 2 * (size_t)batch) * sizeof(double);
   if (p.spsum_bytes < need) {
