@@ -421,6 +421,11 @@ def run_ours(args, W: dict, dist: Dist):
     kname, kfile = kernel_names.get((kind, variant), ("?", "?"))
     if nsub > 1 and variant in (pent.VARIANT_SPLIT, pent.VARIANT_THREAD_DF):
         kname, kfile = "k_steps_df", "pent_steps_df.cu"
+    # systems longer than one CTA holds (64 chunks of 32 rows; 32 when periodic)
+    # run the partitioned solve as several kernels; the step is their sum
+    if kind == "shared" and variant == pent.VARIANT_SPLIT and \
+            (N - (2 if W["cyclic"] else 0)) > (1024 if W["cyclic"] else 2048):
+        kname, kfile = "k_big", "pent_split_big.cu"
     traffic = ncu_traffic(kname, kfile, args.workload, batch)
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
