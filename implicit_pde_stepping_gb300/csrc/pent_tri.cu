@@ -18,17 +18,19 @@
 //   k_tri_split      fp32, N <= 512: each system is cut into P = 2^k chunks of
 //                    L = 8 (N <= 256) or 16 rows, one thread per chunk, and never leaves
 //                    registers, so memory sees the minimum (a, b, c, y read
-//                    once, u written once).  Per chunk [s, e] a downward and an
-//                    upward elimination give
-//                        x_i = y''_i - l_i x_{s-1} - r_i x_{e+1},
-//                    eliminating x_{s+1} ... leaves one equation per chunk in
-//                    the chunk-end unknowns t_c = x_{e_c}:
-//                        l_e t_{c-1} + (1 - r_e l_s') t_c - r_e r_s' t_{c+1}
-//                            = y''_e - r_e y''_s'
-//                    (primes: the next chunk's first row), a P-unknown
-//                    tridiagonal system solved by parallel cyclic reduction
-//                    across P lanes with warp shuffles.  Then every row follows
-//                    from t_{c-1} and x_{s_{c+1}}.
+//                    once, u written once).  Per chunk [s, e] the downward
+//                    elimination gives x_i + c'_i x_{i+1} + l_i x_{s-1} = y'_i;
+//                    the upward elimination from row e-1, with the chunk's own
+//                    last row t_c = x_e as the right unknown, gives
+//                        x_i = y''_i - l'_i t_{c-1} - r_i t_c      (i < e).
+//                    Row e then reads x_e + l_e t_{c-1} + c'_e x_{s'} = y'_e with
+//                    x_{s'} (the next chunk's first row) in the same form, which
+//                    leaves one equation per chunk in the t's:
+//                        l_e t_{c-1} + (1 - c'_e l'_s') t_c - c'_e r_s' t_{c+1}
+//                            = y'_e - c'_e y''_s',
+//                    a P-unknown tridiagonal system solved by parallel cyclic
+//                    reduction across P lanes with warp shuffles.  Then every row
+//                    follows from t_{c-1} and t_c.
 //   The partition trades the page's 8n operations for about twice as many,
 //   which fp32 affords: the kernel is bound by memory, not arithmetic.
 //   A CTA's tile of a, b, c and y (16 systems x all rows) reaches shared memory
@@ -222,8 +224,14 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
       yprev = yv[j];
     }
   }
-  // ---- upward elimination: x_i = y''_i - l'_i x_{s-1} - r_i x_{e+1}
-  //      (in place: yv <- y'', lv <- l', cp <- r)
+  // ---- upward elimination from row e-1 with t_c = x_e as the right unknown:
+  //      x_i = y''_i - l'_i t_{c-1} - r_i t_c  (in place: yv <- y'', lv <- l',
+  //      cp <- r).  Row e keeps its downward form (y'_e, l_e, c'_e) for the
+  //      reduced system and takes the trivial form x_e = t_c (0, 0, -1).
+  const float le = lv[L - 1], ce = cp[L - 1], ye = yv[L - 1];
+  yv[L - 1] = 0.f;
+  lv[L - 1] = 0.f;
+  cp[L - 1] = -1.f;
 #pragma unroll
   for (int j = L - 2; j >= 0; --j) {
     const float cj = cp[j];
@@ -234,9 +242,9 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
   sB[0][c][lane] = lv[0];
   sB[1][c][lane] = cp[0];
   sB[2][c][lane] = yv[0];
-  sB[3][c][lane] = lv[L - 1];
-  sB[4][c][lane] = cp[L - 1];
-  sB[5][c][lane] = yv[L - 1];
+  sB[3][c][lane] = le;
+  sB[4][c][lane] = ce;
+  sB[5][c][lane] = ye;
   __syncthreads();
   if (bad) atomicCAS(&sBad[lane], 0, bad);
 
@@ -278,17 +286,13 @@ __global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
   }
   __syncthreads();
 
-  // ---- 3. every row from t_{c-1} and x at the next chunk's first row
+  // ---- 3. every row from t_{c-1} and t_c
   const float tprev = c > 0 ? sT[c - 1][lane] : 0.f;
-  float xnext = 0.f;
-  if (c < P - 1) {
-    const float tnext = sT[c + 1][lane];
-    xnext = sB[2][c + 1][lane] - sB[0][c + 1][lane] * sT[c][lane] - sB[1][c + 1][lane] * tnext;
-  }
+  const float tcur = sT[c][lane];
 #pragma unroll
   for (int j = 0; j < L; ++j) {
     const int i = row0 + j;
-    const float x = yv[j] - lv[j] * tprev - cp[j] * xnext;
+    const float x = yv[j] - lv[j] * tprev - cp[j] * tcur;
     if (act && i < N) X[(size_t)i * ld + sb] = x;
   }
   if (c == 0 && act && info) info[s] = sBad[lane];
