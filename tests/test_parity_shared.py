@@ -212,3 +212,17 @@ def test_twisted_prefetch_depths(depth, cyclic, monkeypatch):
     F = inputs.rhs_uniform(N, batch, seed=int(depth) + 1)
     ref = oracle.batch_shared(bands, F, cyclic=cyclic)
     assert max_rel_err(solve_gpu(bands, F, cyclic, "thread_df"), ref) < TOL_F64
+
+
+@pytest.mark.parametrize("variant", VARIANTS_F64)
+@pytest.mark.parametrize("cyclic", [False, True])
+@pytest.mark.parametrize("N", [300, 1024, 4099])
+def test_weakly_dominant_hyperdiffusion_matrix(variant, cyclic, N):
+    """sigma = 1000: I + sigma D4 is barely more than sigma D4, the eliminated
+    couplings decay slowly (chunk couplings too slow to truncate, so the exact
+    scans and wide border reaches are exercised); condition ~1.6e4."""
+    batch = 256
+    bands = inputs.hyper_bands(N, 1000.0)
+    F = inputs.rhs_uniform(N, batch, seed=N + 7)
+    ref = oracle.batch_shared(bands, F, cyclic=cyclic)
+    assert max_rel_err(solve_gpu(bands, F, cyclic, variant), ref) < TOL_F64
