@@ -282,7 +282,8 @@ def run_ours(args, W: dict, dist: Dist):
         plan.set_variant(args.variant)
     variant = plan.variant(batch) if plan is not None else pent.VARIANT_THREAD
     tri_variant = args.variant if args.variant in ("thread", "split") else "auto"
-    if kind == "tri":
+    if kind in ("tri", "persys"):
+        # fp32 per-system workloads: the partitioned kernel unless the thread one is asked for
         variant = pent.VARIANT_THREAD if tri_variant == "thread" else pent.VARIANT_SPLIT
     # inputs smaller than twice the L2: write a buffer larger than L2 between timed
     # steps, outside the per-step events, and time the steps by those events
@@ -308,7 +309,7 @@ def run_ours(args, W: dict, dist: Dist):
             pent.tri_factor_solve(*bands, X, variant=tri_variant, work=work, stream=stream,
                                   block_size=W.get("bs", 0))
         else:
-            pent.pent_factor_solve(*bands, X, work=work, stream=stream)
+            pent.pent_factor_solve(*bands, X, work=work, stream=stream, variant=tri_variant)
 
     # ---- device-resident timing
     with torch.cuda.stream(stream):
@@ -362,7 +363,7 @@ def run_ours(args, W: dict, dist: Dist):
                 db.copy_(hb, non_blocking=True)
             Xd.copy_(host_in, non_blocking=True)
             if kind == "persys":
-                pent.pent_factor_solve(*dev_bands, Xd, work=work, stream=stream)
+                pent.pent_factor_solve(*dev_bands, Xd, work=work, stream=stream, variant=tri_variant)
             elif kind == "tri":
                 pent.tri_factor_solve(*dev_bands, Xd, variant=tri_variant, work=work, stream=stream,
                                       block_size=W.get("bs", 0))
@@ -410,6 +411,7 @@ def run_ours(args, W: dict, dist: Dist):
         ("ch", pent.VARIANT_THREAD): ("k_ch_thread_f64", "pent_ch.cu"),
         ("cn", pent.VARIANT_THREAD): ("k_cn_thread_f64", "pent_ch.cu"),
         ("persys", pent.VARIANT_THREAD): ("k_persys_thread", "pent_persys.cu"),
+        ("persys", pent.VARIANT_SPLIT): ("k_persys_split", "pent_persys_split.cu"),
         ("tri", pent.VARIANT_THREAD): ("k_tri_thread", "pent_tri.cu"),
         ("tri", pent.VARIANT_SPLIT): ("k_tri_split", "pent_tri.cu"),
         ("shared", pent.VARIANT_THREAD_DF): (twisted, "pent_twisted_df.cu"),

@@ -323,16 +323,37 @@ size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {
   return persys_work_bytes(N, batch, dtype);
 }
 
-pent_status pent_factor_solve(const void* a, const void* b, const void* c, const void* d,
-                              const void* e, void* rhs, int N, int batch, pent_dtype dtype,
-                              void* work, size_t work_bytes, int* info, void* stream) {
-  if (!a || !b || !c || !d || !e || !rhs || !work || N < 1 || batch < 1) return PENT_ERR_INVALID_ARG;
+pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, const void* d,
+                                 const void* e, void* rhs, int N, int batch, pent_dtype dtype,
+                                 pent_variant variant, void* work, size_t work_bytes, int* info,
+                                 void* stream) {
+  if (!a || !b || !c || !d || !e || !rhs || N < 1 || batch < 1) return PENT_ERR_INVALID_ARG;
   if (dtype != PENT_F64 && dtype != PENT_F32) return PENT_ERR_INVALID_ARG;
-  if (work_bytes < persys_work_bytes(N, batch, dtype) || !aligned(work, 256)) return PENT_ERR_INVALID_ARG;
   const void* ptrs[6] = {a, b, c, d, e, rhs};
   for (const void* q : ptrs)
     if (!aligned(q, 16)) return PENT_ERR_INVALID_ARG;
+  const bool split_ok = dtype == PENT_F32 && persys_split_chunks(N) > 0;
+  bool split;
+  switch (variant) {
+    case PENT_VARIANT_AUTO: split = split_ok; break;
+    case PENT_VARIANT_THREAD: split = false; break;
+    case PENT_VARIANT_SPLIT:
+      if (!split_ok) return PENT_ERR_UNSUPPORTED;
+      split = true;
+      break;
+    default: return PENT_ERR_INVALID_ARG;
+  }
+  if (split) return from_cuda(persys_split(a, b, c, d, e, rhs, N, batch, info, as_stream(stream)));
+  if (!work || work_bytes < persys_work_bytes(N, batch, dtype) || !aligned(work, 256)) return PENT_ERR_INVALID_ARG;
   return from_cuda(persys_thread(a, b, c, d, e, rhs, N, batch, dtype, work, info, as_stream(stream)));
+}
+
+pent_status pent_factor_solve(const void* a, const void* b, const void* c, const void* d,
+                              const void* e, void* rhs, int N, int batch, pent_dtype dtype,
+                              void* work, size_t work_bytes, int* info, void* stream) {
+  if (!work || work_bytes < persys_work_bytes(N, batch, dtype) || !aligned(work, 256)) return PENT_ERR_INVALID_ARG;
+  return pent_factor_solve_ex(a, b, c, d, e, rhs, N, batch, dtype, PENT_VARIANT_AUTO, work, work_bytes, info,
+                              stream);
 }
 
 size_t tri_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {

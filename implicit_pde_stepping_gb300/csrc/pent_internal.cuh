@@ -88,6 +88,10 @@ cudaError_t persys_thread(const void* a, const void* b, const void* c, const voi
                           void* X, int N, int batch, pent_dtype dt, void* work, int* info,
                           cudaStream_t st);
 size_t persys_work_bytes(int N, int batch, pent_dtype dt);
+// persys_split.cu: partitioned fp32 kernel (chunks of 16 rows, TMA tiles)
+int persys_split_chunks(int N);   // chunks per system for N rows, 0 if N > 512
+cudaError_t persys_split(const void* a, const void* b, const void* c, const void* d, const void* e, void* X,
+                         int N, int batch, int* info, cudaStream_t st);
 
 // tri.cu: per-system tridiagonal solves (Thomas algorithm; partitioned fp32 kernel)
 int tri_split_chunks(int N);   // chunks of the partitioned kernel for N rows, 0 if too large

@@ -13,7 +13,9 @@
 // process exits.
 //
 // The caller still passes the bands, the right-hand side and (optionally)
-// info; the kernel and its results are those of pent_factor_solve.
+// info; the kernel and its results are those of pent_factor_solve.  fp32
+// systems of up to 512 rows go to the partitioned kernel, which keeps every
+// intermediate on chip and needs no scratch at all.
 #include <mutex>
 
 #include "pent_internal.cuh"
@@ -64,6 +66,12 @@ extern "C" pent_status pent_factor_solve_noalloc(const void* a, const void* b, c
   const void* ptrs[6] = {a, b, c, d, e, rhs_inout};
   for (const void* q : ptrs)
     if (!aligned16(q)) return PENT_ERR_INVALID_ARG;
+  // fp32 systems of up to 512 rows take the partitioned kernel, which needs no scratch
+  if (dtype == PENT_F32 && pent::persys_split_chunks(N) > 0) {
+    const cudaError_t err = pent::persys_split(a, b, c, d, e, rhs_inout, N, batch, info,
+                                               static_cast<cudaStream_t>(stream));
+    return err == cudaSuccess ? PENT_OK : PENT_ERR_CUDA;
+  }
   if (pent::persys_work_bytes(N, batch, dtype) > kNoAllocScratchBytes) return PENT_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   cudaError_t err = scratch_address(&scratch);

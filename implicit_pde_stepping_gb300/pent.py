@@ -49,6 +49,7 @@ def lib():
             L.pent_solve.argtypes = [vp, vp, i, vp]
             L.pent_solve_host.argtypes = [vp, vp, vp, i, i, vp]
             L.pent_factor_solve.argtypes = [vp] * 6 + [i, i, i, vp, sz, vp, vp]
+            L.pent_factor_solve_ex.argtypes = [vp] * 6 + [i, i, i, i, vp, sz, vp, vp]
             L.pent_factor_solve_work_bytes.argtypes = [i, i, i]
             L.pent_factor_solve_work_bytes.restype = sz
             L.pent_factor_solve_noalloc.argtypes = [vp] * 6 + [i, i, i, vp, vp]
@@ -69,6 +70,7 @@ def lib():
             L.pent_launch_count.argtypes = []
             L.pent_launch_count.restype = ctypes.c_ulonglong
             for fn in ("pent_factor", "pent_solve", "pent_solve_host", "pent_factor_solve",
+                       "pent_factor_solve_ex",
                        "hyperdiffusion_step",
                        "ch_step", "cn_step", "tri_factor_solve", "pent_set_variant",
                        "pent_get_variant", "pent_sync"):
@@ -195,9 +197,10 @@ def pent_factor_solve_work_bytes(N: int, batch: int, dtype) -> int:
     return int(lib().pent_factor_solve_work_bytes(int(N), int(batch), code))
 
 
-def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None):
-    """Per-system factor + solve, in place in rhs.  work: a CUDA uint8 tensor of at least
-    pent_factor_solve_work_bytes() bytes (allocated here if None).  info: CUDA int32 [batch]."""
+def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None, variant: str = "auto"):
+    """Per-system factor + solve, in place in rhs.  variant: "auto", "thread" or "split"
+    (fp32, N <= 512).  work: a CUDA uint8 tensor of at least pent_factor_solve_work_bytes()
+    bytes (allocated here if None; unused by the split kernel).  info: CUDA int32 [batch]."""
     import torch
     N, batch = rhs.shape
     code = _dtype_code(rhs)
@@ -212,9 +215,9 @@ def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None):
         if info.dtype != torch.int32 or info.numel() < batch or not info.is_cuda:
             raise ValueError("info must be a CUDA int32 tensor of >= batch elements")
         ip = ctypes.c_void_p(info.data_ptr())
-    _check(lib().pent_factor_solve(*ptrs, _ptr(rhs, N, code, "rhs"), N, batch, code,
-                                   ctypes.c_void_p(work.data_ptr()),
-                                   work.numel() * work.element_size(), ip, _stream(stream)),
+    _check(lib().pent_factor_solve_ex(*ptrs, _ptr(rhs, N, code, "rhs"), N, batch, code,
+                                      VARIANTS[variant], ctypes.c_void_p(work.data_ptr()),
+                                      work.numel() * work.element_size(), ip, _stream(stream)),
            "pent_factor_solve")
     return work
 

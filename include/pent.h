@@ -119,20 +119,50 @@ pent_status pent_solve_host(pent_plan plan, const void* rhs_host, void* x_host, 
 /*
  * pent_factor_solve — per-system matrices, factor + solve in one call
  * ("cuPentBatchRewrite": a new matrix every call).  Unlike the page, the
- * bands are left unchanged; the factor coefficients go to `work`.
- *   a, b, c, d, e : DEVICE, interleaved [N][batch] each, dtype elements.
- *   rhs_inout     : DEVICE, interleaved [N][batch]; f in, x out.
+ * bands are left unchanged.  Row i of system s:
+ *   a_i x_{i-2} + b_i x_{i-1} + c_i x_i + d_i x_{i+1} + e_i x_{i+2} = f_i
+ * (entries that fall outside the matrix are ignored).
+ *   a, b, c, d, e : DEVICE, interleaved [N][batch] each, dtype elements,
+ *                   16-byte aligned; not modified.
+ *   rhs_inout     : DEVICE, interleaved [N][batch], 16-byte aligned; f in, x out.
  *   N, batch      : >= 1.
  *   work          : DEVICE scratch of at least pent_factor_solve_work_bytes()
  *                   bytes, 256-byte aligned; contents undefined afterwards.
+ *                   (The kernel chosen by PENT_VARIANT_AUTO may not touch it.)
  *   info          : DEVICE int[batch] or NULL.  info[s] = 0 if system s was
- *                   factored, else the 1-based row of its first zero or
- *                   non-finite pivot (its x is then not meaningful).
- * Non-cyclic only.
+ *                   factored, else the 1-based row of the first zero or
+ *                   non-finite pivot the kernel's elimination met (its x is
+ *                   then not meaningful; the row may differ between variants).
+ * Non-cyclic only.  Equivalent to pent_factor_solve_ex with PENT_VARIANT_AUTO.
  */
 pent_status pent_factor_solve(const void* a, const void* b, const void* c, const void* d,
                               const void* e, void* rhs_inout, int N, int batch, pent_dtype dtype,
                               void* work, size_t work_bytes, int* info, void* stream);
+
+/*
+ * pent_factor_solve_ex — pent_factor_solve with the kernel chosen by the caller.
+ *   variant : PENT_VARIANT_THREAD — one thread per system (the page's Rewrite
+ *             scheme): gamma_i and delta_i go to `work`, g_i over the
+ *             right-hand side, read back by the backward sweep;
+ *             PENT_VARIANT_SPLIT — fp32 and N <= 512 only: each system cut
+ *             into chunks of 16 rows, one thread per chunk, its tile loaded
+ *             into shared memory by TMA and kept on chip (partitioned
+ *             elimination; the chunk-end pairs of unknowns by block parallel
+ *             cyclic reduction), so memory sees the bands and f once and x
+ *             once; `work` is not used and may be NULL;
+ *             PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD.
+ *             PENT_VARIANT_THREAD_DF is not a per-system variant.
+ *   other arguments as for pent_factor_solve; `work` is required (non-NULL,
+ *   large enough, 256-byte aligned) only when THREAD runs.
+ * Errors: PENT_ERR_INVALID_ARG for null or misaligned pointers, N or batch < 1,
+ * a bad dtype or variant, or a missing or short work buffer where THREAD
+ * runs; PENT_ERR_UNSUPPORTED for SPLIT outside fp32 / N <= 512.  Nothing is
+ * queued on an error.
+ */
+pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, const void* d,
+                                 const void* e, void* rhs_inout, int N, int batch, pent_dtype dtype,
+                                 pent_variant variant, void* work, size_t work_bytes, int* info,
+                                 void* stream);
 
 /* Bytes of device scratch pent_factor_solve needs for (N, batch, dtype). */
 size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);
@@ -145,14 +175,16 @@ size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);
  * allocate, or a time-critical loop where cudaMalloc/cudaFree are ruled out
  * because they may synchronise the device and take unbounded time.
  *
- * Same kernel and results as pent_factor_solve, but the scratch for the factor
- * coefficients is a fixed 16 MiB array inside the library (every GPU that
+ * Same kernel and results as pent_factor_solve.  fp32 systems of up to 512
+ * rows take the partitioned kernel, which needs no scratch; otherwise the
+ * scratch for the factor coefficients is a fixed 16 MiB array inside the library (every GPU that
  * loads the library holds it until the process exits).  Nothing is allocated:
  * no cudaMalloc, cudaFree or allocating library routine is called.
  *   a..e, rhs_inout, N, batch, dtype, info : as for pent_factor_solve.
- * Limit: 2 * N * batch * sizeof(element) must be <= 16 MiB (for example
- * N = 256 with batch <= 8192 in fp32, or batch <= 4096 in fp64); larger
- * requests return PENT_ERR_UNSUPPORTED and queue nothing.
+ * Limit, where the scratch is used (fp64, or N > 512): 2 * N * batch *
+ * sizeof(element) must be <= 16 MiB (for example N = 300 with batch <= 3495
+ * in fp64, or N = 1024 with batch <= 2048 in fp32); larger requests return
+ * PENT_ERR_UNSUPPORTED and queue nothing.
  * Set-up: the first call on each device looks up the device address of the
  * array (cudaGetSymbolAddress, with that device current); make that first call
  * before any stream capture.
@@ -228,7 +260,7 @@ pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* 
  *   variant   : PENT_VARIANT_THREAD — one thread per system, c'_i kept in `work`
  *               and y'_i written over the right-hand side (the page's scheme);
  *               PENT_VARIANT_SPLIT — fp32 and N <= 512 only: each system held
- *               in registers across a group of threads (chunks of 16 rows,
+ *               in registers across a group of threads (chunks of 8 or 16 rows,
  *               partitioned elimination, chunk-end unknowns by parallel cyclic
  *               reduction), so memory sees a, b, c, y once and x once;
  *               PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD.

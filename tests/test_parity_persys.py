@@ -1,4 +1,5 @@
-"""GPU parity: per-system factor + solve (pent_factor_solve) against the CPU oracle."""
+"""GPU parity: per-system factor + solve (pent_factor_solve) against the CPU oracle, both
+kernels (one thread per system; partitioned fp32 with TMA tiles) and the automatic choice."""
 import numpy as np
 import pytest
 
@@ -8,38 +9,45 @@ from tests.gpu_util import TOL_F32, TOL_F64, dev, host, max_rel_err
 
 pytestmark = pytest.mark.gpu
 
+CASES = [("auto", np.float64, TOL_F64), ("thread", np.float32, TOL_F32),
+         ("split", np.float32, TOL_F32), ("auto", np.float32, TOL_F32)]
+IDS = [f"{v}-{d.__name__}" for v, d, _ in CASES]
 
-def run_gpu(bands, F, dtype, info=True):
+
+def run_gpu(bands, F, dtype, info=True, variant="auto"):
     import torch
     tdt = torch.float64 if dtype == np.float64 else torch.float32
     dB = [dev(v, tdt) for v in bands]
     X = dev(F, tdt)
     inf = torch.full((F.shape[1],), -1, dtype=torch.int32, device="cuda") if info else None
-    pent.pent_factor_solve(*dB, X, info=inf)
+    pent.pent_factor_solve(*dB, X, info=inf, variant=variant)
     pent.pent_sync()
     return host(X), (host(inf) if info else None), [host(b) for b in dB]
 
 
-@pytest.mark.parametrize("dtype,tol", [(np.float32, TOL_F32), (np.float64, TOL_F64)])
-@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 33, 256])
+@pytest.mark.parametrize("variant,dtype,tol", CASES, ids=IDS)
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 15, 16, 17, 33, 100, 255, 256, 257, 300, 512])
 @pytest.mark.parametrize("batch", [1, 5, 127, 1000])
-def test_ragged_shapes(dtype, tol, N, batch):
+def test_ragged_shapes(variant, dtype, tol, N, batch):
+    """batch 1000 takes the TMA-tile path of the split kernel (row pitch a multiple of 16 bytes),
+    1, 5 and 127 its per-thread cp.async path; N spans one to 32 chunks with ragged tails."""
     a, b, c, d, e = inputs.persys_bands(N, batch, seed=N + batch, dtype=dtype)
     F = inputs.rhs_uniform(N, batch, seed=N + batch).astype(dtype)
     ref = oracle.batch_persys(a, b, c, d, e, F)
-    X, info, bands_after = run_gpu((a, b, c, d, e), F, dtype)
+    X, info, bands_after = run_gpu((a, b, c, d, e), F, dtype, variant=variant)
     assert max_rel_err(X, ref) < tol
     assert np.all(info == 0)
     for before, after in zip((a, b, c, d, e), bands_after):   # bands are left unchanged
         assert np.array_equal(before, after)
 
 
-def test_full_size_fp32_workload_sampled():
+@pytest.mark.parametrize("variant", ["split", "thread"])
+def test_full_size_fp32_workload_sampled(variant):
     """N=256, batch 262144, fp32, strictly diagonally dominant per-system bands."""
     N, batch = 256, 262144
     a, b, c, d, e = inputs.persys_bands(N, batch, seed=0)
     F = inputs.rhs_uniform(N, batch, seed=0).astype(np.float32)
-    X, info, _ = run_gpu((a, b, c, d, e), F, np.float32)
+    X, info, _ = run_gpu((a, b, c, d, e), F, np.float32, variant=variant)
     idx = inputs.sample_systems(batch, 2048)
     ref = oracle.batch_persys(a[:, idx], b[:, idx], c[:, idx], d[:, idx], e[:, idx], F[:, idx])
     assert max_rel_err(X[:, idx], ref) < TOL_F32
@@ -47,18 +55,71 @@ def test_full_size_fp32_workload_sampled():
     assert np.all(np.isfinite(X))
 
 
-def test_zero_pivot_reported_per_system():
-    N, batch = 10, 4
-    a, b, c, d, e = inputs.persys_bands(N, batch, seed=1, dtype=np.float64)
+@pytest.mark.parametrize("variant,dtype,tol", CASES, ids=IDS)
+@pytest.mark.parametrize("N", [64, 256, 300, 512])
+def test_weakly_dominant(variant, dtype, tol, N):
+    """[1, -4, 6 + eps, -4, 1] with eps in [0.1, 0.2] per system (condition ~100): the
+    couplings between chunks decay slowly, so an inexact chunk interface would show."""
+    batch = 512
+    rng = np.random.default_rng(N)
+    eps = rng.uniform(0.1, 0.2, batch)
+    one = np.ones((N, batch))
+    a, b, c, d, e = (one, -4 * one, (6 + eps) * one, -4 * one, one)
+    a, b, c, d, e = (v.astype(dtype) for v in (a, b, c, d, e))
+    F = inputs.rhs_uniform(N, batch, seed=N).astype(dtype)
+    ref = oracle.batch_persys(a, b, c, d, e, F)
+    X, info, _ = run_gpu((a, b, c, d, e), F, dtype, variant=variant)
+    assert np.all(info == 0)
+    assert max_rel_err(X, ref) < tol
+
+
+@pytest.mark.parametrize("variant,dtype", [("thread", np.float64), ("thread", np.float32),
+                                           ("split", np.float32)])
+def test_zero_pivot_reported_per_system(variant, dtype):
+    N, batch = 40, 5
+    a, b, c, d, e = inputs.persys_bands(N, batch, seed=1, dtype=dtype)
     c[0, 1] = 0.0          # system 1: alpha_1 = c_1 = 0 -> info 1
-    a[:, 2] = b[:, 2] = d[:, 2] = e[:, 2] = 0.0
-    c[6, 2] = 0.0          # system 2: diagonal matrix with a zero at row 7 -> info 7
-    F = inputs.rhs_uniform(N, batch, seed=1)
-    X, info, _ = run_gpu((a, b, c, d, e), F, np.float64)
-    assert list(info) == [0, 1, 7, 0]
+    for s, row in ((2, 6), (4, 20)):
+        a[:, s] = b[:, s] = d[:, s] = e[:, s] = 0.0
+        c[row, s] = 0.0    # diagonal matrix with a zero at row row + 1 (second chunk for system 4)
+    F = inputs.rhs_uniform(N, batch, seed=1).astype(dtype)
+    X, info, _ = run_gpu((a, b, c, d, e), F, dtype, variant=variant)
+    assert list(info) == [0, 1, 7, 0, 21]
     ok = [0, 3]
     ref = oracle.batch_persys(a[:, ok], b[:, ok], c[:, ok], d[:, ok], e[:, ok], F[:, ok])
-    assert max_rel_err(X[:, ok], ref) < TOL_F64
+    assert max_rel_err(X[:, ok], ref) < (TOL_F64 if dtype == np.float64 else TOL_F32)
+
+
+def test_split_variant_limits():
+    import torch
+    for N, tdt in ((16, torch.float64), (513, torch.float32)):
+        bands = [torch.ones(N, 8, dtype=tdt, device="cuda") for _ in range(5)]
+        X = torch.ones(N, 8, dtype=tdt, device="cuda")
+        with pytest.raises(pent.PentError) as ex:
+            pent.pent_factor_solve(*bands, X, variant="split")
+        assert ex.value.status == pent.ERR_UNSUPPORTED
+
+
+def test_split_needs_no_work_buffer():
+    """Through the C ABI: the split kernel accepts a NULL work buffer; the thread kernel
+    rejects it before queueing anything."""
+    import ctypes
+    import torch
+    L = pent.lib()
+    N, batch = 64, 32
+    bands = [dev(v) for v in inputs.persys_bands(N, batch, seed=3)]
+    F = inputs.rhs_uniform(N, batch, seed=3).astype(np.float32)
+    X = dev(F)
+    vp = [ctypes.c_void_p(t.data_ptr()) for t in bands]
+    st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    assert L.pent_factor_solve_ex(*vp, ctypes.c_void_p(X.data_ptr()), N, batch, pent.F32,
+                                  pent.VARIANT_THREAD, None, 0, None, st) == pent.ERR_INVALID_ARG
+    assert np.array_equal(host(X), F)
+    assert L.pent_factor_solve_ex(*vp, ctypes.c_void_p(X.data_ptr()), N, batch, pent.F32,
+                                  pent.VARIANT_SPLIT, None, 0, None, st) == pent.OK
+    pent.pent_sync()
+    ref = oracle.batch_persys(*[host(t) for t in bands], F)
+    assert max_rel_err(host(X), ref) < TOL_F32
 
 
 def test_work_too_small_rejected():
