@@ -16,7 +16,7 @@
 //                    scratch array and y'_i over the right-hand side, the
 //                    backward substitution reads both back.  Any N, fp32/fp64.
 //   k_tri_split      fp32, N <= 512: each system is cut into P = 2^k chunks of
-//                    L = 8 (N <= 256) or 16 rows, one thread per chunk, and never leaves
+//                    L = 16 rows, one thread per chunk, and never leaves
 //                    registers, so memory sees the minimum (a, b, c, y read
 //                    once, u written once).  Per chunk [s, e] the downward
 //                    elimination gives x_i + c'_i x_{i+1} + l_i x_{s-1} = y'_i;
@@ -122,8 +122,8 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 // ---------------------------------------------------------------------------
-// partitioned fp32 kernel: 16 systems x P chunks of L rows per CTA (2 CTAs/SM for L = 8,
-// so that one CTA's loads overlap the other's arithmetic and barriers)
+// partitioned fp32 kernel: 16 systems x P chunks of L rows per CTA (3 CTAs/SM up to
+// N = 256, so that one CTA's tile load overlaps the others' arithmetic and barriers)
 // ---------------------------------------------------------------------------
 constexpr int kTriSB = 16;    // systems per CTA
 
@@ -144,7 +144,7 @@ struct TriMaps {
 // Staged tile: TMA layout [array][RS rows][SB systems]; cp.async layout
 // [array][L rows][SB * P threads].
 template <int L, int P, bool TMA>
-__global__ void __launch_bounds__(kTriSB * P, L <= 8 ? 2 : 1)
+__global__ void __launch_bounds__(kTriSB * P, P <= 16 ? 3 : 1)
     k_tri_split(const __grid_constant__ TriMaps maps, const float* __restrict__ A,
                 const float* __restrict__ B, const float* __restrict__ C, float* __restrict__ X, int N,
                 int batch, int bs, int RS, int BR, int* __restrict__ info) {
@@ -339,12 +339,14 @@ cudaError_t launch_split(const void* a, const void* b, const void* c, void* X, i
 
 }  // namespace
 
-// rows per chunk of the partitioned kernel: 8 up to N = 256, else 16
-static int tri_split_rows(int N) { return N <= 256 ? 8 : 16; }
+// rows per chunk of the partitioned kernel (at N = 256, batch 262144, 16-row chunks
+// run 3 CTAs of 256 threads per SM in 0.212 ms, 8-row chunks 2 CTAs of 512 threads in
+// 0.261 ms: fewer reduced-system steps per row, and more CTAs to overlap one tile's
+// load with the others' arithmetic)
+constexpr int kTriL = 16;
 
 int tri_split_chunks(int N) {
-  const int L = tri_split_rows(N);
-  const int need = (N + L - 1) / L;
+  const int need = (N + kTriL - 1) / kTriL;
   int P = 2;
   while (P < need) P *= 2;
   return P <= 32 ? P : 0;
@@ -358,13 +360,12 @@ size_t tri_work_bytes(int N, int batch, pent_dtype dt) {
 cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
                             pent_dtype dt, bool split, void* work, int* info, cudaStream_t st) {
   if (split) {
-    if (tri_split_rows(N) == 16) return launch_split<16, 32>(a, b, c, X, N, batch, bs, info, st);
     switch (tri_split_chunks(N)) {
-      case 2: return launch_split<8, 2>(a, b, c, X, N, batch, bs, info, st);
-      case 4: return launch_split<8, 4>(a, b, c, X, N, batch, bs, info, st);
-      case 8: return launch_split<8, 8>(a, b, c, X, N, batch, bs, info, st);
-      case 16: return launch_split<8, 16>(a, b, c, X, N, batch, bs, info, st);
-      case 32: return launch_split<8, 32>(a, b, c, X, N, batch, bs, info, st);
+      case 2: return launch_split<kTriL, 2>(a, b, c, X, N, batch, bs, info, st);
+      case 4: return launch_split<kTriL, 4>(a, b, c, X, N, batch, bs, info, st);
+      case 8: return launch_split<kTriL, 8>(a, b, c, X, N, batch, bs, info, st);
+      case 16: return launch_split<kTriL, 16>(a, b, c, X, N, batch, bs, info, st);
+      case 32: return launch_split<kTriL, 32>(a, b, c, X, N, batch, bs, info, st);
       default: return cudaErrorInvalidValue;
     }
   }

@@ -260,7 +260,7 @@ pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* 
  *   variant   : PENT_VARIANT_THREAD — one thread per system, c'_i kept in `work`
  *               and y'_i written over the right-hand side (the page's scheme);
  *               PENT_VARIANT_SPLIT — fp32 and N <= 512 only: each system held
- *               in registers across a group of threads (chunks of 8 or 16 rows,
+ *               in registers across a group of threads (chunks of 16 rows,
  *               partitioned elimination, chunk-end unknowns by parallel cyclic
  *               reduction), so memory sees a, b, c, y once and x once;
  *               PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD.
