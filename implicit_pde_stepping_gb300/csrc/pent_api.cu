@@ -1,6 +1,9 @@
 // C ABI of libpent: argument checks, plan lifecycle and dispatch to the kernels.
 // Every declaration is documented in include/pent.h.
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <tuple>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -12,6 +15,37 @@ namespace pent {
 static std::atomic<unsigned long long> g_launches{0};
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+namespace {
+std::mutex g_prep_mu;
+std::map<std::pair<const void*, int>, size_t> g_prep_smem;                 // limit set so far
+std::map<std::tuple<const void*, int, size_t, int>, int> g_prep_occ;       // CTAs per SM
+}  // namespace
+
+cudaError_t kernel_prepare(const void* fn, size_t smem, int threads, int* per_sm) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_prep_mu);
+  size_t& cur = g_prep_smem[{fn, dev}];
+  if (smem > cur) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    cur = smem;
+  }
+  if (per_sm) {
+    const auto key = std::make_tuple(fn, dev, smem, threads);
+    auto it = g_prep_occ.find(key);
+    if (it == g_prep_occ.end()) {
+      int n = 0;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem);
+      if (e != cudaSuccess) return e;
+      it = g_prep_occ.emplace(key, n).first;
+    }
+    *per_sm = it->second;
+  }
+  return cudaSuccess;
+}
 
 namespace {
 

@@ -71,6 +71,12 @@ namespace pent {
 
 // launch bookkeeping (host)
 void note_launch();
+// Raise kernel fn's dynamic shared-memory limit to smem bytes on the current
+// device and, if per_sm is not null, report how many CTAs of `threads` threads
+// fit on one SM.  Both are cached per kernel, device and size, so repeated
+// launches make no attribute or occupancy call (each costs microseconds of host
+// time, which a short kernel's stream would otherwise wait through).
+cudaError_t kernel_prepare(const void* fn, size_t smem, int threads, int* per_sm);
 
 // factor.cu
 cudaError_t factor_shared(const double* d_bands, int N, int cyclic, double* coef64, double* tail64,

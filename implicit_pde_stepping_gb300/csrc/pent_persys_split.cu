@@ -297,7 +297,7 @@ cudaError_t launch(const void* a, const void* b, const void* c, const void* d, c
   const size_t iface = (size_t)(kIface + 2) * P * (kSB + 1) * sizeof(float);
   const size_t smem = stage > iface ? stage : iface;
   auto kern = tma_ok ? k_persys_split<P, true> : k_persys_split<P, false>;
-  const cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t err = kernel_prepare((const void*)kern, smem, kSB * P, nullptr);
   if (err != cudaSuccess) return err;
   kern<<<grid, kSB * P, smem, st>>>(maps, static_cast<const float*>(a), static_cast<const float*>(b),
                                      static_cast<const float*>(c), static_cast<const float*>(d),

@@ -32,6 +32,7 @@
 // The per-row tables sit in shared memory with one float4 of padding per
 // chunk, so the four chunks a warp reads fall in different banks.  A CTA holds
 // SB systems x P chunks; the grid is persistent.
+#include "cp_async.cuh"
 #include "df64.cuh"
 #include "pent_internal.cuh"
 
@@ -82,9 +83,10 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
 
   for (int t = threadIdx.x; t < P * L * K4; t += blockDim.x) {
     const int row = t / K4, k = t % K4;
-    rtab[(row / L) * CS + (row % L) * K4 + k] = growtab[(size_t)row * kSpK + k];
+    cp_async16(&rtab[(row / L) * CS + (row % L) * K4 + k], &growtab[(size_t)row * kSpK + k]);
   }
-  for (int t = threadIdx.x; t < P * kSpChunk; t += blockDim.x) ctab[t] = gchunk[t];
+  for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
+  cp_async_wait_all();
   __syncthreads();
   const int T = (int)gextra[18];
 
@@ -343,13 +345,11 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st, 
   const int P = p.sp_P;
   const size_t smem = split_smem_bytes(L, P, SB, CYC);
   auto kern = k_split_df<L, SB, MAXT, CYC, RHS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   const int nblk = (batch + SB - 1) / SB;
   // persistent grid: as many CTAs as fit on every SM at once (registers and
   // shared memory of this instance), capped by the number of system blocks
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, SB * P, smem);
+  const cudaError_t e = kernel_prepare((const void*)kern, smem, SB * P, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;

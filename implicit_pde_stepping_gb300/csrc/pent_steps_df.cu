@@ -24,6 +24,7 @@
 //
 // Launched only when the plan's chunk couplings are truncated (T > 0); the
 // exact serial chunk scan stays with the one-step kernel.
+#include "cp_async.cuh"
 #include "df64.cuh"
 #include "pent_internal.cuh"
 
@@ -87,9 +88,10 @@ __global__ void __launch_bounds__(MAXT, 1)
 
   for (int t = threadIdx.x; t < P * L * K4; t += blockDim.x) {
     const int row = t / K4, k = t % K4;
-    rtab[(row / L) * CS + (row % L) * K4 + k] = growtab[(size_t)row * kSpK + k];
+    cp_async16(&rtab[(row / L) * CS + (row % L) * K4 + k], &growtab[(size_t)row * kSpK + k]);
   }
-  for (int t = threadIdx.x; t < P * kSpChunk; t += blockDim.x) ctab[t] = gchunk[t];
+  for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
+  cp_async_wait_all();
   __syncthreads();
   const int T = (int)gextra[18];
 
@@ -322,10 +324,8 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, doubl
   const int P = p.sp_P;
   const size_t smem = steps_smem(L, P, SB, RHS);
   auto kern = k_steps_df<L, SB, 512, RHS>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, SB * P, smem);
+  const cudaError_t e = kernel_prepare((const void*)kern, smem, SB * P, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int nblk = (batch + SB - 1) / SB;

@@ -328,7 +328,7 @@ cudaError_t launch_split(const void* a, const void* b, const void* c, void* X, i
   const size_t smem = tma_ok ? (size_t)4 * RS * kTriSB * sizeof(float)
                              : (size_t)4 * L * kTriSB * P * sizeof(float);
   auto kern = tma_ok ? k_tri_split<L, P, true> : k_tri_split<L, P, false>;
-  const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = kernel_prepare((const void*)kern, smem, kTriSB * P, nullptr);
   if (e != cudaSuccess) return e;
   kern<<<grid, kTriSB * P, smem, st>>>(maps, static_cast<const float*>(a), static_cast<const float*>(b),
                                           static_cast<const float*>(c), static_cast<float*>(X), N,

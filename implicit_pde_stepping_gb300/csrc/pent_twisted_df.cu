@@ -24,6 +24,7 @@
 //    full blocks run without per-row guards, a ragged last block with them.
 #include <type_traits>
 
+#include "cp_async.cuh"
 #include "df64.cuh"
 #include "pent_internal.cuh"
 
@@ -129,7 +130,8 @@ __global__ void __launch_bounds__(2 * SPB / SPT)
   extern __shared__ float4 stab[];
   __shared__ double sx[TPD][SPT][NX];
   __shared__ double sT[kTwistCount];
-  for (int t = threadIdx.x; t < M * kTwK; t += blockDim.x) stab[t] = gtab[t];
+  for (int t = threadIdx.x; t < M * kTwK; t += blockDim.x) cp_async16(&stab[t], &gtab[t]);
+  cp_async_wait_all();
   if (threadIdx.x < kTwistCount) sT[threadIdx.x] = twist[threadIdx.x];
   __syncthreads();
 
@@ -368,7 +370,8 @@ __global__ void __launch_bounds__(SPB, 2)
   uint4* ring = reinterpret_cast<uint4*>(stab + (size_t)M * KT);  // [D][NT]
   __shared__ double sx[TPD][SPT][NX];
   __shared__ double sT[kTwistCount];
-  for (int t = threadIdx.x; t < M * KT; t += NT) stab[t] = gtab[(size_t)(t / KT) * kTwK + t % KT];
+  for (int t = threadIdx.x; t < M * KT; t += NT) cp_async16(&stab[t], &gtab[(size_t)(t / KT) * kTwK + t % KT]);
+  cp_async_wait_all();
   if (threadIdx.x < kTwistCount) sT[threadIdx.x] = twist[threadIdx.x];
   __syncthreads();
 
@@ -622,7 +625,7 @@ cudaError_t launch_async(const pent_plan_s& p, double* X, int batch, cudaStream_
   constexpr int KT = CYC ? kTwK : 3;
   const size_t smem = (size_t)p.M * KT * sizeof(float4) + (size_t)D * SPB * sizeof(uint4);
   auto kern = k_twisted_async<SPB, D, CYC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = kernel_prepare((const void*)kern, smem, SPB, nullptr);
   if (e != cudaSuccess) return e;
   const int nblk = (batch + SPB - 1) / SPB;
   int grid = p.df_ctas > 0 ? p.df_ctas : 2 * p.num_sms;
@@ -636,7 +639,7 @@ template <int SPT, int SPB, int KU, bool CYC>
 cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   const size_t smem = (size_t)p.M * kTwK * sizeof(float4);
   auto kern = k_twisted_df<SPT, SPB, KU, CYC>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const cudaError_t e = kernel_prepare((const void*)kern, smem, 2 * SPB / SPT, nullptr);
   if (e != cudaSuccess) return e;
   const int nblk = (batch + SPB - 1) / SPB;
   int grid = p.df_ctas > 0 ? p.df_ctas : 2 * p.num_sms;
