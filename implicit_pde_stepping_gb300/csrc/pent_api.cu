@@ -4,6 +4,7 @@
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <vector>
 #include <cstdlib>
 #include <cstring>
 #include <new>
@@ -107,6 +108,34 @@ bool use_steps(const pent_plan_s& p, int nsteps, int kind) {
   if (p.variant != PENT_VARIANT_AUTO && p.variant != PENT_VARIANT_SPLIT) return false;
   if (env_int("PENT_STEPS", 1) == 0) return false;
   return steps_supported(p, kind);
+}
+
+// Longest run of consecutive chunks whose row tables (L x kSpK float4) and
+// chunk tables (kSpChunk doubles) are bitwise equal to those of the run's first
+// chunk; recorded as dup_lo < c <= dup_hi (empty if no two neighbours match).
+cudaError_t find_duplicate_chunks(pent_plan_s& p, int Mpad) {
+  const int L = p.sp_L, P = p.sp_P;
+  std::vector<float4> rows((size_t)Mpad * kSpK);
+  std::vector<double> chunks((size_t)P * kSpChunk);
+  cudaError_t e = cudaMemcpy(rows.data(), p.sptab, rows.size() * sizeof(float4), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess)
+    e = cudaMemcpy(chunks.data(), p.spchunk, chunks.size() * sizeof(double), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  const size_t rb = (size_t)L * kSpK * sizeof(float4), cb = kSpChunk * sizeof(double);
+  auto same = [&](int a, int b) {
+    return std::memcmp(&rows[(size_t)a * L * kSpK], &rows[(size_t)b * L * kSpK], rb) == 0 &&
+           std::memcmp(&chunks[(size_t)a * kSpChunk], &chunks[(size_t)b * kSpChunk], cb) == 0;
+  };
+  int best_lo = 0, best_hi = 0;
+  for (int c = 1; c < P;) {
+    if (!same(c - 1, c)) { ++c; continue; }
+    const int lo = c - 1;
+    while (c < P && same(lo, c)) ++c;
+    if (c - 1 - lo > best_hi - best_lo) { best_lo = lo; best_hi = c - 1; }
+  }
+  p.dup_lo = best_lo;
+  p.dup_hi = best_hi;
+  return cudaSuccess;
 }
 
 }  // namespace
@@ -311,6 +340,15 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
         p->sp_T = (int)Td;
         // the two-kernel form needs the truncated chunk couplings
         p->split_big = !fits && p->sp_T > 0;
+      }
+      // PENT_CHUNK_DEDUP=0 keeps every chunk on its own tables (testing)
+      if (p->split_big && env_int("PENT_CHUNK_DEDUP", 1) != 0) {
+        e = find_duplicate_chunks(*p, (int)Mpad);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          pent_destroy(p);
+          return from_cuda(e);
+        }
       }
     }
   }

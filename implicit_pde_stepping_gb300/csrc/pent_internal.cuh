@@ -54,6 +54,10 @@ struct pent_plan_s {
   int sp_T = 0;              // chunk couplings kept by the parallel scan (0: exact serial scan)
   int split_big = 0;         // tables valid for the two-kernel form (systems too long for one CTA)
   double* spsum = nullptr;   // two-kernel form: per system and chunk summaries, grown on use
+  // chunks dup_lo < c <= dup_hi have row and chunk tables bitwise equal to those of
+  // chunk dup_lo (a matrix with constant bands, far from its ends): the two-kernel
+  // form reads chunk dup_lo's tables for them, which stay in cache
+  int dup_lo = 0, dup_hi = 0;
   size_t spsum_bytes = 0;
   float4* sptab = nullptr;   // [Mpad][kSpK]
   double* spchunk = nullptr; // [sp_P][kSpChunk]

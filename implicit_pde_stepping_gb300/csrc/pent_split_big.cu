@@ -28,6 +28,11 @@ namespace {
 using df::D2;
 
 constexpr int kBigL = 32;       // rows per chunk (the plan's sp_L for long systems)
+
+// Chunk whose tables chunk c uses: chunks dup.x < c <= dup.y have tables
+// bitwise equal to chunk dup.x's (found when the plan was built), so they all
+// read those, which stay in cache.
+__device__ __forceinline__ int table_chunk(int c, int2 dup) { return (c > dup.x && c <= dup.y) ? dup.x : c; }
 constexpr int kBigThreads = 256;
 constexpr int kSum = 8;         // doubles per (chunk, system): e(2) x'start(2) s(2) w(2)
 
@@ -52,7 +57,7 @@ __device__ __forceinline__ void place(int& s, int& c) {
 template <int SPW, bool CYC>
 __global__ void __launch_bounds__(kBigThreads, 2)
     k_big_local(const float4* __restrict__ tab, double* __restrict__ X, double* __restrict__ sum,
-                double* __restrict__ xm, int M, int P, int batch) {
+                double* __restrict__ xm, int M, int P, int batch, int2 dup) {
   constexpr int L = kBigL;
   int s, c;
   place<SPW>(s, c);
@@ -60,7 +65,7 @@ __global__ void __launch_bounds__(kBigThreads, 2)
   const long long ld = batch;
   const int row0 = c * L;
   double* p = X + (long long)row0 * ld + s;
-  const float4* t = tab + (size_t)row0 * kSpK;
+  const float4* t = tab + (size_t)table_chunk(c, dup) * L * kSpK;
   D2 v[L];
   {
     constexpr int G = 16;                         // rows loaded ahead at a time
@@ -113,8 +118,8 @@ __global__ void __launch_bounds__(kBigThreads, 2)
 
 // s_c from the local end values of the T chunks before c
 __device__ __forceinline__ void state_s(const double* __restrict__ ctab, const double* __restrict__ sum,
-                                        int c, int s, int batch, int T, double& s0, double& s1) {
-  const double* ct = ctab + (size_t)c * kSpChunk;
+                                        int c, int s, int batch, int T, int2 dup, double& s0, double& s1) {
+  const double* ct = ctab + (size_t)table_chunk(c, dup) * kSpChunk;
   s0 = s1 = 0.0;
   for (int k = 1; k <= T && k <= c; ++k) {
     const double* e = sum + ((size_t)(c - k) * batch + s) * kSum;
@@ -125,8 +130,9 @@ __device__ __forceinline__ void state_s(const double* __restrict__ ctab, const d
 
 // t_c from w of the T chunks after c
 __device__ __forceinline__ void state_t(const double* __restrict__ ctab, const double* __restrict__ sum,
-                                        int c, int s, int P, int batch, int T, double& t0, double& t1) {
-  const double* ct = ctab + (size_t)c * kSpChunk;
+                                        int c, int s, int P, int batch, int T, int2 dup, double& t0,
+                                        double& t1) {
+  const double* ct = ctab + (size_t)table_chunk(c, dup) * kSpChunk;
   t0 = t1 = 0.0;
   for (int k = 0; k < T && c + 1 + k < P; ++k) {
     const double* w = sum + ((size_t)(c + 1 + k) * batch + s) * kSum + 6;
@@ -137,16 +143,16 @@ __device__ __forceinline__ void state_t(const double* __restrict__ ctab, const d
 
 __global__ void __launch_bounds__(kBigThreads)
     k_big_states(const double* __restrict__ ctab, const double* __restrict__ extra, double* __restrict__ sum,
-                 int P, int batch) {
+                 int P, int batch, int2 dup) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)P * batch) return;
   const int c = (int)(i / batch), s = (int)(i % batch);
   const int T = (int)extra[18];
   double s0, s1;
-  state_s(ctab, sum, c, s, batch, T, s0, s1);
+  state_s(ctab, sum, c, s, batch, T, dup, s0, s1);
   double* o = sum + (size_t)i * kSum;
   double w0 = o[2], w1 = o[3];
-  mv2(ctab + (size_t)c * kSpChunk + 4, s0, s1, w0, w1);   // w_c = x'_start + Mst_c s_c
+  mv2(ctab + (size_t)table_chunk(c, dup) * kSpChunk + 4, s0, s1, w0, w1);   // w_c = x'_start + Mst_c s_c
   o[4] = s0;
   o[5] = s1;
   o[6] = w0;
@@ -156,14 +162,14 @@ __global__ void __launch_bounds__(kBigThreads)
 __global__ void __launch_bounds__(kBigThreads)
     k_big_border(const double* __restrict__ ctab, const double* __restrict__ extra,
                  const double* __restrict__ sum, const double* __restrict__ xm, double* __restrict__ X,
-                 int M, int P, int batch) {
+                 int M, int P, int batch, int2 dup) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
   const long long ld = batch;
   const int T = (int)extra[18];
   // y at rows 0, 1: chunk 0 has s_0 = 0, so y = w_0 + Kst_0 t_0
   double t0, t1;
-  state_t(ctab, sum, 0, s, P, batch, T, t0, t1);
+  state_t(ctab, sum, 0, s, P, batch, T, dup, t0, t1);
   const double* o0 = sum + (size_t)s * kSum;
   double y0 = o0[6], y1 = o0[7];
   mv2(ctab + 8, t0, t1, y0, y1);
@@ -173,7 +179,7 @@ __global__ void __launch_bounds__(kBigThreads)
     const int row = M - 2 + r, c = row / kBigL;
     const double* oc = sum + ((size_t)c * batch + s) * kSum;
     double u0, u1;
-    state_t(ctab, sum, c, s, P, batch, T, u0, u1);
+    state_t(ctab, sum, c, s, P, batch, T, dup, u0, u1);
     const double* mk = extra + 10 + 2 * r;   // M1, M2 at the row; K1, K2 four slots on
     yv[r] = xm[(size_t)s * 2 + r] + mk[0] * oc[4] + mk[1] * oc[5] + mk[4] * u0 + mk[5] * u1;
   }
@@ -188,7 +194,7 @@ template <int SPW, bool CYC>
 __global__ void __launch_bounds__(kBigThreads)
     k_big_fix(const float4* __restrict__ tab, const double* __restrict__ ctab,
               const double* __restrict__ extra, const double* __restrict__ sum, double* __restrict__ X,
-              int M, int P, int batch) {
+              int M, int P, int batch, int2 dup) {
   constexpr int L = kBigL;
   int s, c;
   place<SPW>(s, c);
@@ -199,7 +205,7 @@ __global__ void __launch_bounds__(kBigThreads)
   const int T = (int)extra[18];
   const double* o = sum + ((size_t)c * batch + s) * kSum;
   double t0, t1;
-  state_t(ctab, sum, c, s, P, batch, T, t0, t1);
+  state_t(ctab, sum, c, s, P, batch, T, dup, t0, t1);
   const D2 S0 = df::from_double(o[4]), S1 = df::from_double(o[5]);
   const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
   bool needU = false;
@@ -212,7 +218,7 @@ __global__ void __launch_bounds__(kBigThreads)
   }
   double* p = X + (long long)row0 * ld + s;
   const float2* q = reinterpret_cast<const float2*>(p);
-  const float4* t = tab + (size_t)row0 * kSpK;
+  const float4* t = tab + (size_t)table_chunk(c, dup) * L * kSpK;
   constexpr int G = 8;
 #pragma unroll
   for (int j0 = 0; j0 < L; j0 += G) {
@@ -244,19 +250,20 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   const dim3 grid((batch + SPW - 1) / SPW, (P + CPB - 1) / CPB);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   double* xm = p.spsum + (size_t)P * batch * kSum;
-  k_big_local<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, X, p.spsum, xm, p.M, P, batch);
+  const int2 dup = make_int2(p.dup_lo, p.dup_hi);
+  k_big_local<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, X, p.spsum, xm, p.M, P, batch, dup);
   note_launch();
   const long long n = (long long)P * batch;
   k_big_states<<<(unsigned)((n + kBigThreads - 1) / kBigThreads), kBigThreads, 0, st>>>(
-      p.spchunk, p.spextra, p.spsum, P, batch);
+      p.spchunk, p.spextra, p.spsum, P, batch, dup);
   note_launch();
   if (CYC) {
     k_big_border<<<(batch + kBigThreads - 1) / kBigThreads, kBigThreads, 0, st>>>(
-        p.spchunk, p.spextra, p.spsum, xm, X, p.M, P, batch);
+        p.spchunk, p.spextra, p.spsum, xm, X, p.M, P, batch, dup);
     note_launch();
   }
   k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk, p.spextra, p.spsum, X, p.M, P,
-                                                   batch);
+                                                   batch, dup);
   note_launch();
   return cudaGetLastError();
 }

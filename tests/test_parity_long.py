@@ -65,3 +65,24 @@ def test_long_plan_repeated_solves_and_batch_growth():
         pent.pent_sync()
         assert max_rel_err(host(X), oracle.batch_shared(bands, F)) < TOL_F64
     plan.close()
+
+
+@pytest.mark.parametrize("cyclic", [False, True])
+def test_shared_chunk_tables_change_no_bit(cyclic, monkeypatch):
+    """Interior chunks of a constant-band matrix read one chunk's tables (bitwise equal
+    ones, found when the plan is built); the solution is bit-for-bit that of a plan whose
+    chunks all read their own tables."""
+    N, batch = 40000, 5
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, batch, seed=13)
+    out = []
+    for dedup in ("1", "0"):
+        monkeypatch.setenv("PENT_CHUNK_DEDUP", dedup)
+        plan = pent.pent_factor(bands, batch, cyclic=cyclic)
+        X = dev(F)
+        pent.pent_solve(plan, X)
+        pent.pent_sync()
+        out.append(host(X))
+        plan.close()
+    assert np.array_equal(out[0], out[1])
+    assert max_rel_err(out[0], oracle.batch_shared(bands, F, cyclic=cyclic)) < TOL_F64
