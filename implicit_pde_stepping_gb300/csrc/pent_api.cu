@@ -464,7 +464,7 @@ pent_status hyperdiffusion_step(pent_plan p, void* C, int batch, int nsteps, voi
   if (!p || !C || batch < 1 || nsteps < 0) return PENT_ERR_INVALID_ARG;
   if (!p->cyclic || p->dtype != PENT_F64) return PENT_ERR_INVALID_ARG;
   if (!aligned(C, 16)) return PENT_ERR_INVALID_ARG;
-  // the multi-step kernel is arithmetic-bound (~250 instructions per point and
+  // the multi-step kernel is arithmetic-bound (~160 instructions per point and
   // step); where the twisted kernel runs the single step it is memory-bound and
   // about twice as fast per step, so many steps use it one launch at a time
   if (resolve(*p, batch) != PENT_VARIANT_THREAD_DF && use_steps(*p, nsteps, 0))
