@@ -71,3 +71,39 @@ def test_time_steps_captured_in_cuda_graph(kind):
            "cn": lambda: oracle.batch_cn(C0, sigma, steps)}[kind]()
     assert max_rel_err(host(C), ref) < TOL_F64
     plan.close()
+
+
+@pytest.mark.parametrize("kind", ["persys", "tri"])
+def test_per_system_solves_captured_in_cuda_graph(kind):
+    """The partitioned fp32 kernels build their TMA tensor maps on the host at each
+    call and pass them by value, so a captured call replays on whatever the captured
+    buffers hold at replay time."""
+    import torch
+    from tests.gpu_util import TOL_F32
+    N, batch = 256, 4096
+    if kind == "persys":
+        bands = [dev(v) for v in inputs.persys_bands(N, batch, seed=4)]
+        ref = lambda F: oracle.batch_persys(*[host(b) for b in bands], F)  # noqa: E731
+        call = lambda X, s: pent.pent_factor_solve(*bands, X, stream=s)  # noqa: E731
+    else:
+        bands = [dev(v) for v in inputs.tri_bands(N, batch, seed=4)]
+        ref = lambda F: oracle.batch_tri(*[host(b) for b in bands], F)  # noqa: E731
+        call = lambda X, s: pent.tri_factor_solve(*bands, X, stream=s)  # noqa: E731
+    F1 = inputs.rhs_uniform(N, batch, seed=5).astype(np.float32)
+    F2 = inputs.rhs_uniform(N, batch, seed=6).astype(np.float32)
+    X = dev(F1)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        call(X, s)
+    s.synchronize()
+    X.copy_(dev(F1))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(X, s)
+    g.replay()
+    torch.cuda.synchronize()
+    assert max_rel_err(host(X), ref(F1)) < TOL_F32
+    X.copy_(dev(F2))
+    g.replay()
+    torch.cuda.synchronize()
+    assert max_rel_err(host(X), ref(F2)) < TOL_F32
