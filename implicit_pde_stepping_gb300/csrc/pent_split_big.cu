@@ -19,6 +19,7 @@
 // Memory traffic: f read, x' written and read, x written (four arrays, as the
 // twisted kernel), plus summaries of 64 bytes per chunk.  The parallelism is
 // batch x P threads, so a handful of very long systems still fills the GPU.
+#include "cp_async.cuh"
 #include "df64.cuh"
 #include "pent_internal.cuh"
 
@@ -66,25 +67,24 @@ __global__ void __launch_bounds__(kBigThreads, 2)
   const int row0 = c * L;
   double* p = X + (long long)row0 * ld + s;
   const float4* t = tab + (size_t)table_chunk(c, dup) * L * kSpK;
+  // the chunk's f into this thread's shared-memory column, every row in flight at once
+  extern __shared__ double sf[];                  // [L][kBigThreads]
+  double* mine = sf + threadIdx.x;
+#pragma unroll
+  for (int j = 0; j < L; ++j)
+    if (row0 + j < M) cp_async8(mine + j * kBigThreads, p + (long long)j * ld);
+  cp_async_wait_all();
   D2 v[L];
   {
-    constexpr int G = 16;                         // rows loaded ahead at a time
     D2 a1{0.f, 0.f}, a2{0.f, 0.f};
 #pragma unroll
-    for (int j0 = 0; j0 < L; j0 += G) {
-      double fv[G];
-#pragma unroll
-      for (int u = 0; u < G; ++u) fv[u] = (row0 + j0 + u < M) ? p[(j0 + u) * ld] : 0.0;
-#pragma unroll
-      for (int u = 0; u < G; ++u) {
-        const int j = j0 + u;
-        const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
-        const D2 g = df::sum3p(D2{c0.x, c0.y}, df::from_double(fv[u]), D2{c0.z, c0.w}, a2,
-                               D2{c1.x, c1.y}, a1);
-        v[j] = g;
-        a2 = a1;
-        a1 = g;
-      }
+    for (int j = 0; j < L; ++j) {
+      const double f = (row0 + j < M) ? mine[j * kBigThreads] : 0.0;
+      const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
+      const D2 g = df::sum3p(D2{c0.x, c0.y}, df::from_double(f), D2{c0.z, c0.w}, a2, D2{c1.x, c1.y}, a1);
+      v[j] = g;
+      a2 = a1;
+      a1 = g;
     }
   }
   double* o = sum + ((size_t)c * batch + s) * kSum;
@@ -251,7 +251,10 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   double* xm = p.spsum + (size_t)P * batch * kSum;
   const int2 dup = make_int2(p.dup_lo, p.dup_hi);
-  k_big_local<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, X, p.spsum, xm, p.M, P, batch, dup);
+  const size_t smem_local = (size_t)kBigL * kBigThreads * sizeof(double);
+  cudaError_t e = kernel_prepare((const void*)k_big_local<SPW, CYC>, smem_local, kBigThreads, nullptr);
+  if (e != cudaSuccess) return e;
+  k_big_local<SPW, CYC><<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, p.M, P, batch, dup);
   note_launch();
   const long long n = (long long)P * batch;
   k_big_states<<<(unsigned)((n + kBigThreads - 1) / kBigThreads), kBigThreads, 0, st>>>(
