@@ -34,6 +34,7 @@
 // block in the reduced system is singular or not finite.
 #include <climits>
 
+#include "cp_async.cuh"
 #include "pent_internal.cuh"
 #include "tma.cuh"
 
@@ -50,14 +51,6 @@ struct PsMaps {
 __device__ __forceinline__ bool bad_pivot(float d) { return !(d != 0.f) || !isfinite(d); }
 // fast reciprocal (about 1 ulp; the fp32 solve's tolerance is far wider)
 __device__ __forceinline__ float rcp(float x) { return __fdividef(1.f, x); }
-
-__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_commit_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
 
 // 2x2 blocks, row-major {m00, m01, m10, m11}
 struct M2 {
@@ -142,7 +135,7 @@ __global__ void __launch_bounds__(kSB * P, P <= 16 ? 2 : 1)
         for (int arr = 0; arr < 6; ++arr) cp_async4(&stage[(arr * L + j) * NT + tid], src[arr] + o);
       }
     }
-    cp_commit_wait_all();
+    cp_async_wait_all();
   }
   auto staged = [&](int arr, int j) -> float {
     return TMA ? stage[((size_t)arr * RS + row0 + j) * SB + lane] : stage[(arr * L + j) * NT + tid];

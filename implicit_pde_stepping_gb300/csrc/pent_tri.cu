@@ -39,6 +39,7 @@
 //   Where a tensor map cannot describe the arrays (base or row pitch not a
 //   multiple of 16 bytes) every thread stages its own rows with 4-byte
 //   cp.async instead.
+#include "cp_async.cuh"
 #include "pent_internal.cuh"
 #include "tma.cuh"
 
@@ -127,16 +128,6 @@ __global__ void __launch_bounds__(kThreads)
 // ---------------------------------------------------------------------------
 constexpr int kTriSB = 16;    // systems per CTA
 
-// 4-byte asynchronous global -> shared copy (all of a thread's rows are put in
-// flight at once, without holding registers)
-__device__ __forceinline__ void cp_async4(float* smem, const float* gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_commit_wait_all() {
-  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
 struct TriMaps {
   CUtensorMap m[4];   // a, b, c, y
 };
@@ -195,7 +186,7 @@ __global__ void __launch_bounds__(kTriSB * P, P <= 16 ? 3 : 1)
         cp_async4(&stage[(3 * L + j) * NT + tid], X + o);
       }
     }
-    cp_commit_wait_all();
+    cp_async_wait_all();
   }
   auto staged = [&](int arr, int j) -> float {
     return TMA ? stage[((size_t)arr * RS + row0 + j) * SB + lane] : stage[(arr * L + j) * NT + tid];

@@ -338,16 +338,8 @@ __global__ void __launch_bounds__(2 * SPB / SPT)
   }
 }
 
-// ---- asynchronous row streaming (cp.async: global -> shared, no registers held)
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int NPEND>
-__device__ __forceinline__ void cp_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(NPEND) : "memory");
-}
+// ---- asynchronous row streaming (cp.async: global -> shared, no registers held;
+// the copy helpers are in cp_async.cuh)
 __device__ __forceinline__ void unpack2(const uint4 r, double* v) {
   v[0] = __hiloint2double((int)r.y, (int)r.x);
   v[1] = __hiloint2double((int)r.w, (int)r.z);
