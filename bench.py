@@ -52,6 +52,9 @@ WORKLOADS = {
     "tri_bi16": dict(N=256, batch=262144, kind="tri", dtype="f32", bs=16,
                      desc="per-system tridiagonal factor+solve, block-interleaved layout (blocks of 16 "
                           "systems), N=256, batch=262144, fp32, diagonally dominant"),
+    "persys_bi16": dict(N=256, batch=262144, kind="persys", dtype="f32", bs=16,
+                        desc="per-system factor+solve, block-interleaved layout (blocks of 16 systems), "
+                             "N=256, batch=262144, fp32, diagonally dominant"),
     "persys": dict(N=256, batch=262144, kind="persys", dtype="f32",
                    desc="per-system factor+solve, N=256, batch=262144, fp32, diagonally dominant"),
     "cn": dict(N=512, batch=4096, kind="cn", sigma=0.25, cyclic=True, dtype="f64",
@@ -260,24 +263,19 @@ def run_ours(args, W: dict, dist: Dist):
         plan = pent.pent_factor(inputs.hyper_bands(N, sigma), batch, cyclic=True)
         bufs = [torch.from_numpy(inputs.ch_initial(N, batch, seed=seed + r)).to("cuda")
                 for r in range(2)]
-    elif kind == "tri":
+    elif kind in ("tri", "persys"):
         bs = W.get("bs", 0)
 
         def lay(x):   # interleaved [N][batch] -> the workload's layout
             if not bs:
                 return np.ascontiguousarray(x)
             return np.ascontiguousarray(x.reshape(N, batch // bs, bs).transpose(1, 0, 2))
-        bands = [torch.from_numpy(lay(v)).to("cuda") for v in inputs.tri_bands(N, batch, seed=seed)]
+        gen = inputs.tri_bands if kind == "tri" else inputs.persys_bands
+        bands = [torch.from_numpy(lay(v)).to("cuda") for v in gen(N, batch, seed=seed)]
         bufs = [torch.from_numpy(lay(inputs.rhs_uniform(N, batch, seed=seed + r).astype(np.float32)))
                 .to("cuda") for r in range(2)]
-        work = torch.empty(pent.tri_factor_solve_work_bytes(N, batch, pent.F32),
-                           dtype=torch.uint8, device="cuda")
-    else:  # persys
-        bands = [torch.from_numpy(v).to("cuda") for v in inputs.persys_bands(N, batch, seed=seed)]
-        bufs = [torch.from_numpy(inputs.rhs_uniform(N, batch, seed=seed + r).astype(np.float32))
-                .to("cuda") for r in range(2)]
-        work = torch.empty(pent.pent_factor_solve_work_bytes(N, batch, pent.F32),
-                           dtype=torch.uint8, device="cuda")
+        wb = (pent.tri_factor_solve_work_bytes if kind == "tri" else pent.pent_factor_solve_work_bytes)
+        work = torch.empty(wb(N, batch, pent.F32), dtype=torch.uint8, device="cuda")
     if plan is not None and args.variant != "auto":
         plan.set_variant(args.variant)
     variant = plan.variant(batch) if plan is not None else pent.VARIANT_THREAD
@@ -309,7 +307,8 @@ def run_ours(args, W: dict, dist: Dist):
             pent.tri_factor_solve(*bands, X, variant=tri_variant, work=work, stream=stream,
                                   block_size=W.get("bs", 0))
         else:
-            pent.pent_factor_solve(*bands, X, work=work, stream=stream, variant=tri_variant)
+            pent.pent_factor_solve(*bands, X, work=work, stream=stream, variant=tri_variant,
+                                   block_size=W.get("bs", 0))
 
     # ---- device-resident timing
     with torch.cuda.stream(stream):
@@ -363,7 +362,8 @@ def run_ours(args, W: dict, dist: Dist):
                 db.copy_(hb, non_blocking=True)
             Xd.copy_(host_in, non_blocking=True)
             if kind == "persys":
-                pent.pent_factor_solve(*dev_bands, Xd, work=work, stream=stream, variant=tri_variant)
+                pent.pent_factor_solve(*dev_bands, Xd, work=work, stream=stream, variant=tri_variant,
+                                       block_size=W.get("bs", 0))
             elif kind == "tri":
                 pent.tri_factor_solve(*dev_bands, Xd, variant=tri_variant, work=work, stream=stream,
                                       block_size=W.get("bs", 0))

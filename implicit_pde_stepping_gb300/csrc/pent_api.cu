@@ -397,9 +397,10 @@ size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {
 
 pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, const void* d,
                                  const void* e, void* rhs, int N, int batch, pent_dtype dtype,
-                                 pent_variant variant, void* work, size_t work_bytes, int* info,
-                                 void* stream) {
+                                 pent_variant variant, int block_size, void* work, size_t work_bytes,
+                                 int* info, void* stream) {
   if (!a || !b || !c || !d || !e || !rhs || N < 1 || batch < 1) return PENT_ERR_INVALID_ARG;
+  if (block_size < 0 || (block_size > 0 && batch % block_size != 0)) return PENT_ERR_INVALID_ARG;
   if (dtype != PENT_F64 && dtype != PENT_F32) return PENT_ERR_INVALID_ARG;
   const void* ptrs[6] = {a, b, c, d, e, rhs};
   for (const void* q : ptrs)
@@ -415,17 +416,18 @@ pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, co
       break;
     default: return PENT_ERR_INVALID_ARG;
   }
-  if (split) return from_cuda(persys_split(a, b, c, d, e, rhs, N, batch, info, as_stream(stream)));
+  if (split) return from_cuda(persys_split(a, b, c, d, e, rhs, N, batch, block_size, info, as_stream(stream)));
   if (!work || work_bytes < persys_work_bytes(N, batch, dtype) || !aligned(work, 256)) return PENT_ERR_INVALID_ARG;
-  return from_cuda(persys_thread(a, b, c, d, e, rhs, N, batch, dtype, work, info, as_stream(stream)));
+  return from_cuda(persys_thread(a, b, c, d, e, rhs, N, batch, block_size, dtype, work, info,
+                                 as_stream(stream)));
 }
 
 pent_status pent_factor_solve(const void* a, const void* b, const void* c, const void* d,
                               const void* e, void* rhs, int N, int batch, pent_dtype dtype,
                               void* work, size_t work_bytes, int* info, void* stream) {
   if (!work || work_bytes < persys_work_bytes(N, batch, dtype) || !aligned(work, 256)) return PENT_ERR_INVALID_ARG;
-  return pent_factor_solve_ex(a, b, c, d, e, rhs, N, batch, dtype, PENT_VARIANT_AUTO, work, work_bytes, info,
-                              stream);
+  return pent_factor_solve_ex(a, b, c, d, e, rhs, N, batch, dtype, PENT_VARIANT_AUTO, 0, work, work_bytes,
+                              info, stream);
 }
 
 size_t tri_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {

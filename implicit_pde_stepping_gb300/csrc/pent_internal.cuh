@@ -94,14 +94,15 @@ cudaError_t shared_thread_f32(const pent_plan_s& p, float* X, int batch, cudaStr
 cudaError_t shared_twisted_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 
 // persys.cu
+// bs = 0: interleaved [N][batch]; bs > 0: block-interleaved, blocks of bs systems
 cudaError_t persys_thread(const void* a, const void* b, const void* c, const void* d, const void* e,
-                          void* X, int N, int batch, pent_dtype dt, void* work, int* info,
+                          void* X, int N, int batch, int bs, pent_dtype dt, void* work, int* info,
                           cudaStream_t st);
 size_t persys_work_bytes(int N, int batch, pent_dtype dt);
 // persys_split.cu: partitioned fp32 kernel (chunks of 16 rows, TMA tiles)
 int persys_split_chunks(int N);   // chunks per system for N rows, 0 if N > 512
 cudaError_t persys_split(const void* a, const void* b, const void* c, const void* d, const void* e, void* X,
-                         int N, int batch, int* info, cudaStream_t st);
+                         int N, int batch, int bs, int* info, cudaStream_t st);
 
 // tri.cu: per-system tridiagonal solves (Thomas algorithm; partitioned fp32 kernel)
 int tri_split_chunks(int N);   // chunks of the partitioned kernel for N rows, 0 if too large

@@ -68,7 +68,7 @@ extern "C" pent_status pent_factor_solve_noalloc(const void* a, const void* b, c
     if (!aligned16(q)) return PENT_ERR_INVALID_ARG;
   // fp32 systems of up to 512 rows take the partitioned kernel, which needs no scratch
   if (dtype == PENT_F32 && pent::persys_split_chunks(N) > 0) {
-    const cudaError_t err = pent::persys_split(a, b, c, d, e, rhs_inout, N, batch, info,
+    const cudaError_t err = pent::persys_split(a, b, c, d, e, rhs_inout, N, batch, 0, info,
                                                static_cast<cudaStream_t>(stream));
     return err == cudaSuccess ? PENT_OK : PENT_ERR_CUDA;
   }
@@ -79,7 +79,7 @@ extern "C" pent_status pent_factor_solve_noalloc(const void* a, const void* b, c
     cudaGetLastError();
     return PENT_ERR_CUDA;
   }
-  err = pent::persys_thread(a, b, c, d, e, rhs_inout, N, batch, dtype, scratch, info,
+  err = pent::persys_thread(a, b, c, d, e, rhs_inout, N, batch, 0, dtype, scratch, info,
                             static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? PENT_OK : PENT_ERR_CUDA;
 }

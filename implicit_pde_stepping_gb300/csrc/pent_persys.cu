@@ -11,6 +11,10 @@
 // and stay unchanged: gamma_i and delta_i go to the caller's scratch `work`
 // (two interleaved [N][batch] arrays), and g is written over the right-hand
 // side in place, read back by the backward sweep.
+//
+// Layouts of the bands and the right-hand side: interleaved [N][batch], or
+// block-interleaved with blocks of bs systems ((i, s) at (s / bs) N bs +
+// i bs + s % bs); the scratch stays interleaved.
 #include "pent_internal.cuh"
 
 namespace pent {
@@ -23,10 +27,12 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
     k_persys_thread(const T* __restrict__ A, const T* __restrict__ B, const T* __restrict__ C,
                     const T* __restrict__ D, const T* __restrict__ E, T* __restrict__ X,
-                    T* __restrict__ Wg, T* __restrict__ Wd, int N, int batch, int* __restrict__ info) {
+                    T* __restrict__ Wg, T* __restrict__ Wd, int N, int batch, int bs, int* __restrict__ info) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
-  const size_t ld = (size_t)batch;
+  const size_t ld = bs ? (size_t)bs : (size_t)batch;                          // row stride of the data
+  const size_t sb = bs ? (size_t)(s / bs) * N * bs + s % bs : (size_t)s;     // row 0 of system s
+  const size_t lw = (size_t)batch;                                             // scratch: interleaved
   T gm1 = T(0), gm2 = T(0), dm1 = T(0), dm2 = T(0), g1 = T(0), g2 = T(0);
   int bad = 0;
   for (int i0 = 0; i0 < N; i0 += kUnroll) {
@@ -34,7 +40,7 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 + u;
-      const size_t o = (size_t)i * ld + s;
+      const size_t o = (size_t)i * ld + sb;
       const bool in = i < N;
       a[u] = (in && i >= 2) ? A[o] : T(0);
       b[u] = (in && i >= 1) ? B[o] : T(0);
@@ -47,7 +53,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 + u;
       if (i < N) {
-        const size_t o = (size_t)i * ld + s;
+        const size_t o = (size_t)i * ld + sb, ow = (size_t)i * lw + s;
         const T beta = b[u] - a[u] * gm2;
         const T alpha = c[u] - a[u] * dm2 - beta * gm1;
         if (bad == 0 && !(alpha != T(0) && isfinite(alpha))) bad = i + 1;
@@ -55,8 +61,8 @@ __global__ void __launch_bounds__(kThreads)
         const T gam = (d[u] - beta * dm1) * ra;
         const T del = e[u] * ra;
         const T g = (f[u] - a[u] * g2 - beta * g1) * ra;
-        Wg[o] = gam;
-        Wd[o] = del;
+        Wg[ow] = gam;
+        Wd[ow] = del;
         X[o] = g;
         gm2 = gm1; gm1 = gam;
         dm2 = dm1; dm1 = del;
@@ -70,17 +76,17 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 - u;
-      const size_t o = (size_t)(i >= 0 ? i : 0) * ld + s;
+      const size_t o = (size_t)(i >= 0 ? i : 0) * ld + sb, ow = (size_t)(i >= 0 ? i : 0) * lw + s;
       gv[u] = (i >= 0) ? X[o] : T(0);
-      gm[u] = (i >= 0) ? Wg[o] : T(0);
-      dl[u] = (i >= 0) ? Wd[o] : T(0);
+      gm[u] = (i >= 0) ? Wg[ow] : T(0);
+      dl[u] = (i >= 0) ? Wd[ow] : T(0);
     }
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 - u;
       if (i >= 0) {
         const T x = gv[u] - gm[u] * x1 - dl[u] * x2;
-        X[(size_t)i * ld + s] = x;
+        X[(size_t)i * ld + sb] = x;
         x2 = x1;
         x1 = x;
       }
@@ -91,13 +97,13 @@ __global__ void __launch_bounds__(kThreads)
 
 template <typename T>
 cudaError_t launch(const void* a, const void* b, const void* c, const void* d, const void* e,
-                   void* X, int N, int batch, void* work, int* info, cudaStream_t st) {
+                   void* X, int N, int batch, int bs, void* work, int* info, cudaStream_t st) {
   T* Wg = static_cast<T*>(work);
   T* Wd = Wg + (size_t)N * batch;
   const int grid = (batch + kThreads - 1) / kThreads;
   k_persys_thread<T><<<grid, kThreads, 0, st>>>(
       static_cast<const T*>(a), static_cast<const T*>(b), static_cast<const T*>(c),
-      static_cast<const T*>(d), static_cast<const T*>(e), static_cast<T*>(X), Wg, Wd, N, batch,
+      static_cast<const T*>(d), static_cast<const T*>(e), static_cast<T*>(X), Wg, Wd, N, batch, bs,
       info);
   note_launch();
   return cudaGetLastError();
@@ -111,10 +117,10 @@ size_t persys_work_bytes(int N, int batch, pent_dtype dt) {
 }
 
 cudaError_t persys_thread(const void* a, const void* b, const void* c, const void* d, const void* e,
-                          void* X, int N, int batch, pent_dtype dt, void* work, int* info,
+                          void* X, int N, int batch, int bs, pent_dtype dt, void* work, int* info,
                           cudaStream_t st) {
-  if (dt == PENT_F64) return launch<double>(a, b, c, d, e, X, N, batch, work, info, st);
-  return launch<float>(a, b, c, d, e, X, N, batch, work, info, st);
+  if (dt == PENT_F64) return launch<double>(a, b, c, d, e, X, N, batch, bs, work, info, st);
+  return launch<float>(a, b, c, d, e, X, N, batch, bs, work, info, st);
 }
 
 }  // namespace pent

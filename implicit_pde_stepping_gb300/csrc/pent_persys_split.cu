@@ -28,6 +28,11 @@
 //      reduction over P lanes with warp shuffles (each block row normalised
 //      by its diagonal block first, so that a step exchanges 10 values).
 //   4. Every row from form 2 with t_{c-1} and t_c.
+// Layouts: interleaved [N][batch] (element (i, s) at i * batch + s), or
+// block-interleaved with blocks of bs systems, each block an interleaved
+// [N][bs] array: (i, s) at (s / bs) N bs + i bs + s % bs ("Simulating the
+// behavior of the human brain on GPUs", section 4.1.1).  The TMA path loads a
+// block-interleaved tile with 3-D tensor maps (bs a multiple of 16).
 // No pivoting, as on the page (diagonally dominant or SPD matrices).  The
 // chunk-local pivots are checked, and the first row whose pivot is zero or not
 // finite is reported; failing that, the last row of the first chunk whose 2x2
@@ -93,8 +98,8 @@ template <int P, bool TMA>
 __global__ void __launch_bounds__(kSB * P, P <= 16 ? 2 : 1)
     k_persys_split(const __grid_constant__ PsMaps maps, const float* __restrict__ A,
                    const float* __restrict__ B, const float* __restrict__ C, const float* __restrict__ D,
-                   const float* __restrict__ E, float* __restrict__ X, int N, int batch, int RS, int BR,
-                   int* __restrict__ info) {
+                   const float* __restrict__ E, float* __restrict__ X, int N, int batch, int bs, int RS,
+                   int BR, int* __restrict__ info) {
   constexpr int SB = kSB, L = kL, NT = SB * P;
   extern __shared__ __align__(128) float smem[];
   float* const stage = smem;
@@ -108,7 +113,8 @@ __global__ void __launch_bounds__(kSB * P, P <= 16 ? 2 : 1)
   const int c = tid / SB;        //                 its chunk
   const int s = blockIdx.x * SB + lane;
   const bool act = s < batch;
-  const size_t ld = (size_t)batch;
+  const size_t ld = bs ? (size_t)bs : (size_t)batch;                          // row stride
+  const size_t sb = bs ? (size_t)(s / bs) * N * bs + s % bs : (size_t)s;     // row 0 of system s
   const int row0 = c * L;
   if (tid < SB) sBad[tid] = sBadR[tid] = INT_MAX;
 
@@ -121,7 +127,11 @@ __global__ void __launch_bounds__(kSB * P, P <= 16 ? 2 : 1)
       tma::mbar_expect_tx(&bar, (unsigned)(6 * RS * SB * sizeof(float)));
       for (int arr = 0; arr < 6; ++arr)
         for (int y0 = 0; y0 < RS; y0 += BR)
-          tma::load_2d(stage + ((size_t)arr * RS + y0) * SB, &maps.m[arr], blockIdx.x * SB, y0, &bar);
+          if (bs)
+            tma::load_3d(stage + ((size_t)arr * RS + y0) * SB, &maps.m[arr], (blockIdx.x * SB) % bs, y0,
+                         (blockIdx.x * SB) / bs, &bar);
+          else
+            tma::load_2d(stage + ((size_t)arr * RS + y0) * SB, &maps.m[arr], blockIdx.x * SB, y0, &bar);
     }
     if (!tma::mbar_wait(&bar, 0, 2000000000ull)) bad = -1;   // 2 s: the copy never arrived
   } else {
@@ -130,7 +140,7 @@ __global__ void __launch_bounds__(kSB * P, P <= 16 ? 2 : 1)
     for (int j = 0; j < L; ++j) {
       const int i = row0 + j;
       if (act && i < N) {
-        const size_t o = (size_t)i * ld + s;
+        const size_t o = (size_t)i * ld + sb;
 #pragma unroll
         for (int arr = 0; arr < 6; ++arr) cp_async4(&stage[(arr * L + j) * NT + tid], src[arr] + o);
       }
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(kSB * P, P <= 16 ? 2 : 1)
   for (int j = 0; j < L; ++j) {
     const int i = row0 + j;
     const float x = fmaf(-dl[j], v1, fmaf(-gm[j], v0, fmaf(-qq[j], u1, fmaf(-pp[j], u0, gg[j]))));
-    if (act && i < N) X[(size_t)i * ld + s] = x;
+    if (act && i < N) X[(size_t)i * ld + sb] = x;
   }
   if (c == 0 && act && info) {
     // a failed local pivot also spoils the reduced system: report the pivot
@@ -274,17 +284,20 @@ __global__ void __launch_bounds__(kSB * P, P <= 16 ? 2 : 1)
 
 template <int P>
 cudaError_t launch(const void* a, const void* b, const void* c, const void* d, const void* e, void* X,
-                   int N, int batch, int* info, cudaStream_t st) {
+                   int N, int batch, int bs, int* info, cudaStream_t st) {
   const int grid = (batch + kSB - 1) / kSB;
   // TMA boxes of BR rows (even, <= 256) covering RS >= N rows
   const int BR = N <= 256 ? ((N + 1) & ~1) : 256;
   const int RS = (N + BR - 1) / BR * BR;
   PsMaps maps;
   const void* ptr[6] = {a, b, c, d, e, X};
-  bool tma_ok = true;
+  // a CTA's 16 systems must lie in one block of a block-interleaved array
+  bool tma_ok = bs == 0 || bs % kSB == 0;
   for (int k = 0; k < 6 && tma_ok; ++k)
-    tma_ok = tma::encode_2d(&maps.m[k], ptr[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float), batch, N,
-                            kSB, (unsigned)BR);
+    tma_ok = bs ? tma::encode_3d_blocked(&maps.m[k], ptr[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float),
+                                         bs, N, batch / bs, kSB, (unsigned)BR)
+                : tma::encode_2d(&maps.m[k], ptr[k], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, sizeof(float), batch,
+                                 N, kSB, (unsigned)BR);
   const size_t stage = tma_ok ? (size_t)6 * RS * kSB * sizeof(float)
                               : (size_t)6 * kL * kSB * P * sizeof(float);
   const size_t iface = (size_t)(kIface + 2) * P * (kSB + 1) * sizeof(float);
@@ -294,8 +307,8 @@ cudaError_t launch(const void* a, const void* b, const void* c, const void* d, c
   if (err != cudaSuccess) return err;
   kern<<<grid, kSB * P, smem, st>>>(maps, static_cast<const float*>(a), static_cast<const float*>(b),
                                      static_cast<const float*>(c), static_cast<const float*>(d),
-                                     static_cast<const float*>(e), static_cast<float*>(X), N, batch, RS,
-                                     BR, info);
+                                     static_cast<const float*>(e), static_cast<float*>(X), N, batch, bs,
+                                     RS, BR, info);
   note_launch();
   return cudaGetLastError();
 }
@@ -310,13 +323,13 @@ int persys_split_chunks(int N) {
 }
 
 cudaError_t persys_split(const void* a, const void* b, const void* c, const void* d, const void* e, void* X,
-                         int N, int batch, int* info, cudaStream_t st) {
+                         int N, int batch, int bs, int* info, cudaStream_t st) {
   switch (persys_split_chunks(N)) {
-    case 2: return launch<2>(a, b, c, d, e, X, N, batch, info, st);
-    case 4: return launch<4>(a, b, c, d, e, X, N, batch, info, st);
-    case 8: return launch<8>(a, b, c, d, e, X, N, batch, info, st);
-    case 16: return launch<16>(a, b, c, d, e, X, N, batch, info, st);
-    case 32: return launch<32>(a, b, c, d, e, X, N, batch, info, st);
+    case 2: return launch<2>(a, b, c, d, e, X, N, batch, bs, info, st);
+    case 4: return launch<4>(a, b, c, d, e, X, N, batch, bs, info, st);
+    case 8: return launch<8>(a, b, c, d, e, X, N, batch, bs, info, st);
+    case 16: return launch<16>(a, b, c, d, e, X, N, batch, bs, info, st);
+    case 32: return launch<32>(a, b, c, d, e, X, N, batch, bs, info, st);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -49,7 +49,7 @@ def lib():
             L.pent_solve.argtypes = [vp, vp, i, vp]
             L.pent_solve_host.argtypes = [vp, vp, vp, i, i, vp]
             L.pent_factor_solve.argtypes = [vp] * 6 + [i, i, i, vp, sz, vp, vp]
-            L.pent_factor_solve_ex.argtypes = [vp] * 6 + [i, i, i, i, vp, sz, vp, vp]
+            L.pent_factor_solve_ex.argtypes = [vp] * 6 + [i, i, i, i, i, vp, sz, vp, vp]
             L.pent_factor_solve_work_bytes.argtypes = [i, i, i]
             L.pent_factor_solve_work_bytes.restype = sz
             L.pent_factor_solve_noalloc.argtypes = [vp] * 6 + [i, i, i, vp, vp]
@@ -197,14 +197,30 @@ def pent_factor_solve_work_bytes(N: int, batch: int, dtype) -> int:
     return int(lib().pent_factor_solve_work_bytes(int(N), int(batch), code))
 
 
-def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None, variant: str = "auto"):
+def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None, variant: str = "auto",
+                      block_size: int = 0):
     """Per-system factor + solve, in place in rhs.  variant: "auto", "thread" or "split"
     (fp32, N <= 512).  work: a CUDA uint8 tensor of at least pent_factor_solve_work_bytes()
-    bytes (allocated here if None; unused by the split kernel).  info: CUDA int32 [batch]."""
+    bytes (allocated here if None; unused by the split kernel).  info: CUDA int32 [batch].
+    block_size 0: arrays interleaved [N][batch]; block_size bs > 0: block-interleaved,
+    arrays shaped [batch / bs][N][bs]."""
     import torch
-    N, batch = rhs.shape
-    code = _dtype_code(rhs)
-    ptrs = [_ptr(t, N, code, n) for t, n in zip((a, b, c, d, e), "abcde")]
+    if block_size:
+        nb, N, bs = rhs.shape
+        if bs != block_size:
+            raise ValueError("block-interleaved arrays must be [batch / bs][N][bs]")
+        batch = nb * bs
+        for t, n in zip((a, b, c, d, e, rhs), "abcder"):
+            if t.shape != rhs.shape or not t.is_cuda or not t.is_contiguous() or t.dtype != rhs.dtype:
+                raise ValueError(f"{n} must match rhs: contiguous CUDA [batch / bs][N][bs]")
+        code = _dtype_code(rhs)
+        ptrs = [ctypes.c_void_p(t.data_ptr()) for t in (a, b, c, d, e)]
+        rp = ctypes.c_void_p(rhs.data_ptr())
+    else:
+        N, batch = rhs.shape
+        code = _dtype_code(rhs)
+        ptrs = [_ptr(t, N, code, n) for t, n in zip((a, b, c, d, e), "abcde")]
+        rp = _ptr(rhs, N, code, "rhs")
     need = pent_factor_solve_work_bytes(N, batch, code)
     if work is None:
         work = torch.empty(need, dtype=torch.uint8, device=rhs.device)
@@ -215,10 +231,9 @@ def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None, var
         if info.dtype != torch.int32 or info.numel() < batch or not info.is_cuda:
             raise ValueError("info must be a CUDA int32 tensor of >= batch elements")
         ip = ctypes.c_void_p(info.data_ptr())
-    _check(lib().pent_factor_solve_ex(*ptrs, _ptr(rhs, N, code, "rhs"), N, batch, code,
-                                      VARIANTS[variant], ctypes.c_void_p(work.data_ptr()),
-                                      work.numel() * work.element_size(), ip, _stream(stream)),
-           "pent_factor_solve")
+    _check(lib().pent_factor_solve_ex(*ptrs, rp, N, batch, code, VARIANTS[variant], int(block_size),
+                                      ctypes.c_void_p(work.data_ptr()), work.numel() * work.element_size(),
+                                      ip, _stream(stream)), "pent_factor_solve")
     return work
 
 

@@ -152,17 +152,25 @@ pent_status pent_factor_solve(const void* a, const void* b, const void* c, const
  *             once; `work` is not used and may be NULL;
  *             PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD.
  *             PENT_VARIANT_THREAD_DF is not a per-system variant.
+ *   block_size : 0 — a..e and rhs_inout interleaved [N][batch], element (i, s)
+ *             at i * batch + s; bs > 0 — the block-interleaved layout of
+ *             "Simulating the behavior of the human brain on GPUs", section
+ *             4.1.1: blocks of bs systems, each block an interleaved [N][bs]
+ *             array, (i, s) at (s / bs) * N * bs + i * bs + s % bs; batch must
+ *             be a multiple of bs.  The SPLIT kernel loads a block-interleaved
+ *             tile with one box per array when bs is a multiple of 16.  `work`
+ *             keeps its own layout whatever bs is.
  *   other arguments as for pent_factor_solve; `work` is required (non-NULL,
  *   large enough, 256-byte aligned) only when THREAD runs.
  * Errors: PENT_ERR_INVALID_ARG for null or misaligned pointers, N or batch < 1,
- * a bad dtype or variant, or a missing or short work buffer where THREAD
- * runs; PENT_ERR_UNSUPPORTED for SPLIT outside fp32 / N <= 512.  Nothing is
+ * a bad dtype, variant or block_size, or a missing or short work buffer where
+ * THREAD runs; PENT_ERR_UNSUPPORTED for SPLIT outside fp32 / N <= 512.  Nothing is
  * queued on an error.
  */
 pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, const void* d,
                                  const void* e, void* rhs_inout, int N, int batch, pent_dtype dtype,
-                                 pent_variant variant, void* work, size_t work_bytes, int* info,
-                                 void* stream);
+                                 pent_variant variant, int block_size, void* work, size_t work_bytes,
+                                 int* info, void* stream);
 
 /* Bytes of device scratch pent_factor_solve needs for (N, batch, dtype). */
 size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);

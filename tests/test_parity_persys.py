@@ -113,10 +113,10 @@ def test_split_needs_no_work_buffer():
     vp = [ctypes.c_void_p(t.data_ptr()) for t in bands]
     st = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     assert L.pent_factor_solve_ex(*vp, ctypes.c_void_p(X.data_ptr()), N, batch, pent.F32,
-                                  pent.VARIANT_THREAD, None, 0, None, st) == pent.ERR_INVALID_ARG
+                                  pent.VARIANT_THREAD, 0, None, 0, None, st) == pent.ERR_INVALID_ARG
     assert np.array_equal(host(X), F)
     assert L.pent_factor_solve_ex(*vp, ctypes.c_void_p(X.data_ptr()), N, batch, pent.F32,
-                                  pent.VARIANT_SPLIT, None, 0, None, st) == pent.OK
+                                  pent.VARIANT_SPLIT, 0, None, 0, None, st) == pent.OK
     pent.pent_sync()
     ref = oracle.batch_persys(*[host(t) for t in bands], F)
     assert max_rel_err(host(X), ref) < TOL_F32
@@ -130,3 +130,45 @@ def test_work_too_small_rejected():
     small = torch.empty(16, dtype=torch.uint8, device="cuda")
     with pytest.raises(ValueError):
         pent.pent_factor_solve(*bands, X, work=small)
+
+
+def to_blocked(v, bs):
+    """[N][batch] -> [batch / bs][N][bs]: the block-interleaved layout."""
+    N, batch = v.shape
+    return np.ascontiguousarray(v.reshape(N, batch // bs, bs).transpose(1, 0, 2))
+
+
+def from_blocked(v):
+    nb, N, bs = v.shape
+    return v.transpose(1, 0, 2).reshape(N, nb * bs)
+
+
+@pytest.mark.parametrize("variant,dtype,tol", [("split", np.float32, TOL_F32), ("thread", np.float32, TOL_F32),
+                                               ("thread", np.float64, TOL_F64)])
+@pytest.mark.parametrize("bs", [8, 16, 48, 256])
+@pytest.mark.parametrize("N", [17, 256, 300])
+def test_block_interleaved(variant, dtype, tol, bs, N):
+    """Blocks of bs systems, each an interleaved [N][bs] array (bs = 16, 48, 256: TMA boxes
+    from 3-D tensor maps; bs = 8: per-thread cp.async), against the oracle."""
+    batch = 768
+    bands = inputs.persys_bands(N, batch, seed=N + bs, dtype=dtype)
+    F = inputs.rhs_uniform(N, batch, seed=N + bs).astype(dtype)
+    ref = oracle.batch_persys(*bands, F)
+    dB = [dev(to_blocked(v, bs)) for v in bands]
+    X = dev(to_blocked(F, bs))
+    pent.pent_factor_solve(*dB, X, variant=variant, block_size=bs)
+    pent.pent_sync()
+    assert max_rel_err(from_blocked(host(X)), ref) < tol
+
+
+def test_block_size_must_divide_batch():
+    import torch
+    bands = [torch.ones(2, 10, 8, dtype=torch.float32, device="cuda") for _ in range(5)]
+    X = torch.ones(2, 10, 8, dtype=torch.float32, device="cuda")
+    with pytest.raises(ValueError):
+        pent.pent_factor_solve(*bands, X, block_size=16)      # shape says bs = 8
+    L = pent.lib()
+    import ctypes
+    vp = [ctypes.c_void_p(t.data_ptr()) for t in bands]
+    assert L.pent_factor_solve_ex(*vp, ctypes.c_void_p(X.data_ptr()), 10, 16, pent.F32, pent.VARIANT_AUTO,
+                                  6, None, 0, None, None) == pent.ERR_INVALID_ARG
