@@ -224,6 +224,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   const size_t o_work = off; off = round_up(off + 18 * (Mpad > (size_t)p->M ? Mpad : (size_t)p->M) * sizeof(double), 256);
   const size_t o_sptab = off; off = round_up(off + Mpad * kSpK * sizeof(float4), 256);
   const size_t o_spchunk = off; off = round_up(off + (size_t)spP * kSpChunk * sizeof(double), 256);
+  const size_t o_spchunkdf = off; off = round_up(off + (size_t)spP * kSpChunk * sizeof(float2), 256);
   const size_t o_spextra = off; off = round_up(off + kSpExtra * sizeof(double), 256);
   const size_t o_status = off; off = round_up(off + sizeof(int), 256);
   const size_t o_twtab = off; off = round_up(off + (size_t)p->M * kTwK * sizeof(float4), 256);
@@ -246,6 +247,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   p->twist = reinterpret_cast<double*>(arena + o_twist);
   p->sptab = reinterpret_cast<float4*>(arena + o_sptab);
   p->spchunk = reinterpret_cast<double*>(arena + o_spchunk);
+  p->spchunk_df = reinterpret_cast<float2*>(arena + o_spchunkdf);
   p->spextra = reinterpret_cast<double*>(arena + o_spextra);
   double* d_bands = reinterpret_cast<double*>(arena + o_bands);
   p->bands = d_bands;
@@ -340,6 +342,15 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
         p->sp_T = (int)Td;
         // the two-kernel form needs the truncated chunk couplings
         p->split_big = !fits && p->sp_T > 0;
+      }
+      if (p->split_big) {
+        e = split_big_prepare(*p, 0);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          pent_destroy(p);
+          return from_cuda(e);
+        }
       }
       // PENT_CHUNK_DEDUP=0 keeps every chunk on its own tables (testing)
       if (p->split_big && env_int("PENT_CHUNK_DEDUP", 1) != 0) {

@@ -17,7 +17,10 @@
 //   k_big_fix     one thread per (system, chunk): t_c = sum_k B_{c,k} w_{c+1+k},
 //                 x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 (- U x_t), stored in fp64.
 // Memory traffic: f read, x' written and read, x written (four arrays, as the
-// twisted kernel), plus summaries of 64 bytes per chunk.  The parallelism is
+// twisted kernel), plus summaries of 64 bytes per chunk.  The chunk states are
+// computed in double-float like the sweeps (summaries and a copy of the chunk
+// tables as (hi, lo) pairs), which keeps them off the fp64 pipe; only the
+// periodic border (one thread per system) works in fp64.  The parallelism is
 // batch x P threads, so a handful of very long systems still fills the GPU.
 #include "cp_async.cuh"
 #include "df64.cuh"
@@ -87,9 +90,9 @@ __global__ void __launch_bounds__(kBigThreads, 2)
       a1 = g;
     }
   }
-  double* o = sum + ((size_t)c * batch + s) * kSum;
-  o[0] = df::to_double(v[L - 2]);
-  o[1] = df::to_double(v[L - 1]);
+  float2* o = reinterpret_cast<float2*>(sum) + ((size_t)c * batch + s) * kSum;
+  o[0] = make_float2(v[L - 2].h, v[L - 2].l);
+  o[1] = make_float2(v[L - 1].h, v[L - 1].l);
   {
     D2 a1{0.f, 0.f}, a2{0.f, 0.f};
 #pragma unroll
@@ -101,8 +104,8 @@ __global__ void __launch_bounds__(kBigThreads, 2)
       a1 = y;
     }
   }
-  o[2] = df::to_double(v[0]);
-  o[3] = df::to_double(v[1]);
+  o[2] = make_float2(v[0].h, v[0].l);
+  o[3] = make_float2(v[1].h, v[1].l);
   if (CYC) {                                      // x' at rows M-2, M-1 for the border
 #pragma unroll
     for (int j = 0; j < L; ++j) {
@@ -116,72 +119,87 @@ __global__ void __launch_bounds__(kBigThreads, 2)
     if (row0 + j < M) q[j * ld] = make_float2(v[j].h, v[j].l);
 }
 
-// s_c from the local end values of the T chunks before c
-__device__ __forceinline__ void state_s(const double* __restrict__ ctab, const double* __restrict__ sum,
-                                        int c, int s, int batch, int T, int2 dup, double& s0, double& s1) {
-  const double* ct = ctab + (size_t)table_chunk(c, dup) * kSpChunk;
-  s0 = s1 = 0.0;
+__device__ __forceinline__ D2 d2(float2 v) { return D2{v.x, v.y}; }
+__device__ __forceinline__ float2 f2(D2 v) { return make_float2(v.h, v.l); }
+
+// y += A x for a row-major 2x2 A, double-float
+__device__ __forceinline__ void mv2d(const float2* A, D2 x0, D2 x1, D2& y0, D2& y1) {
+  y0 = df::sum3(y0, d2(A[0]), x0, d2(A[1]), x1);
+  y1 = df::sum3(y1, d2(A[2]), x0, d2(A[3]), x1);
+}
+
+// s_c from the local end values of the T chunks before c (summaries as (hi, lo))
+__device__ __forceinline__ void state_s(const float2* __restrict__ ctab, const float2* __restrict__ sum,
+                                        int c, int s, int batch, int T, int2 dup, D2& s0, D2& s1) {
+  const float2* ct = ctab + (size_t)table_chunk(c, dup) * kSpChunk;
+  s0 = s1 = D2{0.f, 0.f};
   for (int k = 1; k <= T && k <= c; ++k) {
-    const double* e = sum + ((size_t)(c - k) * batch + s) * kSum;
-    if (k == 1) { s0 += e[0]; s1 += e[1]; }
-    else mv2(ct + 12 + 4 * (k - 2), e[0], e[1], s0, s1);
+    const float2* e = sum + ((size_t)(c - k) * batch + s) * kSum;
+    if (k == 1) { s0 = df::add(s0, d2(e[0])); s1 = df::add(s1, d2(e[1])); }
+    else mv2d(ct + 12 + 4 * (k - 2), d2(e[0]), d2(e[1]), s0, s1);
   }
 }
 
 // t_c from w of the T chunks after c
-__device__ __forceinline__ void state_t(const double* __restrict__ ctab, const double* __restrict__ sum,
-                                        int c, int s, int P, int batch, int T, int2 dup, double& t0,
-                                        double& t1) {
-  const double* ct = ctab + (size_t)table_chunk(c, dup) * kSpChunk;
-  t0 = t1 = 0.0;
+__device__ __forceinline__ void state_t(const float2* __restrict__ ctab, const float2* __restrict__ sum,
+                                        int c, int s, int P, int batch, int T, int2 dup, D2& t0, D2& t1) {
+  const float2* ct = ctab + (size_t)table_chunk(c, dup) * kSpChunk;
+  t0 = t1 = D2{0.f, 0.f};
   for (int k = 0; k < T && c + 1 + k < P; ++k) {
-    const double* w = sum + ((size_t)(c + 1 + k) * batch + s) * kSum + 6;
-    if (k == 0) { t0 += w[0]; t1 += w[1]; }
-    else mv2(ct + 24 + 4 * (k - 1), w[0], w[1], t0, t1);
+    const float2* w = sum + ((size_t)(c + 1 + k) * batch + s) * kSum + 6;
+    if (k == 0) { t0 = df::add(t0, d2(w[0])); t1 = df::add(t1, d2(w[1])); }
+    else mv2d(ct + 24 + 4 * (k - 1), d2(w[0]), d2(w[1]), t0, t1);
   }
 }
 
 __global__ void __launch_bounds__(kBigThreads)
-    k_big_states(const double* __restrict__ ctab, const double* __restrict__ extra, double* __restrict__ sum,
+    k_big_states(const float2* __restrict__ ctab, const double* __restrict__ extra, float2* __restrict__ sum,
                  int P, int batch, int2 dup) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)P * batch) return;
   const int c = (int)(i / batch), s = (int)(i % batch);
   const int T = (int)extra[18];
-  double s0, s1;
+  D2 s0, s1;
   state_s(ctab, sum, c, s, batch, T, dup, s0, s1);
-  double* o = sum + (size_t)i * kSum;
-  double w0 = o[2], w1 = o[3];
-  mv2(ctab + (size_t)table_chunk(c, dup) * kSpChunk + 4, s0, s1, w0, w1);   // w_c = x'_start + Mst_c s_c
-  o[4] = s0;
-  o[5] = s1;
-  o[6] = w0;
-  o[7] = w1;
+  float2* o = sum + (size_t)i * kSum;
+  D2 w0 = d2(o[2]), w1 = d2(o[3]);
+  mv2d(ctab + (size_t)table_chunk(c, dup) * kSpChunk + 4, s0, s1, w0, w1);   // w_c = x'_start + Mst_c s_c
+  o[4] = f2(s0);
+  o[5] = f2(s1);
+  o[6] = f2(w0);
+  o[7] = f2(w1);
+}
+
+// the chunk tables as double-float pairs (plan time)
+__global__ void k_chunk_df(const double* __restrict__ src, float2* __restrict__ dst, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) dst[i] = f2(df::from_double(src[i]));
 }
 
 __global__ void __launch_bounds__(kBigThreads)
-    k_big_border(const double* __restrict__ ctab, const double* __restrict__ extra,
-                 const double* __restrict__ sum, const double* __restrict__ xm, double* __restrict__ X,
-                 int M, int P, int batch, int2 dup) {
+    k_big_border(const double* __restrict__ ctab, const float2* __restrict__ ctabd,
+                 const double* __restrict__ extra, const float2* __restrict__ sum,
+                 const double* __restrict__ xm, double* __restrict__ X, int M, int P, int batch, int2 dup) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
   const long long ld = batch;
   const int T = (int)extra[18];
   // y at rows 0, 1: chunk 0 has s_0 = 0, so y = w_0 + Kst_0 t_0
-  double t0, t1;
-  state_t(ctab, sum, 0, s, P, batch, T, dup, t0, t1);
-  const double* o0 = sum + (size_t)s * kSum;
-  double y0 = o0[6], y1 = o0[7];
-  mv2(ctab + 8, t0, t1, y0, y1);
+  D2 td0, td1;
+  state_t(ctabd, sum, 0, s, P, batch, T, dup, td0, td1);
+  const float2* o0 = sum + (size_t)s * kSum;
+  double y0 = df::to_double(d2(o0[6])), y1 = df::to_double(d2(o0[7]));
+  mv2(ctab + 8, df::to_double(td0), df::to_double(td1), y0, y1);
   // y at rows M-2, M-1 from their chunks' s and t
   double yv[2];
   for (int r = 0; r < 2; ++r) {
     const int row = M - 2 + r, c = row / kBigL;
-    const double* oc = sum + ((size_t)c * batch + s) * kSum;
-    double u0, u1;
-    state_t(ctab, sum, c, s, P, batch, T, dup, u0, u1);
+    const float2* oc = sum + ((size_t)c * batch + s) * kSum;
+    D2 u0, u1;
+    state_t(ctabd, sum, c, s, P, batch, T, dup, u0, u1);
     const double* mk = extra + 10 + 2 * r;   // M1, M2 at the row; K1, K2 four slots on
-    yv[r] = xm[(size_t)s * 2 + r] + mk[0] * oc[4] + mk[1] * oc[5] + mk[4] * u0 + mk[5] * u1;
+    yv[r] = xm[(size_t)s * 2 + r] + mk[0] * df::to_double(d2(oc[4])) + mk[1] * df::to_double(d2(oc[5])) +
+            mk[4] * df::to_double(u0) + mk[5] * df::to_double(u1);
   }
   const double r0 = extra[4] * yv[0] + extra[5] * yv[1] + extra[6] * y0;
   const double r1 = extra[7] * yv[1] + extra[8] * y0 + extra[9] * y1;
@@ -192,8 +210,8 @@ __global__ void __launch_bounds__(kBigThreads)
 
 template <int SPW, bool CYC>
 __global__ void __launch_bounds__(kBigThreads)
-    k_big_fix(const float4* __restrict__ tab, const double* __restrict__ ctab,
-              const double* __restrict__ extra, const double* __restrict__ sum, double* __restrict__ X,
+    k_big_fix(const float4* __restrict__ tab, const float2* __restrict__ ctab,
+              const double* __restrict__ extra, const float2* __restrict__ sum, double* __restrict__ X,
               int M, int P, int batch, int2 dup) {
   constexpr int L = kBigL;
   int s, c;
@@ -203,11 +221,10 @@ __global__ void __launch_bounds__(kBigThreads)
   const int row0 = c * L;
   if (row0 >= M) return;
   const int T = (int)extra[18];
-  const double* o = sum + ((size_t)c * batch + s) * kSum;
-  double t0, t1;
-  state_t(ctab, sum, c, s, P, batch, T, dup, t0, t1);
-  const D2 S0 = df::from_double(o[4]), S1 = df::from_double(o[5]);
-  const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
+  const float2* o = sum + ((size_t)c * batch + s) * kSum;
+  D2 T0, T1;
+  state_t(ctab, sum, c, s, P, batch, T, dup, T0, T1);
+  const D2 S0 = d2(o[4]), S1 = d2(o[5]);
   bool needU = false;
   D2 X0{0.f, 0.f}, X1{0.f, 0.f};
   if (CYC) {
@@ -257,15 +274,16 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   k_big_local<SPW, CYC><<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, p.M, P, batch, dup);
   note_launch();
   const long long n = (long long)P * batch;
+  float2* sumd = reinterpret_cast<float2*>(p.spsum);
   k_big_states<<<(unsigned)((n + kBigThreads - 1) / kBigThreads), kBigThreads, 0, st>>>(
-      p.spchunk, p.spextra, p.spsum, P, batch, dup);
+      p.spchunk_df, p.spextra, sumd, P, batch, dup);
   note_launch();
   if (CYC) {
     k_big_border<<<(batch + kBigThreads - 1) / kBigThreads, kBigThreads, 0, st>>>(
-        p.spchunk, p.spextra, p.spsum, xm, X, p.M, P, batch, dup);
+        p.spchunk, p.spchunk_df, p.spextra, sumd, xm, X, p.M, P, batch, dup);
     note_launch();
   }
-  k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk, p.spextra, p.spsum, X, p.M, P,
+  k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, p.M, P,
                                                    batch, dup);
   note_launch();
   return cudaGetLastError();
@@ -280,6 +298,13 @@ cudaError_t run_cyc(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
 }
 
 }  // namespace
+
+cudaError_t split_big_prepare(pent_plan_s& p, cudaStream_t st) {
+  const int n = p.sp_P * kSpChunk;
+  k_chunk_df<<<(n + 255) / 256, 256, 0, st>>>(p.spchunk, p.spchunk_df, n);
+  note_launch();
+  return cudaGetLastError();
+}
 
 cudaError_t shared_split_big(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   if (p.sp_L != kBigL || p.sp_T <= 0) return cudaErrorInvalidValue;
