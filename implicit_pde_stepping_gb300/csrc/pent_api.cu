@@ -417,18 +417,27 @@ pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, co
   for (const void* q : ptrs)
     if (!aligned(q, 16)) return PENT_ERR_INVALID_ARG;
   const bool split_ok = dtype == PENT_F32 && persys_split_chunks(N) > 0;
-  bool split;
+  pent_variant v;
   switch (variant) {
-    case PENT_VARIANT_AUTO: split = split_ok; break;
-    case PENT_VARIANT_THREAD: split = false; break;
+    case PENT_VARIANT_AUTO:
+      v = split_ok ? PENT_VARIANT_SPLIT : dtype == PENT_F64 ? PENT_VARIANT_THREAD_DF : PENT_VARIANT_THREAD;
+      break;
+    case PENT_VARIANT_THREAD: v = variant; break;
+    case PENT_VARIANT_THREAD_DF:
+      if (dtype != PENT_F64) return PENT_ERR_UNSUPPORTED;
+      v = variant;
+      break;
     case PENT_VARIANT_SPLIT:
       if (!split_ok) return PENT_ERR_UNSUPPORTED;
-      split = true;
+      v = variant;
       break;
     default: return PENT_ERR_INVALID_ARG;
   }
-  if (split) return from_cuda(persys_split(a, b, c, d, e, rhs, N, batch, block_size, info, as_stream(stream)));
+  if (v == PENT_VARIANT_SPLIT)
+    return from_cuda(persys_split(a, b, c, d, e, rhs, N, batch, block_size, info, as_stream(stream)));
   if (!work || work_bytes < persys_work_bytes(N, batch, dtype) || !aligned(work, 256)) return PENT_ERR_INVALID_ARG;
+  if (v == PENT_VARIANT_THREAD_DF)
+    return from_cuda(persys_thread_df(a, b, c, d, e, rhs, N, batch, block_size, work, info, as_stream(stream)));
   return from_cuda(persys_thread(a, b, c, d, e, rhs, N, batch, block_size, dtype, work, info,
                                  as_stream(stream)));
 }

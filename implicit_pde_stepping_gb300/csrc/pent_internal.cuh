@@ -100,6 +100,9 @@ cudaError_t persys_thread(const void* a, const void* b, const void* c, const voi
                           void* X, int N, int batch, int bs, pent_dtype dt, void* work, int* info,
                           cudaStream_t st);
 size_t persys_work_bytes(int N, int batch, pent_dtype dt);
+// fp64 matrices computed in double-float (same scratch size as persys_thread)
+cudaError_t persys_thread_df(const void* a, const void* b, const void* c, const void* d, const void* e,
+                             void* X, int N, int batch, int bs, void* work, int* info, cudaStream_t st);
 // persys_split.cu: partitioned fp32 kernel (chunks of 16 rows, TMA tiles)
 int persys_split_chunks(int N);   // chunks per system for N rows, 0 if N > 512
 cudaError_t persys_split(const void* a, const void* b, const void* c, const void* d, const void* e, void* X,

@@ -79,7 +79,10 @@ extern "C" pent_status pent_factor_solve_noalloc(const void* a, const void* b, c
     cudaGetLastError();
     return PENT_ERR_CUDA;
   }
-  err = pent::persys_thread(a, b, c, d, e, rhs_inout, N, batch, 0, dtype, scratch, info,
-                            static_cast<cudaStream_t>(stream));
+  err = dtype == PENT_F64
+            ? pent::persys_thread_df(a, b, c, d, e, rhs_inout, N, batch, 0, scratch, info,
+                                     static_cast<cudaStream_t>(stream))
+            : pent::persys_thread(a, b, c, d, e, rhs_inout, N, batch, 0, dtype, scratch, info,
+                                  static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? PENT_OK : PENT_ERR_CUDA;
 }

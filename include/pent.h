@@ -150,8 +150,12 @@ pent_status pent_factor_solve(const void* a, const void* b, const void* c, const
  *             elimination; the chunk-end pairs of unknowns by block parallel
  *             cyclic reduction), so memory sees the bands and f once and x
  *             once; `work` is not used and may be NULL;
- *             PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD.
- *             PENT_VARIANT_THREAD_DF is not a per-system variant.
+ *             PENT_VARIANT_THREAD_DF — fp64 only: THREAD's sweeps in
+ *             double-float (pairs of floats on the FP32 pipe, ~2^-47 relative;
+ *             values of magnitude below 2^-100 or from 2^127 are outside its
+ *             range), inputs and outputs fp64, the scratch holding pairs;
+ *             PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD_DF for
+ *             fp64, else THREAD.
  *   block_size : 0 — a..e and rhs_inout interleaved [N][batch], element (i, s)
  *             at i * batch + s; bs > 0 — the block-interleaved layout of
  *             "Simulating the behavior of the human brain on GPUs", section
@@ -164,7 +168,8 @@ pent_status pent_factor_solve(const void* a, const void* b, const void* c, const
  *   large enough, 256-byte aligned) only when THREAD runs.
  * Errors: PENT_ERR_INVALID_ARG for null or misaligned pointers, N or batch < 1,
  * a bad dtype, variant or block_size, or a missing or short work buffer where
- * THREAD runs; PENT_ERR_UNSUPPORTED for SPLIT outside fp32 / N <= 512.  Nothing is
+ * THREAD or THREAD_DF runs; PENT_ERR_UNSUPPORTED for SPLIT outside fp32 /
+ * N <= 512 and for THREAD_DF outside fp64.  Nothing is
  * queued on an error.
  */
 pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, const void* d,

@@ -9,7 +9,7 @@ from tests.gpu_util import TOL_F32, TOL_F64, dev, host, max_rel_err
 
 pytestmark = pytest.mark.gpu
 
-CASES = [("auto", np.float64, TOL_F64), ("thread", np.float32, TOL_F32),
+CASES = [("auto", np.float64, TOL_F64), ("thread", np.float64, TOL_F64), ("thread", np.float32, TOL_F32),
          ("split", np.float32, TOL_F32), ("auto", np.float32, TOL_F32)]
 IDS = [f"{v}-{d.__name__}" for v, d, _ in CASES]
 
@@ -73,8 +73,8 @@ def test_weakly_dominant(variant, dtype, tol, N):
     assert max_rel_err(X, ref) < tol
 
 
-@pytest.mark.parametrize("variant,dtype", [("thread", np.float64), ("thread", np.float32),
-                                           ("split", np.float32)])
+@pytest.mark.parametrize("variant,dtype", [("thread", np.float64), ("thread_df", np.float64),
+                                           ("thread", np.float32), ("split", np.float32)])
 def test_zero_pivot_reported_per_system(variant, dtype):
     N, batch = 40, 5
     a, b, c, d, e = inputs.persys_bands(N, batch, seed=1, dtype=dtype)
@@ -92,12 +92,27 @@ def test_zero_pivot_reported_per_system(variant, dtype):
 
 def test_split_variant_limits():
     import torch
-    for N, tdt in ((16, torch.float64), (513, torch.float32)):
+    for N, tdt, v in ((16, torch.float64, "split"), (513, torch.float32, "split"),
+                      (16, torch.float32, "thread_df")):
         bands = [torch.ones(N, 8, dtype=tdt, device="cuda") for _ in range(5)]
         X = torch.ones(N, 8, dtype=tdt, device="cuda")
         with pytest.raises(pent.PentError) as ex:
-            pent.pent_factor_solve(*bands, X, variant="split")
+            pent.pent_factor_solve(*bands, X, variant=v)
         assert ex.value.status == pent.ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("scale", [1e-25, 1e-8, 1e8, 1e25])
+def test_fp64_double_float_dynamic_range(scale):
+    """The double-float fp64 kernel keeps fp64-class relative accuracy when the bands and
+    the right-hand side sit far from 1 (scaled alike, so the pivots, their reciprocals and
+    the intermediate values span 1e-25..1e25 while the solution stays O(1))."""
+    N, batch = 300, 257
+    a, b, c, d, e = (v * scale for v in inputs.persys_bands(N, batch, seed=7, dtype=np.float64))
+    F = inputs.rhs_uniform(N, batch, seed=7) * scale
+    ref = oracle.batch_persys(a, b, c, d, e, F)
+    X, info, _ = run_gpu((a, b, c, d, e), F, np.float64, variant="thread_df")
+    assert np.all(info == 0)
+    assert max_rel_err(X, ref) < TOL_F64
 
 
 def test_split_needs_no_work_buffer():
@@ -144,7 +159,7 @@ def from_blocked(v):
 
 
 @pytest.mark.parametrize("variant,dtype,tol", [("split", np.float32, TOL_F32), ("thread", np.float32, TOL_F32),
-                                               ("thread", np.float64, TOL_F64)])
+                                               ("thread", np.float64, TOL_F64), ("thread_df", np.float64, TOL_F64)])
 @pytest.mark.parametrize("bs", [8, 16, 48, 256])
 @pytest.mark.parametrize("N", [17, 256, 300])
 def test_block_interleaved(variant, dtype, tol, bs, N):
@@ -172,3 +187,16 @@ def test_block_size_must_divide_batch():
     vp = [ctypes.c_void_p(t.data_ptr()) for t in bands]
     assert L.pent_factor_solve_ex(*vp, ctypes.c_void_p(X.data_ptr()), 10, 16, pent.F32, pent.VARIANT_AUTO,
                                   6, None, 0, None, None) == pent.ERR_INVALID_ARG
+
+
+def test_fp64_quarter_size_sampled():
+    """N=256, batch 65536, fp64 per-system bands (the double-float kernel, the fp64
+    default): 1024 sampled systems against the oracle."""
+    N, batch = 256, 65536
+    a, b, c, d, e = inputs.persys_bands(N, batch, seed=2, dtype=np.float64)
+    F = inputs.rhs_uniform(N, batch, seed=2)
+    X, info, _ = run_gpu((a, b, c, d, e), F, np.float64)
+    idx = inputs.sample_systems(batch, 1024)
+    ref = oracle.batch_persys(a[:, idx], b[:, idx], c[:, idx], d[:, idx], e[:, idx], F[:, idx])
+    assert max_rel_err(X[:, idx], ref) < TOL_F64
+    assert np.all(info == 0)
