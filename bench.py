@@ -52,6 +52,8 @@ WORKLOADS = {
     "tri_bi16": dict(N=256, batch=262144, kind="tri", dtype="f32", bs=16,
                      desc="per-system tridiagonal factor+solve, block-interleaved layout (blocks of 16 "
                           "systems), N=256, batch=262144, fp32, diagonally dominant"),
+    "persys64": dict(N=256, batch=262144, kind="persys", dtype="f64",
+                     desc="per-system factor+solve, N=256, batch=262144, fp64, diagonally dominant"),
     "persys_bi16": dict(N=256, batch=262144, kind="persys", dtype="f32", bs=16,
                         desc="per-system factor+solve, block-interleaved layout (blocks of 16 systems), "
                              "N=256, batch=262144, fp32, diagonally dominant"),
@@ -271,18 +273,24 @@ def run_ours(args, W: dict, dist: Dist):
                 return np.ascontiguousarray(x)
             return np.ascontiguousarray(x.reshape(N, batch // bs, bs).transpose(1, 0, 2))
         gen = inputs.tri_bands if kind == "tri" else inputs.persys_bands
-        bands = [torch.from_numpy(lay(v)).to("cuda") for v in gen(N, batch, seed=seed)]
-        bufs = [torch.from_numpy(lay(inputs.rhs_uniform(N, batch, seed=seed + r).astype(np.float32)))
+        npdt = np.float64 if W["dtype"] == "f64" else np.float32
+        bands = [torch.from_numpy(lay(v)).to("cuda") for v in gen(N, batch, seed=seed, dtype=npdt)]
+        bufs = [torch.from_numpy(lay(inputs.rhs_uniform(N, batch, seed=seed + r).astype(npdt)))
                 .to("cuda") for r in range(2)]
         wb = (pent.tri_factor_solve_work_bytes if kind == "tri" else pent.pent_factor_solve_work_bytes)
-        work = torch.empty(wb(N, batch, pent.F32), dtype=torch.uint8, device="cuda")
+        work = torch.empty(wb(N, batch, pent.F64 if W["dtype"] == "f64" else pent.F32), dtype=torch.uint8,
+                           device="cuda")
     if plan is not None and args.variant != "auto":
         plan.set_variant(args.variant)
     variant = plan.variant(batch) if plan is not None else pent.VARIANT_THREAD
-    tri_variant = args.variant if args.variant in ("thread", "split") else "auto"
+    tri_variant = args.variant if args.variant in ("thread", "split", "thread_df") else "auto"
     if kind in ("tri", "persys"):
-        # fp32 per-system workloads: the partitioned kernel unless the thread one is asked for
-        variant = pent.VARIANT_THREAD if tri_variant == "thread" else pent.VARIANT_SPLIT
+        # per-system workloads: fp32 takes the partitioned kernel, fp64 the double-float
+        # one-thread kernel, unless another variant is asked for
+        if tri_variant != "auto":
+            variant = pent.VARIANTS[tri_variant]
+        else:
+            variant = pent.VARIANT_THREAD_DF if W["dtype"] == "f64" else pent.VARIANT_SPLIT
     # inputs smaller than twice the L2: write a buffer larger than L2 between timed
     # steps, outside the per-step events, and time the steps by those events
     l2_bytes = getattr(torch.cuda.get_device_properties(dev_index), "L2_cache_size", 0) or (129 << 20)
@@ -412,6 +420,7 @@ def run_ours(args, W: dict, dist: Dist):
         ("cn", pent.VARIANT_THREAD): ("k_cn_thread_f64", "pent_ch.cu"),
         ("persys", pent.VARIANT_THREAD): ("k_persys_thread", "pent_persys.cu"),
         ("persys", pent.VARIANT_SPLIT): ("k_persys_split", "pent_persys_split.cu"),
+        ("persys", pent.VARIANT_THREAD_DF): ("k_persys_thread_df", "pent_persys.cu"),
         ("tri", pent.VARIANT_THREAD): ("k_tri_thread", "pent_tri.cu"),
         ("tri", pent.VARIANT_SPLIT): ("k_tri_split", "pent_tri.cu"),
         ("shared", pent.VARIANT_THREAD_DF): (twisted, "pent_twisted_df.cu"),
@@ -512,8 +521,9 @@ def run_cpu_baseline(W: dict, seconds: float):
         fn = lambda: oracle.batch_tri(a, b, c, F)  # noqa: E731
     else:
         S = 8192
-        a, b, c, d, e = inputs.persys_bands(N, S)
-        F = inputs.rhs_uniform(N, S).astype(np.float32)
+        npdt = np.float64 if W["dtype"] == "f64" else np.float32
+        a, b, c, d, e = inputs.persys_bands(N, S, dtype=npdt)
+        F = inputs.rhs_uniform(N, S).astype(npdt)
         fn = lambda: oracle.batch_persys(a, b, c, d, e, F)  # noqa: E731
     fn()
     reps, t0 = 0, time.perf_counter()
@@ -556,8 +566,9 @@ def run_reference(args, W: dict, dist: Dist):
         fn = lambda: oracle.batch_tri(a, b, c, F)  # noqa: E731
     else:
         import numpy as np
-        a, b, c, d, e = inputs.persys_bands(N, S)
-        F = inputs.rhs_uniform(N, S).astype(np.float32)
+        npdt = np.float64 if W["dtype"] == "f64" else np.float32
+        a, b, c, d, e = inputs.persys_bands(N, S, dtype=npdt)
+        F = inputs.rhs_uniform(N, S).astype(npdt)
         fn = lambda: oracle.batch_persys(a, b, c, d, e, F)  # noqa: E731
     for _ in range(args.warmup):
         fn()
