@@ -49,6 +49,9 @@ WORKLOADS = {
     "tri": dict(N=256, batch=262144, kind="tri", dtype="f32",
                 desc="per-system tridiagonal factor+solve (Thomas), N=256, batch=262144, fp32, "
                      "diagonally dominant"),
+    "tri64": dict(N=256, batch=262144, kind="tri", dtype="f64",
+                  desc="per-system tridiagonal factor+solve (Thomas), N=256, batch=262144, fp64, "
+                       "diagonally dominant"),
     "tri_bi16": dict(N=256, batch=262144, kind="tri", dtype="f32", bs=16,
                      desc="per-system tridiagonal factor+solve, block-interleaved layout (blocks of 16 "
                           "systems), N=256, batch=262144, fp32, diagonally dominant"),
@@ -423,6 +426,7 @@ def run_ours(args, W: dict, dist: Dist):
         ("persys", pent.VARIANT_THREAD_DF): ("k_persys_thread_df", "pent_persys.cu"),
         ("tri", pent.VARIANT_THREAD): ("k_tri_thread", "pent_tri.cu"),
         ("tri", pent.VARIANT_SPLIT): ("k_tri_split", "pent_tri.cu"),
+        ("tri", pent.VARIANT_THREAD_DF): ("k_tri_thread_df", "pent_tri.cu"),
         ("shared", pent.VARIANT_THREAD_DF): (twisted, "pent_twisted_df.cu"),
         ("hyper", pent.VARIANT_THREAD_DF): (twisted, "pent_twisted_df.cu"),
         ("ch", pent.VARIANT_THREAD_DF): split, ("ch", pent.VARIANT_SPLIT): split,
@@ -516,8 +520,9 @@ def run_cpu_baseline(W: dict, seconds: float):
         fn = lambda: oracle.batch_cn(F, W["sigma"], 1)  # noqa: E731
     elif kind == "tri":
         S = 32768
-        a, b, c = inputs.tri_bands(N, S)
-        F = inputs.rhs_uniform(N, S).astype(np.float32)
+        npdt = np.float64 if W["dtype"] == "f64" else np.float32
+        a, b, c = inputs.tri_bands(N, S, dtype=npdt)
+        F = inputs.rhs_uniform(N, S).astype(npdt)
         fn = lambda: oracle.batch_tri(a, b, c, F)  # noqa: E731
     else:
         S = 8192
@@ -561,8 +566,9 @@ def run_reference(args, W: dict, dist: Dist):
         fn = lambda: oracle.batch_cn(F, W["sigma"], 1)  # noqa: E731
     elif kind == "tri":
         import numpy as np
-        a, b, c = inputs.tri_bands(N, S)
-        F = inputs.rhs_uniform(N, S).astype(np.float32)
+        npdt = np.float64 if W["dtype"] == "f64" else np.float32
+        a, b, c = inputs.tri_bands(N, S, dtype=npdt)
+        F = inputs.rhs_uniform(N, S).astype(npdt)
         fn = lambda: oracle.batch_tri(a, b, c, F)  # noqa: E731
     else:
         import numpy as np

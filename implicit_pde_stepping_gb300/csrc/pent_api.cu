@@ -466,20 +466,28 @@ pent_status tri_factor_solve(const void* a, const void* b, const void* c, void* 
   for (const void* q : ptrs)
     if (!aligned(q, elem)) return PENT_ERR_INVALID_ARG;
   const bool split_ok = dtype == PENT_F32 && tri_split_chunks(N) > 0;
-  bool split;
+  pent_variant v;
   switch (variant) {
-    case PENT_VARIANT_AUTO: split = split_ok; break;
-    case PENT_VARIANT_THREAD: split = false; break;
+    case PENT_VARIANT_AUTO:
+      v = split_ok ? PENT_VARIANT_SPLIT : dtype == PENT_F64 ? PENT_VARIANT_THREAD_DF : PENT_VARIANT_THREAD;
+      break;
+    case PENT_VARIANT_THREAD: v = variant; break;
+    case PENT_VARIANT_THREAD_DF:
+      if (dtype != PENT_F64) return PENT_ERR_UNSUPPORTED;
+      v = variant;
+      break;
     case PENT_VARIANT_SPLIT:
       if (!split_ok) return PENT_ERR_UNSUPPORTED;
-      split = true;
+      v = variant;
       break;
     default: return PENT_ERR_INVALID_ARG;
   }
-  if (!split && (!work || work_bytes < tri_work_bytes(N, batch, dtype) || !aligned(work, 256)))
+  if (v != PENT_VARIANT_SPLIT && (!work || work_bytes < tri_work_bytes(N, batch, dtype) || !aligned(work, 256)))
     return PENT_ERR_INVALID_ARG;
-  return from_cuda(
-      tri_solve_batch(a, b, c, rhs, N, batch, block_size, dtype, split, work, info, as_stream(stream)));
+  if (v == PENT_VARIANT_THREAD_DF)
+    return from_cuda(tri_solve_batch_df(a, b, c, rhs, N, batch, block_size, work, info, as_stream(stream)));
+  return from_cuda(tri_solve_batch(a, b, c, rhs, N, batch, block_size, dtype, v == PENT_VARIANT_SPLIT, work, info,
+                                   as_stream(stream)));
 }
 
 pent_status hyperdiffusion_step(pent_plan p, void* C, int batch, int nsteps, void* stream) {

@@ -114,6 +114,9 @@ size_t tri_work_bytes(int N, int batch, pent_dtype dt);
 // bs = 0: interleaved [N][batch]; bs > 0: block-interleaved, blocks of bs systems
 cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
                             pent_dtype dt, bool split, void* work, int* info, cudaStream_t st);
+// fp64 systems in double-float, one thread per system (same scratch size)
+cudaError_t tri_solve_batch_df(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
+                               void* work, int* info, cudaStream_t st);
 
 // host.cu: shared-matrix solve of host arrays, transfers overlapped with the solves
 void host_pipeline_release(pent_plan_s& p);

@@ -40,11 +40,14 @@
 //   multiple of 16 bytes) every thread stages its own rows with 4-byte
 //   cp.async instead.
 #include "cp_async.cuh"
+#include "df64.cuh"
 #include "pent_internal.cuh"
 #include "tma.cuh"
 
 namespace pent {
 namespace {
+
+using df::D2;
 
 constexpr int kThreads = 128;
 constexpr int kUnroll = 4;
@@ -115,6 +118,86 @@ __global__ void __launch_bounds__(kThreads)
       if (i >= 0) {
         const T x = yv[u] - cv[u] * x1;
         X[(size_t)i * ld + sb] = x;
+        x1 = x;
+      }
+    }
+  }
+  if (info) info[s] = bad;
+}
+
+// ---------------------------------------------------------------------------
+// fp64 systems in double-float, one thread per system: the same Thomas sweeps
+// with every value an unevaluated pair of floats on the FP32 pipe (the fp64
+// pipe runs at ~1/70 of it), fp64 inputs and outputs converted by integer
+// operations; c' goes to the scratch and y' over the right-hand side as
+// (hi, lo) pairs, the same 8 bytes as a double.
+// ---------------------------------------------------------------------------
+
+// 1/a: the float reciprocal refined by one Newton–Raphson step,
+// r = r0 + r0 (1 - a r0), with a r0 formed exactly (relative error ~2^-46)
+__device__ __forceinline__ D2 df_recip(D2 a) {
+  const float r0 = __frcp_rn(a.h);
+  float p, pe;
+  df::two_prod(a.h, r0, p, pe);
+  const float e = __fmaf_rn(-a.l, r0, __fsub_rn(__fsub_rn(1.f, p), pe));
+  return D2{r0, r0 * e};
+}
+
+__global__ void __launch_bounds__(kThreads)
+    k_tri_thread_df(const double* __restrict__ A, const double* __restrict__ B, const double* __restrict__ C,
+                    double* __restrict__ X, float2* __restrict__ Wc, int N, int batch, int bs,
+                    int* __restrict__ info) {
+  const int s = blockIdx.x * blockDim.x + threadIdx.x;
+  if (s >= batch) return;
+  const size_t ld = bs ? (size_t)bs : (size_t)batch;                          // row stride
+  const size_t sb = bs ? (size_t)(s / bs) * N * bs + s % bs : (size_t)s;     // row 0 of system s
+  float2* Xp = reinterpret_cast<float2*>(X);                                   // y' as (hi, lo) in place
+  D2 cp{0.f, 0.f}, yp{0.f, 0.f};
+  int bad = 0;
+  for (int i0 = 0; i0 < N; i0 += kUnroll) {
+    double a[kUnroll], b[kUnroll], c[kUnroll], y[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u;
+      const size_t o = (size_t)i * ld + sb;
+      const bool in = i < N;
+      a[u] = (in && i >= 1) ? A[o] : 0.0;
+      b[u] = in ? B[o] : 1.0;
+      c[u] = (in && i + 1 < N) ? C[o] : 0.0;
+      y[u] = in ? X[o] : 0.0;
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 + u;
+      if (i < N) {
+        const size_t o = (size_t)i * ld + sb;
+        const D2 na = df::neg(df::from_double(a[u]));
+        const D2 den = df::axpy(df::from_double(b[u]), na, cp);
+        if (bad == 0 && !(den.h != 0.f && isfinite(den.h))) bad = i + 1;
+        const D2 rd = df_recip(den);
+        cp = df::mul(df::from_double(c[u]), rd);
+        yp = df::mul(df::axpy(df::from_double(y[u]), na, yp), rd);
+        Wc[(size_t)i * batch + s] = make_float2(cp.h, cp.l);
+        Xp[o] = make_float2(yp.h, yp.l);
+      }
+    }
+  }
+  D2 x1{0.f, 0.f};
+  for (int i0 = N - 1; i0 >= 0; i0 -= kUnroll) {
+    float2 yv[kUnroll], cv[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 - u;
+      const int ii = i >= 0 ? i : 0;
+      yv[u] = (i >= 0) ? Xp[(size_t)ii * ld + sb] : make_float2(0.f, 0.f);
+      cv[u] = (i >= 0) ? Wc[(size_t)ii * batch + s] : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int i = i0 - u;
+      if (i >= 0) {
+        const D2 x = df::axpy(D2{yv[u].x, yv[u].y}, df::neg(D2{cv[u].x, cv[u].y}), x1);
+        X[(size_t)i * ld + sb] = df::to_double(x);
         x1 = x;
       }
     }
@@ -346,6 +429,16 @@ int tri_split_chunks(int N) {
 size_t tri_work_bytes(int N, int batch, pent_dtype dt) {
   const size_t elem = dt == PENT_F64 ? sizeof(double) : sizeof(float);
   return (size_t)N * (size_t)batch * elem;
+}
+
+cudaError_t tri_solve_batch_df(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,
+                               void* work, int* info, cudaStream_t st) {
+  const int grid = (batch + kThreads - 1) / kThreads;
+  k_tri_thread_df<<<grid, kThreads, 0, st>>>(static_cast<const double*>(a), static_cast<const double*>(b),
+                                             static_cast<const double*>(c), static_cast<double*>(X),
+                                             static_cast<float2*>(work), N, batch, bs, info);
+  note_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t tri_solve_batch(const void* a, const void* b, const void* c, void* X, int N, int batch, int bs,

@@ -276,8 +276,12 @@ pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* 
  *               in registers across a group of threads (chunks of 16 rows,
  *               partitioned elimination, chunk-end unknowns by parallel cyclic
  *               reduction), so memory sees a, b, c, y once and x once;
- *               PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD.
- *               PENT_VARIANT_THREAD_DF is not a tridiagonal variant.
+ *               PENT_VARIANT_THREAD_DF — fp64 only: THREAD's sweeps in
+ *               double-float (pairs of floats on the FP32 pipe, ~2^-47 relative;
+ *               values of magnitude below 2^-100 or from 2^127 are outside its
+ *               range), the scratch and y' holding pairs;
+ *               PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD_DF for
+ *               fp64, else THREAD.
  *   work      : DEVICE scratch of tri_factor_solve_work_bytes() bytes,
  *               256-byte aligned (may be NULL with work_bytes 0 when the SPLIT
  *               kernel runs); contents undefined afterwards.
@@ -288,7 +292,7 @@ pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* 
  *               matrices, as the page does.
  * Errors: PENT_ERR_INVALID_ARG for null or misaligned pointers, N or batch < 1,
  * a bad dtype, variant or block_size, or a short work buffer; PENT_ERR_UNSUPPORTED for
- * SPLIT outside fp32 / N <= 512.  Nothing is queued on an error.
+ * SPLIT outside fp32 / N <= 512 and for THREAD_DF outside fp64.  Nothing is queued on an error.
  */
 size_t tri_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);
 pent_status tri_factor_solve(const void* a, const void* b, const void* c, void* rhs_inout, int N,

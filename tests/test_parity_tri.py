@@ -11,7 +11,8 @@ from tests.gpu_util import TOL_F32, TOL_F64, dev, host, max_rel_err
 pytestmark = pytest.mark.gpu
 
 CASES = [("thread", np.float64, TOL_F64), ("thread", np.float32, TOL_F32),
-         ("split", np.float32, TOL_F32), ("auto", np.float32, TOL_F32)]
+         ("split", np.float32, TOL_F32), ("thread_df", np.float64, TOL_F64), ("auto", np.float32, TOL_F32),
+         ("auto", np.float64, TOL_F64)]
 
 
 def run(variant, dtype, N, batch, seed, bz=None):
@@ -57,7 +58,7 @@ def test_tri_full_size_fp32_sampled(variant):
 
 
 @pytest.mark.parametrize("variant,dtype", [("thread", np.float64), ("split", np.float32),
-                                           ("thread", np.float32)])
+                                           ("thread", np.float32), ("thread_df", np.float64)])
 def test_tri_zero_pivot_reported(variant, dtype):
     """b_0 = 0 in system 3 (a zero first pivot for every elimination order that starts
     there): info flags system 3 only; the other systems are solved."""
@@ -79,8 +80,9 @@ def test_tri_argument_errors():
     z32 = torch.zeros((1024, batch), dtype=torch.float32, device="cuda")
     with pytest.raises(pent.PentError):            # ... and N <= 512
         pent.tri_factor_solve(z32, z32, z32, z32.clone(), variant="split")
-    with pytest.raises(pent.PentError):            # not a tridiagonal variant
-        pent.tri_factor_solve(z, z, z, z.clone(), variant="thread_df")
+    z16 = torch.zeros((N, batch), dtype=torch.float32, device="cuda")
+    with pytest.raises(pent.PentError):            # the double-float kernel is for fp64 systems
+        pent.tri_factor_solve(z16, z16, z16, z16.clone(), variant="thread_df")
 
 
 def test_periodic_implicit_diffusion_through_pentadiagonal_plan():
@@ -115,7 +117,7 @@ def from_blocked(x):
     return np.ascontiguousarray(x.transpose(1, 0, 2).reshape(N, nb * bs))
 
 
-@pytest.mark.parametrize("variant,dtype,tol", CASES[:3], ids=[f"{v}-{d.__name__}" for v, d, _ in CASES[:3]])
+@pytest.mark.parametrize("variant,dtype,tol", CASES[:4], ids=[f"{v}-{d.__name__}" for v, d, _ in CASES[:4]])
 @pytest.mark.parametrize("bs", [16, 32, 8, 48])
 @pytest.mark.parametrize("N", [7, 256, 300])
 def test_tri_block_interleaved(variant, dtype, tol, bs, N):
@@ -171,3 +173,15 @@ def test_tri_weakly_dominant(variant, N):
     pent.tri_factor_solve(dev(a), dev(b), dev(c), X, variant=variant)
     pent.pent_sync()
     assert max_rel_err(host(X), oracle.batch_tri(a, b, c, y)) < TOL_F32
+
+
+def test_tri_fp64_double_float_matches_native():
+    """fp64 systems: the double-float kernel (the fp64 default) and the native one agree with
+    the oracle at N = 256, batch 65536 (1024 sampled systems)."""
+    N, batch = 256, 65536
+    for variant in ("thread_df", "thread"):
+        (a, b, c, y), x, info = run(variant, np.float64, N, batch, seed=5)
+        assert not info.any()
+        idx = inputs.sample_systems(batch, 1024)
+        ref = oracle.batch_tri(a[:, idx], b[:, idx], c[:, idx], y[:, idx])
+        assert max_rel_err(x[:, idx], ref) < TOL_F64
