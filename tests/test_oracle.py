@@ -191,6 +191,28 @@ def test_ch_linearised_single_mode():
         assert rel(CT, C0 * G ** steps) < 1e-9
 
 
+@pytest.mark.parametrize("kk,eps", [(5, 0.5), (60, 0.3), (150, 0.8)])
+def test_ch_one_nonlinear_step_closed_form(kk, eps):
+    """One step from C = eps cos(theta), theta = 2 pi k x: on the grid cos^3 = (3 cos(theta)
+    + cos(3 theta)) / 4 exactly, so C^3 - C has modes k and 3k only, D2 = [1, -2, 1]
+    multiplies mode m by -4 sin^2(pi m / N), and the solve divides it by
+    1 + 16 sigma sin^4(pi m / N).  The step is therefore a two-mode closed form; the
+    cubic shows as the 3k mode, which a dropped or mis-powered cubic would miss."""
+    N = 1024
+    sigma, k2 = inputs.ch_params(N)
+    x = np.arange(N) / N
+    th = 2 * np.pi * kk * x
+    C0 = (eps * np.cos(th))[:, None]
+    C1 = oracle.batch_ch(C0, sigma, k2, 1)
+    lam = lambda m: 4.0 * np.sin(np.pi * m / N) ** 2          # noqa: E731
+    den = lambda m: 1.0 + 16.0 * sigma * np.sin(np.pi * m / N) ** 4   # noqa: E731
+    ak = (eps - k2 * lam(kk) * (0.75 * eps ** 3 - eps)) / den(kk)
+    a3k = (-k2 * lam(3 * kk) * 0.25 * eps ** 3) / den(3 * kk)
+    ref = ak * np.cos(th) + a3k * np.cos(3 * th)
+    assert rel(C1[:, 0], ref) < 1e-12
+    assert np.max(np.abs(a3k * np.cos(3 * th))) > 1e-6 * np.max(np.abs(ref))   # the cubic is visible
+
+
 def _golden(name):
     vals = {}
     with open(os.path.join(GOLDEN, name)) as fh:

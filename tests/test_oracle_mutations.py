@@ -37,6 +37,7 @@ MUTATIONS = [
     ("D2 sign", "rhs[i] = C[i] + dt_over_dx2 * (u[im] - 2.0 * u[i] + u[ip]);",
      "rhs[i] = C[i] + dt_over_dx2 * (u[im] - 2.0 * u[i] - u[ip]);"),
     ("cubic sign", "u[i] = C[i] * C[i] * C[i] - C[i];", "u[i] = C[i] * C[i] * C[i] + C[i];"),
+    ("cubic power", "u[i] = C[i] * C[i] * C[i] - C[i];", "u[i] = C[i] * C[i] - C[i];"),
     ("D4 band sign", "b[i] = -4.0 * sigma;", "b[i] = 4.0 * sigma;"),
     ("CN explicit half sign", "rhs[i] = C[i] - sigma_x * d4;", "rhs[i] = C[i] + sigma_x * d4;"),
     ("CN stencil index", "double d4 = C[im2] - 4.0 * C[im1] + 6.0 * C[i] - 4.0 * C[ip1] + C[ip2];",
@@ -61,6 +62,7 @@ def _pins():
     T.test_hyperdiffusion_discrete_amplification()
     T.test_ch_mass_conservation()
     T.test_ch_linearised_single_mode()
+    T.test_ch_one_nonlinear_step_closed_form(60, 0.3)
     T.test_cn_discrete_amplification()
     T.test_cn_conserves_mean_and_matches_one_step_by_hand()
     for N in (2, 5, 33):
