@@ -277,6 +277,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   p->df_spt = env_int("PENT_DF_SPT", 2);
   p->df_ku = env_int("PENT_DF_KU", 4);
   p->df_ctas = env_int("PENT_DF_CTAS", 0);
+  p->steps_sb = env_int("PENT_STEPS_SB", 0);
   p->df_async = env_int("PENT_DF_ASYNC", 6);
   if (dtype == PENT_F64 && p->M >= 8 && p->M <= kMaxTwistedRows) {
     p->m = p->M / 2;

@@ -47,6 +47,7 @@ struct pent_plan_s {
   int df_spt = 2;            // systems per thread (2 needs an even batch)
   int df_ku = 4;             // rows per prefetch block
   int df_ctas = 0;           // CTAs of the double-float kernels (0: two per SM)
+  int steps_sb = 0;          // systems per CTA of the multi-step kernel (0: chosen by shape)
   int df_async = 6;          // cp.async ring depth of the twisted kernel (0: register ring)
   // partitioned double-float variant (pent_factor_split.cu / pent_split_df.cu)
   int split_ok = 0;          // tables valid

@@ -342,8 +342,8 @@ template <int RHS>
 cudaError_t launch_kind(const pent_plan_s& p, double* X, int batch, int nsteps, double k2,
                         cudaStream_t st) {
   if (p.sp_L == 16) return launch<16, 8, RHS>(p, X, batch, nsteps, k2, st);
-  const bool wide = p.sp_P <= 32 && batch > 16 * p.num_sms &&
-                    steps_smem(32, p.sp_P, 16, RHS) <= kStepsSmemMax;
+  const bool fits16 = p.sp_P <= 32 && steps_smem(32, p.sp_P, 16, RHS) <= kStepsSmemMax;
+  const bool wide = p.steps_sb == 16 ? fits16 : p.steps_sb == 8 ? false : fits16 && batch > 16 * p.num_sms;
   return wide ? launch<32, 16, RHS>(p, X, batch, nsteps, k2, st)
               : launch<32, 8, RHS>(p, X, batch, nsteps, k2, st);
 }

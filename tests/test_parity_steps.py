@@ -146,3 +146,17 @@ def test_border_correction_skipped_only_where_negligible(kind, steps, monkeypatc
     b, _ = run(kind, N, batch, steps, C0)
     assert max_rel_err(a, b) < 1e-13
     assert max_rel_err(a, ref(kind, C0, steps)) < TOL_F64
+
+
+@pytest.mark.parametrize("kind", ["hyper", "ch", "cn"])
+@pytest.mark.parametrize("sb", ["8", "16"])
+def test_multistep_systems_per_cta(kind, sb, monkeypatch):
+    """Both CTA shapes of the multi-step kernel (PENT_STEPS_SB), whatever the default
+    for the shape: 8 or 16 systems per CTA give the oracle's result."""
+    monkeypatch.setenv("PENT_STEPS_SB", sb)
+    N, batch, steps = 512, 4100, 4
+    C0 = initial(kind, N, batch, seed=31)
+    out, launches = run(kind, N, batch, steps, C0)
+    assert launches == 1
+    idx = inputs.sample_systems(batch, 200)
+    assert max_rel_err(out[:, idx], ref(kind, C0[:, idx], steps)) < TOL_F64
