@@ -1,6 +1,8 @@
 // C ABI of libpent: argument checks, plan lifecycle and dispatch to the kernels.
 // Every declaration is documented in include/pent.h.
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -135,6 +137,34 @@ cudaError_t find_duplicate_chunks(pent_plan_s& p, int Mpad) {
   }
   p.dup_lo = best_lo;
   p.dup_hi = best_hi;
+  return cudaSuccess;
+}
+
+// 8-row groups whose correction responses are below 2^-24 in every chunk (see
+// pent_plan_s::cheap_k, cheap_m).  M1, M2 decay away from a chunk's start and K1, K2
+// towards it, so the groups found are a prefix (K) and a suffix (M) of the chunk.
+cudaError_t find_cheap_groups(pent_plan_s& p, int Mpad) {
+  const int L = p.sp_L, P = p.sp_P, G = L / 8;
+  std::vector<float4> rows((size_t)Mpad * kSpK);
+  cudaError_t e = cudaMemcpy(rows.data(), p.sptab, rows.size() * sizeof(float4), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return e;
+  std::vector<float> mM(L, 0.f), mK(L, 0.f);
+  for (int c = 0; c < P; ++c)
+    for (int j = 0; j < L; ++j) {
+      const float4 m = rows[((size_t)c * L + j) * kSpK + 3], k = rows[((size_t)c * L + j) * kSpK + 4];
+      mM[j] = std::max(mM[j], std::max(std::fabs(m.x), std::fabs(m.z)));
+      mK[j] = std::max(mK[j], std::max(std::fabs(k.x), std::fabs(k.z)));
+    }
+  auto small = [&](const std::vector<float>& v, int g) {
+    for (int j = 8 * g; j < 8 * g + 8; ++j)
+      if (!(v[j] < 0x1p-24f)) return false;
+    return true;
+  };
+  int gk = 0, gm = G;
+  while (gk < G && small(mK, gk)) ++gk;
+  while (gm > 0 && small(mM, gm - 1)) --gm;
+  p.cheap_k = gk;
+  p.cheap_m = gm;
   return cudaSuccess;
 }
 
@@ -347,6 +377,15 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
       if (p->split_big) {
         e = split_big_prepare(*p, 0);
         if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          pent_destroy(p);
+          return from_cuda(e);
+        }
+      }
+      // PENT_CHEAP_TERMS=0 keeps every correction term in double-float (testing)
+      if (p->split_ok && p->sp_L % 8 == 0 && env_int("PENT_CHEAP_TERMS", 1) != 0) {
+        e = find_cheap_groups(*p, (int)Mpad);
         if (e != cudaSuccess) {
           cudaGetLastError();
           pent_destroy(p);

@@ -59,6 +59,12 @@ struct pent_plan_s {
   // chunk dup_lo (a matrix with constant bands, far from its ends): the two-kernel
   // form reads chunk dup_lo's tables for them, which stay in cache
   int dup_lo = 0, dup_hi = 0;
+  // in the 8-row groups g < cheap_k of every chunk the responses K1, K2 to the
+  // chunk's outgoing state, in the groups g >= cheap_m the responses M1, M2 to its
+  // incoming state, are below 2^-24 in every chunk; the multi-step kernel then adds
+  // their correction terms to the low word alone (one FMA instead of a double-float
+  // multiply-add, at most about 3 * 2^-48 of the state per term)
+  int cheap_k = 0, cheap_m = 1 << 20;
   size_t spsum_bytes = 0;
   float4* sptab = nullptr;   // [Mpad][kSpK]
   double* spchunk = nullptr; // [sp_P][kSpChunk]

@@ -13,7 +13,11 @@
 //   Crank–Nicolson (eqs. (5)–(6)): A C^{n+1} = (2I - A) C^n, i.e.
 //                                  C^{n+1} = 2 A^{-1} C^n - C^n.
 // Between steps the state stays a double-float (hi, lo) pair, renormalised
-// after every step; it is rounded to fp64 once, at the final store.
+// after every step; it is rounded to fp64 once, at the final store.  In the
+// 8-row groups where a chunk's responses to a neighbour's state are below 2^-24
+// in every chunk (found when the plan is built: the last rows of a chunk for the
+// incoming state, the first rows for the outgoing one, when the couplings decay
+// fast), those correction terms take one FMA into the low word.
 //
 // Cross-chunk data per step: the Cahn–Hilliard right-hand side of a chunk's
 // first and last rows needs C of the neighbouring rows, exchanged through
@@ -24,6 +28,8 @@
 //
 // Launched only when the plan's chunk couplings are truncated (T > 0); the
 // exact serial chunk scan stays with the one-step kernel.
+#include <type_traits>
+
 #include "cp_async.cuh"
 #include "df64.cuh"
 #include "pent_internal.cuh"
@@ -65,11 +71,11 @@ __host__ __device__ inline size_t steps_smem(int L, int P, int SB, int rhs) {
   return b;
 }
 
-template <int L, int SB, int MAXT, int RHS>
+template <int L, int SB, int MAXT, int RHS, bool CHEAP>
 __global__ void __launch_bounds__(MAXT, 1)
     k_steps_df(const float4* __restrict__ growtab, const double* __restrict__ gchunk,
                const double* __restrict__ gextra, double* __restrict__ X, int M, int P, int batch,
-               int nsteps, double k2d) {
+               int nsteps, double k2d, int2 cheap) {
   constexpr bool CH = RHS == kStepCH;
   constexpr bool CN = RHS == kStepCN;
   constexpr int K4 = kSpK;
@@ -276,13 +282,54 @@ __global__ void __launch_bounds__(MAXT, 1)
         const D2 S0 = df::from_double(s0), S1 = df::from_double(s1);
         const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
         const D2 X0 = df::from_double(-xt0), X1 = df::from_double(-xt1);
+        // one 8-row group; mode 1: the M responses are below 2^-24 in every chunk
+        // here, mode 2: the K responses are, so those terms go to the low word alone
+        // (dropped cross terms and rounding below about 3 * 2^-48 of the state)
+        auto corr_group = [&](auto gi, auto mode) {
+          constexpr int g = decltype(gi)::value, md = decltype(mode)::value;
 #pragma unroll
-        for (int j = 0; j < L; ++j) {
-          const float4 c3 = ctb[j * K4 + 3], c4 = ctb[j * K4 + 4];
-          D2 x = df::axpy(v[j], D2{c3.x, c3.y}, S0);
-          x = df::axpy(x, D2{c3.z, c3.w}, S1);
-          x = df::axpy(x, D2{c4.x, c4.y}, T0);
-          v[j] = df::axpy(x, D2{c4.z, c4.w}, T1);
+          for (int u = 0; u < 8; ++u) {
+            const int j = g * 8 + u;
+            const float4 c3 = ctb[j * K4 + 3], c4 = ctb[j * K4 + 4];
+            D2 x = v[j];
+            if constexpr (md == 1) {
+              x.l = __fmaf_rn(c3.x, S0.h, x.l);
+              x.l = __fmaf_rn(c3.z, S1.h, x.l);
+            } else {
+              x = df::axpy(x, D2{c3.x, c3.y}, S0);
+              x = df::axpy(x, D2{c3.z, c3.w}, S1);
+            }
+            if constexpr (md == 2) {
+              x.l = __fmaf_rn(c4.x, T0.h, x.l);
+              x.l = __fmaf_rn(c4.z, T1.h, x.l);
+            } else {
+              x = df::axpy(x, D2{c4.x, c4.y}, T0);
+              x = df::axpy(x, D2{c4.z, c4.w}, T1);
+            }
+            v[j] = x;
+          }
+        };
+        // K responses fall towards a chunk's start, M responses towards its end: the
+        // first half of the groups may take mode 2, the second half mode 1
+        auto corr = [&](auto gi) {
+          constexpr int g = decltype(gi)::value;
+          using full = std::integral_constant<int, 0>;
+          if constexpr (!CHEAP) {
+            corr_group(gi, full{});
+          } else if constexpr (g < L / 16) {
+            if (g < cheap.x) corr_group(gi, std::integral_constant<int, 2>{});
+            else corr_group(gi, full{});
+          } else {
+            if (g >= cheap.y) corr_group(gi, std::integral_constant<int, 1>{});
+            else corr_group(gi, full{});
+          }
+        };
+        static_assert(L == 16 || L == 32, "chunks of 16 or 32 rows");
+        corr(std::integral_constant<int, 0>{});
+        corr(std::integral_constant<int, 1>{});
+        if constexpr (L == 32) {
+          corr(std::integral_constant<int, 2>{});
+          corr(std::integral_constant<int, 3>{});
         }
         if (needU) {
 #pragma unroll
@@ -318,12 +365,12 @@ __global__ void __launch_bounds__(MAXT, 1)
   }
 }
 
-template <int L, int SB, int RHS>
+template <int L, int SB, int RHS, bool CHEAP>
 cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, double k2,
                    cudaStream_t st) {
   const int P = p.sp_P;
   const size_t smem = steps_smem(L, P, SB, RHS);
-  auto kern = k_steps_df<L, SB, 512, RHS>;
+  auto kern = k_steps_df<L, SB, 512, RHS, CHEAP>;
   int per_sm = 0;
   const cudaError_t e = kernel_prepare((const void*)kern, smem, SB * P, &per_sm);
   if (e != cudaSuccess) return e;
@@ -331,7 +378,8 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, doubl
   const int nblk = (batch + SB - 1) / SB;
   int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
   if (grid > nblk) grid = nblk;
-  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch, nsteps, k2);
+  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch, nsteps, k2,
+                                   make_int2(p.cheap_k, p.cheap_m));
   note_launch();
   return cudaGetLastError();
 }
@@ -341,11 +389,18 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, doubl
 template <int RHS>
 cudaError_t launch_kind(const pent_plan_s& p, double* X, int batch, int nsteps, double k2,
                         cudaStream_t st) {
-  if (p.sp_L == 16) return launch<16, 8, RHS>(p, X, batch, nsteps, k2, st);
+  if (p.sp_L == 16) return launch<16, 8, RHS, false>(p, X, batch, nsteps, k2, st);
+  // the low-word correction groups only where the plan found some (the kernel that
+  // has them is slower when none apply: measured 4% for Crank–Nicolson, 6% for
+  // Cahn–Hilliard)
+  const bool cheap = p.cheap_k > 0 || p.cheap_m < p.sp_L / 8;
   const bool fits16 = p.sp_P <= 32 && steps_smem(32, p.sp_P, 16, RHS) <= kStepsSmemMax;
   const bool wide = p.steps_sb == 16 ? fits16 : p.steps_sb == 8 ? false : fits16 && batch > 16 * p.num_sms;
-  return wide ? launch<32, 16, RHS>(p, X, batch, nsteps, k2, st)
-              : launch<32, 8, RHS>(p, X, batch, nsteps, k2, st);
+  if (wide)
+    return cheap ? launch<32, 16, RHS, true>(p, X, batch, nsteps, k2, st)
+                 : launch<32, 16, RHS, false>(p, X, batch, nsteps, k2, st);
+  return cheap ? launch<32, 8, RHS, true>(p, X, batch, nsteps, k2, st)
+               : launch<32, 8, RHS, false>(p, X, batch, nsteps, k2, st);
 }
 
 }  // namespace

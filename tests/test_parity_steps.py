@@ -160,3 +160,28 @@ def test_multistep_systems_per_cta(kind, sb, monkeypatch):
     assert launches == 1
     idx = inputs.sample_systems(batch, 200)
     assert max_rel_err(out[:, idx], ref(kind, C0[:, idx], steps)) < TOL_F64
+
+
+@pytest.mark.parametrize("kind,sigma", [("hyper", 0.5), ("cn", 0.25), ("hyper", 0.05), ("ch", 3.0)])
+def test_multistep_low_word_correction_terms(kind, sigma, monkeypatch):
+    """Where a chunk's responses to its neighbours' states are below 2^-24 in every
+    chunk (the first and last 8-row groups when the couplings decay fast), the
+    multi-step kernel adds those terms to the low word alone.  Against every term in
+    double-float (PENT_CHEAP_TERMS=0) after 50 steps: the same state to 2^-40 of
+    max |C|, and both match the oracle."""
+    N, batch, steps = 512, 520, 50
+    C0 = initial(kind, N, batch, seed=41)
+    out = []
+    for cheap in ("1", "0"):
+        monkeypatch.setenv("PENT_CHEAP_TERMS", cheap)
+        SIGMA_SAVED = SIGMA[kind]
+        SIGMA[kind] = sigma
+        try:
+            o, launches = run(kind, N, batch, steps, C0)
+            r = ref(kind, C0, steps)
+        finally:
+            SIGMA[kind] = SIGMA_SAVED
+        assert launches == 1
+        assert max_rel_err(o, r) < TOL_F64
+        out.append(o)
+    assert max_rel_err(out[0], out[1]) < 2.0 ** -40
