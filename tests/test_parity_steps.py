@@ -16,8 +16,8 @@ SIGMA = {"hyper": 0.7, "ch": 3.0, "cn": 0.7}
 K2 = 0.2
 
 
-def run(kind, N, batch, steps, C0, per_step=False):
-    sigma = SIGMA[kind]
+def run(kind, N, batch, steps, C0, per_step=False, sigma=None):
+    sigma = SIGMA[kind] if sigma is None else sigma
     plan = pent.pent_factor(inputs.hyper_bands(N, sigma), batch, cyclic=True)
     C = dev(C0)
     old = os.environ.get("PENT_STEPS")
@@ -44,12 +44,13 @@ def run(kind, N, batch, steps, C0, per_step=False):
     return out, launches
 
 
-def ref(kind, C0, steps):
+def ref(kind, C0, steps, sigma=None):
+    sigma = SIGMA[kind] if sigma is None else sigma
     if kind == "hyper":
-        return oracle.batch_hyperdiffusion(C0, SIGMA[kind], steps)
+        return oracle.batch_hyperdiffusion(C0, sigma, steps)
     if kind == "ch":
-        return oracle.batch_ch(C0, SIGMA[kind], K2, steps)
-    return oracle.batch_cn(C0, SIGMA[kind], steps)
+        return oracle.batch_ch(C0, sigma, K2, steps)
+    return oracle.batch_cn(C0, sigma, steps)
 
 
 def initial(kind, N, batch, seed):
@@ -171,16 +172,11 @@ def test_multistep_low_word_correction_terms(kind, sigma, monkeypatch):
     max |C|, and both match the oracle."""
     N, batch, steps = 512, 520, 50
     C0 = initial(kind, N, batch, seed=41)
+    r = ref(kind, C0, steps, sigma)
     out = []
     for cheap in ("1", "0"):
         monkeypatch.setenv("PENT_CHEAP_TERMS", cheap)
-        SIGMA_SAVED = SIGMA[kind]
-        SIGMA[kind] = sigma
-        try:
-            o, launches = run(kind, N, batch, steps, C0)
-            r = ref(kind, C0, steps)
-        finally:
-            SIGMA[kind] = SIGMA_SAVED
+        o, launches = run(kind, N, batch, steps, C0, sigma=sigma)
         assert launches == 1
         assert max_rel_err(o, r) < TOL_F64
         out.append(o)
