@@ -374,8 +374,10 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
         // the two-kernel form needs the truncated chunk couplings
         p->split_big = !fits && p->sp_T > 0;
       }
-      if (p->split_big) {
-        e = split_big_prepare(*p, 0);
+      // the chunk tables as double-float pairs, for the kernels that run the chunk
+      // scan on the FP32 pipe (the two-kernel form and the multi-step kernel)
+      if (p->split_big || p->split_ok) {
+        e = chunk_tables_df(*p, 0);
         if (e == cudaSuccess) e = cudaStreamSynchronize(0);
         if (e != cudaSuccess) {
           cudaGetLastError();

@@ -43,12 +43,6 @@ constexpr int kStepHyper = 0;
 constexpr int kStepCH = 1;
 constexpr int kStepCN = 2;
 
-// y += A x for a row-major 2x2 A
-__device__ __forceinline__ void mv2(const double* A, double x0, double x1, double& y0, double& y1) {
-  y0 = fma(A[0], x0, fma(A[1], x1, y0));
-  y1 = fma(A[2], x0, fma(A[3], x1, y1));
-}
-
 // u = c^3 - c
 __device__ __forceinline__ D2 cubic_minus(D2 c) { return df::add(df::mul(df::mul(c, c), c), df::neg(c)); }
 
@@ -62,6 +56,12 @@ __device__ __forceinline__ D2 pick(bool p, D2 a, D2 b) { return D2{p ? a.h : b.h
 __device__ __forceinline__ float2 pack(D2 a) { return make_float2(a.h, a.l); }
 __device__ __forceinline__ D2 unpack(float2 a) { return D2{a.x, a.y}; }
 
+// y += A x for a row-major 2x2 A of double-float pairs
+__device__ __forceinline__ void mv2d(const float2* A, D2 x0, D2 x1, D2& y0, D2& y1) {
+  y0 = df::sum3(y0, unpack(A[0]), x0, unpack(A[1]), x1);
+  y1 = df::sum3(y1, unpack(A[2]), x0, unpack(A[3]), x1);
+}
+
 // Shared memory of one CTA (bytes), in the order the kernel carves it.
 __host__ __device__ inline size_t steps_smem(int L, int P, int SB, int rhs) {
   size_t b = (size_t)P * (L * kSpK + 1) * sizeof(float4);        // row tables
@@ -73,7 +73,7 @@ __host__ __device__ inline size_t steps_smem(int L, int P, int SB, int rhs) {
 
 template <int L, int SB, int MAXT, int RHS, bool CHEAP>
 __global__ void __launch_bounds__(MAXT, 1)
-    k_steps_df(const float4* __restrict__ growtab, const double* __restrict__ gchunk,
+    k_steps_df(const float4* __restrict__ growtab, const float2* __restrict__ gchunk,
                const double* __restrict__ gextra, double* __restrict__ X, int M, int P, int batch,
                int nsteps, double k2d, int2 cheap) {
   constexpr bool CH = RHS == kStepCH;
@@ -84,10 +84,10 @@ __global__ void __launch_bounds__(MAXT, 1)
   constexpr int LG = 8;                       // rows per load group
   extern __shared__ float4 smem4[];
   float4* rtab = smem4;                                              // [P][CS]
-  double* ctab = reinterpret_cast<double*>(rtab + (size_t)P * CS);   // [P][kSpChunk]
-  double* sE = ctab + (size_t)P * kSpChunk;      // [SB][P][2] local forward end values
-  double* sW = sE + (size_t)SB * P * 2;          // [SB][P][2] w_c
-  double* sX = sW + (size_t)SB * P * 2;          // [SB][8] y at 4 rows, x_t, tail state
+  float2* ctab = reinterpret_cast<float2*>(rtab + (size_t)P * CS);   // [P][kSpChunk] (hi, lo)
+  float2* sE = ctab + (size_t)P * kSpChunk;      // [SB][P][2] local forward end values
+  float2* sW = sE + (size_t)SB * P * 2;          // [SB][P][2] w_c
+  double* sX = reinterpret_cast<double*>(sW + (size_t)SB * P * 2);   // [SB][8] y at 4 rows, x_t, tail
   float2* sH = reinterpret_cast<float2*>(sX + (size_t)SB * 8);   // CH: [SB][P][2] first, last C
   float2* sA = sH + (CH ? (size_t)SB * P * 2 : 0);               // CH: [SB] C_{M-1}
   float2* sC = sA + (CH ? (size_t)SB : 0);                       // CN: [L][SB * P] C^n
@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(MAXT, 1)
   const int c = (w / SG) * 4 + (lane >> 3);
   const int row0 = c * L;
   const float4* ctb = rtab + (size_t)c * CS;
-  const double* ct = ctab + (size_t)c * kSpChunk;
+  const float2* ct = ctab + (size_t)c * kSpChunk;
   const long long ld = batch;
   const int nblk = (batch + SB - 1) / SB;
   const bool ownM2 = row0 <= M - 2 && M - 2 < row0 + L;
@@ -202,9 +202,9 @@ __global__ void __launch_bounds__(MAXT, 1)
           }
         }
       }
-      double* eo = sE + ((size_t)sys * P + c) * 2;
-      eo[0] = df::to_double(v[L - 2]);
-      eo[1] = df::to_double(v[L - 1]);
+      float2* eo = sE + ((size_t)sys * P + c) * 2;
+      eo[0] = pack(v[L - 2]);
+      eo[1] = pack(v[L - 1]);
       {
         D2 a1{0.f, 0.f}, a2{0.f, 0.f};
 #pragma unroll
@@ -216,7 +216,7 @@ __global__ void __launch_bounds__(MAXT, 1)
           a1 = y;
         }
       }
-      const double xs0 = df::to_double(v[0]), xs1 = df::to_double(v[1]);
+      const D2 xs0 = v[0], xs1 = v[1];
       double xm2 = 0.0, xm1 = 0.0;
       if (ownM2 || ownM1) {
         D2 a = v[0], b = v[0];
@@ -229,39 +229,45 @@ __global__ void __launch_bounds__(MAXT, 1)
         xm1 = df::to_double(b);
       }
 
-      // ---- 2. chunk boundary states s_c, t_c (truncated parallel scan), fp64
-      double s0 = 0.0, s1 = 0.0, t0 = 0.0, t1 = 0.0;
+      // ---- 2. chunk boundary states s_c, t_c (truncated parallel scan), in
+      // double-float on the FP32 pipe: in fp64 these few operations per thread
+      // queue on the slow fp64 pipe between two barriers, with every warp waiting
+      D2 s0{0.f, 0.f}, s1{0.f, 0.f}, t0{0.f, 0.f}, t1{0.f, 0.f};
       __syncthreads();                                      // e_c published
       {
-        const double* E = sE + (size_t)sys * P * 2;
+        const float2* E = sE + (size_t)sys * P * 2;
         for (int k = 1; k <= T && k <= c; ++k) {
-          const double ea = E[2 * (c - k)], eb = E[2 * (c - k) + 1];
-          if (k == 1) { s0 += ea; s1 += eb; }
-          else mv2(ct + 12 + 4 * (k - 2), ea, eb, s0, s1);
+          const D2 ea = unpack(E[2 * (c - k)]), eb = unpack(E[2 * (c - k) + 1]);
+          if (k == 1) { s0 = df::add(s0, ea); s1 = df::add(s1, eb); }
+          else mv2d(ct + 12 + 4 * (k - 2), ea, eb, s0, s1);
         }
       }
-      double w0 = xs0, w1 = xs1;
-      mv2(ct + 4, s0, s1, w0, w1);
-      double* wo = sW + ((size_t)sys * P + c) * 2;
-      wo[0] = w0;
-      wo[1] = w1;
+      D2 w0 = xs0, w1 = xs1;
+      mv2d(ct + 4, s0, s1, w0, w1);
+      float2* wo = sW + ((size_t)sys * P + c) * 2;
+      wo[0] = pack(w0);
+      wo[1] = pack(w1);
       __syncthreads();                                      // w_c published
       {
-        const double* Wv = sW + (size_t)sys * P * 2;
+        const float2* Wv = sW + (size_t)sys * P * 2;
         for (int k = 0; k < T && c + 1 + k < P; ++k) {
-          const double wa = Wv[2 * (c + 1 + k)], wb = Wv[2 * (c + 1 + k) + 1];
-          if (k == 0) { t0 += wa; t1 += wb; }
-          else mv2(ct + 24 + 4 * (k - 1), wa, wb, t0, t1);
+          const D2 wa = unpack(Wv[2 * (c + 1 + k)]), wb = unpack(Wv[2 * (c + 1 + k) + 1]);
+          if (k == 0) { t0 = df::add(t0, wa); t1 = df::add(t1, wb); }
+          else mv2d(ct + 24 + 4 * (k - 1), wa, wb, t0, t1);
         }
       }
       if (c == 0) {
-        double y0 = w0, y1 = w1;
-        mv2(ct + 8, t0, t1, y0, y1);
-        xc[2] = y0;
-        xc[3] = y1;
+        D2 y0 = w0, y1 = w1;
+        mv2d(ct + 8, t0, t1, y0, y1);
+        xc[2] = df::to_double(y0);
+        xc[3] = df::to_double(y1);
       }
-      if (ownM2) xc[0] = xm2 + gextra[10] * s0 + gextra[11] * s1 + gextra[14] * t0 + gextra[15] * t1;
-      if (ownM1) xc[1] = xm1 + gextra[12] * s0 + gextra[13] * s1 + gextra[16] * t0 + gextra[17] * t1;
+      if (ownM2 || ownM1) {
+        const double s0d = df::to_double(s0), s1d = df::to_double(s1);
+        const double t0d = df::to_double(t0), t1d = df::to_double(t1);
+        if (ownM2) xc[0] = xm2 + gextra[10] * s0d + gextra[11] * s1d + gextra[14] * t0d + gextra[15] * t1d;
+        if (ownM1) xc[1] = xm1 + gextra[12] * s0d + gextra[13] * s1d + gextra[16] * t0d + gextra[17] * t1d;
+      }
       __syncthreads();                                      // y at rows M-2, M-1, 0, 1 published
       // periodic rows: x_t = S^{-1}(f_t - H^T y)   (eq. (12)); then the next tail state
       if (c == 0) {
@@ -279,8 +285,7 @@ __global__ void __launch_bounds__(MAXT, 1)
 
       // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 - u0 x_t0 - u1 x_t1: the next state
       {
-        const D2 S0 = df::from_double(s0), S1 = df::from_double(s1);
-        const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
+        const D2 S0 = s0, S1 = s1, T0 = t0, T1 = t1;
         const D2 X0 = df::from_double(-xt0), X1 = df::from_double(-xt1);
         // one 8-row group; mode 1: the M responses are below 2^-24 in every chunk
         // here, mode 2: the K responses are, so those terms go to the low word alone
@@ -378,7 +383,7 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, doubl
   const int nblk = (batch + SB - 1) / SB;
   int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
   if (grid > nblk) grid = nblk;
-  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch, nsteps, k2,
+  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk_df, p.spextra, X, p.M, P, batch, nsteps, k2,
                                    make_int2(p.cheap_k, p.cheap_m));
   note_launch();
   return cudaGetLastError();
