@@ -47,6 +47,12 @@ __device__ __forceinline__ void mv2(const double* A, double x0, double x1, doubl
   y1 = fma(A[2], x0, fma(A[3], x1, y1));
 }
 
+// y += A x for a row-major 2x2 A of double-float pairs
+__device__ __forceinline__ void mv2d(const float2* A, D2 x0, D2 x1, D2& y0, D2& y1) {
+  y0 = df::sum3(y0, D2{A[0].x, A[0].y}, x0, D2{A[1].x, A[1].y}, x1);
+  y1 = df::sum3(y1, D2{A[2].x, A[2].y}, x0, D2{A[3].x, A[3].y}, x1);
+}
+
 // u = c^3 - c (Cahn–Hilliard chemical potential without the gradient term)
 __device__ __forceinline__ D2 cubic_minus(D2 c) { return df::add(df::mul(df::mul(c, c), c), df::neg(c)); }
 
@@ -64,8 +70,8 @@ constexpr int kRhsCN = 2;      // one Crank–Nicolson step
 template <int L, int SB, int MAXT, bool CYC, int RHS>
 __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     k_split_df(const float4* __restrict__ growtab, const double* __restrict__ gchunk,
-               const double* __restrict__ gextra, double* __restrict__ X, int M, int P,
-               int batch, double k2d) {
+               const float2* __restrict__ gchunk_df, const double* __restrict__ gextra,
+               double* __restrict__ X, int M, int P, int batch, double k2d) {
   constexpr bool CH = RHS == kRhsCH;
   constexpr bool CN = RHS == kRhsCN;
   static_assert(RHS == kRhsPlain || CYC, "the fused time steps are periodic");
@@ -74,7 +80,10 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   constexpr int SG = SB / 8;                  // system groups of 8 per CTA
   extern __shared__ float4 smem4[];
   float4* rtab = smem4;                                              // [P][CS]
-  double* ctab = reinterpret_cast<double*>(rtab + (size_t)P * CS);   // [P][kSpChunk]
+  // [P][kSpChunk] chunk tables: fp64 for the exact serial scan (T = 0), (hi, lo)
+  // pairs for the parallel one, which runs in double-float on the FP32 pipe
+  double* ctab = reinterpret_cast<double*>(rtab + (size_t)P * CS);
+  const float2* ctab2 = reinterpret_cast<const float2*>(ctab);
   double* sE = ctab + (size_t)P * kSpChunk;      // [SB][P][2] local forward end values e_c
   double* sW = sE + (size_t)SB * P * 2;          // [SB][P][2] x'_start (serial) or w_c (parallel)
   double* sS = sW + (size_t)SB * P * 2;          // [SB][P][2] s_c (serial scan)
@@ -85,10 +94,15 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     const int row = t / K4, k = t % K4;
     cp_async16(&rtab[(row / L) * CS + (row % L) * K4 + k], &growtab[(size_t)row * kSpK + k]);
   }
-  for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
+  const int T = (int)gextra[18];
+  if (T > 0) {
+    for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x)
+      cp_async16(&ctab[2 * t], &gchunk_df[2 * t]);
+  } else {
+    for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
+  }
   cp_async_wait_all();
   __syncthreads();
-  const int T = (int)gextra[18];
 
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int sys = (w % SG) * 8 + (lane & 7);
@@ -97,7 +111,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   const float4* ctb = rtab + (size_t)c * CS;     // this chunk's rows
   const int reach = CYC ? (int)gextra[19] : 0;
   const bool needU = CYC && (c < reach || c > (M - 1) / L - reach);   // x_t correction not negligible
-  const double* ct = ctab + (size_t)c * kSpChunk;
+  const float2* ct = ctab2 + (size_t)c * kSpChunk;
   const long long ld = batch;
   const int nblk = (batch + SB - 1) / SB;
 
@@ -154,9 +168,15 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         a1 = g;
       }
     }
-    double* eo = sE + ((size_t)sys * P + c) * 2;
-    eo[0] = df::to_double(v[L - 2]);
-    eo[1] = df::to_double(v[L - 1]);
+    if (T > 0) {
+      float2* eo = reinterpret_cast<float2*>(sE) + ((size_t)sys * P + c) * 2;
+      eo[0] = make_float2(v[L - 2].h, v[L - 2].l);
+      eo[1] = make_float2(v[L - 1].h, v[L - 1].l);
+    } else {
+      double* eo = sE + ((size_t)sys * P + c) * 2;
+      eo[0] = df::to_double(v[L - 2]);
+      eo[1] = df::to_double(v[L - 1]);
+    }
     {
       D2 a1{0.f, 0.f}, a2{0.f, 0.f};
 #pragma unroll
@@ -168,7 +188,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         a1 = y;
       }
     }
-    const double xs0 = df::to_double(v[0]), xs1 = df::to_double(v[1]);   // x'_start(c)
+    const D2 xs0 = v[0], xs1 = v[1];   // x'_start(c)
     // x' at rows M-2, M-1 (cyclic): only the owning chunks keep them
     double xm2 = 0.0, xm1 = 0.0;
     if (CYC && row0 <= M - 1 && M - 2 < row0 + L) {
@@ -179,45 +199,53 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
       }
     }
 
-    // ---- 2. boundary states s_c (entering) and t_c (leaving), fp64
-    double s0 = 0.0, s1 = 0.0, t0 = 0.0, t1 = 0.0;
+    // ---- 2. boundary states s_c (entering) and t_c (leaving): the truncated
+    // parallel scan in double-float on the FP32 pipe (in fp64 its few operations
+    // per thread queue on the slow fp64 pipe between two barriers, with every warp
+    // waiting), the exact serial one (testing, slowly decaying couplings) in fp64
+    D2 S0{0.f, 0.f}, S1{0.f, 0.f}, T0{0.f, 0.f}, T1{0.f, 0.f};
     double* xc = sX + (size_t)sys * 8;
     if (T > 0) {
       __syncthreads();                                   // e_c published
-      const double* E = sE + (size_t)sys * P * 2;
+      const float2* E = reinterpret_cast<const float2*>(sE) + (size_t)sys * P * 2;
       for (int k = 1; k <= T && k <= c; ++k) {           // s_c = sum_k A_{c,k} e_{c-k}
-        const double ea = E[2 * (c - k)], eb = E[2 * (c - k) + 1];
-        if (k == 1) { s0 += ea; s1 += eb; }
-        else mv2(ct + 12 + 4 * (k - 2), ea, eb, s0, s1);
+        const D2 ea{E[2 * (c - k)].x, E[2 * (c - k)].y}, eb{E[2 * (c - k) + 1].x, E[2 * (c - k) + 1].y};
+        if (k == 1) { S0 = df::add(S0, ea); S1 = df::add(S1, eb); }
+        else mv2d(ct + 12 + 4 * (k - 2), ea, eb, S0, S1);
       }
-      double w0 = xs0, w1 = xs1;
-      mv2(ct + 4, s0, s1, w0, w1);                       // w_c = x'_start + Mst_c s_c
-      double* wo = sW + ((size_t)sys * P + c) * 2;
-      wo[0] = w0;
-      wo[1] = w1;
+      D2 w0 = xs0, w1 = xs1;
+      mv2d(ct + 4, S0, S1, w0, w1);                      // w_c = x'_start + Mst_c s_c
+      float2* wo = reinterpret_cast<float2*>(sW) + ((size_t)sys * P + c) * 2;
+      wo[0] = make_float2(w0.h, w0.l);
+      wo[1] = make_float2(w1.h, w1.l);
       __syncthreads();                                   // w_c published
-      const double* Wv = sW + (size_t)sys * P * 2;
+      const float2* Wv = reinterpret_cast<const float2*>(sW) + (size_t)sys * P * 2;
       for (int k = 0; k < T && c + 1 + k < P; ++k) {     // t_c = sum_k B_{c,k} w_{c+1+k}
-        const double wa = Wv[2 * (c + 1 + k)], wb = Wv[2 * (c + 1 + k) + 1];
-        if (k == 0) { t0 += wa; t1 += wb; }
-        else mv2(ct + 24 + 4 * (k - 1), wa, wb, t0, t1);
+        const D2 wa{Wv[2 * (c + 1 + k)].x, Wv[2 * (c + 1 + k)].y};
+        const D2 wb{Wv[2 * (c + 1 + k) + 1].x, Wv[2 * (c + 1 + k) + 1].y};
+        if (k == 0) { T0 = df::add(T0, wa); T1 = df::add(T1, wb); }
+        else mv2d(ct + 24 + 4 * (k - 1), wa, wb, T0, T1);
       }
       if (CYC) {
         if (c == 0) {                                    // y at rows 0, 1
-          double y0 = w0, y1 = w1;
-          mv2(ct + 8, t0, t1, y0, y1);
-          xc[2] = y0;
-          xc[3] = y1;
+          D2 y0 = w0, y1 = w1;
+          mv2d(ct + 8, T0, T1, y0, y1);
+          xc[2] = df::to_double(y0);
+          xc[3] = df::to_double(y1);
         }
-        if (row0 <= M - 2 && M - 2 < row0 + L)
-          xc[0] = xm2 + gextra[10] * s0 + gextra[11] * s1 + gextra[14] * t0 + gextra[15] * t1;
-        if (row0 <= M - 1 && M - 1 < row0 + L)
-          xc[1] = xm1 + gextra[12] * s0 + gextra[13] * s1 + gextra[16] * t0 + gextra[17] * t1;
+        if (row0 <= M - 1 && M - 2 < row0 + L) {
+          const double s0 = df::to_double(S0), s1 = df::to_double(S1);
+          const double t0 = df::to_double(T0), t1 = df::to_double(T1);
+          if (row0 <= M - 2 && M - 2 < row0 + L)
+            xc[0] = xm2 + gextra[10] * s0 + gextra[11] * s1 + gextra[14] * t0 + gextra[15] * t1;
+          if (row0 <= M - 1 && M - 1 < row0 + L)
+            xc[1] = xm1 + gextra[12] * s0 + gextra[13] * s1 + gextra[16] * t0 + gextra[17] * t1;
+        }
       }
     } else {
       double* wo = sW + ((size_t)sys * P + c) * 2;
-      wo[0] = xs0;
-      wo[1] = xs1;
+      wo[0] = df::to_double(xs0);
+      wo[1] = df::to_double(xs1);
       if (CYC) {
         if (row0 <= M - 2 && M - 2 < row0 + L) xc[0] = xm2;
         if (row0 <= M - 1 && M - 1 < row0 + L) xc[1] = xm1;
@@ -259,10 +287,10 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         }
       }
       __syncthreads();
-      s0 = sS[((size_t)sys * P + c) * 2];
-      s1 = sS[((size_t)sys * P + c) * 2 + 1];
-      t0 = sT[((size_t)sys * P + c) * 2];
-      t1 = sT[((size_t)sys * P + c) * 2 + 1];
+      S0 = df::from_double(sS[((size_t)sys * P + c) * 2]);
+      S1 = df::from_double(sS[((size_t)sys * P + c) * 2 + 1]);
+      T0 = df::from_double(sT[((size_t)sys * P + c) * 2]);
+      T1 = df::from_double(sT[((size_t)sys * P + c) * 2 + 1]);
     }
     // cyclic: x_t = S^{-1}(f_t - H^T y)   (eq. (12))
     double xt0 = 0.0, xt1 = 0.0;
@@ -305,8 +333,6 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
 
     // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 (- u0 x_t0 - u1 x_t1), store
     {
-      const D2 S0 = df::from_double(s0), S1 = df::from_double(s1);
-      const D2 T0 = df::from_double(t0), T1 = df::from_double(t1);
       const D2 X0 = df::from_double(-xt0), X1 = df::from_double(-xt1);
       if (CYC && needU) {
 #pragma unroll
@@ -354,7 +380,7 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st, 
   if (per_sm < 1) per_sm = 1;
   int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
   if (grid > nblk) grid = nblk;
-  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spextra, X, p.M, P, batch, k2);
+  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spchunk_df, p.spextra, X, p.M, P, batch, k2);
   note_launch();
   return cudaGetLastError();
 }
