@@ -66,6 +66,7 @@ __device__ __forceinline__ void mv2d(const float2* A, D2 x0, D2 x1, D2& y0, D2& 
 __host__ __device__ inline size_t steps_smem(int L, int P, int SB, int rhs) {
   size_t b = (size_t)P * (L * kSpK + 1) * sizeof(float4);        // row tables
   b += ((size_t)P * kSpChunk + 2 * (size_t)SB * P * 2 + (size_t)SB * 8) * sizeof(double);
+  b += kSpExtra * sizeof(float2);                                   // extras as (hi, lo)
   if (rhs == kStepCH) b += ((size_t)SB * P * 2 + SB) * sizeof(float2);   // halo, C_{M-1}
   if (rhs == kStepCN) b += (size_t)L * SB * P * sizeof(float2);          // C^n of every row
   return b;
@@ -87,8 +88,9 @@ __global__ void __launch_bounds__(MAXT, 1)
   float2* ctab = reinterpret_cast<float2*>(rtab + (size_t)P * CS);   // [P][kSpChunk] (hi, lo)
   float2* sE = ctab + (size_t)P * kSpChunk;      // [SB][P][2] local forward end values
   float2* sW = sE + (size_t)SB * P * 2;          // [SB][P][2] w_c
-  double* sX = reinterpret_cast<double*>(sW + (size_t)SB * P * 2);   // [SB][8] y at 4 rows, x_t, tail
-  float2* sH = reinterpret_cast<float2*>(sX + (size_t)SB * 8);   // CH: [SB][P][2] first, last C
+  float2* sX = sW + (size_t)SB * P * 2;         // [SB][8] y at 4 rows, x_t, tail state (hi, lo)
+  float2* sXe = sX + (size_t)SB * 8;             // [kSpExtra] the plan's extras as (hi, lo)
+  float2* sH = sXe + kSpExtra;                   // CH: [SB][P][2] first, last C
   float2* sA = sH + (CH ? (size_t)SB * P * 2 : 0);               // CH: [SB] C_{M-1}
   float2* sC = sA + (CH ? (size_t)SB : 0);                       // CN: [L][SB * P] C^n
 
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(MAXT, 1)
     cp_async16(&rtab[(row / L) * CS + (row % L) * K4 + k], &growtab[(size_t)row * kSpK + k]);
   }
   for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
+  if (threadIdx.x < kSpExtra) sXe[threadIdx.x] = pack(df::from_double(gextra[threadIdx.x]));
   cp_async_wait_all();
   __syncthreads();
   const int T = (int)gextra[18];
@@ -117,7 +120,8 @@ __global__ void __launch_bounds__(MAXT, 1)
   // hyperdiffusion step, where every chunk keeps it)
   const int reach = (int)gextra[19];
   const bool needU = RHS == kStepHyper || c < reach || c > (M - 1) / L - reach;
-  double* xc = sX + (size_t)sys * 8;
+  float2* xc = sX + (size_t)sys * 8;
+  auto ex = [&](int k) { return unpack(sXe[k]); };
 
   for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x) {
     const int s = blk * SB + sys;
@@ -135,14 +139,14 @@ __global__ void __launch_bounds__(MAXT, 1)
       for (int u = 0; u < LG; ++u) v[j0 + u] = df::from_double(fv[u]);
     }
     if (c == 0) {
-      xc[6] = act ? X[(long long)M * ld + s] : 0.0;
-      xc[7] = act ? X[(long long)(M + 1) * ld + s] : 0.0;
+      xc[6] = pack(df::from_double(act ? X[(long long)M * ld + s] : 0.0));
+      xc[7] = pack(df::from_double(act ? X[(long long)(M + 1) * ld + s] : 0.0));
     }
     __syncthreads();
 
     for (int n = 0; n < nsteps; ++n) {
-      const D2 ct0 = df::from_double(xc[6]), ct1 = df::from_double(xc[7]);   // C at rows M, M+1
-      double ft0 = xc[6], ft1 = xc[7];   // right-hand side of the two periodic rows
+      const D2 ct0 = unpack(xc[6]), ct1 = unpack(xc[7]);   // C at rows M, M+1
+      D2 ft0 = ct0, ft1 = ct1;                             // right-hand side of the two periodic rows
 
       // ---- 1. forward substitution with this step's right-hand side (zero incoming state)
       {
@@ -163,8 +167,8 @@ __global__ void __launch_bounds__(MAXT, 1)
             const D2 cA = unpack(sA[sys]);
             const D2 uA = cubic_minus(cA), uB = cubic_minus(ct0), uC = cubic_minus(ct1);
             const D2 uD = cubic_minus(v[0]);
-            ft0 = df::to_double(ch_rhs(ct0, uA, uB, uC, k2));
-            ft1 = df::to_double(ch_rhs(ct1, uB, uC, uD, k2));
+            ft0 = ch_rhs(ct0, uA, uB, uC, k2);
+            ft1 = ch_rhs(ct1, uB, uC, uD, k2);
           }
           const D2 lh = c == 0 ? ct1 : unpack(sH[((size_t)sys * P + c - 1) * 2 + 1]);
           D2 rh = c + 1 < P ? unpack(sH[((size_t)sys * P + c + 1) * 2]) : D2{0.f, 0.f};
@@ -217,7 +221,7 @@ __global__ void __launch_bounds__(MAXT, 1)
         }
       }
       const D2 xs0 = v[0], xs1 = v[1];
-      double xm2 = 0.0, xm1 = 0.0;
+      D2 xm2{0.f, 0.f}, xm1{0.f, 0.f};
       if (ownM2 || ownM1) {
         D2 a = v[0], b = v[0];
 #pragma unroll
@@ -225,8 +229,8 @@ __global__ void __launch_bounds__(MAXT, 1)
           a = pick(row0 + j == M - 2, v[j], a);
           b = pick(row0 + j == M - 1, v[j], b);
         }
-        xm2 = df::to_double(a);
-        xm1 = df::to_double(b);
+        xm2 = a;
+        xm1 = b;
       }
 
       // ---- 2. chunk boundary states s_c, t_c (truncated parallel scan), in
@@ -259,34 +263,33 @@ __global__ void __launch_bounds__(MAXT, 1)
       if (c == 0) {
         D2 y0 = w0, y1 = w1;
         mv2d(ct + 8, t0, t1, y0, y1);
-        xc[2] = df::to_double(y0);
-        xc[3] = df::to_double(y1);
+        xc[2] = pack(y0);
+        xc[3] = pack(y1);
       }
-      if (ownM2 || ownM1) {
-        const double s0d = df::to_double(s0), s1d = df::to_double(s1);
-        const double t0d = df::to_double(t0), t1d = df::to_double(t1);
-        if (ownM2) xc[0] = xm2 + gextra[10] * s0d + gextra[11] * s1d + gextra[14] * t0d + gextra[15] * t1d;
-        if (ownM1) xc[1] = xm1 + gextra[12] * s0d + gextra[13] * s1d + gextra[16] * t0d + gextra[17] * t1d;
-      }
+      // y at rows M-2, M-1 and the border solve below in double-float as well
+      if (ownM2) xc[0] = pack(df::sum3(df::sum3(xm2, ex(10), s0, ex(11), s1), ex(14), t0, ex(15), t1));
+      if (ownM1) xc[1] = pack(df::sum3(df::sum3(xm1, ex(12), s0, ex(13), s1), ex(16), t0, ex(17), t1));
       __syncthreads();                                      // y at rows M-2, M-1, 0, 1 published
       // periodic rows: x_t = S^{-1}(f_t - H^T y)   (eq. (12)); then the next tail state
       if (c == 0) {
-        const double r0 = gextra[4] * xc[0] + gextra[5] * xc[1] + gextra[6] * xc[2];
-        const double r1 = gextra[7] * xc[1] + gextra[8] * xc[2] + gextra[9] * xc[3];
-        const double u0 = gextra[0] * (ft0 - r0) + gextra[1] * (ft1 - r1);
-        const double u1 = gextra[2] * (ft0 - r0) + gextra[3] * (ft1 - r1);
-        xc[4] = u0;
-        xc[5] = u1;
-        xc[6] = CN ? 2.0 * u0 - xc[6] : u0;
-        xc[7] = CN ? 2.0 * u1 - xc[7] : u1;
+        const D2 y0 = unpack(xc[0]), y1 = unpack(xc[1]), y2 = unpack(xc[2]), y3 = unpack(xc[3]);
+        const D2 r0 = df::sum3(df::mul(ex(4), y0), ex(5), y1, ex(6), y2);
+        const D2 r1 = df::sum3(df::mul(ex(7), y1), ex(8), y2, ex(9), y3);
+        const D2 d0 = df::add(ft0, df::neg(r0)), d1 = df::add(ft1, df::neg(r1));
+        const D2 u0 = df::sum3(D2{0.f, 0.f}, ex(0), d0, ex(1), d1);
+        const D2 u1 = df::sum3(D2{0.f, 0.f}, ex(2), d0, ex(3), d1);
+        xc[4] = pack(u0);
+        xc[5] = pack(u1);
+        xc[6] = CN ? pack(df::add(D2{2.f * u0.h, 2.f * u0.l}, df::neg(ct0))) : pack(u0);
+        xc[7] = CN ? pack(df::add(D2{2.f * u1.h, 2.f * u1.l}, df::neg(ct1))) : pack(u1);
       }
       __syncthreads();                                      // x_t published
-      const double xt0 = xc[4], xt1 = xc[5];
+      const D2 xt0 = unpack(xc[4]), xt1 = unpack(xc[5]);
 
       // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 - u0 x_t0 - u1 x_t1: the next state
       {
         const D2 S0 = s0, S1 = s1, T0 = t0, T1 = t1;
-        const D2 X0 = df::from_double(-xt0), X1 = df::from_double(-xt1);
+        const D2 X0 = df::neg(xt0), X1 = df::neg(xt1);
         // one 8-row group; mode 1: the M responses are below 2^-24 in every chunk
         // here, mode 2: the K responses are, so those terms go to the low word alone
         // (dropped cross terms and rounding below about 3 * 2^-48 of the state)
@@ -317,7 +320,7 @@ __global__ void __launch_bounds__(MAXT, 1)
         // K responses fall towards a chunk's start, M responses towards its end: the
         // first half of the groups may take mode 2, the second half mode 1
         auto corr = [&](auto gi) {
-          constexpr int g = decltype(gi)::value;
+          [[maybe_unused]] constexpr int g = decltype(gi)::value;
           using full = std::integral_constant<int, 0>;
           if constexpr (!CHEAP) {
             corr_group(gi, full{});
@@ -363,8 +366,8 @@ __global__ void __launch_bounds__(MAXT, 1)
     for (int j = 0; j < L; ++j)
       if (act && row0 + j < M) __stcs(p + j * ld, df::to_double(v[j]));
     if (c == 0 && act) {
-      X[(long long)M * ld + s] = xc[6];
-      X[(long long)(M + 1) * ld + s] = xc[7];
+      X[(long long)M * ld + s] = df::to_double(unpack(xc[6]));
+      X[(long long)(M + 1) * ld + s] = df::to_double(unpack(xc[7]));
     }
     __syncthreads();                                        // shared state reused by the next block
   }
