@@ -115,11 +115,9 @@ __global__ void __launch_bounds__(MAXT, 1)
   const int nblk = (batch + SB - 1) / SB;
   const bool ownM2 = row0 <= M - 2 && M - 2 < row0 + L;
   const bool ownM1 = row0 <= M - 1 && M - 1 < row0 + L;
-  // x_t correction only where it is not negligible (measured: a gain for the
-  // Cahn–Hilliard and Crank–Nicolson steps, a loss for the lighter
-  // hyperdiffusion step, where every chunk keeps it)
+  // x_t correction only in the chunks where it is not negligible
   const int reach = (int)gextra[19];
-  const bool needU = RHS == kStepHyper || c < reach || c > (M - 1) / L - reach;
+  const bool needU = c < reach || c > (M - 1) / L - reach;
   float2* xc = sX + (size_t)sys * 8;
   auto ex = [&](int k) { return unpack(sXe[k]); };
 
@@ -354,8 +352,9 @@ __global__ void __launch_bounds__(MAXT, 1)
           if (row0 + j >= M) x = D2{0.f, 0.f};
           // renormalise (h, l) so that |l| <= ulp(h)/2: carried unnormalised from
           // step to step, the low word grows and its own rounding error with it
+          // (|l| is a few ulps of h at most, so Fast2Sum is exact here)
           float sh, sl;
-          df::two_sum(x.h, x.l, sh, sl);
+          df::quick_two_sum(x.h, x.l, sh, sl);
           v[j] = D2{sh, sl};
         }
       }
