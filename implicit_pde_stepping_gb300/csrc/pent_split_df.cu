@@ -101,13 +101,21 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   } else {
     for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
   }
-  cp_async_wait_all();
-  __syncthreads();
-
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int sys = (w % SG) * 8 + (lane & 7);
   const int c = (w / SG) * 4 + (lane >> 3);
   const int row0 = c * L;
+  // the first block's rows of this chunk start towards L2 while the tables arrive,
+  // so a short solve waits for one memory latency instead of two
+  if (blockIdx.x * SB + sys < batch) {
+    const double* pf = X + (long long)row0 * batch + blockIdx.x * SB + sys;
+#pragma unroll
+    for (int j = 0; j < L; ++j)
+      if (row0 + j < M) asm volatile("prefetch.global.L2 [%0];" ::"l"(pf + (long long)j * batch));
+  }
+  cp_async_wait_all();
+  __syncthreads();
+
   const float4* ctb = rtab + (size_t)c * CS;     // this chunk's rows
   const int reach = CYC ? (int)gextra[19] : 0;
   const bool needU = CYC && (c < reach || c > (M - 1) / L - reach);   // x_t correction not negligible
