@@ -45,13 +45,6 @@ __device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
   e = __fadd_rn(__fsub_rn(a, ap), __fsub_rn(b, bb));
 }
 
-// a + b = s + e for |a| >= |b| (Dekker's Fast2Sum, three operations); with
-// |b| > |a| the result is still within an ulp of b's low bits
-__device__ __forceinline__ void quick_two_sum(float a, float b, float& s, float& e) {
-  s = __fadd_rn(a, b);
-  e = __fsub_rn(b, __fsub_rn(s, a));
-}
-
 // s = f + c1*y1 + c2*y2 + c3*y3 with f, c_k, y_k double-floats; f may be scaled
 // by a coefficient too (see axpy3).  Products use only the hi part of y in the
 // exact step; the hi*lo and lo*hi cross terms are accumulated in the low word.

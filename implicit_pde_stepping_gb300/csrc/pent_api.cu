@@ -377,7 +377,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
       // the chunk tables as double-float pairs, for the kernels that run the chunk
       // scan on the FP32 pipe (the two-kernel form and the multi-step kernel)
       if (p->split_big || p->split_ok) {
-        e = chunk_tables_df(*p, 0);
+        e = split_big_prepare(*p, 0);
         if (e == cudaSuccess) e = cudaStreamSynchronize(0);
         if (e != cudaSuccess) {
           cudaGetLastError();

@@ -203,7 +203,7 @@ cudaError_t shared_split_df(const pent_plan_s& p, double* X, int batch, cudaStre
 // pent_split_big.cu: the same solve for systems too long for one CTA (two kernels)
 cudaError_t shared_split_big(pent_plan_s& p, double* X, int batch, cudaStream_t st);
 // plan time: the double-float copy of the chunk tables
-cudaError_t chunk_tables_df(pent_plan_s& p, cudaStream_t st);
+cudaError_t split_big_prepare(pent_plan_s& p, cudaStream_t st);
 size_t split_smem_bytes(int L, int P, int SB, int cyclic);
 cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);
 cudaError_t cn_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);

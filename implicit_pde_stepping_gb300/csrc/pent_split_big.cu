@@ -299,7 +299,7 @@ cudaError_t run_cyc(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t chunk_tables_df(pent_plan_s& p, cudaStream_t st) {
+cudaError_t split_big_prepare(pent_plan_s& p, cudaStream_t st) {
   const int n = p.sp_P * kSpChunk;
   k_chunk_df<<<(n + 255) / 256, 256, 0, st>>>(p.spchunk, p.spchunk_df, n);
   note_launch();

@@ -52,6 +52,12 @@ __device__ __forceinline__ D2 ch_rhs(D2 c, D2 um, D2 u0, D2 up, D2 k2) {
   return df::add(c, df::mul(k2, lap));
 }
 
+// a + b = s + e for |a| >= |b| (Dekker's Fast2Sum, three operations)
+__device__ __forceinline__ void quick_two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  e = __fsub_rn(b, __fsub_rn(s, a));
+}
+
 __device__ __forceinline__ D2 pick(bool p, D2 a, D2 b) { return D2{p ? a.h : b.h, p ? a.l : b.l}; }
 __device__ __forceinline__ float2 pack(D2 a) { return make_float2(a.h, a.l); }
 __device__ __forceinline__ D2 unpack(float2 a) { return D2{a.x, a.y}; }
@@ -354,7 +360,7 @@ __global__ void __launch_bounds__(MAXT, 1)
           // step to step, the low word grows and its own rounding error with it
           // (|l| is a few ulps of h at most, so Fast2Sum is exact here)
           float sh, sl;
-          df::quick_two_sum(x.h, x.l, sh, sl);
+          quick_two_sum(x.h, x.l, sh, sl);
           v[j] = D2{sh, sl};
         }
       }
