@@ -375,7 +375,8 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
         p->split_big = !fits && p->sp_T > 0;
       }
       // the chunk tables as double-float pairs, for the kernels that run the chunk
-      // scan on the FP32 pipe (the two-kernel form and the multi-step kernel)
+      // scan on the FP32 pipe (the two-kernel form, the partitioned one-step kernel
+      // and the multi-step kernel)
       if (p->split_big || p->split_ok) {
         e = split_big_prepare(*p, 0);
         if (e == cudaSuccess) e = cudaStreamSynchronize(0);

@@ -68,7 +68,7 @@ struct pent_plan_s {
   size_t spsum_bytes = 0;
   float4* sptab = nullptr;   // [Mpad][kSpK]
   double* spchunk = nullptr; // [sp_P][kSpChunk]
-  float2* spchunk_df = nullptr;   // the same as double-float pairs (two-kernel form, multi-step kernel)
+  float2* spchunk_df = nullptr;   // the same as double-float pairs (the scans on the FP32 pipe)
   double* spextra = nullptr; // [kSpExtra]
   // host-buffer pipeline (pent_host.cu), created on first use
   static constexpr int kHostRing = 3;
