@@ -77,3 +77,37 @@ def test_work_bytes(L):
 
 def test_launch_counter_starts_readable(L):
     assert pent.launch_count() >= 0
+
+
+def test_per_system_argument_errors_before_any_device_work(L):
+    """The per-system entry points reject bad arguments on the host: null or
+    misaligned pointers, sizes, a block size that does not divide the batch, an
+    unknown dtype, and variants that do not exist for the dtype or size."""
+    ok = ctypes.c_void_p(1 << 12)            # aligned, never dereferenced on these paths
+    mis = ctypes.c_void_p((1 << 12) + 8)     # 8-byte aligned only
+    z = ctypes.c_void_p(0)
+    work = ctypes.c_void_p(1 << 16)
+    p6 = [ok] * 6
+    ex = L.pent_factor_solve_ex
+    assert ex(*p6, 0, 4, pent.F64, pent.VARIANT_AUTO, 0, work, 1 << 20, None, None) == pent.ERR_INVALID_ARG
+    assert ex(*p6, 8, 0, pent.F64, pent.VARIANT_AUTO, 0, work, 1 << 20, None, None) == pent.ERR_INVALID_ARG
+    assert ex(z, *p6[1:], 8, 4, pent.F64, pent.VARIANT_AUTO, 0, work, 1 << 20, None, None) == pent.ERR_INVALID_ARG
+    assert ex(*p6[:5], mis, 8, 4, pent.F64, pent.VARIANT_AUTO, 0, work, 1 << 20, None, None) == pent.ERR_INVALID_ARG
+    assert ex(*p6, 8, 6, pent.F64, pent.VARIANT_AUTO, 4, work, 1 << 20, None, None) == pent.ERR_INVALID_ARG
+    assert ex(*p6, 8, 4, 7, pent.VARIANT_AUTO, 0, work, 1 << 20, None, None) == pent.ERR_INVALID_ARG
+    # the double-float kernel is for fp64 systems; the partitioned one for fp32, N <= 512
+    assert ex(*p6, 8, 4, pent.F32, pent.VARIANT_THREAD_DF, 0, work, 1 << 20, None, None) == pent.ERR_UNSUPPORTED
+    assert ex(*p6, 8, 4, pent.F64, pent.VARIANT_SPLIT, 0, work, 1 << 20, None, None) == pent.ERR_UNSUPPORTED
+    assert ex(*p6, 600, 4, pent.F32, pent.VARIANT_SPLIT, 0, work, 1 << 20, None, None) == pent.ERR_UNSUPPORTED
+    tri = L.tri_factor_solve
+    p4 = [ok] * 4
+    assert tri(z, *p4[1:], 8, 4, pent.F64, pent.VARIANT_AUTO, 0, work, 1 << 20, None, None) == pent.ERR_INVALID_ARG
+    assert tri(*p4, 8, 6, pent.F32, pent.VARIANT_AUTO, 4, work, 1 << 20, None, None) == pent.ERR_INVALID_ARG
+    assert tri(*p4, 8, 4, pent.F32, pent.VARIANT_THREAD_DF, 0, work, 1 << 20, None, None) == pent.ERR_UNSUPPORTED
+    assert tri(*p4, 8, 4, pent.F64, pent.VARIANT_SPLIT, 0, work, 1 << 20, None, None) == pent.ERR_UNSUPPORTED
+    na = L.pent_factor_solve_noalloc
+    assert na(*p6, 0, 4, pent.F32, None, None) == pent.ERR_INVALID_ARG
+    assert na(*p6[:5], mis, 8, 4, pent.F32, None, None) == pent.ERR_INVALID_ARG
+    assert na(*p6, 8, 4, 9, None, None) == pent.ERR_INVALID_ARG
+    assert L.pent_solve_host(None, ok, ok, 4, 0, None) == pent.ERR_INVALID_ARG
+    assert L.pent_get_variant(None, 4) == pent.VARIANT_AUTO
