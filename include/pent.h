@@ -43,7 +43,7 @@ typedef enum {
   PENT_ERR_ZERO_PIVOT = 2,  /* zero or non-finite pivot / singular 2x2 border  */
   PENT_ERR_CUDA = 3,        /* a CUDA call or kernel launch failed             */
   PENT_ERR_ALLOC = 4,       /* device or host allocation failed                */
-  PENT_ERR_UNSUPPORTED = 5  /* valid request this build does not implement     */
+  PENT_ERR_UNSUPPORTED = 5  /* valid request the library does not implement   */
 } pent_status;
 
 typedef enum { PENT_F64 = 0, PENT_F32 = 1 } pent_dtype;
