@@ -414,7 +414,7 @@ def run_ours(args, W: dict, dist: Dist):
     peak, peak_kind = hbm_peak()
     # the kernel one launch of the step runs (the fused CH / CN steps use the
     # partitioned kernel for every double-float variant)
-    twisted = "k_twisted_async" if int(os.environ.get("PENT_DF_ASYNC", "6") or 6) > 0 else "k_twisted_df"
+    twisted = "k_twisted_async"
     split = ("k_split_df", "pent_split_df.cu")
     kernel_names = {
         ("shared", pent.VARIANT_THREAD): ("k_shared_thread", "pent_shared.cu"),
@@ -434,6 +434,9 @@ def run_ours(args, W: dict, dist: Dist):
         ("shared", pent.VARIANT_SPLIT): split, ("hyper", pent.VARIANT_SPLIT): split,
     }
     kname, kfile = kernel_names.get((kind, variant), ("?", "?"))
+    # non-cyclic partitioned solves of 256 to 2048 rows run the fixed-grid kernel
+    if kind == "shared" and variant == pent.VARIANT_SPLIT and not W["cyclic"] and 256 <= N <= 2048:
+        kname, kfile = "k_fg", "pent_fg.cu"
     if nsub > 1 and variant in (pent.VARIANT_SPLIT, pent.VARIANT_THREAD_DF):
         kname, kfile = "k_steps_df", "pent_steps_df.cu"
     # systems longer than one CTA holds (64 chunks of 32 rows; 32 when periodic)

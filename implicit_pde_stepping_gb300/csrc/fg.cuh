@@ -1,0 +1,104 @@
+// Fixed-grid double-float arithmetic for the partitioned solves.
+//
+// A value v is held as a pair (a, l) of floats with v = (a - B) + l, where the
+// bias B = 1.5 * 2^(k+23) puts every a in the binade [2^(k+23), 2^(k+24)), so
+// a is v rounded to the grid of multiples of 2^k and l carries the rest.  As
+// long as every partial sum stays below 2^(k+22) in magnitude (the plan derives
+// k from bounds on the solve's intermediate values, for a right-hand side
+// scaled so that max |f| lies in [1, 2)), rounding to the grid happens at one
+// fixed exponent, so
+//   t = fma(c, y, a)            is a + c y rounded to the grid,
+//   a - t                       is exact (same binade), and
+//   fma(c, y, a - t)            recovers the rounding error,
+// and a multiply-add costs six FP32 instructions instead of the twelve of a
+// TwoSum-based double-float one.  The error of each operation is about
+// 2^(k-24): about 2^-46 of the largest intermediate value of the solve.
+//
+// Conversions between fp64 and the pair use integer operations (the fp64 <->
+// fp32 conversion instructions share GB300's slow fp64 pipe), with a
+// per-system power-of-two scale folded into the exponent arithmetic: a system
+// is converted as f * 2^-s with s chosen so that its largest entry lies in
+// [1, 2), and its solution converted back as x * 2^s, both exactly.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace pent {
+namespace fg {
+
+// acc += c * y:  c = (ch, cl) a double-float coefficient, y = (yh, yl) with yh
+// on the grid (unbiased), acc = (a, l) biased.  In a recurrence y is the
+// previous row's result: its low word enters one FMA and one add before the
+// new low word, so a row costs two dependent FP32 latencies on either word.
+__device__ __forceinline__ void madd(float& a, float& l, float ch, float cl, float yh, float yl) {
+  const float t = __fmaf_rn(ch, yh, a);
+  const float e = __fmaf_rn(ch, yh, __fsub_rn(a, t));
+  float m = __fmaf_rn(cl, yh, l);
+  m = __fmaf_rn(ch, yl, m);
+  l = __fadd_rn(m, e);
+  a = t;
+}
+
+// acc += c * y for a response |c| < 2^-24: the product lands in the low word
+// alone (its rounding there is below 2^-48 of |y|).
+__device__ __forceinline__ void madd_low(float& l, float ch, float yh) { l = __fmaf_rn(ch, yh, l); }
+
+// acc = B + r * f:  r = (rh, rl), f = (fh, fl) a split double
+__device__ __forceinline__ void start(float& a, float& l, float B, float rh, float rl, float fh, float fl) {
+  a = __fmaf_rn(rh, fh, B);
+  const float e = __fmaf_rn(rh, fh, __fsub_rn(B, a));
+  l = __fmaf_rn(rl, fh, __fmaf_rn(rh, fl, e));
+}
+
+// Exponent field of the largest |v| seen: the high word's magnitude bits.
+__device__ __forceinline__ uint32_t mag_bits(double v) {
+  return (uint32_t)__double2hiint(v) & 0x7FFFFFFFu;
+}
+
+// Rebias constant for a system whose largest entry has the (biased) fp64
+// exponent field e: a value with exponent field ev converts to a float with
+// exponent field ev - e + 127, i.e. f * 2^-(e - 1023).
+__device__ __forceinline__ uint32_t in_offset(uint32_t e) { return (e - 127u) << 20; }
+
+// Split v * 2^-s into hi (its leading 24 significant bits, truncated) and lo
+// (the next 23 bits) as floats; `off` = in_offset(e) of the system.  Values
+// more than 2^126 below the system's largest entry become zero-like (|.| <
+// 2^-126 after scaling), which is below any solution error.
+__device__ __forceinline__ void split(double v, uint32_t off, float& h, float& lo) {
+  const uint32_t hw = (uint32_t)__double2hiint(v);
+  const uint32_t lw = (uint32_t)__double2loint(v);
+  const uint32_t sign = hw & 0x80000000u;
+  int32_t t = (int32_t)((hw & 0x7FFFFFFFu) - off);
+  t = max(t, 0);
+  const uint32_t hb = __funnelshift_l(lw, (uint32_t)t, 3) | sign;
+  uint32_t eb = hb & 0x7F800000u;
+  eb = max(eb, 0x0C000000u);            // e - 23 >= 1 for the low word's base
+  const uint32_t base = (eb - 0x0B800000u) | sign;
+  const uint32_t m = (lw >> 6) & 0x007FFFFFu;
+  lo = __fsub_rn(__uint_as_float(base | m), __uint_as_float(base));
+  h = __uint_as_float(hb);
+}
+
+// Output constant of a system with largest-entry exponent field e: a float
+// with exponent field fe becomes the double with exponent field fe - 127 + e.
+__device__ __forceinline__ uint32_t out_offset(uint32_t e) { return (e - 127u) << 20; }
+
+// Bits of the double x * 2^s for the float x (x normal; zero and subnormal x
+// map to doubles of magnitude 2^(s-126) or less, far below the solution).
+__device__ __forceinline__ double scaled_double(float x, uint32_t off) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t sh = (uint32_t)((int32_t)b >> 3);   // sign replicated into bits 31..28
+  // positive: sh + off; negative: the sign bit back in place of the replicated ones
+  const uint32_t hi = sh + off - (sh & 0x70000000u);
+  return __hiloint2double((int)hi, (int)(b << 29));
+}
+
+// (h + l) * 2^s rounded to fp64 (one fp64 add).
+__device__ __forceinline__ double join(float h, float l, uint32_t off) {
+  return __dadd_rn(scaled_double(h, off), scaled_double(l, off));
+}
+
+}  // namespace fg
+}  // namespace pent

@@ -2,12 +2,12 @@
 // Every declaration is documented in include/pent.h.
 #include <algorithm>
 #include <atomic>
+#include <initializer_list>
 #include <cmath>
 #include <map>
 #include <mutex>
 #include <tuple>
 #include <vector>
-#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -68,13 +68,18 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 constexpr int kMaxTwistedRows = 2560;
 
 // The kernel variant a plan uses for `batch` systems.  fp64 plans run in
-// double-float: the twisted kernel from about 160 systems per SM on (measured
-// crossover at N = 1024: the partitioned kernel wins at 16384 systems, the
-// twisted one at 32768), else the partitioned kernel (fine-grained, so small
-// batches still spread over the GPU); the native kernel when neither exists.
+// double-float.  Non-cyclic plans with fixed-grid tables take the fixed-grid
+// partitioned kernel at every batch size (at N = 1024, batch 65536: 0.329 ms
+// against 0.333 ms for the twisted kernel, with half its memory traffic, and
+// the full fp64 range through its per-system scaling).  Otherwise: the twisted
+// kernel from about 160 systems per SM on (measured crossover at N = 1024: the
+// partitioned kernel wins at 16384 systems, the twisted one at 32768), else the
+// partitioned kernel (fine-grained, so small batches still spread over the
+// GPU); the native kernel when neither exists.
 pent_variant resolve(const pent_plan_s& p, int batch) {
   if (p.variant != PENT_VARIANT_AUTO) return p.variant;
   if (p.dtype != PENT_F64) return PENT_VARIANT_THREAD;
+  if (p.fg_ok && p.fg_use && p.sp_T > 0) return PENT_VARIANT_SPLIT;
   const long long fill = 160LL * (p.num_sms > 0 ? p.num_sms : 1);
   if (p.twist_ok && batch % 2 == 0 && batch >= fill) return PENT_VARIANT_THREAD_DF;
   if (p.split_ok || p.split_big) return PENT_VARIANT_SPLIT;   // long systems: two-kernel form
@@ -96,19 +101,13 @@ bool variant_exists(const pent_plan_s& p, pent_variant v) {
   }
 }
 
-int env_int(const char* name, int dflt) {
-  const char* v = std::getenv(name);
-  if (!v || !*v) return dflt;
-  return std::atoi(v);
-}
-
 // Whether nsteps of scheme `kind` run in the persistent multi-step kernel:
-// two or more steps, the default or partitioned variant, a plan it supports;
-// PENT_STEPS=0 keeps one launch per step.
+// two or more steps, the default or partitioned variant, a plan it supports
+// (PENT_OPT_MULTI_STEP = 0 keeps one launch per step).
 bool use_steps(const pent_plan_s& p, int nsteps, int kind) {
   if (nsteps < 2) return false;
   if (p.variant != PENT_VARIANT_AUTO && p.variant != PENT_VARIANT_SPLIT) return false;
-  if (env_int("PENT_STEPS", 1) == 0) return false;
+  if (!p.steps_on) return false;
   return steps_supported(p, kind);
 }
 
@@ -179,6 +178,7 @@ cudaError_t solve_device(pent_plan_s& p, void* rhs, int batch, cudaStream_t st) 
     case PENT_VARIANT_THREAD: return shared_thread_f64(p, static_cast<double*>(rhs), batch, st);
     case PENT_VARIANT_THREAD_DF: return shared_twisted_df(p, static_cast<double*>(rhs), batch, st);
     case PENT_VARIANT_SPLIT:
+      if (p.fg_ok && p.fg_use && p.sp_T > 0) return shared_fg(p, static_cast<double*>(rhs), batch, st);
       return p.split_ok ? shared_split_df(p, static_cast<double*>(rhs), batch, st)
                         : shared_split_big(p, static_cast<double*>(rhs), batch, st);
     default: return cudaErrorInvalidValue;
@@ -257,6 +257,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   const size_t o_spchunkdf = off; off = round_up(off + (size_t)spP * kSpChunk * sizeof(float2), 256);
   const size_t o_spextra = off; off = round_up(off + kSpExtra * sizeof(double), 256);
   const size_t o_status = off; off = round_up(off + sizeof(int), 256);
+  const size_t o_kerr = off; off = round_up(off + sizeof(int), 256);
   const size_t o_twtab = off; off = round_up(off + (size_t)p->M * kTwK * sizeof(float4), 256);
   const size_t o_twist = off; off = round_up(off + kTwistCount * sizeof(double), 256);
   char* arena = nullptr;
@@ -283,6 +284,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   p->bands = d_bands;
   double* d_work = reinterpret_cast<double*>(arena + o_work);
   int* d_status = reinterpret_cast<int*>(arena + o_status);
+  p->kern_err = reinterpret_cast<int*>(arena + o_kerr);
 
   int status = 0;
   e = cudaMemset(arena, 0, off);
@@ -303,12 +305,6 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   }
   // twisted double-float tables (fp64 plans whose sweep fits the kernel)
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
-  p->df_spb = env_int("PENT_DF_SPB", 256);
-  p->df_spt = env_int("PENT_DF_SPT", 2);
-  p->df_ku = env_int("PENT_DF_KU", 4);
-  p->df_ctas = env_int("PENT_DF_CTAS", 0);
-  p->steps_sb = env_int("PENT_STEPS_SB", 0);
-  p->df_async = env_int("PENT_DF_ASYNC", 6);
   if (dtype == PENT_F64 && p->M >= 8 && p->M <= kMaxTwistedRows) {
     p->m = p->M / 2;
     int tstatus = 0;
@@ -342,40 +338,21 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
       }
       const bool tables = (sstatus == 0);
       p->split_ok = tables && fits;
-      // PENT_SPLIT_T=0 forces the exact serial chunk scan (testing)
-      if (p->split_ok && std::getenv("PENT_SPLIT_T") && env_int("PENT_SPLIT_T", -1) == 0) {
-        const double zero = 0.0;
-        e = cudaMemcpy(p->spextra + 18, &zero, sizeof(double), cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) {
-          cudaGetLastError();
-          pent_destroy(p);
-          return from_cuda(e);
-        }
-      }
-      // PENT_BORDER_ALL=1 applies the x_t correction in every chunk (testing)
-      if (tables && cyclic && env_int("PENT_BORDER_ALL", 0) == 1) {
-        const double all = (double)spP;
-        e = cudaMemcpy(p->spextra + 19, &all, sizeof(double), cudaMemcpyHostToDevice);
-        if (e != cudaSuccess) {
-          cudaGetLastError();
-          pent_destroy(p);
-          return from_cuda(e);
-        }
-      }
       if (tables) {
-        double Td = 0.0;
-        e = cudaMemcpy(&Td, p->spextra + 18, sizeof(double), cudaMemcpyDeviceToHost);
+        double ex[2] = {0.0, 0.0};
+        e = cudaMemcpy(ex, p->spextra + 18, sizeof(ex), cudaMemcpyDeviceToHost);
         if (e != cudaSuccess) {
           cudaGetLastError();
           pent_destroy(p);
           return from_cuda(e);
         }
-        p->sp_T = (int)Td;
+        p->sp_T = p->sp_T0 = (int)ex[0];
+        p->reach0 = (int)ex[1];
         // the two-kernel form needs the truncated chunk couplings
         p->split_big = !fits && p->sp_T > 0;
       }
       // the chunk tables as double-float pairs, for the kernels that run the chunk
-      // scan on the FP32 pipe (the two-kernel form, the partitioned one-step kernel
+      // scan on the FP32 pipe (the two-kernel form, the partitioned one-step kernels
       // and the multi-step kernel)
       if (p->split_big || p->split_ok) {
         e = split_big_prepare(*p, 0);
@@ -386,23 +363,36 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
           return from_cuda(e);
         }
       }
-      // PENT_CHEAP_TERMS=0 keeps every correction term in double-float (testing)
-      if (p->split_ok && p->sp_L % 8 == 0 && env_int("PENT_CHEAP_TERMS", 1) != 0) {
-        e = find_cheap_groups(*p, (int)Mpad);
+      // fixed-grid partitioned kernel: grid and correction groups
+      if (tables) {
+        e = fg_prepare(*p);
         if (e != cudaSuccess) {
           cudaGetLastError();
           pent_destroy(p);
           return from_cuda(e);
         }
       }
-      // PENT_CHUNK_DEDUP=0 keeps every chunk on its own tables (testing)
-      if (p->split_big && env_int("PENT_CHUNK_DEDUP", 1) != 0) {
+      // correction-term groups of the multi-step kernel
+      if (p->split_ok && p->sp_L % 8 == 0) {
+        e = find_cheap_groups(*p, (int)Mpad);
+        if (e != cudaSuccess) {
+          cudaGetLastError();
+          pent_destroy(p);
+          return from_cuda(e);
+        }
+        p->cheap_k0 = p->cheap_k;
+        p->cheap_m0 = p->cheap_m;
+      }
+      // long systems: chunks with equal tables share one copy
+      if (p->split_big) {
         e = find_duplicate_chunks(*p, (int)Mpad);
         if (e != cudaSuccess) {
           cudaGetLastError();
           pent_destroy(p);
           return from_cuda(e);
         }
+        p->dup_lo0 = p->dup_lo;
+        p->dup_hi0 = p->dup_hi;
       }
     }
   }
@@ -415,6 +405,88 @@ pent_status pent_set_variant(pent_plan p, pent_variant v) {
   if (!variant_exists(*p, v)) return PENT_ERR_UNSUPPORTED;
   p->variant = v;
   return PENT_OK;
+}
+
+pent_status pent_set_option(pent_plan p, pent_option opt, int v) {
+  if (!p) return PENT_ERR_INVALID_ARG;
+  auto in = [v](std::initializer_list<int> ok) {
+    for (int o : ok)
+      if (v == o) return true;
+    return false;
+  };
+  auto put = [&](int k, double val) {
+    cudaError_t e = cudaMemcpy(p->spextra + k, &val, sizeof(double), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) cudaGetLastError();
+    return from_cuda(e);
+  };
+  switch (opt) {
+    case PENT_OPT_FIXED_GRID:
+      if (!in({0, 1})) return PENT_ERR_INVALID_ARG;
+      p->fg_use = v;
+      return PENT_OK;
+    case PENT_OPT_SERIAL_CHUNK_SCAN: {
+      if (!in({0, 1})) return PENT_ERR_INVALID_ARG;
+      if (!p->split_ok) return p->split_big ? PENT_ERR_UNSUPPORTED : PENT_OK;
+      const int T = v ? 0 : p->sp_T0;
+      const pent_status st = put(18, (double)T);
+      if (st == PENT_OK) p->sp_T = T;
+      return st;
+    }
+    case PENT_OPT_BORDER_ALL_CHUNKS:
+      if (!in({0, 1})) return PENT_ERR_INVALID_ARG;
+      if (!p->cyclic || !(p->split_ok || p->split_big)) return PENT_OK;
+      return put(19, v ? (double)p->sp_P : (double)p->reach0);
+    case PENT_OPT_MULTI_STEP:
+      if (!in({0, 1})) return PENT_ERR_INVALID_ARG;
+      p->steps_on = v;
+      return PENT_OK;
+    case PENT_OPT_CHEAP_TERMS:
+      if (!in({0, 1})) return PENT_ERR_INVALID_ARG;
+      p->cheap_k = v ? p->cheap_k0 : 0;
+      p->cheap_m = v ? p->cheap_m0 : 1 << 20;
+      return PENT_OK;
+    case PENT_OPT_CHUNK_DEDUP:
+      if (!in({0, 1})) return PENT_ERR_INVALID_ARG;
+      p->dup_lo = v ? p->dup_lo0 : 0;
+      p->dup_hi = v ? p->dup_hi0 : 0;
+      return PENT_OK;
+    case PENT_OPT_TWISTED_RING:
+      if (!in({0, 4, 6, 8, 12})) return PENT_ERR_INVALID_ARG;
+      p->df_async = v;
+      return PENT_OK;
+    case PENT_OPT_STEPS_SYSTEMS:
+      if (!in({0, 8, 16})) return PENT_ERR_INVALID_ARG;
+      p->steps_sb = v;
+      return PENT_OK;
+    case PENT_OPT_TWISTED_SYSTEMS_PER_CTA:
+      if (!in({64, 128, 160, 256, 320})) return PENT_ERR_INVALID_ARG;
+      p->df_spb = v;
+      return PENT_OK;
+    case PENT_OPT_TWISTED_SYSTEMS_PER_THREAD:
+      if (!in({1, 2})) return PENT_ERR_INVALID_ARG;
+      p->df_spt = v;
+      return PENT_OK;
+    case PENT_OPT_TWISTED_PREFETCH_ROWS:
+      if (!in({4, 8})) return PENT_ERR_INVALID_ARG;
+      p->df_ku = v;
+      return PENT_OK;
+    case PENT_OPT_PERSISTENT_CTAS:
+      if (v < 0) return PENT_ERR_INVALID_ARG;
+      p->df_ctas = v;
+      return PENT_OK;
+  }
+  return PENT_ERR_INVALID_ARG;
+}
+
+pent_status pent_plan_error(pent_plan p) {
+  if (!p) return PENT_ERR_INVALID_ARG;
+  int v = 0;
+  const cudaError_t e = cudaMemcpy(&v, p->kern_err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return from_cuda(e);
+  }
+  return v ? PENT_ERR_CUDA : PENT_OK;
 }
 
 pent_variant pent_get_variant(pent_plan p, int batch) {

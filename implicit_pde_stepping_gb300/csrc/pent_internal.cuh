@@ -49,6 +49,9 @@ struct pent_plan_s {
   int df_ctas = 0;           // CTAs of the double-float kernels (0: two per SM)
   int steps_sb = 0;          // systems per CTA of the multi-step kernel (0: chosen by shape)
   int df_async = 6;          // cp.async ring depth of the twisted kernel (0: register ring)
+  int steps_on = 1;          // multi-step kernel for nsteps >= 2 where supported
+  // as found when the plan was built (pent_set_option switches back to them)
+  int sp_T0 = 0, reach0 = 0, cheap_k0 = 0, cheap_m0 = 1 << 20, dup_lo0 = 0, dup_hi0 = 0;
   // partitioned double-float variant (pent_factor_split.cu / pent_split_df.cu)
   int split_ok = 0;          // tables valid
   int sp_L = 0, sp_P = 0;    // chunk length, chunks per system (Mpad = sp_L * sp_P)
@@ -66,6 +69,15 @@ struct pent_plan_s {
   // multiply-add, at most about 3 * 2^-48 of the state per term)
   int cheap_k = 0, cheap_m = 1 << 20;
   size_t spsum_bytes = 0;
+  // fixed-grid partitioned kernel (pent_fg.cu): valid for this plan, grid bias,
+  // correction-term groups (see fg_prepare), bound on the intermediate values
+  int fg_ok = 0;
+  int fg_use = 1;            // test option: 0 keeps the TwoSum double-float kernel
+  float fg_bias = 0.f;
+  int fg_gm_full = 0, fg_gm_none = 0, fg_gk_none = 0, fg_gk_full = 0;
+  int fg_dup_lo = 0, fg_dup_hi = 0;   // chunks dup_lo < c <= dup_hi share chunk dup_lo's row tables
+  int* kern_err = nullptr;   // device word: 1 once a kernel gave up waiting for a tile copy
+  double fg_bound = 0.0;
   float4* sptab = nullptr;   // [Mpad][kSpK]
   double* spchunk = nullptr; // [sp_P][kSpChunk]
   float2* spchunk_df = nullptr;   // the same as double-float pairs (the scans on the FP32 pipe)
@@ -207,6 +219,12 @@ cudaError_t split_big_prepare(pent_plan_s& p, cudaStream_t st);
 size_t split_smem_bytes(int L, int P, int SB, int cyclic);
 cudaError_t ch_split_df(const pent_plan_s& p, double* X, int batch, double k2, cudaStream_t st);
 cudaError_t cn_split_df(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
+
+// pent_fg.cu: the partitioned solve in fixed-grid double-float (non-cyclic
+// plans with L = 32 chunks and a truncated chunk scan); fg_prepare decides at
+// plan time whether it applies and sets its grid
+cudaError_t fg_prepare(pent_plan_s& p);
+cudaError_t shared_fg(const pent_plan_s& p, double* X, int batch, cudaStream_t st);
 
 // pent_steps_df.cu: nsteps of a periodic scheme in one launch, state in registers.
 // kind 0 = hyperdiffusion, 1 = Cahn–Hilliard (k2 = dt/dx^2), 2 = Crank–Nicolson.

@@ -14,6 +14,7 @@
 // the backward sweep.  Loads are issued kUnroll rows at a time so that each
 // thread keeps several rows in flight.
 #include "pent_internal.cuh"
+#include "pent_native.cuh"
 
 namespace pent {
 namespace {
@@ -27,69 +28,7 @@ __global__ void __launch_bounds__(kThreads)
                     int M, int batch) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
-  T* col = X + s;
-  const size_t ld = (size_t)batch;
-  const T* R = coef + (size_t)kR * M;
-  const T* P = coef + (size_t)kP * M;
-  const T* Q = coef + (size_t)kQ * M;
-  const T* W0 = coef + (size_t)kW0 * M;
-  const T* W1 = coef + (size_t)kW1 * M;
-  const T* G = coef + (size_t)kGam * M;
-  const T* D = coef + (size_t)kDel * M;
-  const T* U0 = coef + (size_t)kU0 * M;
-  const T* U1 = coef + (size_t)kU1 * M;
-
-  T g1 = T(0), g2 = T(0), acc0 = T(0), acc1 = T(0);
-  for (int i0 = 0; i0 < M; i0 += kUnroll) {
-    T f[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = i0 + u;
-      f[u] = (i < M) ? col[(size_t)i * ld] : T(0);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = i0 + u;
-      if (i < M) {
-        const T g = R[i] * f[u] - P[i] * g2 - Q[i] * g1;
-        col[(size_t)i * ld] = g;
-        if (CYC) {
-          acc0 += W0[i] * g;
-          acc1 += W1[i] * g;
-        }
-        g2 = g1;
-        g1 = g;
-      }
-    }
-  }
-  T xt0 = T(0), xt1 = T(0);
-  if (CYC) {
-    const T t0 = col[(size_t)M * ld] - acc0;
-    const T t1 = col[(size_t)(M + 1) * ld] - acc1;
-    xt0 = tail[0] * t0 + tail[1] * t1;
-    xt1 = tail[2] * t0 + tail[3] * t1;
-    col[(size_t)M * ld] = xt0;
-    col[(size_t)(M + 1) * ld] = xt1;
-  }
-  T y1 = T(0), y2 = T(0);
-  for (int i0 = M - 1; i0 >= 0; i0 -= kUnroll) {
-    T gv[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = i0 - u;
-      gv[u] = (i >= 0) ? col[(size_t)i * ld] : T(0);
-    }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = i0 - u;
-      if (i >= 0) {
-        const T y = gv[u] - G[i] * y1 - D[i] * y2;
-        col[(size_t)i * ld] = CYC ? (y - U0[i] * xt0 - U1[i] * xt1) : y;
-        y2 = y1;
-        y1 = y;
-      }
-    }
-  }
+  native_shared_column<T, CYC, kUnroll>(coef, tail, X + s, M, (size_t)batch);
 }
 
 template <typename T>

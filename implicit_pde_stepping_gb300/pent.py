@@ -23,6 +23,11 @@ F64, F32 = 0, 1
 VARIANT_AUTO, VARIANT_THREAD, VARIANT_THREAD_DF, VARIANT_SPLIT = range(4)
 VARIANTS = {"auto": VARIANT_AUTO, "thread": VARIANT_THREAD, "thread_df": VARIANT_THREAD_DF,
             "split": VARIANT_SPLIT}
+# plan options (pent_set_option; tuning and testing hooks, see include/pent.h)
+OPTIONS = {"fixed_grid": 1, "serial_chunk_scan": 2, "border_all_chunks": 3, "multi_step": 4,
+           "cheap_terms": 5, "chunk_dedup": 6, "twisted_ring": 7, "steps_systems": 8,
+           "twisted_systems_per_cta": 9, "twisted_systems_per_thread": 10,
+           "twisted_prefetch_rows": 11, "persistent_ctas": 12}
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +67,8 @@ def lib():
             L.tri_factor_solve.argtypes = [vp] * 4 + [i, i, i, i, i, vp, sz, vp, vp]
             L.pent_set_variant.argtypes = [vp, i]
             L.pent_get_variant.argtypes = [vp, i]
+            L.pent_set_option.argtypes = [vp, i, i]
+            L.pent_plan_error.argtypes = [vp]
             L.pent_destroy.argtypes = [vp]
             L.pent_destroy.restype = None
             L.pent_sync.argtypes = [vp]
@@ -72,7 +79,7 @@ def lib():
             for fn in ("pent_factor", "pent_solve", "pent_solve_host", "pent_factor_solve",
                        "pent_factor_solve_ex",
                        "hyperdiffusion_step",
-                       "ch_step", "cn_step", "tri_factor_solve", "pent_set_variant",
+                       "ch_step", "cn_step", "tri_factor_solve", "pent_set_variant", "pent_set_option", "pent_plan_error",
                        "pent_get_variant", "pent_sync"):
                 getattr(L, fn).restype = i
             _lib = L
@@ -147,6 +154,15 @@ class Plan:
     def set_variant(self, variant):
         code = VARIANTS[variant] if isinstance(variant, str) else int(variant)
         _check(lib().pent_set_variant(self.handle, code), "pent_set_variant")
+
+    def set_option(self, option, value: int):
+        """pent_set_option: a tuning / testing hook (names in OPTIONS)."""
+        code = OPTIONS[option] if isinstance(option, str) else int(option)
+        _check(lib().pent_set_option(self.handle, code, int(value)), "pent_set_option")
+
+    def error(self) -> int:
+        """pent_plan_error: PENT_ERR_CUDA if a kernel of this plan gave up waiting for a copy."""
+        return int(lib().pent_plan_error(self.handle))
 
     def variant(self, batch=None) -> int:
         return int(lib().pent_get_variant(self.handle, int(batch or self.batch)))

@@ -306,6 +306,69 @@ pent_status pent_set_variant(pent_plan plan, pent_variant variant);
 /* The variant the next call on this plan with `batch` systems would use. */
 pent_variant pent_get_variant(pent_plan plan, int batch);
 
+/*
+ * pent_set_option — tuning and testing hooks of a plan.  The defaults are the
+ * measured best; the other values exist so that tests can run the code paths
+ * against one another (every setting computes the same solve to within the
+ * library's tolerance).  Nothing here has a counterpart on the pages.  The
+ * call may rewrite the plan's device tables synchronously: do not call it
+ * while work that uses the plan is queued.
+ *   PENT_OPT_FIXED_GRID            1 (default): partitioned fp64 solves use the
+ *                                  fixed-grid kernel where the plan qualifies;
+ *                                  0: the TwoSum double-float kernel.
+ *   PENT_OPT_SERIAL_CHUNK_SCAN     1: exact serial chunk scan in the partitioned
+ *                                  kernels; 0 (default): the plan's truncated
+ *                                  parallel scan.  Plans of systems too long
+ *                                  for one CTA: PENT_ERR_UNSUPPORTED.
+ *   PENT_OPT_BORDER_ALL_CHUNKS     1: periodic border correction in every chunk;
+ *                                  0 (default): only where it exceeds 2^-60.
+ *   PENT_OPT_MULTI_STEP            1 (default): nsteps >= 2 in one launch where
+ *                                  supported; 0: one launch per time step.
+ *   PENT_OPT_CHEAP_TERMS           1 (default): the multi-step kernel adds
+ *                                  correction terms below 2^-24 to the low word
+ *                                  alone; 0: every term in double-float.
+ *   PENT_OPT_CHUNK_DEDUP           1 (default): long systems read one copy of
+ *                                  bitwise-equal chunk tables; 0: each its own.
+ *   PENT_OPT_TWISTED_RING          cp.async ring depth of the twisted kernel:
+ *                                  4, 6 (default), 8 or 12; 0: register ring.
+ *   PENT_OPT_STEPS_SYSTEMS         systems per CTA of the multi-step kernel:
+ *                                  0 (default: by shape), 8 or 16.
+ *   PENT_OPT_TWISTED_SYSTEMS_PER_CTA    register-ring twisted kernel: 64, 128,
+ *                                  160, 256 (default) or 320.
+ *   PENT_OPT_TWISTED_SYSTEMS_PER_THREAD 1 or 2 (default).
+ *   PENT_OPT_TWISTED_PREFETCH_ROWS 4 (default) or 8.
+ *   PENT_OPT_PERSISTENT_CTAS       CTAs of the persistent double-float kernels;
+ *                                  0 (default): as many as fit on every SM.
+ * Errors: PENT_ERR_INVALID_ARG for a null plan, an unknown option or a value
+ * outside its list; PENT_ERR_CUDA if updating the device tables fails.
+ */
+typedef enum {
+  PENT_OPT_FIXED_GRID = 1,
+  PENT_OPT_SERIAL_CHUNK_SCAN = 2,
+  PENT_OPT_BORDER_ALL_CHUNKS = 3,
+  PENT_OPT_MULTI_STEP = 4,
+  PENT_OPT_CHEAP_TERMS = 5,
+  PENT_OPT_CHUNK_DEDUP = 6,
+  PENT_OPT_TWISTED_RING = 7,
+  PENT_OPT_STEPS_SYSTEMS = 8,
+  PENT_OPT_TWISTED_SYSTEMS_PER_CTA = 9,
+  PENT_OPT_TWISTED_SYSTEMS_PER_THREAD = 10,
+  PENT_OPT_TWISTED_PREFETCH_ROWS = 11,
+  PENT_OPT_PERSISTENT_CTAS = 12
+} pent_option;
+pent_status pent_set_option(pent_plan plan, pent_option option, int value);
+
+/*
+ * pent_plan_error — whether a kernel of this plan gave up: PENT_ERR_CUDA if a
+ * kernel stopped because a bulk copy into shared memory did not complete
+ * within its time limit (2 s) or could not be issued safely, PENT_OK
+ * otherwise.  Such a kernel leaves the systems it had not finished unchanged
+ * or partly solved.  Reads a device word of the plan synchronously (ordered
+ * after the work already queued on the legacy default stream).  Library
+ * service; nothing on the pages corresponds to it.
+ */
+pent_status pent_plan_error(pent_plan plan);
+
 /* Free a plan (NULL is allowed).  Waits for nothing: the caller must not free
  * a plan while work using it is still queued. */
 void pent_destroy(pent_plan plan);

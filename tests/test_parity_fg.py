@@ -1,0 +1,148 @@
+"""GPU parity: the fixed-grid partitioned shared-matrix solve (pent_fg.cu) against the
+CPU oracle and against the TwoSum double-float partitioned kernel, and the fp64 range of
+the shared solve: systems scaled by powers of ten from 1e-310 to 1e305, zero systems,
+non-finite entries and batches that mix all of them.
+
+The fixed-grid kernel scales every system by the power of two that puts its largest
+|f| in [1, 2) before it computes, so its accuracy does not depend on the magnitude of
+the data; systems whose largest entry is zero, subnormal, non-finite or beyond the
+kernel's exponent window are solved by a native fp64 sweep instead."""
+import numpy as np
+import pytest
+
+import oracle
+from implicit_pde_stepping_gb300 import inputs, pent
+from tests.gpu_util import TOL_F64, dev, host, max_rel_err, random_dd_bands
+
+pytestmark = pytest.mark.gpu
+
+
+def solve(bands, F, variant="split", cyclic=False, opts=None):
+    plan = pent.pent_factor(bands, F.shape[1], cyclic=cyclic)
+    if variant != "auto":
+        plan.set_variant(variant)
+    for k, v in (opts or {}).items():
+        plan.set_option(k, v)
+    X = dev(F)
+    pent.pent_solve(plan, X)
+    pent.pent_sync()
+    out = host(X)
+    assert plan.error() == pent.OK
+    plan.close()
+    return out
+
+
+@pytest.mark.parametrize("N", [256, 300, 777, 1024, 1500, 2048])
+@pytest.mark.parametrize("batch", [1, 7, 100, 1029])
+@pytest.mark.parametrize("sigma", [0.25, 1.0, 10.48576])
+def test_fixed_grid_hyper_bands(N, batch, sigma):
+    """Constant-band hyperdiffusion matrices, ragged batches (partial system groups) and
+    chunk counts from 8 to 64, against the oracle."""
+    bands = inputs.hyper_bands(N, sigma)
+    F = inputs.rhs_uniform(N, batch, seed=N + batch)
+    ref = oracle.batch_shared(bands, F)
+    assert max_rel_err(solve(bands, F), ref) < TOL_F64
+
+
+@pytest.mark.parametrize("N", [256, 513, 1024])
+@pytest.mark.parametrize("seed", [1, 2])
+def test_fixed_grid_random_bands(N, seed):
+    """Random diagonally dominant bands (every row's coefficients different)."""
+    rng = np.random.default_rng(seed * 1000 + N)
+    bands = random_dd_bands(N, rng)
+    F = rng.uniform(-1, 1, (N, 333))
+    ref = oracle.batch_shared(bands, F)
+    assert max_rel_err(solve(bands, F), ref) < TOL_F64
+
+
+def test_fixed_grid_matches_twosum_kernel():
+    """The same solve by the fixed-grid and by the TwoSum double-float partitioned
+    kernels: they agree far inside the tolerance."""
+    N, batch = 1024, 2000
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, batch, seed=5)
+    a = solve(bands, F)
+    b = solve(bands, F, opts={"fixed_grid": 0})
+    assert max_rel_err(a, b) < 1e-11
+    assert max_rel_err(a, oracle.batch_shared(bands, F)) < TOL_F64
+
+
+def test_fixed_grid_structured_rhs():
+    """Right-hand sides that stress the grid bound: constant, alternating, a single
+    spike per system, smooth modes, and the sign pattern of the forward operator's
+    largest row of |L^-1 R| (the f that maximises |g|)."""
+    N = 1024
+    bands = inputs.hyper_bands(N, 1.0)
+    cols = [np.ones(N), (-1.0) ** np.arange(N), np.cos(2 * np.pi * 3 * np.arange(N) / N)]
+    spike = np.zeros(N)
+    spike[500] = 1.0
+    cols.append(spike)
+    # sign pattern maximising g at row 600: the signs of row 600 of the forward
+    # operator L^-1 R (g_i = (f_i - beta_i g_{i-1} - eps_i g_{i-2}) / alpha_i, the
+    # oracle's factors), applied to every unit vector at once
+    al, be, _, _, ep = oracle.factor(*bands)
+    G = np.zeros((N, N))
+    for i in range(N):
+        G[i] = np.eye(N)[i]
+        if i >= 1:
+            G[i] -= be[i] * G[i - 1]
+        if i >= 2:
+            G[i] -= ep[i] * G[i - 2]
+        G[i] /= al[i]
+    cols.append(np.where(G[600] < 0, -1.0, 1.0))
+    F = np.stack(cols, axis=1)
+    ref = oracle.batch_shared(bands, F)
+    assert max_rel_err(solve(bands, F), ref) < TOL_F64
+
+
+@pytest.mark.parametrize("variant", ["split", "auto"])
+@pytest.mark.parametrize("scale", [1e-310, 1e-300, 1e-40, 1e-35, 1e40, 1e300, 1e305])
+def test_shared_solve_fp64_range(variant, scale):
+    """Right-hand sides scaled across the fp64 range match the oracle (which solves in
+    fp64) to the fp64 tolerance; 1e-310 is subnormal, 1e-300 and 1e305 lie outside the
+    scaled kernel's exponent window (native fp64 path)."""
+    N, batch = 1024, 640
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, batch, seed=17) * scale
+    ref = oracle.batch_shared(bands, F)
+    X = solve(bands, F, variant)
+    assert np.all(np.isfinite(X))
+    assert max_rel_err(X, ref) < TOL_F64
+
+
+@pytest.mark.parametrize("variant", ["split", "auto"])
+def test_shared_solve_mixed_batch(variant):
+    """One batch mixing a huge system, a tiny one, a zero one, a subnormal one, systems
+    whose entries span 600 orders of magnitude and normal systems: every system matches
+    the oracle and the zero system gives exact zeros."""
+    N, batch = 1024, 512
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, batch, seed=23)
+    F[:, 3] *= 1e300
+    F[:, 4] *= 1e-300
+    F[:, 5] = 0.0
+    F[:, 6] *= 1e-310
+    F[:, 7] *= np.logspace(-300, 300, N)
+    F[:, 8] *= 1e-35
+    F[:, 9] *= 1e40
+    F[:100, 10] = 0.0
+    X = solve(bands, F, variant)
+    assert np.all(X[:, 5] == 0.0)
+    ref = oracle.batch_shared(bands, F)
+    assert max_rel_err(X, ref) < TOL_F64
+
+
+def test_shared_solve_non_finite_entries():
+    """A system with an inf or NaN entry gives non-finite output in that system only
+    (as fp64 arithmetic does); its neighbours are unaffected."""
+    N, batch = 512, 64
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, batch, seed=29)
+    F[100, 2] = np.inf
+    F[200, 3] = np.nan
+    X = solve(bands, F)
+    assert not np.all(np.isfinite(X[:, 2]))
+    assert not np.all(np.isfinite(X[:, 3]))
+    keep = [s for s in range(batch) if s not in (2, 3)]
+    ref = oracle.batch_shared(bands, F[:, keep])
+    assert max_rel_err(X[:, keep], ref) < TOL_F64

@@ -68,7 +68,7 @@ def test_long_plan_repeated_solves_and_batch_growth():
 
 
 @pytest.mark.parametrize("cyclic", [False, True])
-def test_shared_chunk_tables_change_no_bit(cyclic, monkeypatch):
+def test_shared_chunk_tables_change_no_bit(cyclic):
     """Interior chunks of a constant-band matrix read one chunk's tables (bitwise equal
     ones, found when the plan is built); the solution is bit-for-bit that of a plan whose
     chunks all read their own tables."""
@@ -76,9 +76,9 @@ def test_shared_chunk_tables_change_no_bit(cyclic, monkeypatch):
     bands = inputs.hyper_bands(N, 1.0)
     F = inputs.rhs_uniform(N, batch, seed=13)
     out = []
-    for dedup in ("1", "0"):
-        monkeypatch.setenv("PENT_CHUNK_DEDUP", dedup)
+    for dedup in (1, 0):
         plan = pent.pent_factor(bands, batch, cyclic=cyclic)
+        plan.set_option("chunk_dedup", dedup)
         X = dev(F)
         pent.pent_solve(plan, X)
         pent.pent_sync()

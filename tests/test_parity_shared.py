@@ -11,10 +11,12 @@ pytestmark = pytest.mark.gpu
 VARIANTS_F64 = ["thread", "thread_df", "split"]
 
 
-def solve_gpu(bands, F, cyclic, variant="auto", dtype="f64"):
+def solve_gpu(bands, F, cyclic, variant="auto", dtype="f64", opts=None):
     import torch
     tdt = torch.float64 if dtype == "f64" else torch.float32
     plan = pent.pent_factor(bands, F.shape[1], cyclic=cyclic, dtype=dtype)
+    for k, v in (opts or {}).items():
+        plan.set_option(k, v)
     if variant != "auto":
         try:
             plan.set_variant(variant)
@@ -119,7 +121,7 @@ def test_df_zero_and_spike_systems(cyclic):
 
 @pytest.mark.parametrize("cyclic", [False, True])
 @pytest.mark.parametrize("N,sigma", [(1024, 1e4), (300, 50.0), (1024, 1.0)])
-def test_split_serial_and_parallel_scans(cyclic, N, sigma, monkeypatch):
+def test_split_serial_and_parallel_scans(cyclic, N, sigma):
     """The partitioned kernel with its parallel (truncated-coupling) scan and with the
     exact serial scan forced; sigma = 1e4 couples chunks too strongly for truncation,
     so the plan itself falls back to the serial scan there."""
@@ -127,8 +129,8 @@ def test_split_serial_and_parallel_scans(cyclic, N, sigma, monkeypatch):
     F = inputs.rhs_uniform(N, 96, seed=N)
     ref = oracle.batch_shared(bands, F, cyclic=cyclic)
     assert max_rel_err(solve_gpu(bands, F, cyclic, "split"), ref) < TOL_F64
-    monkeypatch.setenv("PENT_SPLIT_T", "0")
-    assert max_rel_err(solve_gpu(bands, F, cyclic, "split"), ref) < TOL_F64
+    assert max_rel_err(solve_gpu(bands, F, cyclic, "split", opts={"serial_chunk_scan": 1}),
+                       ref) < TOL_F64
 
 
 def test_zero_pivot_is_reported():
@@ -185,7 +187,7 @@ def test_batch_smaller_than_plan_and_stream_order():
 
 @pytest.mark.parametrize("sigma", [0.05, 1.0, 50.0])
 @pytest.mark.parametrize("N", [64, 1000, 2051])
-def test_cyclic_twisted_border_reach(sigma, N, monkeypatch):
+def test_cyclic_twisted_border_reach(sigma, N):
     """The twisted kernel applies the periodic-border terms only in the rows near the
     two ends where they exceed 2^-60 (few rows for small sigma, all rows for large):
     parity with the oracle on random right-hand sides."""
@@ -203,15 +205,15 @@ def test_cyclic_twisted_border_reach(sigma, N, monkeypatch):
 
 @pytest.mark.parametrize("depth", ["0", "4", "8", "12"])
 @pytest.mark.parametrize("cyclic", [False, True])
-def test_twisted_prefetch_depths(depth, cyclic, monkeypatch):
+def test_twisted_prefetch_depths(depth, cyclic):
     """The twisted kernel's cp.async ring depths other than the default 6, and the
-    register-ring kernel (PENT_DF_ASYNC=0), against the oracle."""
-    monkeypatch.setenv("PENT_DF_ASYNC", depth)
+    register-ring kernel (ring depth 0), against the oracle."""
     N, batch = 700, 1024
     bands = inputs.hyper_bands(N, 0.9)
     F = inputs.rhs_uniform(N, batch, seed=int(depth) + 1)
     ref = oracle.batch_shared(bands, F, cyclic=cyclic)
-    assert max_rel_err(solve_gpu(bands, F, cyclic, "thread_df"), ref) < TOL_F64
+    assert max_rel_err(solve_gpu(bands, F, cyclic, "thread_df", opts={"twisted_ring": int(depth)}),
+                       ref) < TOL_F64
 
 
 @pytest.mark.parametrize("variant", VARIANTS_F64)

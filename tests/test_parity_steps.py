@@ -1,8 +1,6 @@
 """GPU parity: the persistent multi-step kernel (nsteps >= 2 of hyperdiffusion,
 Cahn–Hilliard and Crank–Nicolson in one launch, state kept in registers) against
 the oracle, against one launch per step, and its launch count."""
-import os
-
 import numpy as np
 import pytest
 
@@ -16,29 +14,23 @@ SIGMA = {"hyper": 0.7, "ch": 3.0, "cn": 0.7}
 K2 = 0.2
 
 
-def run(kind, N, batch, steps, C0, per_step=False, sigma=None):
+def run(kind, N, batch, steps, C0, per_step=False, sigma=None, opts=None):
     sigma = SIGMA[kind] if sigma is None else sigma
     plan = pent.pent_factor(inputs.hyper_bands(N, sigma), batch, cyclic=True)
-    C = dev(C0)
-    old = os.environ.get("PENT_STEPS")
     if per_step:
-        os.environ["PENT_STEPS"] = "0"
-    try:
-        l0 = pent.launch_count()
-        if kind == "hyper":
-            pent.hyperdiffusion_step(plan, C, steps)
-        elif kind == "ch":
-            pent.ch_step(plan, C, K2, steps)
-        else:
-            pent.cn_step(plan, C, steps)
-        pent.pent_sync()
-        launches = pent.launch_count() - l0
-    finally:
-        if per_step:
-            if old is None:
-                del os.environ["PENT_STEPS"]
-            else:
-                os.environ["PENT_STEPS"] = old
+        plan.set_option("multi_step", 0)
+    for k, v in (opts or {}).items():
+        plan.set_option(k, v)
+    C = dev(C0)
+    l0 = pent.launch_count()
+    if kind == "hyper":
+        pent.hyperdiffusion_step(plan, C, steps)
+    elif kind == "ch":
+        pent.ch_step(plan, C, K2, steps)
+    else:
+        pent.cn_step(plan, C, steps)
+    pent.pent_sync()
+    launches = pent.launch_count() - l0
     out = host(C)
     plan.close()
     return out, launches
@@ -123,60 +115,56 @@ def test_multistep_hyperdiffusion_closed_form():
     plan.close()
 
 
-def test_serial_scan_plans_step_one_launch_at_a_time(monkeypatch):
-    """With the exact serial chunk scan (PENT_SPLIT_T=0) the multi-step kernel is
-    not used: one launch per step, same results."""
-    monkeypatch.setenv("PENT_SPLIT_T", "0")
+def test_serial_scan_plans_step_one_launch_at_a_time():
+    """With the exact serial chunk scan forced (option serial_chunk_scan) the
+    multi-step kernel is not used: one launch per step, same results."""
     N, batch, steps = 333, 40, 4
     C0 = inputs.rhs_uniform(N, batch, seed=2)
-    out, launches = run("hyper", N, batch, steps, C0)
+    out, launches = run("hyper", N, batch, steps, C0, opts={"serial_chunk_scan": 1})
     assert launches == steps
     assert max_rel_err(out, ref("hyper", C0, steps)) < TOL_F64
 
 
 @pytest.mark.parametrize("kind", ["ch", "cn", "hyper"])
 @pytest.mark.parametrize("steps", [1, 9])
-def test_border_correction_skipped_only_where_negligible(kind, steps, monkeypatch):
+def test_border_correction_skipped_only_where_negligible(kind, steps):
     """Chunks far from the periodic border skip the x_t correction (its E^{-1} G
     entries are below 2^-60 there); the results match plans that apply it in
-    every chunk (PENT_BORDER_ALL=1) and the oracle."""
+    every chunk (option border_all_chunks) and the oracle."""
     N, batch = 1024, 64
     C0 = initial(kind, N, batch, seed=21)
     a, _ = run(kind, N, batch, steps, C0)
-    monkeypatch.setenv("PENT_BORDER_ALL", "1")
-    b, _ = run(kind, N, batch, steps, C0)
+    b, _ = run(kind, N, batch, steps, C0, opts={"border_all_chunks": 1})
     assert max_rel_err(a, b) < 1e-13
     assert max_rel_err(a, ref(kind, C0, steps)) < TOL_F64
 
 
 @pytest.mark.parametrize("kind", ["hyper", "ch", "cn"])
 @pytest.mark.parametrize("sb", ["8", "16"])
-def test_multistep_systems_per_cta(kind, sb, monkeypatch):
-    """Both CTA shapes of the multi-step kernel (PENT_STEPS_SB), whatever the default
-    for the shape: 8 or 16 systems per CTA give the oracle's result."""
-    monkeypatch.setenv("PENT_STEPS_SB", sb)
+def test_multistep_systems_per_cta(kind, sb):
+    """Both CTA shapes of the multi-step kernel (option steps_systems), whatever the
+    default for the shape: 8 or 16 systems per CTA give the oracle's result."""
     N, batch, steps = 512, 4100, 4
     C0 = initial(kind, N, batch, seed=31)
-    out, launches = run(kind, N, batch, steps, C0)
+    out, launches = run(kind, N, batch, steps, C0, opts={"steps_systems": int(sb)})
     assert launches == 1
     idx = inputs.sample_systems(batch, 200)
     assert max_rel_err(out[:, idx], ref(kind, C0[:, idx], steps)) < TOL_F64
 
 
 @pytest.mark.parametrize("kind,sigma", [("hyper", 0.5), ("cn", 0.25), ("hyper", 0.05), ("ch", 3.0)])
-def test_multistep_low_word_correction_terms(kind, sigma, monkeypatch):
+def test_multistep_low_word_correction_terms(kind, sigma):
     """Where a chunk's responses to its neighbours' states are below 2^-24 in every
     chunk (the first and last 8-row groups when the couplings decay fast), the
     multi-step kernel adds those terms to the low word alone.  Against every term in
-    double-float (PENT_CHEAP_TERMS=0) after 50 steps: the same state to 2^-40 of
+    double-float (option cheap_terms = 0) after 50 steps: the same state to 2^-40 of
     max |C|, and both match the oracle."""
     N, batch, steps = 512, 520, 50
     C0 = initial(kind, N, batch, seed=41)
     r = ref(kind, C0, steps, sigma)
     out = []
-    for cheap in ("1", "0"):
-        monkeypatch.setenv("PENT_CHEAP_TERMS", cheap)
-        o, launches = run(kind, N, batch, steps, C0, sigma=sigma)
+    for cheap in (1, 0):
+        o, launches = run(kind, N, batch, steps, C0, sigma=sigma, opts={"cheap_terms": cheap})
         assert launches == 1
         assert max_rel_err(o, r) < TOL_F64
         out.append(o)
