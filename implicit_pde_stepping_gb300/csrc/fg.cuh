@@ -100,5 +100,21 @@ __device__ __forceinline__ double join(float h, float l, uint32_t off) {
   return __dadd_rn(scaled_double(h, off), scaled_double(l, off));
 }
 
+// Exponent window (fp64 biased exponent field of a system's largest entry) of
+// the scaled double-float paths; Cahn–Hilliard also needs 2^(2s) (the factor of
+// its cubic) in float range at the top.  Systems outside go to native fp64.
+constexpr uint32_t kEMin = 1023 - 860, kEMax = 1023 + 1000, kEMaxCH = 1023 + 50;
+
+// 2^(2s) as a float for the system exponent field e (s = e - 1023); zero when
+// the cubic is below 2^-126 of the state and cannot matter
+__device__ __forceinline__ float cubic_scale(uint32_t e) {
+  const int t = 2 * ((int)e - 1023) + 127;
+  return t >= 1 ? __uint_as_float((uint32_t)t << 23) : 0.f;
+}
+
+// 2^-s and 2^s as doubles (exact) for the system exponent field e
+__device__ __forceinline__ double pow2_neg(uint32_t e) { return __hiloint2double((int)((2046u - e) << 20), 0); }
+__device__ __forceinline__ double pow2_pos(uint32_t e) { return __hiloint2double((int)(e << 20), 0); }
+
 }  // namespace fg
 }  // namespace pent

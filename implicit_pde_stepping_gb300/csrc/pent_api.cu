@@ -68,22 +68,21 @@ size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 constexpr int kMaxTwistedRows = 2560;
 
 // The kernel variant a plan uses for `batch` systems.  fp64 plans run in
-// double-float.  Non-cyclic plans with fixed-grid tables take the fixed-grid
-// partitioned kernel at every batch size (at N = 1024, batch 65536: 0.329 ms
-// against 0.333 ms for the twisted kernel, with half its memory traffic, and
-// the full fp64 range through its per-system scaling).  Otherwise: the twisted
-// kernel from about 160 systems per SM on (measured crossover at N = 1024: the
-// partitioned kernel wins at 16384 systems, the twisted one at 32768), else the
-// partitioned kernel (fine-grained, so small batches still spread over the
-// GPU); the native kernel when neither exists.
+// double-float, and AUTO only picks kernels that keep the whole fp64 range
+// (each system scaled by a power of two before it is converted): the
+// fixed-grid partitioned kernel for non-cyclic plans that have its tables (at
+// N = 1024, batch 65536: 0.329 ms, against 0.333 ms for the twisted kernel
+// with twice the memory traffic), else the TwoSum partitioned kernels (one CTA
+// per group of systems, or the multi-kernel form for long systems), else the
+// native kernel.  The twisted kernel (PENT_VARIANT_THREAD_DF) runs only on
+// request: it writes g over f as it goes and cannot rescale a system it has
+// already started.
 pent_variant resolve(const pent_plan_s& p, int batch) {
+  (void)batch;
   if (p.variant != PENT_VARIANT_AUTO) return p.variant;
   if (p.dtype != PENT_F64) return PENT_VARIANT_THREAD;
   if (p.fg_ok && p.fg_use && p.sp_T > 0) return PENT_VARIANT_SPLIT;
-  const long long fill = 160LL * (p.num_sms > 0 ? p.num_sms : 1);
-  if (p.twist_ok && batch % 2 == 0 && batch >= fill) return PENT_VARIANT_THREAD_DF;
-  if (p.split_ok || p.split_big) return PENT_VARIANT_SPLIT;   // long systems: two-kernel form
-  if (p.twist_ok) return PENT_VARIANT_THREAD_DF;
+  if (p.split_ok || p.split_big) return PENT_VARIANT_SPLIT;
   return PENT_VARIANT_THREAD;
 }
 

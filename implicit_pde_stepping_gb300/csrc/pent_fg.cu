@@ -46,9 +46,8 @@ namespace {
 
 using df::D2;
 
-// exponent window (fp64 biased exponent field of a system's largest |f|) of
-// the scaled fixed-grid path; systems outside it are solved natively
-constexpr uint32_t kEMin = 1023 - 860, kEMax = 1023 + 1000;
+using fg::kEMin;
+using fg::kEMax;
 
 struct FgArgs {
   const float4* rowtab;     // [Mpad][kSpK] double-float row tables
@@ -290,7 +289,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     }
     // systems outside the scaled path: one thread solves the column in fp64
     // (its f is untouched: nothing of this system has been stored)
-    if (native && c == 0) native_shared_column<double, false>(g.coef64, g.tail64, g.X + s, M, (size_t)ld);
+    if (native && c == 0) native_solve_col(NativeTabs{g.coef64, g.tail64, nullptr}, g.X + s, M, (size_t)ld, 0);
   }
 }
 

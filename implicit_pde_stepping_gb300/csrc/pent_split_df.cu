@@ -27,6 +27,14 @@
 //     f = C and stores 2y - C, re-reading its own C_i (still in L2) at the
 //     store.
 //
+// Range: each system is scaled by the power of two that puts its largest
+// entry in [1, 2) (an exact operation folded into the integer fp64 <-> pair
+// conversions; the Cahn–Hilliard cubic then carries the factor 2^(2s)), so the
+// pairs' float exponent range never limits the fp64 contract.  Systems whose
+// largest entry is zero, subnormal, non-finite or outside the window of the
+// scaled path are solved natively in fp64 by one thread, from their untouched
+// input (every store of a block comes after its last load).
+//
 // Warp layout: 8 consecutive systems x 4 chunks per warp, so every load or
 // store instruction moves four 64-byte runs of one row each (whole sectors).
 // The per-row tables sit in shared memory with one float4 of padding per
@@ -34,7 +42,9 @@
 // SB systems x P chunks; the grid is persistent.
 #include "cp_async.cuh"
 #include "df64.cuh"
+#include "fg.cuh"
 #include "pent_internal.cuh"
+#include "pent_native.cuh"
 
 namespace pent {
 namespace {
@@ -53,8 +63,19 @@ __device__ __forceinline__ void mv2d(const float2* A, D2 x0, D2 x1, D2& y0, D2& 
   y1 = df::sum3(y1, D2{A[2].x, A[2].y}, x0, D2{A[3].x, A[3].y}, x1);
 }
 
-// u = c^3 - c (Cahn–Hilliard chemical potential without the gradient term)
-__device__ __forceinline__ D2 cubic_minus(D2 c) { return df::add(df::mul(df::mul(c, c), c), df::neg(c)); }
+// u = q c^3 - c (Cahn–Hilliard chemical potential without the gradient term) for
+// c = C 2^-s: the scaled u = (C^3 - C) 2^-s needs q = 2^(2s), an exact power of two
+__device__ __forceinline__ D2 cubic_minus(D2 c, float q) {
+  const D2 c3 = df::mul(df::mul(c, c), c);
+  return df::add(D2{c3.h * q, c3.l * q}, df::neg(c));
+}
+
+using fg::kEMin;
+using fg::kEMax;
+using fg::kEMaxCH;
+using fg::cubic_scale;
+using fg::pow2_neg;
+using fg::pow2_pos;
 
 // rhs_i = C_i + k2 (u_{i-1} - 2 u_i + u_{i+1})   (eq. (2), D2 = [1, -2, 1]/dx^2, k2 = dt/dx^2)
 __device__ __forceinline__ D2 ch_rhs(D2 c, D2 um, D2 u0, D2 up, D2 k2) {
@@ -71,7 +92,7 @@ template <int L, int SB, int MAXT, bool CYC, int RHS>
 __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     k_split_df(const float4* __restrict__ growtab, const double* __restrict__ gchunk,
                const float2* __restrict__ gchunk_df, const double* __restrict__ gextra,
-               double* __restrict__ X, int M, int P, int batch, double k2d) {
+               double* __restrict__ X, int M, int P, int batch, double k2d, const NativeTabs nt) {
   constexpr bool CH = RHS == kRhsCH;
   constexpr bool CN = RHS == kRhsCN;
   static_assert(RHS == kRhsPlain || CYC, "the fused time steps are periodic");
@@ -89,6 +110,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   double* sS = sW + (size_t)SB * P * 2;          // [SB][P][2] s_c (serial scan)
   double* sT = sS + (size_t)SB * P * 2;          // [SB][P][2] t_c (serial scan)
   double* sX = sT + (size_t)SB * P * 2;          // [SB][8]   cyclic: y and x_t
+  uint32_t* smax = reinterpret_cast<uint32_t*>(sX + (size_t)SB * 8);   // [SB] largest |entry| bits
 
   for (int t = threadIdx.x; t < P * L * K4; t += blockDim.x) {
     const int row = t / K4, k = t % K4;
@@ -101,6 +123,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   } else {
     for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
   }
+  for (int t = threadIdx.x; t < SB; t += blockDim.x) smax[t] = 0u;
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int sys = (w % SG) * 8 + (lane & 7);
   const int c = (w / SG) * 4 + (lane >> 3);
@@ -128,7 +151,39 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     const bool act = s < batch;
     double* p = X + (long long)row0 * ld + (act ? s : 0);
 
-    // ---- 1. load, local forward (zero incoming state), local backward
+    // ---- 1. the system's largest entry sets its scale: a first pass over this
+    // chunk's rows (and, for the chunk-0 thread of a cyclic plan, the two border
+    // rows) takes the maximum, one barrier shares it; the loads below then find
+    // the rows in cache.  Then: load, local forward (zero incoming state), local
+    // backward.
+    // off = (e - 127) << 20 for the system's exponent field e: the rebias of
+    // both conversions (f 2^-s in, x 2^s out); e = (off >> 20) + 127
+    uint32_t off = 0u;
+    bool native = false;
+    float q = 1.f;
+    {
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int j = 0; j < L; ++j)
+        if (act && row0 + j < M) mx = max(mx, fg::mag_bits(p[j * ld]));
+      if (CYC && c == 0 && act) {
+        mx = max(mx, fg::mag_bits(X[(long long)M * ld + s]));
+        mx = max(mx, fg::mag_bits(X[(long long)(M + 1) * ld + s]));
+      }
+      atomicMax(&smax[sys], mx);
+      __syncthreads();
+      const uint32_t e = smax[sys] >> 20;
+      const bool fast = e >= kEMin && e <= (CH ? kEMaxCH : kEMax);
+      native = act && !fast;
+      off = fg::in_offset(fast ? e : 1023u);
+      if constexpr (CH) q = cubic_scale(fast ? e : 1023u);
+    }
+    // f * 2^-s as a pair
+    auto sdf = [&](double v) {
+      float h, lo;
+      fg::split(v, off, h, lo);
+      return D2{h, lo};
+    };
     D2 v[L];
     if constexpr (CH) {
       // right-hand side from C_{i-1}, C_i, C_{i+1} (row -1 wraps to N-1 = M+1);
@@ -141,13 +196,13 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         cv[j] = (act && i <= M) ? X[(long long)iw * ld + s] : 0.0;
       }
       const D2 k2 = df::from_double(k2d);
-      D2 cc = df::from_double(cv[1]);
-      D2 um = cubic_minus(df::from_double(cv[0])), u0 = cubic_minus(cc);
+      D2 cc = sdf(cv[1]);
+      D2 um = cubic_minus(sdf(cv[0]), q), u0 = cubic_minus(cc, q);
       D2 a1{0.f, 0.f}, a2{0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < L; ++j) {
-        const D2 cn = df::from_double(cv[j + 2]);
-        const D2 up = cubic_minus(cn);
+        const D2 cn = sdf(cv[j + 2]);
+        const D2 up = cubic_minus(cn, q);
         D2 f = ch_rhs(cc, um, u0, up, k2);
         if (row0 + j >= M) f = D2{0.f, 0.f};
         const float4 c0 = ctb[j * K4];
@@ -169,7 +224,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
       for (int j = 0; j < L; ++j) {
         const float4 c0 = ctb[j * K4];
         const float4 c1 = ctb[j * K4 + 1];
-        const D2 g = df::sum3p(D2{c0.x, c0.y}, df::from_double(fv[j]), D2{c0.z, c0.w}, a2,
+        const D2 g = df::sum3p(D2{c0.x, c0.y}, sdf(fv[j]), D2{c0.z, c0.w}, a2,
                                D2{c1.x, c1.y}, a1);
         v[j] = g;
         a2 = a1;
@@ -214,7 +269,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     D2 S0{0.f, 0.f}, S1{0.f, 0.f}, T0{0.f, 0.f}, T1{0.f, 0.f};
     double* xc = sX + (size_t)sys * 8;
     if (T > 0) {
-      __syncthreads();                                   // e_c published
+      __syncthreads();                                   // e_c published, smax read
+      if (c == 0) smax[sys] = 0u;                        // next block (ordered by the next barrier)
       const float2* E = reinterpret_cast<const float2*>(sE) + (size_t)sys * P * 2;
       for (int k = 1; k <= T && k <= c; ++k) {           // s_c = sum_k A_{c,k} e_{c-k}
         const D2 ea{E[2 * (c - k)].x, E[2 * (c - k)].y}, eb{E[2 * (c - k) + 1].x, E[2 * (c - k) + 1].y};
@@ -258,7 +314,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         if (row0 <= M - 2 && M - 2 < row0 + L) xc[0] = xm2;
         if (row0 <= M - 1 && M - 1 < row0 + L) xc[1] = xm1;
       }
-      __syncthreads();
+      __syncthreads();                                   // e_c, x'_start published, smax read
+      if (c == 0) smax[sys] = 0u;                        // next block (ordered by the next barrier)
       if (c == 0) {                                      // exact serial scan, one thread per system
         const double* E = sE + (size_t)sys * P * 2;
         const double* Wv = sW + (size_t)sys * P * 2;
@@ -307,31 +364,32 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
       if (c == 0) {
         const double r0 = gextra[4] * xc[0] + gextra[5] * xc[1] + gextra[6] * xc[2];
         const double r1 = gextra[7] * xc[1] + gextra[8] * xc[2] + gextra[9] * xc[3];
+        // the border rows in the system's scale (all doubles here are scaled)
         double ft0 = 0.0, ft1 = 0.0;
         if (act) {
           if constexpr (CH) {
             // tail rows N-2 = M and N-1 = M+1 need C at M-1, M, M+1 and 0
             const D2 k2 = df::from_double(k2d);
-            const D2 cA = df::from_double(X[(long long)(M - 1) * ld + s]);
-            const D2 cB = df::from_double(X[(long long)M * ld + s]);
-            const D2 cC = df::from_double(X[(long long)(M + 1) * ld + s]);
-            const D2 cD = df::from_double(X[s]);
-            const D2 uA = cubic_minus(cA), uB = cubic_minus(cB), uC = cubic_minus(cC);
-            const D2 uD = cubic_minus(cD);
+            const D2 cA = sdf(X[(long long)(M - 1) * ld + s]);
+            const D2 cB = sdf(X[(long long)M * ld + s]);
+            const D2 cC = sdf(X[(long long)(M + 1) * ld + s]);
+            const D2 cD = sdf(X[s]);
+            const D2 uA = cubic_minus(cA, q), uB = cubic_minus(cB, q), uC = cubic_minus(cC, q);
+            const D2 uD = cubic_minus(cD, q);
             ft0 = df::to_double(ch_rhs(cB, uA, uB, uC, k2));
             ft1 = df::to_double(ch_rhs(cC, uB, uC, uD, k2));
           } else {
-            ft0 = X[(long long)M * ld + s];
-            ft1 = X[(long long)(M + 1) * ld + s];
+            ft0 = X[(long long)M * ld + s] * pow2_neg((off >> 20) + 127u);
+            ft1 = X[(long long)(M + 1) * ld + s] * pow2_neg((off >> 20) + 127u);
           }
         }
         const double u0 = gextra[0] * (ft0 - r0) + gextra[1] * (ft1 - r1);
         const double u1 = gextra[2] * (ft0 - r0) + gextra[3] * (ft1 - r1);
         xc[4] = u0;
         xc[5] = u1;
-        if (act) {
-          X[(long long)M * ld + s] = CN ? 2.0 * u0 - ft0 : u0;
-          X[(long long)(M + 1) * ld + s] = CN ? 2.0 * u1 - ft1 : u1;
+        if (act && !native) {
+          X[(long long)M * ld + s] = (CN ? 2.0 * u0 - ft0 : u0) * pow2_pos((off >> 20) + 127u);
+          X[(long long)(M + 1) * ld + s] = (CN ? 2.0 * u1 - ft1 : u1) * pow2_pos((off >> 20) + 127u);
         }
       }
       __syncthreads();
@@ -366,10 +424,17 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
           x = df::axpy(x, D2{c3.z, c3.w}, S1);
           x = df::axpy(x, D2{c4.x, c4.y}, T0);
           x = df::axpy(x, D2{c4.z, c4.w}, T1);
-          if constexpr (CN) x = df::add(D2{2.f * x.h, 2.f * x.l}, df::neg(df::from_double(cold[u])));
-          if (act && row0 + j < M) __stcs(p + j * ld, df::to_double(x));
+          if constexpr (CN) x = df::add(D2{2.f * x.h, 2.f * x.l}, df::neg(sdf(cold[u])));
+          if (act && !native && row0 + j < M) __stcs(p + j * ld, fg::join(x.h, x.l, off));
         }
       }
+    }
+    // systems outside the scaled path: one thread solves the column in fp64 from
+    // its untouched input (cyclic plans: N = M + 2 rows)
+    if (native && c == 0) {
+      if constexpr (CH) native_ch_col(nt, X + s, M + 2, (size_t)ld, k2d, 1);
+      else if constexpr (CN) native_cn_col(nt, X + s, M + 2, (size_t)ld, 1);
+      else native_solve_col(nt, X + s, M, (size_t)ld, CYC ? 1 : 0);
     }
   }
 }
@@ -388,7 +453,8 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st, 
   if (per_sm < 1) per_sm = 1;
   int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
   if (grid > nblk) grid = nblk;
-  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spchunk_df, p.spextra, X, p.M, P, batch, k2);
+  const NativeTabs nt{p.coef64, p.tail64, p.bands};
+  kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk, p.spchunk_df, p.spextra, X, p.M, P, batch, k2, nt);
   note_launch();
   return cudaGetLastError();
 }
@@ -398,7 +464,8 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st, 
 size_t split_smem_bytes(int L, int P, int SB, int cyclic) {
   const int K4 = cyclic ? kSpK : kSpK - 1;
   return (size_t)P * (L * K4 + 1) * sizeof(float4) +
-         ((size_t)P * kSpChunk + 4 * (size_t)SB * P * 2 + (size_t)SB * 8) * sizeof(double);
+         ((size_t)P * kSpChunk + 4 * (size_t)SB * P * 2 + (size_t)SB * 8) * sizeof(double) +
+         (size_t)SB * sizeof(uint32_t);
 }
 
 // Cyclic plans with L = 32 and P <= 32 run 16 systems per CTA (one copy of the

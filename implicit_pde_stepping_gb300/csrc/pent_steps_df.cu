@@ -28,11 +28,21 @@
 //
 // Launched only when the plan's chunk couplings are truncated (T > 0); the
 // exact serial chunk scan stays with the one-step kernel.
+//
+// Range: as in the one-step kernel, each system is scaled by the power of two
+// that puts the largest entry of C^0 in [1, 2) (the Cahn–Hilliard cubic then
+// carries 2^(2s)).  The scale is kept for all steps; the kernel watches the
+// state, and a system that grows beyond 2^8 in these units (only the explicit
+// Cahn–Hilliard cubic can make it grow, when |C| is well above 1) is not
+// stored: like the systems outside the scaled path's window, it is stepped
+// natively in fp64 by one thread from its untouched C^0.
 #include <type_traits>
 
 #include "cp_async.cuh"
 #include "df64.cuh"
+#include "fg.cuh"
 #include "pent_internal.cuh"
+#include "pent_native.cuh"
 
 namespace pent {
 namespace {
@@ -43,8 +53,11 @@ constexpr int kStepHyper = 0;
 constexpr int kStepCH = 1;
 constexpr int kStepCN = 2;
 
-// u = c^3 - c
-__device__ __forceinline__ D2 cubic_minus(D2 c) { return df::add(df::mul(df::mul(c, c), c), df::neg(c)); }
+// u = q c^3 - c for the scaled state c = C 2^-s, q = 2^(2s)
+__device__ __forceinline__ D2 cubic_minus(D2 c, float q) {
+  const D2 c3 = df::mul(df::mul(c, c), c);
+  return df::add(D2{c3.h * q, c3.l * q}, df::neg(c));
+}
 
 // C_i + k2 (u_{i-1} - 2 u_i + u_{i+1})
 __device__ __forceinline__ D2 ch_rhs(D2 c, D2 um, D2 u0, D2 up, D2 k2) {
@@ -75,6 +88,7 @@ __host__ __device__ inline size_t steps_smem(int L, int P, int SB, int rhs) {
   b += kSpExtra * sizeof(float2);                                   // extras as (hi, lo)
   if (rhs == kStepCH) b += ((size_t)SB * P * 2 + SB) * sizeof(float2);   // halo, C_{M-1}
   if (rhs == kStepCN) b += (size_t)L * SB * P * sizeof(float2);          // C^n of every row
+  b += 2 * (size_t)SB * sizeof(uint32_t);                                // largest |C^0| bits, growth flags
   return b;
 }
 
@@ -82,7 +96,7 @@ template <int L, int SB, int MAXT, int RHS, bool CHEAP>
 __global__ void __launch_bounds__(MAXT, 1)
     k_steps_df(const float4* __restrict__ growtab, const float2* __restrict__ gchunk,
                const double* __restrict__ gextra, double* __restrict__ X, int M, int P, int batch,
-               int nsteps, double k2d, int2 cheap) {
+               int nsteps, double k2d, int2 cheap, const NativeTabs nt) {
   constexpr bool CH = RHS == kStepCH;
   constexpr bool CN = RHS == kStepCN;
   constexpr int K4 = kSpK;
@@ -99,6 +113,8 @@ __global__ void __launch_bounds__(MAXT, 1)
   float2* sH = sXe + kSpExtra;                   // CH: [SB][P][2] first, last C
   float2* sA = sH + (CH ? (size_t)SB * P * 2 : 0);               // CH: [SB] C_{M-1}
   float2* sC = sA + (CH ? (size_t)SB : 0);                       // CN: [L][SB * P] C^n
+  uint32_t* smax = reinterpret_cast<uint32_t*>(sC + (CN ? (size_t)L * SB * P : 0));   // [SB]
+  uint32_t* sgrow = smax + SB;                                                          // [SB]
 
   for (int t = threadIdx.x; t < P * L * K4; t += blockDim.x) {
     const int row = t / K4, k = t % K4;
@@ -106,6 +122,7 @@ __global__ void __launch_bounds__(MAXT, 1)
   }
   for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
   if (threadIdx.x < kSpExtra) sXe[threadIdx.x] = pack(df::from_double(gextra[threadIdx.x]));
+  for (int t = threadIdx.x; t < SB; t += blockDim.x) smax[t] = sgrow[t] = 0u;
   cp_async_wait_all();
   __syncthreads();
   const int T = (int)gextra[18];
@@ -132,6 +149,32 @@ __global__ void __launch_bounds__(MAXT, 1)
     const bool act = s < batch;
     double* p = X + (long long)row0 * ld + (act ? s : 0);
 
+    // ---- the system's scale: its largest |C^0| (one pass over the rows; the
+    // loads below find them in cache)
+    {
+      uint32_t mx = 0u;
+#pragma unroll
+      for (int j = 0; j < L; ++j)
+        if (act && row0 + j < M) mx = max(mx, fg::mag_bits(p[j * ld]));
+      if (c == 0 && act) {
+        mx = max(mx, fg::mag_bits(X[(long long)M * ld + s]));
+        mx = max(mx, fg::mag_bits(X[(long long)(M + 1) * ld + s]));
+      }
+      atomicMax(&smax[sys], mx);
+    }
+    __syncthreads();
+    const uint32_t emax = smax[sys] >> 20;
+    const bool fast = emax >= fg::kEMin && emax <= (CH ? fg::kEMaxCH : fg::kEMax);
+    const bool native = act && !fast;
+    const uint32_t esys = fast ? emax : 1023u;
+    const uint32_t ioff = fg::in_offset(esys), ooff = fg::out_offset(esys);
+    const float q = fg::cubic_scale(esys);
+    auto sdf = [&](double x) {
+      float h, lo;
+      fg::split(x, ioff, h, lo);
+      return D2{h, lo};
+    };
+
     // ---- C^0: rows of this chunk into registers (padding rows 0), tail into shared memory
     D2 v[L];
 #pragma unroll
@@ -140,13 +183,15 @@ __global__ void __launch_bounds__(MAXT, 1)
 #pragma unroll
       for (int u = 0; u < LG; ++u) fv[u] = (act && row0 + j0 + u < M) ? p[(j0 + u) * ld] : 0.0;
 #pragma unroll
-      for (int u = 0; u < LG; ++u) v[j0 + u] = df::from_double(fv[u]);
+      for (int u = 0; u < LG; ++u) v[j0 + u] = sdf(fv[u]);
     }
     if (c == 0) {
-      xc[6] = pack(df::from_double(act ? X[(long long)M * ld + s] : 0.0));
-      xc[7] = pack(df::from_double(act ? X[(long long)(M + 1) * ld + s] : 0.0));
+      xc[6] = pack(sdf(act ? X[(long long)M * ld + s] : 0.0));
+      xc[7] = pack(sdf(act ? X[(long long)(M + 1) * ld + s] : 0.0));
     }
     __syncthreads();
+    if (c == 0) smax[sys] = sgrow[sys] = 0u;                // next block (ordered by the next barrier)
+    float grow = 0.f;                                       // largest |state| after any step
 
     for (int n = 0; n < nsteps; ++n) {
       const D2 ct0 = unpack(xc[6]), ct1 = unpack(xc[7]);   // C at rows M, M+1
@@ -169,8 +214,8 @@ __global__ void __launch_bounds__(MAXT, 1)
           const D2 k2 = df::from_double(k2d);
           if (c == 0) {                                     // rows M, M+1 need C_{M-1}, C_0
             const D2 cA = unpack(sA[sys]);
-            const D2 uA = cubic_minus(cA), uB = cubic_minus(ct0), uC = cubic_minus(ct1);
-            const D2 uD = cubic_minus(v[0]);
+            const D2 uA = cubic_minus(cA, q), uB = cubic_minus(ct0, q), uC = cubic_minus(ct1, q);
+            const D2 uD = cubic_minus(v[0], q);
             ft0 = ch_rhs(ct0, uA, uB, uC, k2);
             ft1 = ch_rhs(ct1, uB, uC, uD, k2);
           }
@@ -178,12 +223,12 @@ __global__ void __launch_bounds__(MAXT, 1)
           D2 rh = c + 1 < P ? unpack(sH[((size_t)sys * P + c + 1) * 2]) : D2{0.f, 0.f};
           rh = pick(row0 + L == M, ct0, rh);
           D2 cc = v[0];
-          D2 um = cubic_minus(lh), u0 = cubic_minus(cc);
+          D2 um = cubic_minus(lh, q), u0 = cubic_minus(cc, q);
 #pragma unroll
           for (int j = 0; j < L; ++j) {
             D2 cn = (j + 1 < L) ? v[j + 1 < L ? j + 1 : j] : rh;
             cn = pick(row0 + j + 1 == M, ct0, cn);          // row M is periodic state
-            const D2 up = cubic_minus(cn);
+            const D2 up = cubic_minus(cn, q);
             D2 f = ch_rhs(cc, um, u0, up, k2);
             if (row0 + j >= M) f = D2{0.f, 0.f};
             const float4 c0 = ctb[j * K4];
@@ -362,17 +407,29 @@ __global__ void __launch_bounds__(MAXT, 1)
           float sh, sl;
           quick_two_sum(x.h, x.l, sh, sl);
           v[j] = D2{sh, sl};
+          grow = fmaxf(grow, fabsf(sh));
         }
       }
     }
 
-    // ---- C^nsteps back to memory
+    // ---- C^nsteps back to memory, unless the system outgrew its scale
+    if (c == 0) grow = fmaxf(grow, fmaxf(fabsf(unpack(xc[6]).h), fabsf(unpack(xc[7]).h)));
+    if (!(grow <= 256.f)) atomicOr(&sgrow[sys], 1u);      // also catches NaN
+    __syncthreads();
+    const bool nat = native || (act && sgrow[sys] != 0u);
 #pragma unroll
     for (int j = 0; j < L; ++j)
-      if (act && row0 + j < M) __stcs(p + j * ld, df::to_double(v[j]));
-    if (c == 0 && act) {
-      X[(long long)M * ld + s] = df::to_double(unpack(xc[6]));
-      X[(long long)(M + 1) * ld + s] = df::to_double(unpack(xc[7]));
+      if (act && !nat && row0 + j < M) __stcs(p + j * ld, fg::join(v[j].h, v[j].l, ooff));
+    if (c == 0 && act && !nat) {
+      const D2 t0 = unpack(xc[6]), t1 = unpack(xc[7]);
+      X[(long long)M * ld + s] = fg::join(t0.h, t0.l, ooff);
+      X[(long long)(M + 1) * ld + s] = fg::join(t1.h, t1.l, ooff);
+    }
+    // systems outside the scaled path: one thread steps the column natively
+    if (nat && c == 0) {
+      if constexpr (CH) native_ch_col(nt, X + s, M + 2, (size_t)ld, k2d, nsteps);
+      else if constexpr (CN) native_cn_col(nt, X + s, M + 2, (size_t)ld, nsteps);
+      else native_hyper_col(nt, X + s, M, (size_t)ld, nsteps);
     }
     __syncthreads();                                        // shared state reused by the next block
   }
@@ -391,8 +448,9 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, doubl
   const int nblk = (batch + SB - 1) / SB;
   int grid = p.df_ctas > 0 ? p.df_ctas : per_sm * p.num_sms;
   if (grid > nblk) grid = nblk;
+  const NativeTabs nt{p.coef64, p.tail64, p.bands};
   kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk_df, p.spextra, X, p.M, P, batch, nsteps, k2,
-                                   make_int2(p.cheap_k, p.cheap_m));
+                                   make_int2(p.cheap_k, p.cheap_m), nt);
   note_launch();
   return cudaGetLastError();
 }
