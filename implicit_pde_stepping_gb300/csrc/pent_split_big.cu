@@ -16,15 +16,24 @@
 //                 x_t = S^{-1}(f_t - H^T y), written to rows M, M+1;
 //   k_big_fix     one thread per (system, chunk): t_c = sum_k B_{c,k} w_{c+1+k},
 //                 x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 (- U x_t), stored in fp64.
-// Memory traffic: f read, x' written and read, x written (four arrays, as the
-// twisted kernel), plus summaries of 64 bytes per chunk.  The chunk states are
+// Range: a first kernel (k_big_scale) takes each system's largest |entry|, and
+// the others work on the system scaled by the power of two that puts it in
+// [1, 2) (folded into the fp64 <-> pair conversions), so the pairs' float
+// exponent range never limits the result; a system outside the scaled path's
+// window (largest entry zero, subnormal, non-finite or extreme) is left
+// untouched by the first kernels and solved natively in fp64 by one thread of
+// k_big_fix.
+// Memory traffic: f read twice (the scale pass and k_big_local), x' written
+// and read, x written, plus summaries of 64 bytes per chunk.  The chunk states are
 // computed in double-float like the sweeps (summaries and a copy of the chunk
 // tables as (hi, lo) pairs), which keeps them off the fp64 pipe; only the
 // periodic border (one thread per system) works in fp64.  The parallelism is
 // batch x P threads, so a handful of very long systems still fills the GPU.
 #include "cp_async.cuh"
 #include "df64.cuh"
+#include "fg.cuh"
 #include "pent_internal.cuh"
+#include "pent_native.cuh"
 
 namespace pent {
 namespace {
@@ -58,14 +67,52 @@ __device__ __forceinline__ void place(int& s, int& c) {
   c = (blockIdx.y * (kBigThreads / 32) + w) * CPW + lane / SPW;
 }
 
+// the system's exponent window check (largest-entry exponent field e)
+__device__ __forceinline__ bool big_fast(uint32_t e) { return e >= fg::kEMin && e <= fg::kEMax; }
+
+// largest |entry| of each system (rows 0..N-1): SPW systems per warp row, the
+// rows strided over the grid; lanes of one system, then the CTA's warps reduce,
+// and one atomic per CTA and system combines into smax[s] (zeroed before)
+template <int SPW>
+__global__ void __launch_bounds__(kBigThreads)
+    k_big_scale(const double* __restrict__ X, unsigned* __restrict__ smax, int rows, int batch) {
+  constexpr int RPW = 32 / SPW;                   // rows per warp and step
+  constexpr int NW = kBigThreads / 32;
+  __shared__ unsigned red[NW][SPW];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int s = blockIdx.x * SPW + lane % SPW;
+  unsigned mx = 0u;
+  if (s < batch) {
+    const long long ld = batch;
+    const int stride = gridDim.y * NW * RPW;
+#pragma unroll 8
+    for (int i = (blockIdx.y * NW + w) * RPW + lane / SPW; i < rows; i += stride)
+      mx = max(mx, fg::mag_bits(X[(long long)i * ld + s]));
+  }
+#pragma unroll
+  for (int o = SPW; o < 32; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane < SPW) red[w][lane] = mx;
+  __syncthreads();
+  if (threadIdx.x < SPW && blockIdx.x * SPW + (int)threadIdx.x < batch) {
+    unsigned m = 0u;
+#pragma unroll
+    for (int k = 0; k < NW; ++k) m = max(m, red[k][threadIdx.x]);
+    atomicMax(smax + blockIdx.x * SPW + threadIdx.x, m);
+  }
+}
+
 template <int SPW, bool CYC>
 __global__ void __launch_bounds__(kBigThreads, 2)
     k_big_local(const float4* __restrict__ tab, double* __restrict__ X, double* __restrict__ sum,
-                double* __restrict__ xm, int M, int P, int batch, int2 dup) {
+                double* __restrict__ xm, const unsigned* __restrict__ smax, int M, int P, int batch,
+                int2 dup) {
   constexpr int L = kBigL;
   int s, c;
   place<SPW>(s, c);
   if (s >= batch || c >= P) return;
+  const uint32_t e = smax[s] >> 20;
+  if (!big_fast(e)) return;                       // solved natively by k_big_fix
+  const uint32_t off = fg::in_offset(e);
   const long long ld = batch;
   const int row0 = c * L;
   double* p = X + (long long)row0 * ld + s;
@@ -84,7 +131,9 @@ __global__ void __launch_bounds__(kBigThreads, 2)
     for (int j = 0; j < L; ++j) {
       const double f = (row0 + j < M) ? mine[j * kBigThreads] : 0.0;
       const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
-      const D2 g = df::sum3p(D2{c0.x, c0.y}, df::from_double(f), D2{c0.z, c0.w}, a2, D2{c1.x, c1.y}, a1);
+      float fh, fl;
+      fg::split(f, off, fh, fl);
+      const D2 g = df::sum3p(D2{c0.x, c0.y}, D2{fh, fl}, D2{c0.z, c0.w}, a2, D2{c1.x, c1.y}, a1);
       v[j] = g;
       a2 = a1;
       a1 = g;
@@ -179,9 +228,12 @@ __global__ void k_chunk_df(const double* __restrict__ src, float2* __restrict__ 
 __global__ void __launch_bounds__(kBigThreads)
     k_big_border(const double* __restrict__ ctab, const float2* __restrict__ ctabd,
                  const double* __restrict__ extra, const float2* __restrict__ sum,
-                 const double* __restrict__ xm, double* __restrict__ X, int M, int P, int batch, int2 dup) {
+                 const double* __restrict__ xm, double* __restrict__ X, const unsigned* __restrict__ smax,
+                 int M, int P, int batch, int2 dup) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
+  const uint32_t e = smax[s] >> 20;
+  if (!big_fast(e)) return;                       // solved natively by k_big_fix
   const long long ld = batch;
   const int T = (int)extra[18];
   // y at rows 0, 1: chunk 0 has s_0 = 0, so y = w_0 + Kst_0 t_0
@@ -203,21 +255,28 @@ __global__ void __launch_bounds__(kBigThreads)
   }
   const double r0 = extra[4] * yv[0] + extra[5] * yv[1] + extra[6] * y0;
   const double r1 = extra[7] * yv[1] + extra[8] * y0 + extra[9] * y1;
-  const double f0 = X[(long long)M * ld + s], f1 = X[(long long)(M + 1) * ld + s];
-  X[(long long)M * ld + s] = extra[0] * (f0 - r0) + extra[1] * (f1 - r1);
-  X[(long long)(M + 1) * ld + s] = extra[2] * (f0 - r0) + extra[3] * (f1 - r1);
+  // in the system's scale; the border solution back at its own scale
+  const double f0 = X[(long long)M * ld + s] * fg::pow2_neg(e), f1 = X[(long long)(M + 1) * ld + s] * fg::pow2_neg(e);
+  X[(long long)M * ld + s] = (extra[0] * (f0 - r0) + extra[1] * (f1 - r1)) * fg::pow2_pos(e);
+  X[(long long)(M + 1) * ld + s] = (extra[2] * (f0 - r0) + extra[3] * (f1 - r1)) * fg::pow2_pos(e);
 }
 
 template <int SPW, bool CYC>
 __global__ void __launch_bounds__(kBigThreads)
     k_big_fix(const float4* __restrict__ tab, const float2* __restrict__ ctab,
               const double* __restrict__ extra, const float2* __restrict__ sum, double* __restrict__ X,
-              int M, int P, int batch, int2 dup) {
+              const unsigned* __restrict__ smax, const NativeTabs nt, int M, int P, int batch, int2 dup) {
   constexpr int L = kBigL;
   int s, c;
   place<SPW>(s, c);
   if (s >= batch || c >= P) return;
   const long long ld = batch;
+  const uint32_t e = smax[s] >> 20;
+  if (!big_fast(e)) {                             // the whole column, natively, by one thread
+    if (c == 0) native_solve_col(nt, X + s, M, (size_t)ld, CYC ? 1 : 0);
+    return;
+  }
+  const uint32_t off = fg::in_offset(e);
   const int row0 = c * L;
   if (row0 >= M) return;
   const int T = (int)extra[18];
@@ -230,8 +289,8 @@ __global__ void __launch_bounds__(kBigThreads)
   if (CYC) {
     const int reach = (int)extra[19];
     needU = c < reach || c > (M - 1) / L - reach;
-    X0 = df::from_double(-X[(long long)M * ld + s]);
-    X1 = df::from_double(-X[(long long)(M + 1) * ld + s]);
+    X0 = df::from_double(-X[(long long)M * ld + s] * fg::pow2_neg(e));
+    X1 = df::from_double(-X[(long long)(M + 1) * ld + s] * fg::pow2_neg(e));
   }
   double* p = X + (long long)row0 * ld + s;
   const float2* q = reinterpret_cast<const float2*>(p);
@@ -255,7 +314,7 @@ __global__ void __launch_bounds__(kBigThreads)
         x = df::axpy(x, D2{c1.z, c1.w}, X0);
         x = df::axpy(x, D2{c5.x, c5.y}, X1);
       }
-      if (row0 + j < M) __stcs(p + j * ld, df::to_double(x));
+      if (row0 + j < M) __stcs(p + j * ld, fg::join(x.h, x.l, off));
     }
   }
 }
@@ -267,11 +326,27 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   const dim3 grid((batch + SPW - 1) / SPW, (P + CPB - 1) / CPB);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   double* xm = p.spsum + (size_t)P * batch * kSum;
+  unsigned* smax = reinterpret_cast<unsigned*>(xm + 2 * (size_t)batch);
   const int2 dup = make_int2(p.dup_lo, p.dup_hi);
   const size_t smem_local = (size_t)kBigL * kBigThreads * sizeof(double);
   cudaError_t e = kernel_prepare((const void*)k_big_local<SPW, CYC>, smem_local, kBigThreads, nullptr);
   if (e != cudaSuccess) return e;
-  k_big_local<SPW, CYC><<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, p.M, P, batch, dup);
+  e = cudaMemsetAsync(smax, 0, (size_t)batch * sizeof(unsigned), st);
+  if (e != cudaSuccess) return e;
+  {
+    // enough CTAs over the rows to fill the GPU (each loops over its rows)
+    const int rows = p.M + (CYC ? 2 : 0);
+    const unsigned gx = (batch + SPW - 1) / SPW;
+    const int per_cta = (kBigThreads / 32) * (32 / SPW);
+    unsigned gy = (unsigned)((rows + per_cta - 1) / per_cta);
+    const unsigned cap = (unsigned)(8 * (p.num_sms > 0 ? p.num_sms : 1)) / gx + 1;
+    if (gy > cap) gy = cap;
+    if (gy > 65535u) gy = 65535u;
+    k_big_scale<SPW><<<dim3(gx, gy), kBigThreads, 0, st>>>(X, smax, rows, batch);
+    note_launch();
+  }
+  k_big_local<SPW, CYC><<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, smax, p.M, P, batch,
+                                                               dup);
   note_launch();
   const long long n = (long long)P * batch;
   float2* sumd = reinterpret_cast<float2*>(p.spsum);
@@ -280,11 +355,12 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   note_launch();
   if (CYC) {
     k_big_border<<<(batch + kBigThreads - 1) / kBigThreads, kBigThreads, 0, st>>>(
-        p.spchunk, p.spchunk_df, p.spextra, sumd, xm, X, p.M, P, batch, dup);
+        p.spchunk, p.spchunk_df, p.spextra, sumd, xm, X, smax, p.M, P, batch, dup);
     note_launch();
   }
-  k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, p.M, P,
-                                                   batch, dup);
+  const NativeTabs nt{p.coef64, p.tail64, p.bands};
+  k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, smax, nt, p.M,
+                                                   P, batch, dup);
   note_launch();
   return cudaGetLastError();
 }
@@ -308,8 +384,10 @@ cudaError_t split_big_prepare(pent_plan_s& p, cudaStream_t st) {
 
 cudaError_t shared_split_big(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   if (p.sp_L != kBigL || p.sp_T <= 0) return cudaErrorInvalidValue;
-  // summaries: kSum doubles per (chunk, system), then x' at rows M-2, M-1 per system
-  const size_t need = ((size_t)p.sp_P * batch * kSum + 2 * (size_t)batch) * sizeof(double);
+  // summaries: kSum doubles per (chunk, system), then x' at rows M-2, M-1 per
+  // system, then each system's largest |entry| bits
+  const size_t need = ((size_t)p.sp_P * batch * kSum + 2 * (size_t)batch) * sizeof(double) +
+                      (size_t)batch * sizeof(unsigned);
   if (p.spsum_bytes < need) {
     if (p.spsum) {
       cudaError_t e = cudaStreamSynchronize(st);   // earlier solves may still read it

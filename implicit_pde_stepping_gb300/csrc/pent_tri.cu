@@ -41,6 +41,7 @@
 //   cp.async instead.
 #include "cp_async.cuh"
 #include "df64.cuh"
+#include "fg.cuh"
 #include "pent_internal.cuh"
 #include "tma.cuh"
 
@@ -143,6 +144,50 @@ __device__ __forceinline__ D2 df_recip(D2 a) {
   return D2{r0, r0 * e};
 }
 
+// Range, as in the per-system pentadiagonal kernel: row i scaled by the power
+// of two of its diagonal b_i (c' and y' are unchanged), the solution scale 2^S
+// fixed at the first nonzero y_i from |y_i / b_i|, and native fp64 from the
+// first row the pairs cannot represent in that scale (more than 2^60 above it;
+// zero, subnormal or non-finite b_i or y_i; S outside [2^-890, 2^890]).  A zero
+// right-hand side gives exact zeros.
+__device__ __forceinline__ D2 tsdf(double v, uint32_t off) {
+  float h, l;
+  fg::split(v, off, h, l);
+  return D2{h, l};
+}
+
+__device__ __noinline__ void native_tri_rest(const double* __restrict__ A, const double* __restrict__ B,
+                                             const double* __restrict__ C, double* __restrict__ X,
+                                             float2* __restrict__ Wc, int N, int batch, size_t ld, size_t sb,
+                                             int s, int isw, uint32_t os, bool sset, D2 cpp, D2 ypp, int& bad) {
+  double* Wcd = reinterpret_cast<double*>(Wc);
+  const float2* Xp = reinterpret_cast<const float2*>(X);
+  double cp = (double)cpp.h + cpp.l;
+  double yp = (sset && isw > 0) ? fg::join(ypp.h, ypp.l, os) : 0.0;
+  if (isw == 0) cp = 0.0;
+  for (int i = isw; i < N; ++i) {
+    const size_t o = (size_t)i * ld + sb, ow = (size_t)i * batch + s;
+    const double a = i >= 1 ? A[o] : 0.0, b = B[o], c = i + 1 < N ? C[o] : 0.0, y = X[o];
+    const double den = b - cp * a;
+    if (bad == 0 && !(den != 0.0 && isfinite(den))) bad = i + 1;
+    const double rd = 1.0 / den;
+    cp = c * rd;
+    yp = (y - yp * a) * rd;
+    Wcd[ow] = cp;
+    X[o] = yp;
+  }
+  double x1 = 0.0;
+  for (int i = N - 1; i >= 0; --i) {
+    const size_t o = (size_t)i * ld + sb, ow = (size_t)i * batch + s;
+    const bool nat = i >= isw;
+    const double y = nat ? X[o] : (sset ? fg::join(Xp[o].x, Xp[o].y, os) : 0.0);
+    const double c = nat ? Wcd[ow] : (double)Wc[ow].x + (double)Wc[ow].y;
+    const double x = y - c * x1;
+    X[o] = x;
+    x1 = x;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads)
     k_tri_thread_df(const double* __restrict__ A, const double* __restrict__ B, const double* __restrict__ C,
                     double* __restrict__ X, float2* __restrict__ Wc, int N, int batch, int bs,
@@ -154,7 +199,10 @@ __global__ void __launch_bounds__(kThreads)
   float2* Xp = reinterpret_cast<float2*>(X);                                   // y' as (hi, lo) in place
   D2 cp{0.f, 0.f}, yp{0.f, 0.f};
   int bad = 0;
-  for (int i0 = 0; i0 < N; i0 += kUnroll) {
+  int S = 0;            // solution-scale exponent (set at the first nonzero y_i)
+  bool sset = false;
+  int isw = N;          // first row handled natively (N: none)
+  for (int i0 = 0; i0 < N && isw == N; i0 += kUnroll) {
     double a[kUnroll], b[kUnroll], c[kUnroll], y[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
@@ -169,38 +217,66 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int i = i0 + u;
-      if (i < N) {
-        const size_t o = (size_t)i * ld + sb;
-        const D2 na = df::neg(df::from_double(a[u]));
-        const D2 den = df::axpy(df::from_double(b[u]), na, cp);
-        if (bad == 0 && !(den.h != 0.f && isfinite(den.h))) bad = i + 1;
-        const D2 rd = df_recip(den);
-        cp = df::mul(df::from_double(c[u]), rd);
-        yp = df::mul(df::axpy(df::from_double(y[u]), na, yp), rd);
-        Wc[(size_t)i * batch + s] = make_float2(cp.h, cp.l);
-        Xp[o] = make_float2(yp.h, yp.l);
+      if (i < N && isw == N) {
+        const uint32_t mb = fg::mag_bits(b[u]), my = fg::mag_bits(y[u]);
+        const uint32_t eb = mb >> 20, ey = my >> 20;
+        bool nat = eb == 0u || eb >= 2047u || ey >= 2047u || (ey == 0u && my != 0u);
+        if (!nat && my != 0u) {
+          const int rel = (int)ey - (int)eb;
+          if (!sset) {
+            S = rel;
+            sset = true;
+            nat = rel < -890 || rel > 890;
+          } else {
+            nat = rel - S > 60;
+          }
+        }
+        if (nat) {
+          isw = i;
+        } else {
+          const size_t o = (size_t)i * ld + sb;
+          const uint32_t ob = (eb - 127u) << 20;                 // row i: x 2^-(eb - 1023)
+          const uint32_t oy = ob + ((uint32_t)S << 20);           // y_i: also x 2^-S
+          const D2 na = df::neg(tsdf(a[u], ob));
+          const D2 den = df::axpy(tsdf(b[u], ob), na, cp);
+          if (bad == 0 && !(den.h != 0.f && isfinite(den.h))) bad = i + 1;
+          const D2 rd = df_recip(den);
+          cp = df::mul(tsdf(c[u], ob), rd);
+          yp = df::mul(df::axpy(tsdf(y[u], oy), na, yp), rd);
+          Wc[(size_t)i * batch + s] = make_float2(cp.h, cp.l);
+          Xp[o] = make_float2(yp.h, yp.l);
+        }
       }
     }
   }
-  D2 x1{0.f, 0.f};
-  for (int i0 = N - 1; i0 >= 0; i0 -= kUnroll) {
-    float2 yv[kUnroll], cv[kUnroll];
+  const uint32_t os = ((uint32_t)S + 1023u - 127u) << 20;         // pairs x 2^S back to fp64
+  if (isw == N) {
+    if (!sset) {                                                  // y = 0: x = 0
+      for (int i = 0; i < N; ++i) X[(size_t)i * ld + sb] = 0.0;
+    } else {
+      D2 x1{0.f, 0.f};
+      for (int i0 = N - 1; i0 >= 0; i0 -= kUnroll) {
+        float2 yv[kUnroll], cv[kUnroll];
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = i0 - u;
-      const int ii = i >= 0 ? i : 0;
-      yv[u] = (i >= 0) ? Xp[(size_t)ii * ld + sb] : make_float2(0.f, 0.f);
-      cv[u] = (i >= 0) ? Wc[(size_t)ii * batch + s] : make_float2(0.f, 0.f);
-    }
+        for (int u = 0; u < kUnroll; ++u) {
+          const int i = i0 - u;
+          const int ii = i >= 0 ? i : 0;
+          yv[u] = (i >= 0) ? Xp[(size_t)ii * ld + sb] : make_float2(0.f, 0.f);
+          cv[u] = (i >= 0) ? Wc[(size_t)ii * batch + s] : make_float2(0.f, 0.f);
+        }
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int i = i0 - u;
-      if (i >= 0) {
-        const D2 x = df::axpy(D2{yv[u].x, yv[u].y}, df::neg(D2{cv[u].x, cv[u].y}), x1);
-        X[(size_t)i * ld + sb] = df::to_double(x);
-        x1 = x;
+        for (int u = 0; u < kUnroll; ++u) {
+          const int i = i0 - u;
+          if (i >= 0) {
+            const D2 x = df::axpy(D2{yv[u].x, yv[u].y}, df::neg(D2{cv[u].x, cv[u].y}), x1);
+            X[(size_t)i * ld + sb] = fg::join(x.h, x.l, os);
+            x1 = x;
+          }
+        }
       }
     }
+  } else {
+    native_tri_rest(A, B, C, X, Wc, N, batch, ld, sb, s, isw, os, sset, cp, yp, bad);
   }
   if (info) info[s] = bad;
 }

@@ -148,3 +148,119 @@ def test_ch_large_state_native_path():
     out = step("ch", N, C0, 1, sigma)
     assert np.all(np.isfinite(ref))
     assert max_rel_err(out, ref) < TOL_F64
+
+
+# ---------------------------------------------------------------------------
+# per-system matrices (pent_factor_solve, tri_factor_solve), fp64, AUTO variant
+# ---------------------------------------------------------------------------
+def persys(bands, F):
+    import torch
+    N, batch = F.shape
+    A = [dev(b) for b in bands]
+    X = dev(F)
+    info = torch.full((batch,), -1, dtype=torch.int32, device="cuda")
+    pent.pent_factor_solve(*A, X, info=info)
+    pent.pent_sync()
+    assert np.all(host(info) == 0)
+    return host(X)
+
+
+def tri(bands, Y):
+    import torch
+    N, batch = Y.shape
+    A = [dev(b) for b in bands]
+    X = dev(Y)
+    info = torch.full((batch,), -1, dtype=torch.int32, device="cuda")
+    pent.tri_factor_solve(*A, X, info=info)
+    pent.pent_sync()
+    assert np.all(host(info) == 0)
+    return host(X)
+
+
+@pytest.mark.parametrize("kind", ["pent", "tri"])
+@pytest.mark.parametrize("what", ["rhs", "bands", "both"])
+@pytest.mark.parametrize("scale", SCALES)
+def test_per_system_scaled(kind, what, scale):
+    """Right-hand side, matrix or both scaled; the solution scales by scale,
+    1/scale or not at all."""
+    N, batch = 300, 256
+    if kind == "pent":
+        bands = list(inputs.persys_bands(N, batch, seed=5, dtype=np.float64))
+    else:
+        bands = list(inputs.tri_bands(N, batch, seed=5, dtype=np.float64))
+    F = inputs.rhs_uniform(N, batch, seed=6)
+    if what in ("rhs", "both"):
+        F = F * scale
+    if what in ("bands", "both"):
+        if scale < 1e-300:
+            pytest.skip("subnormal matrix entries: fp64's own factorization degenerates")
+        bands = [b * scale for b in bands]
+    if kind == "pent":
+        ref = oracle.batch_persys(*bands, F)
+        out = persys(bands, F)
+    else:
+        ref = oracle.batch_tri(*bands, F)
+        out = tri(bands, F)
+    if not np.all(np.isfinite(ref)):
+        pytest.skip("the solution leaves the fp64 range")
+    assert np.all(np.isfinite(out))
+    assert max_rel_err(out, ref) < TOL_F64
+
+
+@pytest.mark.parametrize("kind", ["pent", "tri"])
+def test_per_system_mixed_batch(kind):
+    """Systems with scaled matrices, scaled right-hand sides, zero and subnormal
+    right-hand sides, and rows whose scales span 200 decades inside one system."""
+    N, batch = 257, 128
+    if kind == "pent":
+        bands = [b.copy() for b in inputs.persys_bands(N, batch, seed=8, dtype=np.float64)]
+    else:
+        bands = [b.copy() for b in inputs.tri_bands(N, batch, seed=8, dtype=np.float64)]
+    F = inputs.rhs_uniform(N, batch, seed=9)
+    for b in bands:
+        b[:, 1] *= 1e300
+        b[:, 2] *= 1e-250
+        b[:, 7] *= 1e200
+    F[:, 3] *= 1e300
+    F[:, 4] *= 1e-300
+    F[:, 5] = 0.0
+    F[:, 6] *= 1e-310
+    F[:, 7] *= 1e200
+    rowscale = np.logspace(-100, 100, N)
+    for b in bands:
+        b[:, 8] *= rowscale
+    F[:, 8] *= rowscale
+    F[: N // 2, 9] = 0.0
+    if kind == "pent":
+        ref = oracle.batch_persys(*bands, F)
+        out = persys(bands, F)
+    else:
+        ref = oracle.batch_tri(*bands, F)
+        out = tri(bands, F)
+    assert np.all(out[:, 5] == 0.0)
+    assert np.all(np.isfinite(ref))
+    assert max_rel_err(out, ref) < TOL_F64
+
+
+# ---------------------------------------------------------------------------
+# systems too long for one CTA (the multi-kernel partitioned form)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("cyclic", [False, True])
+@pytest.mark.parametrize("scale", [1e-310, 1e-300, 1e-35, 1e40, 1e300, 1e305])
+def test_long_systems_scaled(cyclic, scale):
+    N, batch = 5003, 6
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, batch, seed=31) * scale
+    X = run_solve(bands, F, cyclic)
+    assert np.all(np.isfinite(X))
+    assert max_rel_err(X, oracle.batch_shared(bands, F, cyclic=cyclic)) < TOL_F64
+
+
+@pytest.mark.parametrize("cyclic", [False, True])
+def test_long_systems_mixed_batch(cyclic):
+    N = 5003
+    bands = inputs.hyper_bands(N, 1.0)
+    F = mixed(N, 10, seed=33)
+    X = run_solve(bands, F, cyclic)
+    assert np.all(X[:, 3] == 0.0)
+    assert max_rel_err(X, oracle.batch_shared(bands, F, cyclic=cyclic)) < TOL_F64
