@@ -77,6 +77,10 @@ WORKLOADS = {
     "ch": dict(N=1024, batch=16384, kind="ch", cyclic=True, dtype="f64",
                desc="semi-implicit Cahn-Hilliard step (fused RHS + cyclic solve), N=1024, "
                     "batch=16384, fp64, gamma=1e-4, dt=0.1dx^2"),
+    "ch2000": dict(N=1024, batch=16384, kind="ch", cyclic=True, dtype="f64", nsub=2000,
+                   desc="semi-implicit Cahn-Hilliard, 2000 steps per call (the whole run of the "
+                        "workload in one persistent multi-step launch), N=1024, batch=16384, fp64, "
+                        "gamma=1e-4, dt=0.1dx^2, C0 ~ U[-0.1, 0.1]"),
 }
 
 
@@ -221,9 +225,10 @@ def source_digest(kernel_file: str) -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(kernel: str, kernel_file: str, workload: str, units: int):
-    """DRAM bytes per launch from the committed ncu summary, scaled to `units` systems when
-    the capture was taken on a smaller case; None if the kernel changed since the capture."""
+def ncu_record(kernel: str, kernel_file: str, workload: str):
+    """The committed ncu summary of `kernel` on `workload` (profiles/ncu_traffic.json):
+    DRAM bytes and, where captured, warp instructions and issue activity of one launch
+    on `units` systems.  None if missing or if the kernel changed since the capture."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as fh:
@@ -232,6 +237,15 @@ def ncu_traffic(kernel: str, kernel_file: str, workload: str, units: int):
         return None
     rec = table.get(f"{kernel}@{workload}")
     if not rec or rec.get("source_digest") != source_digest(kernel_file):
+        return None
+    return rec
+
+
+def ncu_traffic(kernel: str, kernel_file: str, workload: str, units: int):
+    """DRAM bytes per launch from the committed ncu summary, scaled to `units` systems when
+    the capture was taken on a smaller case; None if the kernel changed since the capture."""
+    rec = ncu_record(kernel, kernel_file, workload)
+    if rec is None or "dram_bytes_per_launch" not in rec:
         return None
     return float(rec["dram_bytes_per_launch"]) * units / float(rec["units"])
 
@@ -280,9 +294,13 @@ def run_ours(args, W: dict, dist: Dist):
         bands = [torch.from_numpy(lay(v)).to("cuda") for v in gen(N, batch, seed=seed, dtype=npdt)]
         bufs = [torch.from_numpy(lay(inputs.rhs_uniform(N, batch, seed=seed + r).astype(npdt)))
                 .to("cuda") for r in range(2)]
+        # scratch only where the kernel that runs uses it: the fp32 partitioned kernels
+        # (N <= 512) keep everything on chip and take none
+        code = pent.F64 if W["dtype"] == "f64" else pent.F32
+        split_runs = (W["dtype"] == "f32" and N <= 512 and args.variant in ("auto", "split"))
         wb = (pent.tri_factor_solve_work_bytes if kind == "tri" else pent.pent_factor_solve_work_bytes)
-        work = torch.empty(wb(N, batch, pent.F64 if W["dtype"] == "f64" else pent.F32), dtype=torch.uint8,
-                           device="cuda")
+        need = 0 if split_runs else wb(N, batch, code)
+        work = torch.empty(need, dtype=torch.uint8, device="cuda") if need else None
     if plan is not None and args.variant != "auto":
         plan.set_variant(args.variant)
     variant = plan.variant(batch) if plan is not None else pent.VARIANT_THREAD
@@ -452,26 +470,45 @@ def run_ours(args, W: dict, dist: Dist):
                 "kernel": kname, "kernel_ms": round(kernel_ms, 4),
                 "algorithmic_bytes_per_launch": alg_bytes,
                 "bytes_per_unit": per_unit, "units_per_launch": batch}
+    # instruction counts of the same capture, where recorded: instructions per point
+    # (per point and step for the multi-step kernel)
+    wl_rec = args.workload if nsub == 1 else ("cyclic100" if kind == "hyper" else
+                                              "cn100" if kind == "cn" else "ch100")
+    rec = ncu_record(kname, kfile, wl_rec)
+    if rec is not None and "warp_inst_per_launch" in rec:
+        rec_steps = float(rec.get("steps_per_launch", 1))
+        roofline["inst_per_point"] = round(32.0 * float(rec["warp_inst_per_launch"]) /
+                                           (float(rec["units"]) * N * rec_steps), 1)
+        roofline["issue_active_pct_ncu"] = rec.get("issue_active_pct")
     if nsub > 1:
-        # many steps per launch: memory is touched once per launch, the bound is arithmetic.
-        # Algorithmic fp64 flops per point and step (cyclic sweep 9 + bordering 4 FMA = 17;
-        # Crank-Nicolson +2 for 2y - C; Cahn-Hilliard +8 for the explicit right-hand side).
-        # The kernel computes them in double-float on the FP32 pipe, so the peak is that
-        # pipe's double-float multiply-add rate: 152 SMs x 128 FP32 lanes x 2.07 GHz, one
-        # multiply-add (2 flops) per 12 FP32 instructions.  The ratio to GB300's nominal
-        # fp64 rate (1.25 TFLOP/s) is reported beside it.
-        fpp = {"hyper": 17, "cn": 19, "ch": 25}[kind]
-        flops = fpp * N * batch * nsub
-        alu_peak = 152 * 128 * 2.07e9 * 2 / 12
-        rate = flops / (kernel_ms / 1e3)
-        roofline = {"bound": "alu", "achieved": round(rate / 1e9, 1),
-                    "peak": round(alu_peak / 1e9, 1), "unit": "GFLOP/s", "frac": round(rate / alu_peak, 4),
+        # Many steps per launch: memory is touched once per launch and the kernel is
+        # bound by instruction issue (double-float arithmetic on the FP32 pipe).  The
+        # roof is the GPU's issue rate, one warp instruction per cycle per SM
+        # sub-partition at the SM clock sampled during the run; the achieved rate is the
+        # kernel's warp instructions (ncu, scaled per point and step from the committed
+        # capture) over its CUDA-event time.  Both come from measurements.
+        sms = torch.cuda.get_device_properties(dev_index).multi_processor_count
+        clk = clocks.summary().get("sm_mhz") or 0.0
+        peak_issue = sms * 4 * clk * 1e6
+        achieved = None
+        if rec is not None and "warp_inst_per_launch" in rec:
+            per_ps = float(rec["warp_inst_per_launch"]) / (float(rec["units"]) * float(rec.get("steps_per_launch", 1)))
+            achieved = per_ps * batch * nsub / (kernel_ms / 1e3)
+        roofline = {"bound": "issue",
+                    "achieved": None if achieved is None else round(achieved / 1e9, 2),
+                    "peak": round(peak_issue / 1e9, 2) if peak_issue else None,
+                    "unit": "G warp-instructions/s",
+                    "frac": None if (achieved is None or not peak_issue) else round(achieved / peak_issue, 4),
                     "traffic": traffic,
-                    "peak_source": "derived: double-float multiply-add rate of the FP32 pipe "
-                                   "(152 SMs x 128 lanes x 2.07 GHz / 12 instructions x 2 flops)",
-                    "vs_fp64_nominal": round(rate / 1.25e12, 4),
+                    "peak_source": f"{sms} SMs x 4 sub-partitions x 1 warp instruction per cycle x "
+                                   f"the median SM clock sampled during the run ({clk} MHz)",
                     "kernel": kname, "kernel_ms": round(kernel_ms, 4),
-                    "algorithmic_flops_per_launch": flops, "flops_per_point_step": fpp,
+                    "inst_per_point_step": None if rec is None or "warp_inst_per_launch" not in rec else
+                    round(32.0 * float(rec["warp_inst_per_launch"]) /
+                          (float(rec["units"]) * N * float(rec.get("steps_per_launch", 1))), 1),
+                    "issue_active_pct_ncu": None if rec is None else rec.get("issue_active_pct"),
+                    "instruction_source": f"ncu smsp__inst_executed.sum of {kname} on {wl_rec} "
+                                          "(profiles/ncu_traffic.json)",
                     "steps_per_launch": nsub, "units_per_launch": batch * nsub,
                     "hbm_bytes_per_launch": alg_bytes}
 
@@ -496,58 +533,12 @@ def run_ours(args, W: dict, dist: Dist):
     return res
 
 
-def run_cpu_baseline(W: dict, seconds: float):
-    """The oracle as it stands, on this host's cores, on a bounded sample of the workload."""
+def oracle_sample(W: dict):
+    """The bounded sample of a workload that the CPU oracle is timed on (the same for
+    the cpu_baseline of our arm and for the reference arm): S systems, one call of
+    the oracle per step (one solve, or one time step for the stepping workloads)."""
     import numpy as np
 
-    import oracle
-    from implicit_pde_stepping_gb300 import inputs
-    N, kind = W["N"], W["kind"]
-    if kind == "shared":
-        S = max(1, min(4096, (4096 * 1024) // N))   # about 4M rows of work per call
-        bands = inputs.hyper_bands(N, W["sigma"])
-        F = inputs.rhs_uniform(N, S, seed=0)
-        fn = lambda: oracle.batch_shared(bands, F, cyclic=W["cyclic"])  # noqa: E731
-    elif kind == "hyper":
-        S = 512
-        F = inputs.fourier_initial(N, S)
-        fn = lambda: oracle.batch_hyperdiffusion(F, W["sigma"], 1)  # noqa: E731
-    elif kind == "ch":
-        S = 256
-        sigma, k2 = inputs.ch_params(N)
-        F = inputs.ch_initial(N, S)
-        fn = lambda: oracle.batch_ch(F, sigma, k2, 1)  # noqa: E731
-    elif kind == "cn":
-        S = 512
-        F = inputs.fourier_initial(N, S)
-        fn = lambda: oracle.batch_cn(F, W["sigma"], 1)  # noqa: E731
-    elif kind == "tri":
-        S = 32768
-        npdt = np.float64 if W["dtype"] == "f64" else np.float32
-        a, b, c = inputs.tri_bands(N, S, dtype=npdt)
-        F = inputs.rhs_uniform(N, S).astype(npdt)
-        fn = lambda: oracle.batch_tri(a, b, c, F)  # noqa: E731
-    else:
-        S = 8192
-        npdt = np.float64 if W["dtype"] == "f64" else np.float32
-        a, b, c, d, e = inputs.persys_bands(N, S, dtype=npdt)
-        F = inputs.rhs_uniform(N, S).astype(npdt)
-        fn = lambda: oracle.batch_persys(a, b, c, d, e, F)  # noqa: E731
-    fn()
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        fn()
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
-    unit = "system-solves/s" if kind in ("shared", "persys", "tri") else "system-steps/s"
-    return {"value": S * reps / el, "unit": unit, "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{S} systems of the workload (N={N}) x {reps} repetitions, {el:.1f} s"}
-
-
-def run_reference(args, W: dict, dist: Dist):
-    """Reference arm: the CPU oracle as it stands, timed on this host's cores."""
     import oracle
     from implicit_pde_stepping_gb300 import inputs
     N, kind = W["N"], W["kind"]
@@ -568,33 +559,79 @@ def run_reference(args, W: dict, dist: Dist):
         F = inputs.fourier_initial(N, S)
         fn = lambda: oracle.batch_cn(F, W["sigma"], 1)  # noqa: E731
     elif kind == "tri":
-        import numpy as np
         npdt = np.float64 if W["dtype"] == "f64" else np.float32
         a, b, c = inputs.tri_bands(N, S, dtype=npdt)
         F = inputs.rhs_uniform(N, S).astype(npdt)
         fn = lambda: oracle.batch_tri(a, b, c, F)  # noqa: E731
     else:
-        import numpy as np
         npdt = np.float64 if W["dtype"] == "f64" else np.float32
         a, b, c, d, e = inputs.persys_bands(N, S, dtype=npdt)
         F = inputs.rhs_uniform(N, S).astype(npdt)
         fn = lambda: oracle.batch_persys(a, b, c, d, e, F)  # noqa: E731
+    unit = "system-solves/s" if kind in ("shared", "persys", "tri") else "system-steps/s"
+    return S, fn, unit
+
+
+def time_oracle(W: dict, seconds: float):
+    """Oracle rate (systems per second) on this process's OpenMP threads."""
+    import oracle
+    S, fn, unit = oracle_sample(W)
+    fn()
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        fn()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": S * reps / el, "unit": unit, "cores": oracle.num_threads(), "systems": S,
+            "reps": reps, "seconds": round(el, 2)}
+
+
+def run_cpu_baseline(W: dict, seconds: float, workload: str):
+    """The oracle as it stands, on this host's cores (OpenMP over systems, the pages'
+    parallel baseline) and on one core (their serial baseline), same sample."""
+    omp = time_oracle(W, seconds)
+    single = None
+    try:
+        # one thread: a child interpreter with OMP_NUM_THREADS=1 (the oracle reads it
+        # when its OpenMP runtime starts)
+        env = dict(os.environ, OMP_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-child", workload,
+                            "--cpu-seconds", str(max(2.0, seconds / 2))],
+                           capture_output=True, text=True, env=env, timeout=600)
+        if r.returncode == 0:
+            single = json.loads(r.stdout.strip().splitlines()[-1])
+    except (OSError, ValueError, subprocess.SubprocessError, IndexError):
+        single = None
+    sample = f"{omp['systems']} systems of the workload (N={W['N']}) per call"
+    return {"value": omp["value"], "unit": omp["unit"], "cores": omp["cores"], "kind": "oracle",
+            "sample": sample + f" x {omp['reps']} calls, {omp['seconds']} s",
+            "single_thread": None if single is None else
+            {"value": single["value"], "unit": single["unit"], "cores": single["cores"],
+             "sample": sample + f" x {single['reps']} calls, {single['seconds']} s"}}
+
+
+def run_reference(args, W: dict, dist: Dist):
+    """Reference arm: the CPU oracle as it stands, timed on this host's cores on the
+    same sample as our arm's cpu_baseline."""
+    import oracle
+    S, fn, unit = oracle_sample(W)
     for _ in range(args.warmup):
         fn()
     t0 = time.perf_counter()
     for _ in range(args.steps):
         fn()
     el = time.perf_counter() - t0
-    unit = "system-solves/s" if kind in ("shared", "persys", "tri") else "system-steps/s"
     value = S * args.steps / el
-    sample = f"{S} systems of the workload (N={N}) per step"
+    sample = f"{S} systems of the workload (N={W['N']}) per step"
     return {
         "impl": "reference", "metric": METRIC if args.workload == "shared" else
         f"{W['desc']} throughput", "value": value, "unit": unit, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": W["dtype"],
         "data": "synthetic (seeded SplitMix64 counter-based generator)",
-        "config": {"workload": W["desc"], "N": N, "sample_systems_per_step": S},
+        "config": {"workload": W["desc"], "N": W["N"], "sample_systems_per_step": S},
         "cpu_baseline": {"value": value, "unit": unit, "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -618,7 +655,12 @@ def main(argv=None):
                     help="blocks of systems the host-buffer solve pipelines (shared workloads; 0: "
                          "the library's choice)")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--cpu-child", choices=sorted(WORKLOADS), default=None,
+                    help=argparse.SUPPRESS)   # internal: time the oracle in this process and exit
     args = ap.parse_args(argv)
+    if args.cpu_child:
+        print(json.dumps(time_oracle(WORKLOADS[args.cpu_child], args.cpu_seconds)), flush=True)
+        return 0
     if args.warmup < 3:
         log("warning: fewer than 3 warm-up steps")
     W = WORKLOADS[args.workload]
@@ -635,7 +677,7 @@ def main(argv=None):
         res = run_ours(args, W, dist)
         if dist.rank == 0:
             if dist.world == 1 and not args.no_cpu_baseline:
-                res["cpu_baseline"] = run_cpu_baseline(W, args.cpu_seconds)
+                res["cpu_baseline"] = run_cpu_baseline(W, args.cpu_seconds, args.workload)
             else:
                 res["cpu_baseline"] = None
             print(json.dumps(res), flush=True)

@@ -559,9 +559,15 @@ pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, co
 pent_status pent_factor_solve(const void* a, const void* b, const void* c, const void* d,
                               const void* e, void* rhs, int N, int batch, pent_dtype dtype,
                               void* work, size_t work_bytes, int* info, void* stream) {
-  if (!work || work_bytes < persys_work_bytes(N, batch, dtype) || !aligned(work, 256)) return PENT_ERR_INVALID_ARG;
+  // the scratch is checked where the chosen kernel needs it (pent_factor_solve_ex)
   return pent_factor_solve_ex(a, b, c, d, e, rhs, N, batch, dtype, PENT_VARIANT_AUTO, 0, work, work_bytes,
                               info, stream);
+}
+
+size_t pent_factor_solve_needs_work(int N, int batch, pent_dtype dtype) {
+  if (N < 1 || batch < 1 || (dtype != PENT_F64 && dtype != PENT_F32)) return 0;
+  if (dtype == PENT_F32 && persys_split_chunks(N) > 0) return 0;   // the partitioned kernel keeps all on chip
+  return persys_work_bytes(N, batch, dtype);
 }
 
 size_t tri_factor_solve_work_bytes(int N, int batch, pent_dtype dtype) {

@@ -55,6 +55,13 @@ cudaError_t scratch_address(void** out) {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// the status pent_factor_solve reports for the same CUDA error
+inline pent_status status_of(cudaError_t e) {
+  if (e == cudaSuccess) return PENT_OK;
+  if (e == cudaErrorMemoryAllocation) return PENT_ERR_ALLOC;
+  return PENT_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" pent_status pent_factor_solve_noalloc(const void* a, const void* b, const void* c,
@@ -70,19 +77,19 @@ extern "C" pent_status pent_factor_solve_noalloc(const void* a, const void* b, c
   if (dtype == PENT_F32 && pent::persys_split_chunks(N) > 0) {
     const cudaError_t err = pent::persys_split(a, b, c, d, e, rhs_inout, N, batch, 0, info,
                                                static_cast<cudaStream_t>(stream));
-    return err == cudaSuccess ? PENT_OK : PENT_ERR_CUDA;
+    return status_of(err);
   }
   if (pent::persys_work_bytes(N, batch, dtype) > kNoAllocScratchBytes) return PENT_ERR_UNSUPPORTED;
   void* scratch = nullptr;
   cudaError_t err = scratch_address(&scratch);
   if (err != cudaSuccess) {
     cudaGetLastError();
-    return PENT_ERR_CUDA;
+    return status_of(err);
   }
   err = dtype == PENT_F64
             ? pent::persys_thread_df(a, b, c, d, e, rhs_inout, N, batch, 0, scratch, info,
                                      static_cast<cudaStream_t>(stream))
             : pent::persys_thread(a, b, c, d, e, rhs_inout, N, batch, 0, dtype, scratch, info,
                                   static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? PENT_OK : PENT_ERR_CUDA;
+  return status_of(err);
 }

@@ -57,6 +57,8 @@ def lib():
             L.pent_factor_solve_ex.argtypes = [vp] * 6 + [i, i, i, i, i, vp, sz, vp, vp]
             L.pent_factor_solve_work_bytes.argtypes = [i, i, i]
             L.pent_factor_solve_work_bytes.restype = sz
+            L.pent_factor_solve_needs_work.argtypes = [i, i, i]
+            L.pent_factor_solve_needs_work.restype = sz
             L.pent_factor_solve_noalloc.argtypes = [vp] * 6 + [i, i, i, vp, vp]
             L.pent_factor_solve_noalloc.restype = i
             L.hyperdiffusion_step.argtypes = [vp, vp, i, i, vp]
@@ -213,6 +215,12 @@ def pent_factor_solve_work_bytes(N: int, batch: int, dtype) -> int:
     return int(lib().pent_factor_solve_work_bytes(int(N), int(batch), code))
 
 
+def pent_factor_solve_needs_work(N: int, batch: int, dtype) -> int:
+    """Scratch bytes the AUTO variant needs (0 where the partitioned kernel runs)."""
+    code = dtype if isinstance(dtype, int) else (F64 if str(dtype).endswith("64") else F32)
+    return int(lib().pent_factor_solve_needs_work(int(N), int(batch), code))
+
+
 def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None, variant: str = "auto",
                       block_size: int = 0):
     """Per-system factor + solve, in place in rhs.  variant: "auto", "thread" or "split"
@@ -237,19 +245,24 @@ def pent_factor_solve(a, b, c, d, e, rhs, work=None, info=None, stream=None, var
         code = _dtype_code(rhs)
         ptrs = [_ptr(t, N, code, n) for t, n in zip((a, b, c, d, e), "abcde")]
         rp = _ptr(rhs, N, code, "rhs")
-    need = pent_factor_solve_work_bytes(N, batch, code)
-    if work is None:
+    # scratch only where the chosen kernel uses it (none for the fp32 partitioned kernel)
+    need = (pent_factor_solve_needs_work(N, batch, code) if variant == "auto" and not block_size
+            else pent_factor_solve_work_bytes(N, batch, code))
+    if variant == "split":
+        need = 0
+    if work is None and need > 0:
         work = torch.empty(need, dtype=torch.uint8, device=rhs.device)
-    if work.numel() * work.element_size() < need:
+    nbytes = 0 if work is None else work.numel() * work.element_size()
+    if nbytes < need:
         raise ValueError("work too small")
     ip = None
     if info is not None:
         if info.dtype != torch.int32 or info.numel() < batch or not info.is_cuda:
             raise ValueError("info must be a CUDA int32 tensor of >= batch elements")
         ip = ctypes.c_void_p(info.data_ptr())
+    wp = ctypes.c_void_p(work.data_ptr() if work is not None else None)
     _check(lib().pent_factor_solve_ex(*ptrs, rp, N, batch, code, VARIANTS[variant], int(block_size),
-                                      ctypes.c_void_p(work.data_ptr()), work.numel() * work.element_size(),
-                                      ip, _stream(stream)), "pent_factor_solve")
+                                      wp, nbytes, ip, _stream(stream)), "pent_factor_solve")
     return work
 
 
@@ -298,17 +311,20 @@ def tri_factor_solve(a, b, c, rhs, variant: str = "auto", work=None, info=None, 
         code = _dtype_code(rhs)
         ptrs = [_ptr(t, N, code, n) for t, n in zip((a, b, c), "abc")]
         rp = _ptr(rhs, N, code, "rhs")
-    need = tri_factor_solve_work_bytes(N, batch, code)
-    if work is None:
+    # scratch only where the chosen kernel uses it (none for the fp32 partitioned kernel)
+    split_runs = code == F32 and N <= 512 and variant in ("auto", "split")
+    need = 0 if split_runs else tri_factor_solve_work_bytes(N, batch, code)
+    if work is None and need > 0:
         work = torch.empty(need, dtype=torch.uint8, device=rhs.device)
+    nbytes = 0 if work is None else work.numel() * work.element_size()
     ip = None
     if info is not None:
         if info.dtype != torch.int32 or info.numel() < batch or not info.is_cuda:
             raise ValueError("info must be a CUDA int32 tensor of >= batch elements")
         ip = ctypes.c_void_p(info.data_ptr())
+    wp = ctypes.c_void_p(work.data_ptr() if work is not None else None)
     _check(lib().tri_factor_solve(*ptrs, rp, N, batch, code, VARIANTS[variant], int(block_size),
-                                  ctypes.c_void_p(work.data_ptr()), work.numel() * work.element_size(),
-                                  ip, _stream(stream)), "tri_factor_solve")
+                                  wp, nbytes, ip, _stream(stream)), "tri_factor_solve")
     return work
 
 

@@ -54,7 +54,11 @@ typedef enum {
   PENT_VARIANT_AUTO = 0,
   PENT_VARIANT_THREAD = 1,    /* one thread per system, native arithmetic of the plan dtype */
   PENT_VARIANT_THREAD_DF = 2, /* one thread per system, fp64 plans computed in double-float
-                                 (pairs of fp32) on the FP32 pipe                        */
+                                 (pairs of fp32) on the FP32 pipe.  For shared-matrix
+                                 plans this is the twisted kernel, which writes g over f
+                                 as it sweeps and so cannot rescale a system: its pairs
+                                 cover |values| in (2^-100, 2^127) only, and AUTO never
+                                 picks it                                              */
   PENT_VARIANT_SPLIT = 3      /* each system split over a warp (partitioned solve)       */
 } pent_variant;
 
@@ -89,6 +93,12 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
  *   rhs_inout : DEVICE, interleaved [N][batch] of the plan dtype; holds f on
  *               entry and x on return.  Base address 16-byte aligned.
  *   batch     : >= 1.
+ * fp64 plans (AUTO variant) compute in double-float on the FP32 pipe and keep
+ * the whole fp64 range: every system is scaled by the power of two that puts
+ * its largest |f| in [1, 2) before it is converted, and systems whose largest
+ * entry is zero, subnormal, non-finite or beyond the scaled kernels' window
+ * are solved in native fp64.  Accuracy is relative to each system's largest
+ * |x| (about 1e-13 against an fp64 solve).
  */
 pent_status pent_solve(pent_plan plan, void* rhs_inout, int batch, void* stream);
 
@@ -126,9 +136,15 @@ pent_status pent_solve_host(pent_plan plan, const void* rhs_host, void* x_host, 
  *                   16-byte aligned; not modified.
  *   rhs_inout     : DEVICE, interleaved [N][batch], 16-byte aligned; f in, x out.
  *   N, batch      : >= 1.
- *   work          : DEVICE scratch of at least pent_factor_solve_work_bytes()
- *                   bytes, 256-byte aligned; contents undefined afterwards.
- *                   (The kernel chosen by PENT_VARIANT_AUTO may not touch it.)
+ *   work          : DEVICE scratch, 256-byte aligned, contents undefined
+ *                   afterwards, of at least pent_factor_solve_needs_work()
+ *                   bytes; NULL (with work_bytes 0) when that is 0 (fp32
+ *                   systems of up to 512 rows, which the partitioned kernel
+ *                   keeps on chip).  The page's Rewrite scheme overwrites the
+ *                   caller's bands with the factors; this library keeps them
+ *                   and asks the caller for the factor storage instead, in
+ *                   line with its rule that the caller owns every device
+ *                   buffer of a call.
  *   info          : DEVICE int[batch] or NULL.  info[s] = 0 if system s was
  *                   factored, else the 1-based row of the first zero or
  *                   non-finite pivot the kernel's elimination met (its x is
@@ -151,9 +167,13 @@ pent_status pent_factor_solve(const void* a, const void* b, const void* c, const
  *             cyclic reduction), so memory sees the bands and f once and x
  *             once; `work` is not used and may be NULL;
  *             PENT_VARIANT_THREAD_DF — fp64 only: THREAD's sweeps in
- *             double-float (pairs of floats on the FP32 pipe, ~2^-47 relative;
- *             values of magnitude below 2^-100 or from 2^127 are outside its
- *             range), inputs and outputs fp64, the scratch holding pairs;
+ *             double-float (pairs of floats on the FP32 pipe, ~2^-47 relative),
+ *             inputs and outputs fp64, the scratch holding pairs; every row is
+ *             scaled by the power of two of its diagonal and the solution by a
+ *             per-system power of two, and from the first row the pairs
+ *             cannot represent (or a zero, subnormal or non-finite diagonal or
+ *             right-hand side) the thread continues in native fp64, so the
+ *             whole fp64 range is kept;
  *             PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD_DF for
  *             fp64, else THREAD.
  *   block_size : 0 — a..e and rhs_inout interleaved [N][batch], element (i, s)
@@ -177,8 +197,15 @@ pent_status pent_factor_solve_ex(const void* a, const void* b, const void* c, co
                                  pent_variant variant, int block_size, void* work, size_t work_bytes,
                                  int* info, void* stream);
 
-/* Bytes of device scratch pent_factor_solve needs for (N, batch, dtype). */
+/* Bytes of device scratch the one-thread-per-system kernels of
+ * pent_factor_solve_ex use for (N, batch, dtype) (variants THREAD and
+ * THREAD_DF). */
 size_t pent_factor_solve_work_bytes(int N, int batch, pent_dtype dtype);
+
+/* Bytes of device scratch pent_factor_solve (the AUTO variant) needs for
+ * (N, batch, dtype): 0 where it picks the partitioned kernel (fp32, N <= 512),
+ * else pent_factor_solve_work_bytes(). */
+size_t pent_factor_solve_needs_work(int N, int batch, pent_dtype dtype);
 
 /*
  * pent_factor_solve_noalloc — pent_factor_solve for callers that cannot
@@ -277,9 +304,11 @@ pent_status cn_step(pent_plan plan, void* C_inout, int batch, int nsteps, void* 
  *               partitioned elimination, chunk-end unknowns by parallel cyclic
  *               reduction), so memory sees a, b, c, y once and x once;
  *               PENT_VARIANT_THREAD_DF — fp64 only: THREAD's sweeps in
- *               double-float (pairs of floats on the FP32 pipe, ~2^-47 relative;
- *               values of magnitude below 2^-100 or from 2^127 are outside its
- *               range), the scratch and y' holding pairs;
+ *               double-float (pairs of floats on the FP32 pipe, ~2^-47
+ *               relative), the scratch and y' holding pairs; rows scaled by
+ *               their diagonal's power of two, the solution by a per-system
+ *               power of two, native fp64 from the first row the pairs cannot
+ *               represent: the whole fp64 range is kept;
  *               PENT_VARIANT_AUTO — SPLIT where it applies, else THREAD_DF for
  *               fp64, else THREAD.
  *   work      : DEVICE scratch of tri_factor_solve_work_bytes() bytes,

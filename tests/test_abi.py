@@ -111,3 +111,15 @@ def test_per_system_argument_errors_before_any_device_work(L):
     assert na(*p6, 8, 4, 9, None, None) == pent.ERR_INVALID_ARG
     assert L.pent_solve_host(None, ok, ok, 4, 0, None) == pent.ERR_INVALID_ARG
     assert L.pent_get_variant(None, 4) == pent.VARIANT_AUTO
+
+
+def test_factor_solve_needs_work():
+    """The AUTO per-system solve needs no scratch where the fp32 partitioned kernel runs
+    (N <= 512) and the one-thread kernels' factor storage elsewhere."""
+    L = pent.lib()
+    assert pent.pent_factor_solve_needs_work(256, 262144, pent.F32) == 0
+    assert pent.pent_factor_solve_needs_work(512, 7, pent.F32) == 0
+    assert pent.pent_factor_solve_needs_work(513, 7, pent.F32) == 2 * 513 * 7 * 4
+    assert pent.pent_factor_solve_needs_work(256, 3, pent.F64) == 2 * 256 * 3 * 8
+    assert L.pent_factor_solve_needs_work(0, 3, 0) == 0
+    assert L.pent_factor_solve_needs_work(3, 3, 7) == 0

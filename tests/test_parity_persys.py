@@ -200,3 +200,30 @@ def test_fp64_quarter_size_sampled():
     ref = oracle.batch_persys(a[:, idx], b[:, idx], c[:, idx], d[:, idx], e[:, idx], F[:, idx])
     assert max_rel_err(X[:, idx], ref) < TOL_F64
     assert np.all(info == 0)
+
+
+def test_auto_takes_null_work_where_no_kernel_needs_it():
+    """pent_factor_solve through the C ABI with work = NULL: accepted for fp32 systems
+    of up to 512 rows (the partitioned kernel keeps every intermediate on chip),
+    refused where the chosen kernel needs factor storage (fp64)."""
+    import ctypes
+    import torch
+    L = pent.lib()
+    N, batch = 256, 2048
+    assert pent.pent_factor_solve_needs_work(N, batch, pent.F32) == 0
+    assert pent.pent_factor_solve_needs_work(N, batch, pent.F64) == pent.pent_factor_solve_work_bytes(
+        N, batch, pent.F64)
+    bands = inputs.persys_bands(N, batch, seed=77, dtype=np.float32)
+    F = inputs.rhs_uniform(N, batch, seed=78).astype(np.float32)
+    A = [dev(b) for b in bands]
+    X = dev(F)
+    vp = [ctypes.c_void_p(t.data_ptr()) for t in A + [X]]
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    st = L.pent_factor_solve(*vp, N, batch, pent.F32, None, 0, None, stream)
+    assert st == pent.OK
+    assert L.pent_sync(stream) == pent.OK
+    assert max_rel_err(host(X), oracle.batch_persys(*bands, F)) < TOL_F32
+    A64 = [dev(b.astype(np.float64)) for b in bands]
+    X64 = dev(F.astype(np.float64))
+    vp64 = [ctypes.c_void_p(t.data_ptr()) for t in A64 + [X64]]
+    assert L.pent_factor_solve(*vp64, N, batch, pent.F64, None, 0, None, stream) == pent.ERR_INVALID_ARG
