@@ -59,7 +59,9 @@ __device__ __forceinline__ uint32_t mag_bits(double v) {
 
 // Rebias constant for a system whose largest entry has the (biased) fp64
 // exponent field e: a value with exponent field ev converts to a float with
-// exponent field ev - e + 127, i.e. f * 2^-(e - 1023).
+// exponent field ev - e + 127, i.e. f * 2^-(e - 1023).  Any 1 <= e <= 2046
+// works: for e < 127 the unsigned difference wraps and the signed value of
+// (magnitude - offset) in split() is still exact.
 __device__ __forceinline__ uint32_t in_offset(uint32_t e) { return (e - 127u) << 20; }
 
 // Split v * 2^-s into hi (its leading 24 significant bits, truncated) and lo
@@ -100,10 +102,61 @@ __device__ __forceinline__ double join(float h, float l, uint32_t off) {
   return __dadd_rn(scaled_double(h, off), scaled_double(l, off));
 }
 
+// Streaming store of v to *p where pred holds, as one predicated instruction:
+// an unrolled output loop stays one basic block (a branch per row would cut
+// it into blocks whose latency chains cannot overlap).
+__device__ __forceinline__ void store_cs_if(double* p, double v, bool pred) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.cs.f64 [%0], %1;\n\t}" ::"l"(p), "d"(v),
+      "r"((int)pred));
+}
+
 // Exponent window (fp64 biased exponent field of a system's largest entry) of
 // the scaled double-float paths; Cahn–Hilliard also needs 2^(2s) (the factor of
 // its cubic) in float range at the top.  Systems outside go to native fp64.
 constexpr uint32_t kEMin = 1023 - 860, kEMax = 1023 + 1000, kEMaxCH = 1023 + 50;
+
+// 2^d as a double, exact, for -1022 <= d <= 1023
+__device__ __forceinline__ double pow2i(int d) { return __hiloint2double((1023 + d) << 20, 0); }
+
+// What a linear solve does with one system, from the largest magnitude word of
+// its entries (fp64 high word without sign, with bit 0 set if any low word is
+// nonzero, so that only an all-zero system gives 0):
+//   fast  largest exponent e in the window: converted in with 2^-s and out
+//         with 2^s, s = e - 1023;
+//   zero  every entry +-0: the solution is zero (an in-place solve has
+//         nothing to store);
+//   resc  a finite largest entry above the window: converted in the same way
+//         (the integer split is exact for normal entries, and subnormal ones
+//         are then far below the largest and flushed), but converted out with
+//         the window's top eo (the join needs its outputs' exponents in range)
+//         and then multiplied by 2^(e - eo) in fp64;
+//   otherwise (largest entry below the window, where subnormal entries could
+//         matter and the split would misread them, or an inf or NaN entry)
+//         the kernel falls back to native fp64.
+struct SysClass {
+  uint32_t ein, eo;   // exponent fields of the conversions in and out
+  int d;              // rescaled systems: e - eo
+  bool fast, zero, resc;
+};
+__device__ __forceinline__ SysClass classify(uint32_t smax, uint32_t emin, uint32_t emax) {
+  SysClass r;
+  const uint32_t e = smax >> 20;
+  r.zero = smax == 0u;
+  r.fast = e >= emin && e <= emax;
+  r.resc = e > emax && e != 0x7FFu;
+  r.ein = (r.fast || r.resc) ? e : 1023u;
+  r.eo = r.fast ? e : (r.resc ? emax : 1023u);
+  r.d = (int)r.ein - (int)r.eo;
+  return r;
+}
+
+// One term of the magnitude word above for two entries: the larger high-word
+// magnitude, and the OR of both low words folded into nz.
+__device__ __forceinline__ uint32_t mag_pair(double u, double v, uint32_t& nz) {
+  nz |= (uint32_t)__double2loint(u) | (uint32_t)__double2loint(v);
+  return max(mag_bits(u), mag_bits(v));
+}
 
 // 2^(2s) as a float for the system exponent field e (s = e - 1023); zero when
 // the cubic is below 2^-126 of the state and cannot matter

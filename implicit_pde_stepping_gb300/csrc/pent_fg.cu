@@ -19,9 +19,13 @@
 // conversions); the plan bounds every intermediate value of the solve for
 // such a right-hand side (rows sums of |L^-1 R|, |A^-1| and the chunk-local
 // |R^-1|) and picks the grid from that bound.  The scale also gives the
-// kernel the full fp64 exponent range: only systems whose largest entry is
-// zero, subnormal, non-finite or outside [2^-860, 2^1001) are left to a
-// native fp64 solve of the column by one thread.
+// kernel the full fp64 exponent range: all-zero systems are left as they are
+// (zero is their solution), systems
+// whose largest entry is at or above 2^1001 are converted out at 2^1000 and
+// scaled back in fp64, and only systems whose largest entry is below 2^-860
+// or not finite are left to a native fp64 solve of the column by one thread
+// (a sequential fp64 sweep: on GB300 it takes about as long as the whole
+// batch's solve, so it is kept for those inputs alone).
 //
 // Correction terms whose responses are below 2^-24 over a whole 8-row group
 // of every chunk go to the low word with one FMA, and those below 2^-56 are
@@ -159,17 +163,25 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         if (threadIdx.x == 0) atomicExch(g.err, 1);
         return;
       }
+      // Chunks start 2 KB apart, so the four chunks of a warp would read the
+      // same 16 banks; odd chunks read each pair of rows in swapped order,
+      // which puts them on the other 16 banks.
       const double* tr = tile + (size_t)row0 * SB + sys;
+      const int sw = c & 1;
 #pragma unroll
-      for (int j = 0; j < L; ++j) fv[j] = tr[j * SB];
+      for (int j = 0; j < L; j += 2) {
+        const double u0 = tr[(j + sw) * SB], u1 = tr[(j + 1 - sw) * SB];
+        fv[j] = sw ? u1 : u0;
+        fv[j + 1] = sw ? u0 : u1;
+      }
     } else {
 #pragma unroll
       for (int j = 0; j < L; ++j) fv[j] = (act && row0 + j < M) ? p[j * ld] : 0.0;
     }
-    uint32_t mx = 0u;
+    uint32_t mx = 0u, nz = 0u;
 #pragma unroll
-    for (int j = 0; j < L; ++j) mx = max(mx, fg::mag_bits(fv[j]));
-    atomicMax(&smax[sys], mx);
+    for (int j = 0; j < L; j += 2) mx = max(mx, fg::mag_pair(fv[j], fv[j + 1], nz));
+    atomicMax(&smax[sys], mx | (nz != 0u ? 1u : 0u));
     __syncthreads();                                     // tile read, smax complete
     if constexpr (TMA) {
       // the next block's tile streams in behind the rest of this block
@@ -179,11 +191,11 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
           tma::load_2d(tile + (size_t)y * SB, &fmap, (blk + gridDim.x) * SB, y, &bar);
       }
     }
-    const uint32_t esys = smax[sys] >> 20;
-    const bool fast = esys >= kEMin && esys <= kEMax;
-    const bool native = act && !fast;
-    const uint32_t eo = fast ? esys : 1023u;
-    const uint32_t ioff = fg::in_offset(eo), ooff = fg::out_offset(eo);
+    const fg::SysClass sc = fg::classify(smax[sys], kEMin, kEMax);
+    const bool native = act && !sc.fast && !sc.zero && !sc.resc;
+    const uint32_t ioff = fg::in_offset(sc.ein), ooff = fg::out_offset(sc.eo);
+    const bool zero = sc.zero, resc = sc.resc;
+    const int dres = sc.d;
 
     // local forward sweep, zero incoming state: g_j = r f_j + P g_{j-2} + Q g_{j-1}
     float va[L], vl[L];
@@ -259,7 +271,8 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     }
 
     // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1, joined to fp64 and stored
-    const bool store = act && !native;
+    // an all-zero system already holds its solution (the solve is in place)
+    const bool store = act && !native && !zero;
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
       const bool mfull = gi < g.gm_full, mlow = !mfull && gi < g.gm_none;
@@ -284,11 +297,20 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
           fg::madd_low(l, c4.x, T0.h);
           fg::madd_low(l, c4.z, T1.h);
         }
-        if (store && row0 + j < M) __stcs(p + j * ld, fg::join(__fsub_rn(a, B), l, ooff));
+        fg::store_cs_if(p + j * ld, fg::join(__fsub_rn(a, B), l, ooff), store && row0 + j < M);
       }
     }
-    // systems outside the scaled path: one thread solves the column in fp64
-    // (its f is untouched: nothing of this system has been stored)
+    // rescaled systems: their stored rows are x * 2^(eo - e), scaled back here
+    // (this thread's own stores, re-read in program order)
+    if (act && resc) {
+      const double post = fg::pow2i(dres);
+      asm volatile("" ::: "memory");
+#pragma unroll
+      for (int j = 0; j < L; ++j)
+        if (row0 + j < M) p[j * ld] *= post;
+    }
+    // systems whose largest entry is subnormal or not finite: one thread solves
+    // the column in fp64 (its f is untouched: nothing of it has been stored)
     if (native && c == 0) native_solve_col(NativeTabs{g.coef64, g.tail64, nullptr}, g.X + s, M, (size_t)ld, 0);
   }
 }

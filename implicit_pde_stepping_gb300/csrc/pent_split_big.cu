@@ -72,7 +72,10 @@ __device__ __forceinline__ bool big_fast(uint32_t e) { return e >= fg::kEMin && 
 
 // largest |entry| of each system (rows 0..N-1): SPW systems per warp row, the
 // rows strided over the grid; lanes of one system, then the CTA's warps reduce,
-// and one atomic per CTA and system combines into smax[s] (zeroed before)
+// and one atomic per CTA and system combines into smax[s] (zeroed before).
+// The word is the largest fp64 high word without sign, with bit 0 set if any
+// low word is nonzero: 0 marks an all-zero system, which the other kernels
+// leave untouched (zero is its solution, in place).
 template <int SPW>
 __global__ void __launch_bounds__(kBigThreads)
     k_big_scale(const double* __restrict__ X, unsigned* __restrict__ smax, int rows, int batch) {
@@ -81,14 +84,18 @@ __global__ void __launch_bounds__(kBigThreads)
   __shared__ unsigned red[NW][SPW];
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   const int s = blockIdx.x * SPW + lane % SPW;
-  unsigned mx = 0u;
+  unsigned mx = 0u, nz = 0u;
   if (s < batch) {
     const long long ld = batch;
     const int stride = gridDim.y * NW * RPW;
 #pragma unroll 8
-    for (int i = (blockIdx.y * NW + w) * RPW + lane / SPW; i < rows; i += stride)
-      mx = max(mx, fg::mag_bits(X[(long long)i * ld + s]));
+    for (int i = (blockIdx.y * NW + w) * RPW + lane / SPW; i < rows; i += stride) {
+      const double v = X[(long long)i * ld + s];
+      mx = max(mx, fg::mag_bits(v));
+      nz |= (uint32_t)__double2loint(v);
+    }
   }
+  mx |= nz != 0u ? 1u : 0u;                       // only an all-zero system ends at 0
 #pragma unroll
   for (int o = SPW; o < 32; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (lane < SPW) red[w][lane] = mx;
@@ -110,6 +117,7 @@ __global__ void __launch_bounds__(kBigThreads, 2)
   int s, c;
   place<SPW>(s, c);
   if (s >= batch || c >= P) return;
+  if (smax[s] == 0u) return;                      // all zero: already solved
   const uint32_t e = smax[s] >> 20;
   if (!big_fast(e)) return;                       // solved natively by k_big_fix
   const uint32_t off = fg::in_offset(e);
@@ -232,6 +240,7 @@ __global__ void __launch_bounds__(kBigThreads)
                  int M, int P, int batch, int2 dup) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
+  if (smax[s] == 0u) return;                      // all zero: already solved
   const uint32_t e = smax[s] >> 20;
   if (!big_fast(e)) return;                       // solved natively by k_big_fix
   const long long ld = batch;
@@ -271,6 +280,7 @@ __global__ void __launch_bounds__(kBigThreads)
   place<SPW>(s, c);
   if (s >= batch || c >= P) return;
   const long long ld = batch;
+  if (smax[s] == 0u) return;                      // all zero: already solved
   const uint32_t e = smax[s] >> 20;
   if (!big_fast(e)) {                             // the whole column, natively, by one thread
     if (c == 0) native_solve_col(nt, X + s, M, (size_t)ld, CYC ? 1 : 0);

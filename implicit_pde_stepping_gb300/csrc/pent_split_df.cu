@@ -159,25 +159,34 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     // off = (e - 127) << 20 for the system's exponent field e: the rebias of
     // both conversions (f 2^-s in, x 2^s out); e = (off >> 20) + 127
     uint32_t off = 0u;
-    bool native = false;
+    bool native = false, keep = false;
     float q = 1.f;
     {
-      uint32_t mx = 0u;
+      // magnitude word: largest high word, bit 0 set if any low word is nonzero
+      uint32_t mx = 0u, nz = 0u;
 #pragma unroll
       for (int j = 0; j < L; ++j)
-        if (act && row0 + j < M) mx = max(mx, fg::mag_bits(p[j * ld]));
+        if (act && row0 + j < M) {
+          const double v = p[j * ld];
+          mx = max(mx, fg::mag_bits(v));
+          nz |= (uint32_t)__double2loint(v);
+        }
       if (CYC && c == 0 && act) {
-        mx = max(mx, fg::mag_bits(X[(long long)M * ld + s]));
-        mx = max(mx, fg::mag_bits(X[(long long)(M + 1) * ld + s]));
+        const double v0 = X[(long long)M * ld + s], v1 = X[(long long)(M + 1) * ld + s];
+        mx = max(mx, fg::mag_pair(v0, v1, nz));
       }
-      atomicMax(&smax[sys], mx);
+      atomicMax(&smax[sys], mx | (nz != 0u ? 1u : 0u));
       __syncthreads();
       const uint32_t e = smax[sys] >> 20;
       const bool fast = e >= kEMin && e <= (CH ? kEMaxCH : kEMax);
-      native = act && !fast;
+      // an all-zero state is its own result (solve, Crank–Nicolson and
+      // Cahn–Hilliard all map 0 to 0, in place): nothing is stored
+      keep = smax[sys] == 0u;
+      native = act && !fast && !keep;
       off = fg::in_offset(fast ? e : 1023u);
       if constexpr (CH) q = cubic_scale(fast ? e : 1023u);
     }
+    const bool store = act && !native && !keep;
     // f * 2^-s as a pair
     auto sdf = [&](double v) {
       float h, lo;
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         const double u1 = gextra[2] * (ft0 - r0) + gextra[3] * (ft1 - r1);
         xc[4] = u0;
         xc[5] = u1;
-        if (act && !native) {
+        if (store) {
           X[(long long)M * ld + s] = (CN ? 2.0 * u0 - ft0 : u0) * pow2_pos((off >> 20) + 127u);
           X[(long long)(M + 1) * ld + s] = (CN ? 2.0 * u1 - ft1 : u1) * pow2_pos((off >> 20) + 127u);
         }
@@ -425,7 +434,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
           x = df::axpy(x, D2{c4.x, c4.y}, T0);
           x = df::axpy(x, D2{c4.z, c4.w}, T1);
           if constexpr (CN) x = df::add(D2{2.f * x.h, 2.f * x.l}, df::neg(sdf(cold[u])));
-          if (act && !native && row0 + j < M) __stcs(p + j * ld, fg::join(x.h, x.l, off));
+          fg::store_cs_if(p + j * ld, fg::join(x.h, x.l, off), store && row0 + j < M);
         }
       }
     }

@@ -152,20 +152,27 @@ __global__ void __launch_bounds__(MAXT, 1)
     // ---- the system's scale: its largest |C^0| (one pass over the rows; the
     // loads below find them in cache)
     {
-      uint32_t mx = 0u;
+      // magnitude word: largest high word, bit 0 set if any low word is nonzero
+      uint32_t mx = 0u, nz = 0u;
 #pragma unroll
       for (int j = 0; j < L; ++j)
-        if (act && row0 + j < M) mx = max(mx, fg::mag_bits(p[j * ld]));
+        if (act && row0 + j < M) {
+          const double v = p[j * ld];
+          mx = max(mx, fg::mag_bits(v));
+          nz |= (uint32_t)__double2loint(v);
+        }
       if (c == 0 && act) {
-        mx = max(mx, fg::mag_bits(X[(long long)M * ld + s]));
-        mx = max(mx, fg::mag_bits(X[(long long)(M + 1) * ld + s]));
+        const double v0 = X[(long long)M * ld + s], v1 = X[(long long)(M + 1) * ld + s];
+        mx = max(mx, fg::mag_pair(v0, v1, nz));
       }
-      atomicMax(&smax[sys], mx);
+      atomicMax(&smax[sys], mx | (nz != 0u ? 1u : 0u));
     }
     __syncthreads();
     const uint32_t emax = smax[sys] >> 20;
     const bool fast = emax >= fg::kEMin && emax <= (CH ? fg::kEMaxCH : fg::kEMax);
-    const bool native = act && !fast;
+    // an all-zero state stays zero under every step: nothing to store
+    const bool keep = smax[sys] == 0u;
+    const bool native = act && !fast && !keep;
     const uint32_t esys = fast ? emax : 1023u;
     const uint32_t ioff = fg::in_offset(esys), ooff = fg::out_offset(esys);
     const float q = fg::cubic_scale(esys);
@@ -416,11 +423,11 @@ __global__ void __launch_bounds__(MAXT, 1)
     if (c == 0) grow = fmaxf(grow, fmaxf(fabsf(unpack(xc[6]).h), fabsf(unpack(xc[7]).h)));
     if (!(grow <= 256.f)) atomicOr(&sgrow[sys], 1u);      // also catches NaN
     __syncthreads();
-    const bool nat = native || (act && sgrow[sys] != 0u);
+    const bool nat = native || (act && !keep && sgrow[sys] != 0u);
 #pragma unroll
     for (int j = 0; j < L; ++j)
-      if (act && !nat && row0 + j < M) __stcs(p + j * ld, fg::join(v[j].h, v[j].l, ooff));
-    if (c == 0 && act && !nat) {
+      if (act && !nat && !keep && row0 + j < M) __stcs(p + j * ld, fg::join(v[j].h, v[j].l, ooff));
+    if (c == 0 && act && !nat && !keep) {
       const D2 t0 = unpack(xc[6]), t1 = unpack(xc[7]);
       X[(long long)M * ld + s] = fg::join(t0.h, t0.l, ooff);
       X[(long long)(M + 1) * ld + s] = fg::join(t1.h, t1.l, ooff);
