@@ -273,31 +273,48 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1, joined to fp64 and stored
     // an all-zero system already holds its solution (the solve is in place)
     const bool store = act && !native && !zero;
+    // Groups where both terms are full (the middle of every chunk) run as
+    // straight-line code; the others test the term kinds per row.
 #pragma unroll
     for (int gi = 0; gi < NG; ++gi) {
       const bool mfull = gi < g.gm_full, mlow = !mfull && gi < g.gm_none;
       const bool kfull = gi >= g.gk_full, klow = !kfull && gi >= g.gk_none;
+      if (mfull && kfull) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int j = gi * 8 + u;
-        float a = va[j], l = vl[j];
-        const float4 c3 = ctb[j * K4 + 3];
-        const float4 c4 = ctb[j * K4 + 4];
-        if (mfull) {
+        for (int u = 0; u < 8; ++u) {
+          const int j = gi * 8 + u;
+          float a = va[j], l = vl[j];
+          const float4 c3 = ctb[j * K4 + 3];
+          const float4 c4 = ctb[j * K4 + 4];
           fg::madd(a, l, c3.x, c3.y, S0.h, S0.l);
           fg::madd(a, l, c3.z, c3.w, S1.h, S1.l);
-        } else if (mlow) {
-          fg::madd_low(l, c3.x, S0.h);
-          fg::madd_low(l, c3.z, S1.h);
-        }
-        if (kfull) {
           fg::madd(a, l, c4.x, c4.y, T0.h, T0.l);
           fg::madd(a, l, c4.z, c4.w, T1.h, T1.l);
-        } else if (klow) {
-          fg::madd_low(l, c4.x, T0.h);
-          fg::madd_low(l, c4.z, T1.h);
+          fg::store_cs_if(p + j * ld, fg::join(__fsub_rn(a, B), l, ooff), store && row0 + j < M);
         }
-        fg::store_cs_if(p + j * ld, fg::join(__fsub_rn(a, B), l, ooff), store && row0 + j < M);
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = gi * 8 + u;
+          float a = va[j], l = vl[j];
+          const float4 c3 = ctb[j * K4 + 3];
+          const float4 c4 = ctb[j * K4 + 4];
+          if (mfull) {
+            fg::madd(a, l, c3.x, c3.y, S0.h, S0.l);
+            fg::madd(a, l, c3.z, c3.w, S1.h, S1.l);
+          } else if (mlow) {
+            fg::madd_low(l, c3.x, S0.h);
+            fg::madd_low(l, c3.z, S1.h);
+          }
+          if (kfull) {
+            fg::madd(a, l, c4.x, c4.y, T0.h, T0.l);
+            fg::madd(a, l, c4.z, c4.w, T1.h, T1.l);
+          } else if (klow) {
+            fg::madd_low(l, c4.x, T0.h);
+            fg::madd_low(l, c4.z, T1.h);
+          }
+          fg::store_cs_if(p + j * ld, fg::join(__fsub_rn(a, B), l, ooff), store && row0 + j < M);
+        }
       }
     }
     // rescaled systems: their stored rows are x * 2^(eo - e), scaled back here
