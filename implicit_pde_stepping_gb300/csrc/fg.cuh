@@ -72,7 +72,7 @@ __device__ __forceinline__ void split(double v, uint32_t off, float& h, float& l
   const uint32_t hw = (uint32_t)__double2hiint(v);
   const uint32_t lw = (uint32_t)__double2loint(v);
   const uint32_t sign = hw & 0x80000000u;
-  int32_t t = (int32_t)((hw & 0x7FFFFFFFu) - off);
+  int32_t t = (int32_t)(hw - sign - off);   // magnitude word minus the rebias
   t = max(t, 0);
   const uint32_t hb = __funnelshift_l(lw, (uint32_t)t, 3) | sign;
   uint32_t eb = hb & 0x7F800000u;

@@ -36,6 +36,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstring>
+#include <type_traits>
 #include <vector>
 
 #include "cp_async.cuh"
@@ -273,43 +274,73 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1, joined to fp64 and stored
     // an all-zero system already holds its solution (the solve is in place)
     const bool store = act && !native && !zero;
-    // Groups where both terms are full (the middle of every chunk) run as
-    // straight-line code; the others test the term kinds per row.
+    // One 8-row group of corrections, join and store, with the kinds of its M
+    // and K terms fixed (1 low word, 2 full): straight-line code.  The kinds
+    // the plans produce are full/full in the middle of a chunk and full/low,
+    // low/full near its ends; other groups test the kinds per row.
+    auto group = [&](const int j0, auto mkind, auto kkind) {
+      constexpr int MK = decltype(mkind)::value, KK = decltype(kkind)::value;
 #pragma unroll
-    for (int gi = 0; gi < NG; ++gi) {
-      const bool mfull = gi < g.gm_full, mlow = !mfull && gi < g.gm_none;
-      const bool kfull = gi >= g.gk_full, klow = !kfull && gi >= g.gk_none;
-      if (mfull && kfull) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = gi * 8 + u;
-          float a = va[j], l = vl[j];
+      for (int u = 0; u < 8; ++u) {
+        const int j = j0 + u;
+        float a = va[j], l = vl[j];
+        if constexpr (MK > 0) {
           const float4 c3 = ctb[j * K4 + 3];
-          const float4 c4 = ctb[j * K4 + 4];
-          fg::madd(a, l, c3.x, c3.y, S0.h, S0.l);
-          fg::madd(a, l, c3.z, c3.w, S1.h, S1.l);
-          fg::madd(a, l, c4.x, c4.y, T0.h, T0.l);
-          fg::madd(a, l, c4.z, c4.w, T1.h, T1.l);
-          fg::store_cs_if(p + j * ld, fg::join(__fsub_rn(a, B), l, ooff), store && row0 + j < M);
-        }
-      } else {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int j = gi * 8 + u;
-          float a = va[j], l = vl[j];
-          const float4 c3 = ctb[j * K4 + 3];
-          const float4 c4 = ctb[j * K4 + 4];
-          if (mfull) {
+          if constexpr (MK == 2) {
             fg::madd(a, l, c3.x, c3.y, S0.h, S0.l);
             fg::madd(a, l, c3.z, c3.w, S1.h, S1.l);
-          } else if (mlow) {
+          } else {
             fg::madd_low(l, c3.x, S0.h);
             fg::madd_low(l, c3.z, S1.h);
           }
-          if (kfull) {
+        }
+        if constexpr (KK > 0) {
+          const float4 c4 = ctb[j * K4 + 4];
+          if constexpr (KK == 2) {
             fg::madd(a, l, c4.x, c4.y, T0.h, T0.l);
             fg::madd(a, l, c4.z, c4.w, T1.h, T1.l);
-          } else if (klow) {
+          } else {
+            fg::madd_low(l, c4.x, T0.h);
+            fg::madd_low(l, c4.z, T1.h);
+          }
+        }
+        fg::store_cs_if(p + j * ld, fg::join(__fsub_rn(a, B), l, ooff), store && row0 + j < M);
+      }
+    };
+    using K1 = std::integral_constant<int, 1>;
+    using K2 = std::integral_constant<int, 2>;
+    // one test per group picks its kinds (0 none, 1 low word, 2 full; the plan
+    // fixed them per 8-row group)
+#pragma unroll
+    for (int gi = 0; gi < NG; ++gi) {
+      const int mk = gi < g.gm_full ? 2 : (gi < g.gm_none ? 1 : 0);
+      const int kk = gi >= g.gk_full ? 2 : (gi >= g.gk_none ? 1 : 0);
+      const int j0 = gi * 8;
+      if (mk == 2 && kk == 2) {
+        group(j0, K2{}, K2{});
+      } else if (mk == 2 && kk == 1) {
+        group(j0, K2{}, K1{});
+      } else if (mk == 1 && kk == 2) {
+        group(j0, K1{}, K2{});
+      } else {
+        // other kinds: tested per row
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int j = j0 + u;
+          float a = va[j], l = vl[j];
+          const float4 c3 = ctb[j * K4 + 3];
+          const float4 c4 = ctb[j * K4 + 4];
+          if (mk == 2) {
+            fg::madd(a, l, c3.x, c3.y, S0.h, S0.l);
+            fg::madd(a, l, c3.z, c3.w, S1.h, S1.l);
+          } else if (mk == 1) {
+            fg::madd_low(l, c3.x, S0.h);
+            fg::madd_low(l, c3.z, S1.h);
+          }
+          if (kk == 2) {
+            fg::madd(a, l, c4.x, c4.y, T0.h, T0.l);
+            fg::madd(a, l, c4.z, c4.w, T1.h, T1.l);
+          } else if (kk == 1) {
             fg::madd_low(l, c4.x, T0.h);
             fg::madd_low(l, c4.z, T1.h);
           }
