@@ -102,6 +102,34 @@ __device__ __forceinline__ double join(float h, float l, uint32_t off) {
   return __dadd_rn(scaled_double(h, off), scaled_double(l, off));
 }
 
+// (h + l) * 2^s as a double without the fp64 pipe, for h and l as join()
+// takes them.  s1 = h + l rounded toward zero, so that e1 = (h + l) - s1 has the
+// sign of s1 and |e1| <= one float ulp of s1; the double of s1 comes from its
+// bits as in scaled_double(); e1, rounded to a multiple of 2^8 double ulps of
+// s1 (at most 2^21 of them, by the magic-number float add), is added to its
+// magnitude bits (carrying into the exponent where the sum reaches the next
+// binade).  Error: at most 2^-45 of |s1| beyond the rounding of e1's own two
+// float adds (2^-24 of |e1|), against 2^-53 for join().  Eleven integer and
+// five FP32 operations: a kernel that joins many outputs can split them
+// between this and join() to balance the FP32/integer lanes against GB300's
+// slow fp64 pipe.
+__device__ __forceinline__ double join_int(float h, float l, uint32_t off) {
+  const float s1 = __fadd_rz(h, l);
+  const float e1 = __fadd_rn(__fsub_rn(h, s1), l);
+  const uint32_t b = __float_as_uint(s1);
+  const uint32_t sh = (uint32_t)((int32_t)b >> 3);
+  const uint32_t hi = sh + off - (sh & 0x70000000u);
+  // 2^(171 - E) for the float exponent field E of s1 (E >= 44: smaller s1 are
+  // below 2^-83 of the system's largest value, where e1 cannot matter)
+  const uint32_t es = max(b & 0x7F800000u, 44u << 23);
+  const float fac = __uint_as_float((298u << 23) - es);
+  const float t = __fadd_rn(__fmul_rn(e1, fac), 12582912.0f);      // + 1.5 * 2^23: round to an integer
+  const unsigned long long n = (unsigned long long)abs((int)__float_as_uint(t) - 0x4B400000);
+  const unsigned long long bits =
+      (((unsigned long long)hi << 32) | (unsigned long long)(b << 29)) + (n << 8);
+  return __longlong_as_double((long long)bits);
+}
+
 // Streaming store of v to *p where pred holds, as one predicated instruction:
 // an unrolled output loop stays one basic block (a branch per row would cut
 // it into blocks whose latency chains cannot overlap).

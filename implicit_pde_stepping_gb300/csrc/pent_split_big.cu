@@ -324,7 +324,9 @@ __global__ void __launch_bounds__(kBigThreads)
         x = df::axpy(x, D2{c1.z, c1.w}, X0);
         x = df::axpy(x, D2{c5.x, c5.y}, X1);
       }
-      if (row0 + j < M) __stcs(p + j * ld, fg::join(x.h, x.l, off));
+      // three rows in four join through integers, off the slow fp64 pipe
+      const double xo = (j & 3) != 0 ? fg::join_int(x.h, x.l, off) : fg::join(x.h, x.l, off);
+      fg::store_cs_if(p + j * ld, xo, row0 + j < M);
     }
   }
 }

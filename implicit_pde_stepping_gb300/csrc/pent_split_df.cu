@@ -434,7 +434,9 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
           x = df::axpy(x, D2{c4.x, c4.y}, T0);
           x = df::axpy(x, D2{c4.z, c4.w}, T1);
           if constexpr (CN) x = df::add(D2{2.f * x.h, 2.f * x.l}, df::neg(sdf(cold[u])));
-          fg::store_cs_if(p + j * ld, fg::join(x.h, x.l, off), store && row0 + j < M);
+          // three rows in four join through integers, off the slow fp64 pipe
+          const double xo = (j & 3) != 0 ? fg::join_int(x.h, x.l, off) : fg::join(x.h, x.l, off);
+          fg::store_cs_if(p + j * ld, xo, store && row0 + j < M);
         }
       }
     }
