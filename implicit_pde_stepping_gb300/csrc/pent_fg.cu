@@ -9,10 +9,9 @@
 //   1. each chunk runs both sweeps locally with zero boundary values -> x';
 //   2. the chunk boundary states s_c (g entering) and t_c (x leaving) follow
 //      from the T nearest chunks' end values (the plan kept every coupling
-//      above 2^-64);
+//      above 2^-64), on the same grid;
 //   3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1, joined to fp64 and stored.
-// What differs is the arithmetic of steps 1 and 3, which hold all but a few
-// operations per point: values live on a per-system fixed grid (fg.cuh), so a
+// What differs is the arithmetic of all three steps: values live on a per-system fixed grid (fg.cuh), so a
 // multiply-add takes six FP32 instructions instead of twelve.  The grid needs
 // a scale, so every system is first scaled by the power of two that brings
 // its largest |f| into [1, 2) (an exact operation folded into the fp64
@@ -77,12 +76,6 @@ __host__ __device__ __forceinline__ int row_slot(int c, int lo, int hi) {
 
 // Bytes of the f tile: RS rows of SB systems (fp64).
 __host__ __device__ __forceinline__ size_t tile_bytes(int RS, int SB) { return (size_t)RS * SB * sizeof(double); }
-
-// y += A x for a row-major 2x2 A of double-float pairs
-__device__ __forceinline__ void mv2d(const float2* A, D2 x0, D2 x1, D2& y0, D2& y1) {
-  y0 = df::sum3(y0, D2{A[0].x, A[0].y}, x0, D2{A[1].x, A[1].y}, x1);
-  y1 = df::sum3(y1, D2{A[2].x, A[2].y}, x0, D2{A[3].x, A[3].y}, x1);
-}
 
 template <int L, int SB, int MAXT, bool TMA>
 __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
@@ -241,34 +234,61 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
         x1l = l;
       }
     }
-    const D2 xs0{__fsub_rn(va[0], B), vl[0]}, xs1{__fsub_rn(va[1], B), vl[1]};   // x'_start(c)
 
-    // ---- 2. boundary states (truncated parallel scan in double-float)
+    // ---- 2. boundary states (truncated parallel scan), on the solve's grid: the
+    // plan's bound covers them, and a fixed-grid multiply-add has a two-FMA
+    // critical path where a TwoSum sum of products has about ten
     __syncthreads();                                     // e_c published, smax read
     if (c == 0) smax[sys] = 0u;                          // for the next block (ordered by the next barrier)
     D2 S0{0.f, 0.f}, S1{0.f, 0.f}, T0{0.f, 0.f}, T1{0.f, 0.f};
     {
       const float2* E = sE + (size_t)sys * P * 2;
+      float s0a = B, s0l = 0.f, s1a = B, s1l = 0.f;      // biased accumulators
       for (int k = 1; k <= T && k <= c; ++k) {           // s_c = sum_k A_{c,k} e_{c-k}
-        const D2 ea{E[2 * (c - k)].x, E[2 * (c - k)].y}, eb{E[2 * (c - k) + 1].x, E[2 * (c - k) + 1].y};
-        if (k == 1) { S0 = df::add(S0, ea); S1 = df::add(S1, eb); }
-        else mv2d(ct + 12 + 4 * (k - 2), ea, eb, S0, S1);
+        const float2 ea = E[2 * (c - k)], eb = E[2 * (c - k) + 1];
+        if (k == 1) {
+          s0a = __fadd_rn(s0a, ea.x); s0l = __fadd_rn(s0l, ea.y);
+          s1a = __fadd_rn(s1a, eb.x); s1l = __fadd_rn(s1l, eb.y);
+        } else {
+          const float2* A = ct + 12 + 4 * (k - 2);
+          fg::madd(s0a, s0l, A[0].x, A[0].y, ea.x, ea.y);
+          fg::madd(s0a, s0l, A[1].x, A[1].y, eb.x, eb.y);
+          fg::madd(s1a, s1l, A[2].x, A[2].y, ea.x, ea.y);
+          fg::madd(s1a, s1l, A[3].x, A[3].y, eb.x, eb.y);
+        }
       }
-      D2 w0 = xs0, w1 = xs1;
-      mv2d(ct + 4, S0, S1, w0, w1);                      // w_c = x'_start + Mst_c s_c
+      S0 = D2{__fsub_rn(s0a, B), s0l};
+      S1 = D2{__fsub_rn(s1a, B), s1l};
+      // w_c = x'_start + Mst_c s_c
+      float w0a = va[0], w0l = vl[0], w1a = va[1], w1l = vl[1];
+      const float2* Ms = ct + 4;
+      fg::madd(w0a, w0l, Ms[0].x, Ms[0].y, S0.h, S0.l);
+      fg::madd(w0a, w0l, Ms[1].x, Ms[1].y, S1.h, S1.l);
+      fg::madd(w1a, w1l, Ms[2].x, Ms[2].y, S0.h, S0.l);
+      fg::madd(w1a, w1l, Ms[3].x, Ms[3].y, S1.h, S1.l);
       float2* wo = sW + ((size_t)sys * P + c) * 2;
-      wo[0] = make_float2(w0.h, w0.l);
-      wo[1] = make_float2(w1.h, w1.l);
+      wo[0] = make_float2(__fsub_rn(w0a, B), w0l);
+      wo[1] = make_float2(__fsub_rn(w1a, B), w1l);
     }
     __syncthreads();                                     // w_c published
     {
       const float2* Wv = sW + (size_t)sys * P * 2;
+      float t0a = B, t0l = 0.f, t1a = B, t1l = 0.f;
       for (int k = 0; k < T && c + 1 + k < P; ++k) {     // t_c = sum_k B_{c,k} w_{c+1+k}
-        const D2 wa{Wv[2 * (c + 1 + k)].x, Wv[2 * (c + 1 + k)].y};
-        const D2 wb{Wv[2 * (c + 1 + k) + 1].x, Wv[2 * (c + 1 + k) + 1].y};
-        if (k == 0) { T0 = df::add(T0, wa); T1 = df::add(T1, wb); }
-        else mv2d(ct + 24 + 4 * (k - 1), wa, wb, T0, T1);
+        const float2 wa = Wv[2 * (c + 1 + k)], wb = Wv[2 * (c + 1 + k) + 1];
+        if (k == 0) {
+          t0a = __fadd_rn(t0a, wa.x); t0l = __fadd_rn(t0l, wa.y);
+          t1a = __fadd_rn(t1a, wb.x); t1l = __fadd_rn(t1l, wb.y);
+        } else {
+          const float2* Bk = ct + 24 + 4 * (k - 1);
+          fg::madd(t0a, t0l, Bk[0].x, Bk[0].y, wa.x, wa.y);
+          fg::madd(t0a, t0l, Bk[1].x, Bk[1].y, wb.x, wb.y);
+          fg::madd(t1a, t1l, Bk[2].x, Bk[2].y, wa.x, wa.y);
+          fg::madd(t1a, t1l, Bk[3].x, Bk[3].y, wb.x, wb.y);
+        }
       }
+      T0 = D2{__fsub_rn(t0a, B), t0l};
+      T1 = D2{__fsub_rn(t1a, B), t1l};
     }
 
     // ---- 3. x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1, joined to fp64 and stored
