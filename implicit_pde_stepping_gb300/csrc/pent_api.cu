@@ -86,6 +86,22 @@ pent_variant resolve(const pent_plan_s& p, int batch) {
   return PENT_VARIANT_THREAD;
 }
 
+// The twisted variant's tables, made once, synchronously, on the plan's
+// device (its bands and plan-time scratch live in the arena).
+cudaError_t ensure_twisted(pent_plan_s& p) {
+  if (!p.twist_eligible || p.twist_built) return cudaSuccess;
+  int tstatus = 0;
+  cudaError_t e = factor_twisted(p.bands, p.N, p.cyclic, p.m, p.twtab, p.twist, p.work_area, p.status_area, 0);
+  if (e == cudaSuccess) e = cudaMemcpy(&tstatus, p.status_area, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return e;
+  }
+  p.twist_ok = (tstatus == 0);
+  p.twist_built = 1;
+  return cudaSuccess;
+}
+
 bool variant_exists(const pent_plan_s& p, pent_variant v) {
   switch (v) {
     case PENT_VARIANT_AUTO:
@@ -302,19 +318,14 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
     pent_destroy(p);
     return PENT_ERR_ZERO_PIVOT;
   }
-  // twisted double-float tables (fp64 plans whose sweep fits the kernel)
+  // twisted double-float tables (fp64 plans whose sweep fits the kernel): made
+  // when that variant is first selected, since the default path never uses them
   cudaDeviceGetAttribute(&p->num_sms, cudaDevAttrMultiProcessorCount, p->device);
+  p->work_area = d_work;
+  p->status_area = d_status;
   if (dtype == PENT_F64 && p->M >= 8 && p->M <= kMaxTwistedRows) {
     p->m = p->M / 2;
-    int tstatus = 0;
-    e = factor_twisted(d_bands, N, cyclic, p->m, p->twtab, p->twist, d_work, d_status, 0);
-    if (e == cudaSuccess) e = cudaMemcpy(&tstatus, d_status, sizeof(int), cudaMemcpyDeviceToHost);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      pent_destroy(p);
-      return from_cuda(e);
-    }
-    p->twist_ok = (tstatus == 0);
+    p->twist_eligible = 1;
   }
   // partitioned double-float tables
   {
@@ -401,6 +412,10 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
 
 pent_status pent_set_variant(pent_plan p, pent_variant v) {
   if (!p) return PENT_ERR_INVALID_ARG;
+  if (v == PENT_VARIANT_THREAD_DF) {
+    const cudaError_t e = ensure_twisted(*p);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
   if (!variant_exists(*p, v)) return PENT_ERR_UNSUPPORTED;
   p->variant = v;
   return PENT_OK;

@@ -40,6 +40,10 @@ struct pent_plan_s {
   // twisted double-float variant (pent_factor_twisted.cu / pent_twisted_df.cu)
   int m = 0;                 // meeting row: top rows 0..m-1, bottom rows m..M-1
   int twist_ok = 0;          // tables valid and the 4x4 meeting system nonsingular
+  int twist_eligible = 0;    // fp64 plan whose block suits the twisted kernel
+  int twist_built = 0;       // tables made (on first selection of the variant)
+  double* work_area = nullptr;   // plan-time scratch in the arena
+  int* status_area = nullptr;
   float4* twtab = nullptr;   // [M][kTwK]
   double* twist = nullptr;   // [kTwistCount]
   int num_sms = 0;           // SMs of the plan's device (persistent grid size)

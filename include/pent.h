@@ -329,7 +329,11 @@ pent_status tri_factor_solve(const void* a, const void* b, const void* c, void* 
                              void* work, size_t work_bytes, int* info, void* stream);
 
 /* Select the kernel variant of a plan (PENT_VARIANT_AUTO restores the default).
- * PENT_ERR_UNSUPPORTED if the variant does not exist for this plan. */
+ * PENT_ERR_UNSUPPORTED if the variant does not exist for this plan.  The
+ * twisted variant (PENT_VARIANT_THREAD_DF on a shared-matrix plan) has its own
+ * tables, which the default path never uses: the first selection of it makes
+ * them, synchronously, so do not select it while work on the plan is queued
+ * (PENT_ERR_CUDA if that fails). */
 pent_status pent_set_variant(pent_plan plan, pent_variant variant);
 
 /* The variant the next call on this plan with `batch` systems would use. */
