@@ -16,15 +16,21 @@
 //                 x_t = S^{-1}(f_t - H^T y), written to rows M, M+1;
 //   k_big_fix     one thread per (system, chunk): t_c = sum_k B_{c,k} w_{c+1+k},
 //                 x = x' + M1 s0 + M2 s1 + K1 t0 + K2 t1 (- U x_t), stored in fp64.
-// Range: a first kernel (k_big_scale) takes each system's largest |entry|, and
-// the others work on the system scaled by the power of two that puts it in
-// [1, 2) (folded into the fp64 <-> pair conversions), so the pairs' float
-// exponent range never limits the result; a system outside the scaled path's
-// window (largest entry zero, subnormal, non-finite or extreme) is left
-// untouched by the first kernels and solved natively in fp64 by one thread of
-// k_big_fix.
-// Memory traffic: f read twice (the scale pass and k_big_local), x' written
-// and read, x written, plus summaries of 64 bytes per chunk.  The chunk states are
+// Range: every chunk converts its rows with its own power of two (the one that
+// puts its largest |entry| in [1, 2), known from the rows it loads; a chunk
+// whose largest entry is subnormal is first multiplied by 2^600 in fp64, which
+// is exact), so the pairs' float exponent range never limits a chunk.  Each
+// chunk records its exponent, and k_big_local folds two words per system into
+// global memory with one atomic per CTA: the largest magnitude (a system with an
+// inf or NaN entry returns NaN everywhere; an all-zero one is left as it is, its
+// own solution) and the largest chunk exponent E.  k_big_states and k_big_fix
+// bring each chunk's pairs to the system's scale 2^E by exact power-of-two
+// multiplications (terms more than 2^-126 below the system's largest value are
+// flushed), and k_big_fix joins the result to fp64 at 2^E, or for E outside the
+// window of the integer conversion at the window's edge followed by one fp64
+// multiplication.
+// Memory traffic: f read once (k_big_local), x' written and read, x written,
+// plus summaries of 64 bytes and one exponent per chunk.  The chunk states are
 // computed in double-float like the sweeps (summaries and a copy of the chunk
 // tables as (hi, lo) pairs), which keeps them off the fp64 pipe; only the
 // periodic border (one thread per system) works in fp64.  The parallelism is
@@ -33,7 +39,6 @@
 #include "df64.cuh"
 #include "fg.cuh"
 #include "pent_internal.cuh"
-#include "pent_native.cuh"
 
 namespace pent {
 namespace {
@@ -67,71 +72,126 @@ __device__ __forceinline__ void place(int& s, int& c) {
   c = (blockIdx.y * (kBigThreads / 32) + w) * CPW + lane / SPW;
 }
 
-// the system's exponent window check (largest-entry exponent field e)
-__device__ __forceinline__ bool big_fast(uint32_t e) { return e >= fg::kEMin && e <= fg::kEMax; }
+constexpr int kZeroChunk = -(1 << 20);   // chunk exponent of an all-zero (or non-finite) chunk
+constexpr int kExpBias = 1024;           // the per-system exponent word holds E + kExpBias (0: none)
 
-// largest |entry| of each system (rows 0..N-1): SPW systems per warp row, the
-// rows strided over the grid; lanes of one system, then the CTA's warps reduce,
-// and one atomic per CTA and system combines into smax[s] (zeroed before).
-// The word is the largest fp64 high word without sign, with bit 0 set if any
-// low word is nonzero: 0 marks an all-zero system, which the other kernels
-// leave untouched (zero is its solution, in place).
-template <int SPW>
-__global__ void __launch_bounds__(kBigThreads)
-    k_big_scale(const double* __restrict__ X, unsigned* __restrict__ smax, int rows, int batch) {
-  constexpr int RPW = 32 / SPW;                   // rows per warp and step
-  constexpr int NW = kBigThreads / 32;
-  __shared__ unsigned red[NW][SPW];
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  const int s = blockIdx.x * SPW + lane % SPW;
-  unsigned mx = 0u, nz = 0u;
-  if (s < batch) {
-    const long long ld = batch;
-    const int stride = gridDim.y * NW * RPW;
-#pragma unroll 8
-    for (int i = (blockIdx.y * NW + w) * RPW + lane / SPW; i < rows; i += stride) {
-      const double v = X[(long long)i * ld + s];
-      mx = max(mx, fg::mag_bits(v));
-      nz |= (uint32_t)__double2loint(v);
-    }
-  }
-  mx |= nz != 0u ? 1u : 0u;                       // only an all-zero system ends at 0
-#pragma unroll
-  for (int o = SPW; o < 32; o <<= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (lane < SPW) red[w][lane] = mx;
-  __syncthreads();
-  if (threadIdx.x < SPW && blockIdx.x * SPW + (int)threadIdx.x < batch) {
-    unsigned m = 0u;
-#pragma unroll
-    for (int k = 0; k < NW; ++k) m = max(m, red[k][threadIdx.x]);
-    atomicMax(smax + blockIdx.x * SPW + threadIdx.x, m);
-  }
+// x 2^d for |d| up to about 2000: two exact power-of-two products (only the
+// last can round, where the result is subnormal)
+__device__ __forceinline__ double scale2(double x, int d) {
+  const int d1 = d / 2;
+  return (x * fg::pow2i(d1)) * fg::pow2i(d - d1);
 }
 
+// 2^d as a float for d <= 0, flushed to 0 below 2^-126
+__device__ __forceinline__ float pow2f(int d) { return d >= -126 ? __uint_as_float((uint32_t)(127 + d) << 23) : 0.f; }
+__device__ __forceinline__ D2 scaled(D2 v, float f) { return D2{v.h * f, v.l * f}; }
+
+// Magnitude word of n values at a stride of kBigThreads doubles (a separate
+// call, so that the sweeps that follow reload f instead of keeping it live)
+__device__ __noinline__ uint32_t column_word(const double* v, int n) {
+  uint32_t mx = 0u, nz = 0u;
+  for (int j = 0; j < n; ++j) {
+    const double f = v[j * kBigThreads];
+    mx = max(mx, fg::mag_bits(f));
+    nz |= (uint32_t)__double2loint(f);
+  }
+  return mx | (nz != 0u ? 1u : 0u);
+}
+
+// One thread per (system, chunk): the chunk's exponent from its own rows, the
+// local sweeps in that scale, x' in place of f, the summaries, and the two
+// per-system words (largest magnitude, largest chunk exponent), reduced over
+// the CTA and folded in with one atomic each (both zeroed before).
 template <int SPW, bool CYC>
 __global__ void __launch_bounds__(kBigThreads, 2)
     k_big_local(const float4* __restrict__ tab, double* __restrict__ X, double* __restrict__ sum,
-                double* __restrict__ xm, const unsigned* __restrict__ smax, int M, int P, int batch,
-                int2 dup) {
+                double* __restrict__ xm, unsigned* __restrict__ smag, unsigned* __restrict__ sexp,
+                int* __restrict__ cexp, int M, int P, int batch, int2 dup) {
   constexpr int L = kBigL;
+  constexpr int NW = kBigThreads / 32;
+  __shared__ unsigned red[2][NW][SPW];
   int s, c;
   place<SPW>(s, c);
-  if (s >= batch || c >= P) return;
-  if (smax[s] == 0u) return;                      // all zero: already solved
-  const uint32_t e = smax[s] >> 20;
-  if (!big_fast(e)) return;                       // solved natively by k_big_fix
-  const uint32_t off = fg::in_offset(e);
+  const bool act = s < batch && c < P;
   const long long ld = batch;
   const int row0 = c * L;
-  double* p = X + (long long)row0 * ld + s;
-  const float4* t = tab + (size_t)table_chunk(c, dup) * L * kSpK;
+  double* p = X + (long long)row0 * ld + (act ? s : 0);
   // the chunk's f into this thread's shared-memory column, every row in flight at once
   extern __shared__ double sf[];                  // [L][kBigThreads]
   double* mine = sf + threadIdx.x;
+  if (act) {
 #pragma unroll
-  for (int j = 0; j < L; ++j)
-    if (row0 + j < M) cp_async8(mine + j * kBigThreads, p + (long long)j * ld);
+    for (int j = 0; j < L; ++j)
+      if (row0 + j < M) cp_async8(mine + j * kBigThreads, p + (long long)j * ld);
+  }
   cp_async_wait_all();
+  // magnitude word: largest high word without sign, bit 0 set if any low word is nonzero
+  const uint32_t mword = act ? column_word(mine, row0 + L <= M ? L : M - row0) : 0u;
+  const uint32_t mx = mword & ~1u;
+  int ce = kZeroChunk;                            // the chunk's exponent: pairs = f 2^-(ce - 1023)
+  uint32_t econv = 1023u;                         // exponent field the conversion rebiases by
+  if (mword != 0u && (mx >> 20) != 0x7FFu) {
+    if ((mx >> 20) == 0u) {
+      // largest entry subnormal: the chunk times 2^600 first (exact), so that the
+      // integer conversion reads normal numbers
+      uint32_t m2 = 0u;
+#pragma unroll
+      for (int j = 0; j < L; ++j)
+        if (row0 + j < M) {
+          const double f = mine[j * kBigThreads] * 0x1p600;
+          mine[j * kBigThreads] = f;
+          m2 = max(m2, fg::mag_bits(f));
+        }
+      econv = m2 >> 20;
+      ce = (int)econv - 600;
+    } else {
+      econv = mx >> 20;
+      ce = (int)econv;
+    }
+  }
+  // per-system words over the CTA (its warps share the same SPW systems), one
+  // atomic each per CTA and system
+  {
+    uint32_t a = act ? mword : 0u, b = (act && ce != kZeroChunk) ? (uint32_t)(ce + kExpBias) : 0u;
+#pragma unroll
+    for (int o = SPW; o < 32; o <<= 1) {
+      a = max(a, __shfl_xor_sync(0xffffffffu, a, o));
+      b = max(b, __shfl_xor_sync(0xffffffffu, b, o));
+    }
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    if (lane < SPW) {
+      red[0][w][lane] = a;
+      red[1][w][lane] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x < SPW && blockIdx.x * SPW + (int)threadIdx.x < batch) {
+      uint32_t ma = 0u, mb = 0u;
+#pragma unroll
+      for (int k = 0; k < NW; ++k) {
+        ma = max(ma, red[0][k][threadIdx.x]);
+        mb = max(mb, red[1][k][threadIdx.x]);
+      }
+      if (ma) atomicMax(smag + blockIdx.x * SPW + threadIdx.x, ma);
+      if (mb) atomicMax(sexp + blockIdx.x * SPW + threadIdx.x, mb);
+    }
+  }
+  if (!act) return;
+  cexp[(size_t)c * batch + s] = ce;
+  float2* o = reinterpret_cast<float2*>(sum) + ((size_t)c * batch + s) * kSum;
+  if (ce == kZeroChunk) {
+    // all zero (already its own x') or not finite (the system returns NaN)
+    o[0] = o[1] = o[2] = o[3] = make_float2(0.f, 0.f);
+    if (CYC) {
+#pragma unroll
+      for (int j = 0; j < L; ++j) {
+        if (row0 + j == M - 2) xm[(size_t)s * 2] = 0.0;
+        if (row0 + j == M - 1) xm[(size_t)s * 2 + 1] = 0.0;
+      }
+    }
+    return;
+  }
+  const uint32_t off = fg::in_offset(econv);
+  const float4* t = tab + (size_t)table_chunk(c, dup) * L * kSpK;
   D2 v[L];
   {
     D2 a1{0.f, 0.f}, a2{0.f, 0.f};
@@ -147,7 +207,6 @@ __global__ void __launch_bounds__(kBigThreads, 2)
       a1 = g;
     }
   }
-  float2* o = reinterpret_cast<float2*>(sum) + ((size_t)c * batch + s) * kSum;
   o[0] = make_float2(v[L - 2].h, v[L - 2].l);
   o[1] = make_float2(v[L - 1].h, v[L - 1].l);
   {
@@ -163,14 +222,14 @@ __global__ void __launch_bounds__(kBigThreads, 2)
   }
   o[2] = make_float2(v[0].h, v[0].l);
   o[3] = make_float2(v[1].h, v[1].l);
-  if (CYC) {                                      // x' at rows M-2, M-1 for the border
+  if (CYC) {                                      // x' at rows M-2, M-1 for the border, in the chunk's scale
 #pragma unroll
     for (int j = 0; j < L; ++j) {
       if (row0 + j == M - 2) xm[(size_t)s * 2] = df::to_double(v[j]);
       if (row0 + j == M - 1) xm[(size_t)s * 2 + 1] = df::to_double(v[j]);
     }
   }
-  float2* q = reinterpret_cast<float2*>(p);       // x' in place of f, as (hi, lo)
+  float2* q = reinterpret_cast<float2*>(p);       // x' in place of f, as (hi, lo), in the chunk's scale
 #pragma unroll
   for (int j = 0; j < L; ++j)
     if (row0 + j < M) q[j * ld] = make_float2(v[j].h, v[j].l);
@@ -185,19 +244,32 @@ __device__ __forceinline__ void mv2d(const float2* A, D2 x0, D2 x1, D2& y0, D2& 
   y1 = df::sum3(y1, d2(A[2]), x0, d2(A[3]), x1);
 }
 
-// s_c from the local end values of the T chunks before c (summaries as (hi, lo))
+// The system's exponent E (the largest chunk exponent) from its two words:
+// false for an all-zero system (nothing to do) and a non-finite one.
+__device__ __forceinline__ bool system_exp(const unsigned* smag, const unsigned* sexp, int s, int& E) {
+  const unsigned mag = smag[s], ew = sexp[s];
+  E = (int)ew - kExpBias;
+  return ew != 0u && (mag >> 20) != 0x7FFu;
+}
+
+// s_c from the local end values of the T chunks before c (summaries as (hi, lo),
+// each in its own chunk's scale, brought to the system's scale 2^E)
 __device__ __forceinline__ void state_s(const float2* __restrict__ ctab, const float2* __restrict__ sum,
-                                        int c, int s, int batch, int T, int2 dup, D2& s0, D2& s1) {
+                                        const int* __restrict__ cexp, int c, int s, int batch, int T, int2 dup,
+                                        int E, D2& s0, D2& s1) {
   const float2* ct = ctab + (size_t)table_chunk(c, dup) * kSpChunk;
   s0 = s1 = D2{0.f, 0.f};
   for (int k = 1; k <= T && k <= c; ++k) {
-    const float2* e = sum + ((size_t)(c - k) * batch + s) * kSum;
-    if (k == 1) { s0 = df::add(s0, d2(e[0])); s1 = df::add(s1, d2(e[1])); }
-    else mv2d(ct + 12 + 4 * (k - 2), d2(e[0]), d2(e[1]), s0, s1);
+    const size_t i = (size_t)(c - k) * batch + s;
+    const float2* e = sum + i * kSum;
+    const float f = pow2f(cexp[i] - E);
+    const D2 ea = scaled(d2(e[0]), f), eb = scaled(d2(e[1]), f);
+    if (k == 1) { s0 = df::add(s0, ea); s1 = df::add(s1, eb); }
+    else mv2d(ct + 12 + 4 * (k - 2), ea, eb, s0, s1);
   }
 }
 
-// t_c from w of the T chunks after c
+// t_c from w of the T chunks after c (already in the system's scale)
 __device__ __forceinline__ void state_t(const float2* __restrict__ ctab, const float2* __restrict__ sum,
                                         int c, int s, int P, int batch, int T, int2 dup, D2& t0, D2& t1) {
   const float2* ct = ctab + (size_t)table_chunk(c, dup) * kSpChunk;
@@ -211,15 +283,19 @@ __device__ __forceinline__ void state_t(const float2* __restrict__ ctab, const f
 
 __global__ void __launch_bounds__(kBigThreads)
     k_big_states(const float2* __restrict__ ctab, const double* __restrict__ extra, float2* __restrict__ sum,
-                 int P, int batch, int2 dup) {
+                 const unsigned* __restrict__ smag, const unsigned* __restrict__ sexp,
+                 const int* __restrict__ cexp, int P, int batch, int2 dup) {
   const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (long long)P * batch) return;
   const int c = (int)(i / batch), s = (int)(i % batch);
+  int E;
+  if (!system_exp(smag, sexp, s, E)) return;
   const int T = (int)extra[18];
   D2 s0, s1;
-  state_s(ctab, sum, c, s, batch, T, dup, s0, s1);
+  state_s(ctab, sum, cexp, c, s, batch, T, dup, E, s0, s1);
   float2* o = sum + (size_t)i * kSum;
-  D2 w0 = d2(o[2]), w1 = d2(o[3]);
+  const float f = pow2f(cexp[i] - E);
+  D2 w0 = scaled(d2(o[2]), f), w1 = scaled(d2(o[3]), f);
   mv2d(ctab + (size_t)table_chunk(c, dup) * kSpChunk + 4, s0, s1, w0, w1);   // w_c = x'_start + Mst_c s_c
   o[4] = f2(s0);
   o[5] = f2(s1);
@@ -236,13 +312,13 @@ __global__ void k_chunk_df(const double* __restrict__ src, float2* __restrict__ 
 __global__ void __launch_bounds__(kBigThreads)
     k_big_border(const double* __restrict__ ctab, const float2* __restrict__ ctabd,
                  const double* __restrict__ extra, const float2* __restrict__ sum,
-                 const double* __restrict__ xm, double* __restrict__ X, const unsigned* __restrict__ smax,
-                 int M, int P, int batch, int2 dup) {
+                 const double* __restrict__ xm, double* __restrict__ X, const unsigned* __restrict__ smag,
+                 const unsigned* __restrict__ sexp, const int* __restrict__ cexp, int M, int P, int batch,
+                 int2 dup) {
   const int s = blockIdx.x * blockDim.x + threadIdx.x;
   if (s >= batch) return;
-  if (smax[s] == 0u) return;                      // all zero: already solved
-  const uint32_t e = smax[s] >> 20;
-  if (!big_fast(e)) return;                       // solved natively by k_big_fix
+  int E;
+  if (!system_exp(smag, sexp, s, E)) return;
   const long long ld = batch;
   const int T = (int)extra[18];
   // y at rows 0, 1: chunk 0 has s_0 = 0, so y = w_0 + Kst_0 t_0
@@ -251,7 +327,7 @@ __global__ void __launch_bounds__(kBigThreads)
   const float2* o0 = sum + (size_t)s * kSum;
   double y0 = df::to_double(d2(o0[6])), y1 = df::to_double(d2(o0[7]));
   mv2(ctab + 8, df::to_double(td0), df::to_double(td1), y0, y1);
-  // y at rows M-2, M-1 from their chunks' s and t
+  // y at rows M-2, M-1 from their chunks' x' (in the chunk's scale), s and t
   double yv[2];
   for (int r = 0; r < 2; ++r) {
     const int row = M - 2 + r, c = row / kBigL;
@@ -259,36 +335,48 @@ __global__ void __launch_bounds__(kBigThreads)
     D2 u0, u1;
     state_t(ctabd, sum, c, s, P, batch, T, dup, u0, u1);
     const double* mk = extra + 10 + 2 * r;   // M1, M2 at the row; K1, K2 four slots on
-    yv[r] = xm[(size_t)s * 2 + r] + mk[0] * df::to_double(d2(oc[4])) + mk[1] * df::to_double(d2(oc[5])) +
-            mk[4] * df::to_double(u0) + mk[5] * df::to_double(u1);
+    yv[r] = scale2(xm[(size_t)s * 2 + r], cexp[(size_t)c * batch + s] - E) + mk[0] * df::to_double(d2(oc[4])) +
+            mk[1] * df::to_double(d2(oc[5])) + mk[4] * df::to_double(u0) + mk[5] * df::to_double(u1);
   }
   const double r0 = extra[4] * yv[0] + extra[5] * yv[1] + extra[6] * y0;
   const double r1 = extra[7] * yv[1] + extra[8] * y0 + extra[9] * y1;
   // in the system's scale; the border solution back at its own scale
-  const double f0 = X[(long long)M * ld + s] * fg::pow2_neg(e), f1 = X[(long long)(M + 1) * ld + s] * fg::pow2_neg(e);
-  X[(long long)M * ld + s] = (extra[0] * (f0 - r0) + extra[1] * (f1 - r1)) * fg::pow2_pos(e);
-  X[(long long)(M + 1) * ld + s] = (extra[2] * (f0 - r0) + extra[3] * (f1 - r1)) * fg::pow2_pos(e);
+  const double f0 = scale2(X[(long long)M * ld + s], 1023 - E), f1 = scale2(X[(long long)(M + 1) * ld + s], 1023 - E);
+  X[(long long)M * ld + s] = scale2(extra[0] * (f0 - r0) + extra[1] * (f1 - r1), E - 1023);
+  X[(long long)(M + 1) * ld + s] = scale2(extra[2] * (f0 - r0) + extra[3] * (f1 - r1), E - 1023);
 }
 
 template <int SPW, bool CYC>
 __global__ void __launch_bounds__(kBigThreads)
     k_big_fix(const float4* __restrict__ tab, const float2* __restrict__ ctab,
               const double* __restrict__ extra, const float2* __restrict__ sum, double* __restrict__ X,
-              const unsigned* __restrict__ smax, const NativeTabs nt, int M, int P, int batch, int2 dup) {
+              const unsigned* __restrict__ smag, const unsigned* __restrict__ sexp,
+              const int* __restrict__ cexp, int M, int P, int batch, int2 dup) {
   constexpr int L = kBigL;
   int s, c;
   place<SPW>(s, c);
   if (s >= batch || c >= P) return;
   const long long ld = batch;
-  if (smax[s] == 0u) return;                      // all zero: already solved
-  const uint32_t e = smax[s] >> 20;
-  if (!big_fast(e)) {                             // the whole column, natively, by one thread
-    if (c == 0) native_solve_col(nt, X + s, M, (size_t)ld, CYC ? 1 : 0);
-    return;
-  }
-  const uint32_t off = fg::in_offset(e);
   const int row0 = c * L;
   if (row0 >= M) return;
+  double* p = X + (long long)row0 * ld + s;
+  if (sexp[s] != 0u && (smag[s] >> 20) == 0x7FFu) {
+    // an inf or NaN entry: the system's solution is not finite
+#pragma unroll
+    for (int j = 0; j < L; ++j)
+      if (row0 + j < M) p[j * ld] = __longlong_as_double(0x7FF8000000000000ll);
+    if (CYC && c == 0) {
+      X[(long long)M * ld + s] = __longlong_as_double(0x7FF8000000000000ll);
+      X[(long long)(M + 1) * ld + s] = __longlong_as_double(0x7FF8000000000000ll);
+    }
+    return;
+  }
+  int E;
+  if (!system_exp(smag, sexp, s, E)) return;      // all zero: already solved
+  // the join to fp64 at 2^E, or at the edge of its window and then one fp64 product
+  const int eo = E < (int)fg::kEMin ? (int)fg::kEMin : (E > (int)fg::kEMax ? (int)fg::kEMax : E);
+  const uint32_t off = fg::out_offset((uint32_t)eo);
+  const float fx = pow2f(cexp[(size_t)c * batch + s] - E);   // x' from the chunk's scale to the system's
   const int T = (int)extra[18];
   const float2* o = sum + ((size_t)c * batch + s) * kSum;
   D2 T0, T1;
@@ -299,10 +387,9 @@ __global__ void __launch_bounds__(kBigThreads)
   if (CYC) {
     const int reach = (int)extra[19];
     needU = c < reach || c > (M - 1) / L - reach;
-    X0 = df::from_double(-X[(long long)M * ld + s] * fg::pow2_neg(e));
-    X1 = df::from_double(-X[(long long)(M + 1) * ld + s] * fg::pow2_neg(e));
+    X0 = df::from_double(-scale2(X[(long long)M * ld + s], 1023 - E));
+    X1 = df::from_double(-scale2(X[(long long)(M + 1) * ld + s], 1023 - E));
   }
-  double* p = X + (long long)row0 * ld + s;
   const float2* q = reinterpret_cast<const float2*>(p);
   const float4* t = tab + (size_t)table_chunk(c, dup) * L * kSpK;
   constexpr int G = 8;
@@ -315,7 +402,7 @@ __global__ void __launch_bounds__(kBigThreads)
     for (int u = 0; u < G; ++u) {
       const int j = j0 + u;
       const float4 c3 = __ldg(t + j * kSpK + 3), c4 = __ldg(t + j * kSpK + 4);
-      D2 x = df::axpy(D2{xv[u].x, xv[u].y}, D2{c3.x, c3.y}, S0);
+      D2 x = df::axpy(scaled(D2{xv[u].x, xv[u].y}, fx), D2{c3.x, c3.y}, S0);
       x = df::axpy(x, D2{c3.z, c3.w}, S1);
       x = df::axpy(x, D2{c4.x, c4.y}, T0);
       x = df::axpy(x, D2{c4.z, c4.w}, T1);
@@ -329,6 +416,15 @@ __global__ void __launch_bounds__(kBigThreads)
       fg::store_cs_if(p + j * ld, xo, row0 + j < M);
     }
   }
+  if (eo != E) {
+    // outside the join's window: the stored rows are x 2^(eo - E), scaled back
+    // (this thread's own stores, re-read in program order)
+    const double post = fg::pow2i(E - eo);
+    asm volatile("" ::: "memory");
+#pragma unroll
+    for (int j = 0; j < L; ++j)
+      if (row0 + j < M) p[j * ld] *= post;
+  }
 }
 
 template <int SPW, bool CYC>
@@ -337,42 +433,32 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   constexpr int CPB = (kBigThreads / 32) * (32 / SPW);     // chunks per CTA
   const dim3 grid((batch + SPW - 1) / SPW, (P + CPB - 1) / CPB);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
+  // scratch: summaries, x' at rows M-2, M-1, the two per-system words, chunk exponents
   double* xm = p.spsum + (size_t)P * batch * kSum;
-  unsigned* smax = reinterpret_cast<unsigned*>(xm + 2 * (size_t)batch);
+  unsigned* smag = reinterpret_cast<unsigned*>(xm + 2 * (size_t)batch);
+  unsigned* sexp = smag + batch;
+  int* cexp = reinterpret_cast<int*>(sexp + batch);
   const int2 dup = make_int2(p.dup_lo, p.dup_hi);
   const size_t smem_local = (size_t)kBigL * kBigThreads * sizeof(double);
   cudaError_t e = kernel_prepare((const void*)k_big_local<SPW, CYC>, smem_local, kBigThreads, nullptr);
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(smax, 0, (size_t)batch * sizeof(unsigned), st);
+  e = cudaMemsetAsync(smag, 0, 2 * (size_t)batch * sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
-  {
-    // enough CTAs over the rows to fill the GPU (each loops over its rows)
-    const int rows = p.M + (CYC ? 2 : 0);
-    const unsigned gx = (batch + SPW - 1) / SPW;
-    const int per_cta = (kBigThreads / 32) * (32 / SPW);
-    unsigned gy = (unsigned)((rows + per_cta - 1) / per_cta);
-    const unsigned cap = (unsigned)(8 * (p.num_sms > 0 ? p.num_sms : 1)) / gx + 1;
-    if (gy > cap) gy = cap;
-    if (gy > 65535u) gy = 65535u;
-    k_big_scale<SPW><<<dim3(gx, gy), kBigThreads, 0, st>>>(X, smax, rows, batch);
-    note_launch();
-  }
-  k_big_local<SPW, CYC><<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, smax, p.M, P, batch,
-                                                               dup);
+  k_big_local<SPW, CYC><<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, smag, sexp, cexp, p.M,
+                                                               P, batch, dup);
   note_launch();
   const long long n = (long long)P * batch;
   float2* sumd = reinterpret_cast<float2*>(p.spsum);
   k_big_states<<<(unsigned)((n + kBigThreads - 1) / kBigThreads), kBigThreads, 0, st>>>(
-      p.spchunk_df, p.spextra, sumd, P, batch, dup);
+      p.spchunk_df, p.spextra, sumd, smag, sexp, cexp, P, batch, dup);
   note_launch();
   if (CYC) {
     k_big_border<<<(batch + kBigThreads - 1) / kBigThreads, kBigThreads, 0, st>>>(
-        p.spchunk, p.spchunk_df, p.spextra, sumd, xm, X, smax, p.M, P, batch, dup);
+        p.spchunk, p.spchunk_df, p.spextra, sumd, xm, X, smag, sexp, cexp, p.M, P, batch, dup);
     note_launch();
   }
-  const NativeTabs nt{p.coef64, p.tail64, p.bands};
-  k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, smax, nt, p.M,
-                                                   P, batch, dup);
+  k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, smag, sexp, cexp,
+                                                   p.M, P, batch, dup);
   note_launch();
   return cudaGetLastError();
 }
@@ -397,9 +483,9 @@ cudaError_t split_big_prepare(pent_plan_s& p, cudaStream_t st) {
 cudaError_t shared_split_big(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   if (p.sp_L != kBigL || p.sp_T <= 0) return cudaErrorInvalidValue;
   // summaries: kSum doubles per (chunk, system), then x' at rows M-2, M-1 per
-  // system, then each system's largest |entry| bits
+  // system, two words per system, one exponent per (chunk, system)
   const size_t need = ((size_t)p.sp_P * batch * kSum + 2 * (size_t)batch) * sizeof(double) +
-                      (size_t)batch * sizeof(unsigned);
+                      2 * (size_t)batch * sizeof(unsigned) + (size_t)p.sp_P * batch * sizeof(int);
   if (p.spsum_bytes < need) {
     if (p.spsum) {
       cudaError_t e = cudaStreamSynchronize(st);   // earlier solves may still read it

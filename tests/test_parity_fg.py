@@ -146,3 +146,38 @@ def test_shared_solve_non_finite_entries():
     keep = [s for s in range(batch) if s not in (2, 3)]
     ref = oracle.batch_shared(bands, F[:, keep])
     assert max_rel_err(X[:, keep], ref) < TOL_F64
+
+
+
+def banded_matvec(bands, X, cyclic):
+    """A @ X for the [5][N] band array (row i: a_i x_{i-2} + b_i x_{i-1} + c_i x_i +
+    d_i x_{i+1} + e_i x_{i+2}); X [N][batch].  Cyclic: the indices wrap around."""
+    if cyclic:
+        return (bands[0][:, None] * np.roll(X, 2, axis=0) + bands[1][:, None] * np.roll(X, 1, axis=0) +
+                bands[2][:, None] * X + bands[3][:, None] * np.roll(X, -1, axis=0) +
+                bands[4][:, None] * np.roll(X, -2, axis=0))
+    Y = bands[2][:, None] * X
+    Y[1:] += bands[1][1:, None] * X[:-1]
+    Y[2:] += bands[0][2:, None] * X[:-2]
+    Y[:-1] += bands[3][:-1, None] * X[1:]
+    Y[:-2] += bands[4][:-2, None] * X[2:]
+    return Y
+
+
+@pytest.mark.parametrize("cyclic", [False, True])
+@pytest.mark.parametrize("N", [300, 1024])
+def test_outputs_on_binade_edges(cyclic, N):
+    """Solutions whose entries are signed powers of two, some moved one ulp below or
+    above, so that many outputs fall on or next to a binade edge, where joining a pair
+    to fp64 (by integers: a carry into the exponent; by an fp64 add: renormalisation)
+    must not lose a factor of two.  x is known exactly; f = A x in fp64 (non-cyclic:
+    the fixed-grid kernel; cyclic: the TwoSum partitioned kernel)."""
+    rng = np.random.default_rng(17)
+    batch = 333
+    X = np.ldexp(1.0, rng.integers(-12, 12, (N, batch))) * rng.choice([-1.0, 1.0], (N, batch))
+    X[::3] = np.nextafter(X[::3], 0.0)                 # one ulp below the edge
+    X[1::7] = np.nextafter(X[1::7], 2.0 * X[1::7])     # one ulp above it
+    bands = inputs.hyper_bands(N, 1.0)
+    F = banded_matvec(bands, X, cyclic)
+    out = solve(bands, F, variant="auto", cyclic=cyclic)
+    assert max_rel_err(out, X) < TOL_F64

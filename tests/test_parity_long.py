@@ -33,8 +33,8 @@ def solve(N, batch, sigma, cyclic, seed, variant="auto"):
 def test_long_systems_match_oracle(cyclic, N, batch):
     bands, F, out, launches, v = solve(N, batch, 1.0, cyclic, seed=N + batch)
     assert v == pent.VARIANT_SPLIT
-    # the scale pass, the local sweeps, the chunk states, (the periodic border,) the fix-up
-    assert launches == (5 if cyclic else 4)
+    # the local sweeps (with the scales), the chunk states, (the periodic border,) the fix-up
+    assert launches == (4 if cyclic else 3)
     assert max_rel_err(out, oracle.batch_shared(bands, F, cyclic=cyclic)) < TOL_F64
 
 

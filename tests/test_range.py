@@ -264,3 +264,43 @@ def test_long_systems_mixed_batch(cyclic):
     X = run_solve(bands, F, cyclic)
     assert np.all(X[:, 3] == 0.0)
     assert max_rel_err(X, oracle.batch_shared(bands, F, cyclic=cyclic)) < TOL_F64
+
+
+@pytest.mark.parametrize("cyclic", [False, True])
+def test_long_systems_chunk_scales(cyclic):
+    """Systems too long for one CTA scale every chunk by its own power of two: rows
+    whose magnitudes differ by hundreds of decades between chunks, a system that is
+    zero except for one chunk, a system whose largest entry is subnormal, and one
+    with a single subnormal chunk among normal ones."""
+    N, batch = 5003, 6
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, batch, seed=35)
+    F[:, 0] *= np.repeat(np.logspace(-250, 250, (N + 31) // 32), 32)[:N]   # a scale per chunk
+    F[:, 1] = 0.0
+    F[2000:2032, 1] = inputs.rhs_uniform(32, 1, seed=36)[:, 0] * 1e-20      # one nonzero chunk
+    F[:, 2] *= 1e-312                                                       # subnormal largest entry
+    F[1000:1100, 3] *= 1e-320                                               # a subnormal stretch
+    F[:, 4] *= 1e306                                                        # above the join's window
+    X = run_solve(bands, F, cyclic)
+    assert np.all(np.isfinite(X))
+    ref = oracle.batch_shared(bands, F, cyclic=cyclic)
+    # the subnormal system: the oracle's own fp64 loses bits on subnormal data, so
+    # its reference is the oracle on the data times 2^600 (exact), scaled back (at
+    # 1e-312 one subnormal ulp of the output is still only 5e-12 of it)
+    ref[:, 2] = np.ldexp(oracle.batch_shared(bands, np.ldexp(F[:, 2:3], 600), cyclic=cyclic)[:, 0], -600)
+    assert max_rel_err(X, ref) < TOL_F64
+
+
+@pytest.mark.parametrize("cyclic", [False, True])
+def test_long_systems_non_finite_entry(cyclic):
+    """A long system with an inf or NaN entry returns NaN in every entry; the other
+    systems of the batch are unaffected."""
+    N, batch = 5003, 4
+    bands = inputs.hyper_bands(N, 1.0)
+    F = inputs.rhs_uniform(N, batch, seed=37)
+    F[1234, 1] = np.inf
+    F[4321, 2] = np.nan
+    X = run_solve(bands, F, cyclic)
+    assert np.all(np.isnan(X[:, 1])) and np.all(np.isnan(X[:, 2]))
+    ok = [0, 3]
+    assert max_rel_err(X[:, ok], oracle.batch_shared(bands, np.ascontiguousarray(F[:, ok]), cyclic=cyclic)) < TOL_F64
