@@ -63,13 +63,13 @@ def test_multistep_matches_oracle(kind, N, batch):
     # otherwise (N = 2000: 64 chunks of 32 rows, beyond the one-CTA partitioned
     # cyclic kernel; sigma = 3 with 16-row chunks: couplings decay too slowly to
     # truncate) one solve per step: the fused CH / CN steps in one native launch,
-    # hyperdiffusion through the five-launch partitioned solve for long systems
-    # (scale pass, local sweeps, chunk states, periodic border, fix-up)
-    assert launches in (1, steps, 5 * steps)
+    # hyperdiffusion through the four-launch partitioned solve for long systems
+    # (local sweeps, chunk states, periodic border, fix-up)
+    assert launches in (1, steps, 4 * steps)
     if kind != "ch" and N <= 1024:
         assert launches == 1
     if N == 2000:
-        assert launches == (5 * steps if kind == "hyper" else steps)
+        assert launches == (4 * steps if kind == "hyper" else steps)
 
 
 @pytest.mark.parametrize("kind", ["hyper", "ch", "cn"])
