@@ -346,6 +346,14 @@ __global__ void __launch_bounds__(kBigThreads)
   X[(long long)(M + 1) * ld + s] = scale2(extra[2] * (f0 - r0) + extra[3] * (f1 - r1), E - 1023);
 }
 
+// cold paths of k_big_fix, out of line
+__device__ __noinline__ void fill_nan(double* p, long long ld, int n) {
+  for (int j = 0; j < n; ++j) p[j * ld] = __longlong_as_double(0x7FF8000000000000ll);
+}
+__device__ __noinline__ void scale_rows(double* p, long long ld, int n, double f) {
+  for (int j = 0; j < n; ++j) p[j * ld] *= f;
+}
+
 template <int SPW, bool CYC>
 __global__ void __launch_bounds__(kBigThreads)
     k_big_fix(const float4* __restrict__ tab, const float2* __restrict__ ctab,
@@ -362,13 +370,8 @@ __global__ void __launch_bounds__(kBigThreads)
   double* p = X + (long long)row0 * ld + s;
   if (sexp[s] != 0u && (smag[s] >> 20) == 0x7FFu) {
     // an inf or NaN entry: the system's solution is not finite
-#pragma unroll
-    for (int j = 0; j < L; ++j)
-      if (row0 + j < M) p[j * ld] = __longlong_as_double(0x7FF8000000000000ll);
-    if (CYC && c == 0) {
-      X[(long long)M * ld + s] = __longlong_as_double(0x7FF8000000000000ll);
-      X[(long long)(M + 1) * ld + s] = __longlong_as_double(0x7FF8000000000000ll);
-    }
+    fill_nan(p, ld, M - row0 < L ? M - row0 : L);
+    if (CYC && c == 0) fill_nan(X + (long long)M * ld + s, ld, 2);
     return;
   }
   int E;
@@ -419,11 +422,8 @@ __global__ void __launch_bounds__(kBigThreads)
   if (eo != E) {
     // outside the join's window: the stored rows are x 2^(eo - E), scaled back
     // (this thread's own stores, re-read in program order)
-    const double post = fg::pow2i(E - eo);
     asm volatile("" ::: "memory");
-#pragma unroll
-    for (int j = 0; j < L; ++j)
-      if (row0 + j < M) p[j * ld] *= post;
+    scale_rows(p, ld, M - row0 < L ? M - row0 : L, fg::pow2i(E - eo));
   }
 }
 
