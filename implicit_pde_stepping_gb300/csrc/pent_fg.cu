@@ -498,12 +498,17 @@ void inverse_row_sums(const std::vector<double>& cf, int M, double& Gg, double& 
 
 // Decide whether the plan's partitioned solves can run on a fixed grid and
 // set the grid and the correction-term groups.  Needs the partitioned tables
-// (L = 32, truncated chunk scan, at most 64 chunks) and the native tables on
-// the device.
+// (L = 32, truncated chunk scan, non-cyclic) and the native tables on the
+// device; up to 64 chunks the one-CTA kernel runs on it (fg_ok), beyond that
+// the local sweeps and the fix-up of the long-system kernels (big_fg).
 cudaError_t fg_prepare(pent_plan_s& p) {
   p.fg_ok = 0;
-  if (p.cyclic || p.sp_L != 32 || p.sp_T <= 0 || p.sp_P > 64) return cudaSuccess;
+  p.big_fg = 0;
+  if (p.cyclic || p.sp_L != 32 || p.sp_T <= 0) return cudaSuccess;
   const int M = p.M, L = p.sp_L, P = p.sp_P, Mpad = L * P;
+  // up to 64 chunks: the one-CTA kernel (k_fg); beyond: the grid for the
+  // kernels of systems too long for one CTA
+  const bool one_cta = P <= 64;
   std::vector<double> cf((size_t)kCoefCount * M);
   std::vector<float4> rows((size_t)Mpad * kSpK);
   cudaError_t e = cudaMemcpy(cf.data(), p.coef64, cf.size() * sizeof(double), cudaMemcpyDeviceToHost);
@@ -512,7 +517,7 @@ cudaError_t fg_prepare(pent_plan_s& p) {
   if (e != cudaSuccess) return e;
   // longest run of chunks whose kernel row tables (kSpK - 1 float4 per row) are
   // bitwise equal to the run's first: they share one shared-memory slot
-  {
+  if (one_cta) {
     const int K4 = kSpK - 1;
     auto same = [&](int a, int b) {
       for (int j = 0; j < L; ++j)
@@ -531,7 +536,7 @@ cudaError_t fg_prepare(pent_plan_s& p) {
     p.fg_dup_lo = best_lo;
     p.fg_dup_hi = best_hi;
   }
-  {
+  if (one_cta) {
     int BR = 0, RS = 0;
     tile_rows(M, BR, RS);
     const int nslot = P - (p.fg_dup_hi - p.fg_dup_lo);
@@ -602,7 +607,8 @@ cudaError_t fg_prepare(pent_plan_s& p) {
   p.fg_gk_full = gk_full;
   p.fg_gk_none = std::min(gk_none, gk_full);
   p.fg_bound = bound;
-  p.fg_ok = 1;
+  if (one_cta) p.fg_ok = 1;
+  else p.big_fg = 1;
   return cudaSuccess;
 }
 

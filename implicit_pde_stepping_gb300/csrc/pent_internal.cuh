@@ -76,6 +76,7 @@ struct pent_plan_s {
   // fixed-grid partitioned kernel (pent_fg.cu): valid for this plan, grid bias,
   // correction-term groups (see fg_prepare), bound on the intermediate values
   int fg_ok = 0;
+  int big_fg = 0;             // the long-system kernels may use the grid (fg_bias)
   int fg_use = 1;            // test option: 0 keeps the TwoSum double-float kernel
   float fg_bias = 0.f;
   int fg_gm_full = 0, fg_gm_none = 0, fg_gk_none = 0, fg_gk_full = 0;

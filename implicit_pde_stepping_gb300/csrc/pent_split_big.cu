@@ -102,11 +102,11 @@ __device__ __noinline__ uint32_t column_word(const double* v, int n) {
 // local sweeps in that scale, x' in place of f, the summaries, and the two
 // per-system words (largest magnitude, largest chunk exponent), reduced over
 // the CTA and folded in with one atomic each (both zeroed before).
-template <int SPW, bool CYC>
+template <int SPW, bool CYC, bool FG>
 __global__ void __launch_bounds__(kBigThreads, 2)
     k_big_local(const float4* __restrict__ tab, double* __restrict__ X, double* __restrict__ sum,
                 double* __restrict__ xm, unsigned* __restrict__ smag, unsigned* __restrict__ sexp,
-                int* __restrict__ cexp, int M, int P, int batch, int2 dup) {
+                int* __restrict__ cexp, int M, int P, int batch, int2 dup, float B) {
   constexpr int L = kBigL;
   constexpr int NW = kBigThreads / 32;
   __shared__ unsigned red[2][NW][SPW];
@@ -193,31 +193,73 @@ __global__ void __launch_bounds__(kBigThreads, 2)
   const uint32_t off = fg::in_offset(econv);
   const float4* t = tab + (size_t)table_chunk(c, dup) * L * kSpK;
   D2 v[L];
-  {
-    D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+  if constexpr (FG) {
+    // the sweeps on the plan's fixed grid (pent_fg.cu, fg.cuh): bias B, values
+    // (a - B) + l; the plan bounds them for a chunk whose largest |f| is in [1, 2)
+    float va[L], vl[L];
+    {
+      float y1h = 0.f, y1l = 0.f, y2h = 0.f, y2l = 0.f;
 #pragma unroll
-    for (int j = 0; j < L; ++j) {
-      const double f = (row0 + j < M) ? mine[j * kBigThreads] : 0.0;
-      const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
-      float fh, fl;
-      fg::split(f, off, fh, fl);
-      const D2 g = df::sum3p(D2{c0.x, c0.y}, D2{fh, fl}, D2{c0.z, c0.w}, a2, D2{c1.x, c1.y}, a1);
-      v[j] = g;
-      a2 = a1;
-      a1 = g;
+      for (int j = 0; j < L; ++j) {
+        const double f = (row0 + j < M) ? mine[j * kBigThreads] : 0.0;
+        const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
+        float fh, fl, a, l;
+        fg::split(f, off, fh, fl);
+        fg::start(a, l, B, c0.x, c0.y, fh, fl);
+        fg::madd(a, l, c0.z, c0.w, y2h, y2l);
+        fg::madd(a, l, c1.x, c1.y, y1h, y1l);
+        va[j] = a;
+        vl[j] = l;
+        y2h = y1h;
+        y2l = y1l;
+        y1h = __fsub_rn(a, B);
+        y1l = l;
+      }
     }
-  }
-  o[0] = make_float2(v[L - 2].h, v[L - 2].l);
-  o[1] = make_float2(v[L - 1].h, v[L - 1].l);
-  {
-    D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+    o[0] = make_float2(__fsub_rn(va[L - 2], B), vl[L - 2]);
+    o[1] = make_float2(__fsub_rn(va[L - 1], B), vl[L - 1]);
+    {
+      float x1h = 0.f, x1l = 0.f, x2h = 0.f, x2l = 0.f;
 #pragma unroll
-    for (int j = L - 1; j >= 0; --j) {
-      const float4 c2 = __ldg(t + j * kSpK + 2);
-      const D2 y = df::sum3(v[j], D2{c2.x, c2.y}, a1, D2{c2.z, c2.w}, a2);
-      v[j] = y;
-      a2 = a1;
-      a1 = y;
+      for (int j = L - 1; j >= 0; --j) {
+        const float4 c2 = __ldg(t + j * kSpK + 2);
+        float a = va[j], l = vl[j];
+        fg::madd(a, l, c2.z, c2.w, x2h, x2l);
+        fg::madd(a, l, c2.x, c2.y, x1h, x1l);
+        x2h = x1h;
+        x2l = x1l;
+        x1h = __fsub_rn(a, B);
+        x1l = l;
+        v[j] = D2{x1h, l};
+      }
+    }
+  } else {
+    {
+      D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < L; ++j) {
+        const double f = (row0 + j < M) ? mine[j * kBigThreads] : 0.0;
+        const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
+        float fh, fl;
+        fg::split(f, off, fh, fl);
+        const D2 g = df::sum3p(D2{c0.x, c0.y}, D2{fh, fl}, D2{c0.z, c0.w}, a2, D2{c1.x, c1.y}, a1);
+        v[j] = g;
+        a2 = a1;
+        a1 = g;
+      }
+    }
+    o[0] = make_float2(v[L - 2].h, v[L - 2].l);
+    o[1] = make_float2(v[L - 1].h, v[L - 1].l);
+    {
+      D2 a1{0.f, 0.f}, a2{0.f, 0.f};
+#pragma unroll
+      for (int j = L - 1; j >= 0; --j) {
+        const float4 c2 = __ldg(t + j * kSpK + 2);
+        const D2 y = df::sum3(v[j], D2{c2.x, c2.y}, a1, D2{c2.z, c2.w}, a2);
+        v[j] = y;
+        a2 = a1;
+        a1 = y;
+      }
     }
   }
   o[2] = make_float2(v[0].h, v[0].l);
@@ -354,12 +396,12 @@ __device__ __noinline__ void scale_rows(double* p, long long ld, int n, double f
   for (int j = 0; j < n; ++j) p[j * ld] *= f;
 }
 
-template <int SPW, bool CYC>
+template <int SPW, bool CYC, bool FG>
 __global__ void __launch_bounds__(kBigThreads)
     k_big_fix(const float4* __restrict__ tab, const float2* __restrict__ ctab,
               const double* __restrict__ extra, const float2* __restrict__ sum, double* __restrict__ X,
               const unsigned* __restrict__ smag, const unsigned* __restrict__ sexp,
-              const int* __restrict__ cexp, int M, int P, int batch, int2 dup) {
+              const int* __restrict__ cexp, int M, int P, int batch, int2 dup, float B) {
   constexpr int L = kBigL;
   int s, c;
   place<SPW>(s, c);
@@ -405,14 +447,28 @@ __global__ void __launch_bounds__(kBigThreads)
     for (int u = 0; u < G; ++u) {
       const int j = j0 + u;
       const float4 c3 = __ldg(t + j * kSpK + 3), c4 = __ldg(t + j * kSpK + 4);
-      D2 x = df::axpy(scaled(D2{xv[u].x, xv[u].y}, fx), D2{c3.x, c3.y}, S0);
-      x = df::axpy(x, D2{c3.z, c3.w}, S1);
-      x = df::axpy(x, D2{c4.x, c4.y}, T0);
-      x = df::axpy(x, D2{c4.z, c4.w}, T1);
-      if (CYC && needU) {
-        const float4 c1 = __ldg(t + j * kSpK + 1), c5 = __ldg(t + j * kSpK + 5);
-        x = df::axpy(x, D2{c1.z, c1.w}, X0);
-        x = df::axpy(x, D2{c5.x, c5.y}, X1);
+      D2 x;
+      if constexpr (FG) {
+        // on the plan's grid: x' (brought to the system's scale) onto it exactly,
+        // then the four correction terms as fixed-grid multiply-adds
+        const float hs = xv[u].x * fx, ls = xv[u].y * fx;
+        float a = __fadd_rn(B, hs);
+        float l = __fadd_rn(ls, __fsub_rn(hs, __fsub_rn(a, B)));
+        fg::madd(a, l, c3.x, c3.y, S0.h, S0.l);
+        fg::madd(a, l, c3.z, c3.w, S1.h, S1.l);
+        fg::madd(a, l, c4.x, c4.y, T0.h, T0.l);
+        fg::madd(a, l, c4.z, c4.w, T1.h, T1.l);
+        x = D2{__fsub_rn(a, B), l};
+      } else {
+        x = df::axpy(scaled(D2{xv[u].x, xv[u].y}, fx), D2{c3.x, c3.y}, S0);
+        x = df::axpy(x, D2{c3.z, c3.w}, S1);
+        x = df::axpy(x, D2{c4.x, c4.y}, T0);
+        x = df::axpy(x, D2{c4.z, c4.w}, T1);
+        if (CYC && needU) {
+          const float4 c1 = __ldg(t + j * kSpK + 1), c5 = __ldg(t + j * kSpK + 5);
+          x = df::axpy(x, D2{c1.z, c1.w}, X0);
+          x = df::axpy(x, D2{c5.x, c5.y}, X1);
+        }
       }
       // three rows in four join through integers, off the slow fp64 pipe
       const double xo = (j & 3) != 0 ? fg::join_int(x.h, x.l, off) : fg::join(x.h, x.l, off);
@@ -440,12 +496,16 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   int* cexp = reinterpret_cast<int*>(sexp + batch);
   const int2 dup = make_int2(p.dup_lo, p.dup_hi);
   const size_t smem_local = (size_t)kBigL * kBigThreads * sizeof(double);
-  cudaError_t e = kernel_prepare((const void*)k_big_local<SPW, CYC>, smem_local, kBigThreads, nullptr);
+  // non-cyclic plans whose grid the plan derived: sweeps and fix-up on it
+  const bool fgrid = !CYC && p.big_fg && p.fg_use;
+  auto local = fgrid ? k_big_local<SPW, CYC, true> : k_big_local<SPW, CYC, false>;
+  auto fix = fgrid ? k_big_fix<SPW, CYC, true> : k_big_fix<SPW, CYC, false>;
+  cudaError_t e = kernel_prepare((const void*)local, smem_local, kBigThreads, nullptr);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(smag, 0, 2 * (size_t)batch * sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
-  k_big_local<SPW, CYC><<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, smag, sexp, cexp, p.M,
-                                                               P, batch, dup);
+  local<<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, smag, sexp, cexp, p.M, P, batch, dup,
+                                               p.fg_bias);
   note_launch();
   const long long n = (long long)P * batch;
   float2* sumd = reinterpret_cast<float2*>(p.spsum);
@@ -457,8 +517,8 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
         p.spchunk, p.spchunk_df, p.spextra, sumd, xm, X, smag, sexp, cexp, p.M, P, batch, dup);
     note_launch();
   }
-  k_big_fix<SPW, CYC><<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, smag, sexp, cexp,
-                                                   p.M, P, batch, dup);
+  fix<<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, smag, sexp, cexp, p.M, P, batch,
+                                    dup, p.fg_bias);
   note_launch();
   return cudaGetLastError();
 }
