@@ -273,6 +273,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   const size_t o_spextra = off; off = round_up(off + kSpExtra * sizeof(double), 256);
   const size_t o_status = off; off = round_up(off + sizeof(int), 256);
   const size_t o_kerr = off; off = round_up(off + sizeof(int), 256);
+  const size_t o_sched = off; off = round_up(off + 2 * sizeof(unsigned), 256);
   const size_t o_twtab = off; off = round_up(off + (size_t)p->M * kTwK * sizeof(float4), 256);
   const size_t o_twist = off; off = round_up(off + kTwistCount * sizeof(double), 256);
   char* arena = nullptr;
@@ -300,6 +301,7 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   double* d_work = reinterpret_cast<double*>(arena + o_work);
   int* d_status = reinterpret_cast<int*>(arena + o_status);
   p->kern_err = reinterpret_cast<int*>(arena + o_kerr);
+  p->sched = reinterpret_cast<unsigned*>(arena + o_sched);
 
   int status = 0;
   e = cudaMemset(arena, 0, off);

@@ -60,6 +60,7 @@ struct FgArgs {
   const double* tail64;
   double* X;
   int* err;                 // set to 1 if a tile copy never completed
+  unsigned* sched;          // {next block, CTAs done}: the block queue, zero at launch
   int M, P, batch, T;
   int dup_lo, dup_hi;       // chunks dup_lo < c <= dup_hi read chunk dup_lo's row tables
   int RS, BR;               // staged rows (multiple of BR) and rows per TMA box
@@ -96,6 +97,7 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   float2* sW = sE + (size_t)SB * P * 2;                                      // [SB][P][2]
   uint32_t* smax = reinterpret_cast<uint32_t*>(sW + (size_t)SB * P * 2);     // [SB]
   __shared__ uint64_t bar;
+  __shared__ int s_next;                     // the CTA's next block (thread 0 writes it after barrier 1)
 
   for (int t = threadIdx.x; t < P * L * K4; t += blockDim.x) {
     const int row = t / K4, k = t % K4, cc = row / L;
@@ -141,21 +143,30 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
   const float2* ct = ctab2 + (size_t)c * kSpChunk;
   const float B = g.B;
 
+  // Blocks after the first gridDim.x come from a queue (an atomic counter), so
+  // CTAs that run faster take more of them: of the two CTAs sharing an SM the
+  // warp scheduler favours one, which with a fixed share of the blocks finished
+  // in 70% of the other's time, leaving the SM to one CTA (at under half the
+  // two-CTA rate) for the rest of the launch.
   unsigned phase = 0;
-  for (int blk = blockIdx.x; blk < nblk; blk += gridDim.x, phase ^= 1u) {
+  for (int blk = blockIdx.x; blk < nblk; phase ^= 1u) {
     const int s = blk * SB + sys;
     const bool act = s < batch;
     double* p = g.X + (long long)row0 * ld + (act ? s : 0);
 
     // ---- 1. load; the system's largest |f| sets its scale
     double fv[L];
+    // the block after the next one is claimed now; the claim returns while the
+    // tile is read, and its tile is requested after barrier 1
+    unsigned claim = 0u;
+    if (threadIdx.x == 0) claim = atomicAdd(&g.sched[0], 1u);
     if constexpr (TMA) {
       // bounded wait for the tile (2 s); every thread of the CTA agrees on the
       // outcome before anyone reaches the next barrier
       const bool ok = tma::mbar_wait(&bar, phase, 2000000000ull);
       if (__syncthreads_or(!ok)) {
         if (threadIdx.x == 0) atomicExch(g.err, 1);
-        return;
+        break;
       }
       // Chunks start 2 KB apart, so the four chunks of a warp would read the
       // same 16 banks; odd chunks read each pair of rows in swapped order,
@@ -177,12 +188,13 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     for (int j = 0; j < L; j += 2) mx = max(mx, fg::mag_pair(fv[j], fv[j + 1], nz));
     atomicMax(&smax[sys], mx | (nz != 0u ? 1u : 0u));
     __syncthreads();                                     // tile read, smax complete
-    if constexpr (TMA) {
+    if (threadIdx.x == 0) {
+      const int nb = (int)gridDim.x + (int)claim;
+      s_next = nb;
       // the next block's tile streams in behind the rest of this block
-      if (threadIdx.x == 0 && blk + (int)gridDim.x < nblk) {
+      if (TMA && nb < nblk) {
         tma::mbar_expect_tx(&bar, (unsigned)tile_bytes(g.RS, SB));
-        for (int y = 0; y < g.RS; y += g.BR)
-          tma::load_2d(tile + (size_t)y * SB, &fmap, (blk + gridDim.x) * SB, y, &bar);
+        for (int y = 0; y < g.RS; y += g.BR) tma::load_2d(tile + (size_t)y * SB, &fmap, nb * SB, y, &bar);
       }
     }
     const fg::SysClass sc = fg::classify(smax[sys], kEMin, kEMax);
@@ -388,6 +400,16 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     // systems whose largest entry is subnormal or not finite: one thread solves
     // the column in fp64 (its f is untouched: nothing of it has been stored)
     if (native && c == 0) native_solve_col(NativeTabs{g.coef64, g.tail64, nullptr}, g.X + s, M, (size_t)ld, 0);
+    blk = s_next;                                        // written before barrier 2
+  }
+  // the last CTA out leaves the queue at zero for the next launch (its claims,
+  // and every other CTA's, precede their count)
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&g.sched[1], 1u) == gridDim.x - 1u) {
+      atomicExch(&g.sched[0], 0u);
+      atomicExch(&g.sched[1], 0u);
+    }
   }
 }
 
@@ -432,6 +454,7 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, cudaStream_t st) 
   a.tail64 = p.tail64;
   a.X = X;
   a.err = p.kern_err;
+  a.sched = p.sched;
   a.M = p.M;
   a.P = P;
   a.batch = batch;

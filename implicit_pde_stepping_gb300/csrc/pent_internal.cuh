@@ -82,6 +82,8 @@ struct pent_plan_s {
   int fg_gm_full = 0, fg_gm_none = 0, fg_gk_none = 0, fg_gk_full = 0;
   int fg_dup_lo = 0, fg_dup_hi = 0;   // chunks dup_lo < c <= dup_hi share chunk dup_lo's row tables
   int* kern_err = nullptr;   // device word: 1 once a kernel gave up waiting for a tile copy
+  unsigned* sched = nullptr; // device words {next block, CTAs done} of the persistent solve's
+                             // block queue; zero between launches (the last CTA resets them)
   double fg_bound = 0.0;
   float4* sptab = nullptr;   // [Mpad][kSpK]
   double* spchunk = nullptr; // [sp_P][kSpChunk]
