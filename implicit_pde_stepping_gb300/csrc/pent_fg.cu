@@ -160,14 +160,11 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
     // tile is read, and its tile is requested after barrier 1
     unsigned claim = 0u;
     if (threadIdx.x == 0) claim = atomicAdd(&g.sched[0], 1u);
+    bool tile_ok = true;
     if constexpr (TMA) {
-      // bounded wait for the tile (2 s); every thread of the CTA agrees on the
-      // outcome before anyone reaches the next barrier
-      const bool ok = tma::mbar_wait(&bar, phase, 2000000000ull);
-      if (__syncthreads_or(!ok)) {
-        if (threadIdx.x == 0) atomicExch(g.err, 1);
-        break;
-      }
+      // bounded wait for the tile (2 s); the CTA agrees on the outcome at
+      // barrier 1 (a thread whose wait failed reads stale data, which no one uses)
+      tile_ok = tma::mbar_wait(&bar, phase, 2000000000ull);
       // Chunks start 2 KB apart, so the four chunks of a warp would read the
       // same 16 banks; odd chunks read each pair of rows in swapped order,
       // which puts them on the other 16 banks.
@@ -187,7 +184,13 @@ __global__ void __launch_bounds__(MAXT, (MAXT <= 256 ? 2 : 1))
 #pragma unroll
     for (int j = 0; j < L; j += 2) mx = max(mx, fg::mag_pair(fv[j], fv[j + 1], nz));
     atomicMax(&smax[sys], mx | (nz != 0u ? 1u : 0u));
-    __syncthreads();                                     // tile read, smax complete
+    // barrier 1: tile read, smax complete (the warps of the previous block are
+    // all past its barrier 3, after which nothing reads what this block writes
+    // before here)
+    if (__syncthreads_or(!tile_ok)) {
+      if (threadIdx.x == 0) atomicExch(g.err, 1);
+      break;
+    }
     if (threadIdx.x == 0) {
       const int nb = (int)gridDim.x + (int)claim;
       s_next = nb;

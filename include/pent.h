@@ -99,6 +99,12 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
  * entry is zero, subnormal, non-finite or beyond the scaled kernels' window
  * are solved in native fp64.  Accuracy is relative to each system's largest
  * |x| (about 1e-13 against an fp64 solve).
+ * Ordering: the plan holds device state that a solve uses while it runs (the
+ * block queue of the persistent kernel, the chunk summaries of long systems),
+ * so solves with one plan must be ordered (issued on one stream, or separated
+ * by events); solves on different streams at once need one plan each.  The
+ * state is back in its initial form when a solve completes, so a solve
+ * captured in a CUDA graph can be replayed.
  */
 pent_status pent_solve(pent_plan plan, void* rhs_inout, int batch, void* stream);
 

@@ -181,3 +181,23 @@ def test_outputs_on_binade_edges(cyclic, N):
     F = banded_matvec(bands, X, cyclic)
     out = solve(bands, F, variant="auto", cyclic=cyclic)
     assert max_rel_err(out, X) < TOL_F64
+
+
+def test_block_queue_across_solves():
+    """The persistent kernel takes every block after a CTA's first from a counter in
+    the plan, which the last CTA resets.  One plan solves batches of 1, exactly one
+    block per CTA, one block more, several blocks per CTA and a ragged batch in turn:
+    a counter left over from an earlier solve would leave blocks unsolved."""
+    N = 1024                                  # 32 chunks: CTAs of 8 systems x 32 threads
+    bands = inputs.hyper_bands(N, 1.0)
+    plan = pent.pent_factor(bands, 4096)
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count   # two CTAs of 8 systems each
+    for k, batch in enumerate([1, 16 * sms, 16 * sms + 8, 5000, 37, 16 * sms + 8]):
+        F = inputs.rhs_uniform(N, batch, seed=100 + k)
+        X = dev(F)
+        pent.pent_solve(plan, X)
+        pent.pent_sync()
+        assert plan.error() == pent.OK
+        assert max_rel_err(host(X), oracle.batch_shared(bands, F)) < TOL_F64, batch
+    plan.close()
