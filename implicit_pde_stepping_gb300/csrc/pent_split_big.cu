@@ -35,6 +35,8 @@
 // tables as (hi, lo) pairs), which keeps them off the fp64 pipe; only the
 // periodic border (one thread per system) works in fp64.  The parallelism is
 // batch x P threads, so a handful of very long systems still fills the GPU.
+#include <type_traits>
+
 #include "cp_async.cuh"
 #include "df64.cuh"
 #include "fg.cuh"
@@ -52,6 +54,10 @@ constexpr int kBigL = 32;       // rows per chunk (the plan's sp_L for long syst
 // read those, which stay in cache.
 __device__ __forceinline__ int table_chunk(int c, int2 dup) { return (c > dup.x && c <= dup.y) ? dup.x : c; }
 constexpr int kBigThreads = 256;
+// threads of k_big_local and k_big_fix: CTAs of 4 warps, each staging its rows in
+// 32 KB of shared memory, four CTAs to an SM (0.164 -> 0.161 ms per solve of 16
+// systems of 2^20 rows against CTAs of 8 warps, two to an SM)
+constexpr int kLocalThreads = 128;
 constexpr int kSum = 8;         // doubles per (chunk, system): e(2) x'start(2) s(2) w(2)
 
 __device__ __forceinline__ void mv2(const double* A, double x0, double x1, double& y0, double& y1) {
@@ -64,12 +70,12 @@ __device__ __forceinline__ void mv2(const double* A, double x0, double x1, doubl
 // runs over groups of systems and y over groups of chunks, so the CTAs that
 // read the same table rows for different systems are scheduled together and
 // share them through L2.
-template <int SPW>
+template <int SPW, int NT>
 __device__ __forceinline__ void place(int& s, int& c) {
   constexpr int CPW = 32 / SPW;                      // chunks per warp
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
   s = blockIdx.x * SPW + lane % SPW;
-  c = (blockIdx.y * (kBigThreads / 32) + w) * CPW + lane / SPW;
+  c = (blockIdx.y * (NT / 32) + w) * CPW + lane / SPW;
 }
 
 constexpr int kZeroChunk = -(1 << 20);   // chunk exponent of an all-zero (or non-finite) chunk
@@ -86,12 +92,12 @@ __device__ __forceinline__ double scale2(double x, int d) {
 __device__ __forceinline__ float pow2f(int d) { return d >= -126 ? __uint_as_float((uint32_t)(127 + d) << 23) : 0.f; }
 __device__ __forceinline__ D2 scaled(D2 v, float f) { return D2{v.h * f, v.l * f}; }
 
-// Magnitude word of n values at a stride of kBigThreads doubles (a separate
+// Magnitude word of n values at a stride of kLocalThreads doubles (a separate
 // call, so that the sweeps that follow reload f instead of keeping it live)
 __device__ __noinline__ uint32_t column_word(const double* v, int n) {
   uint32_t mx = 0u, nz = 0u;
   for (int j = 0; j < n; ++j) {
-    const double f = v[j * kBigThreads];
+    const double f = v[j * kLocalThreads];
     mx = max(mx, fg::mag_bits(f));
     nz |= (uint32_t)__double2loint(f);
   }
@@ -103,26 +109,27 @@ __device__ __noinline__ uint32_t column_word(const double* v, int n) {
 // per-system words (largest magnitude, largest chunk exponent), reduced over
 // the CTA and folded in with one atomic each (both zeroed before).
 template <int SPW, bool CYC, bool FG>
-__global__ void __launch_bounds__(kBigThreads, 2)
+__global__ void __launch_bounds__(kLocalThreads, 4)
     k_big_local(const float4* __restrict__ tab, double* __restrict__ X, double* __restrict__ sum,
                 double* __restrict__ xm, unsigned* __restrict__ smag, unsigned* __restrict__ sexp,
                 int* __restrict__ cexp, int M, int P, int batch, int2 dup, float B) {
   constexpr int L = kBigL;
-  constexpr int NW = kBigThreads / 32;
+  constexpr int NT = kLocalThreads;
+  constexpr int NW = NT / 32;
   __shared__ unsigned red[2][NW][SPW];
   int s, c;
-  place<SPW>(s, c);
+  place<SPW, NT>(s, c);
   const bool act = s < batch && c < P;
   const long long ld = batch;
   const int row0 = c * L;
   double* p = X + (long long)row0 * ld + (act ? s : 0);
   // the chunk's f into this thread's shared-memory column, every row in flight at once
-  extern __shared__ double sf[];                  // [L][kBigThreads]
+  extern __shared__ double sf[];                  // [L][NT]
   double* mine = sf + threadIdx.x;
   if (act) {
 #pragma unroll
     for (int j = 0; j < L; ++j)
-      if (row0 + j < M) cp_async8(mine + j * kBigThreads, p + (long long)j * ld);
+      if (row0 + j < M) cp_async8(mine + j * NT, p + (long long)j * ld);
   }
   cp_async_wait_all();
   // magnitude word: largest high word without sign, bit 0 set if any low word is nonzero
@@ -138,8 +145,8 @@ __global__ void __launch_bounds__(kBigThreads, 2)
 #pragma unroll
       for (int j = 0; j < L; ++j)
         if (row0 + j < M) {
-          const double f = mine[j * kBigThreads] * 0x1p600;
-          mine[j * kBigThreads] = f;
+          const double f = mine[j * NT] * 0x1p600;
+          mine[j * NT] = f;
           m2 = max(m2, fg::mag_bits(f));
         }
       econv = m2 >> 20;
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(kBigThreads, 2)
       float y1h = 0.f, y1l = 0.f, y2h = 0.f, y2l = 0.f;
 #pragma unroll
       for (int j = 0; j < L; ++j) {
-        const double f = (row0 + j < M) ? mine[j * kBigThreads] : 0.0;
+        const double f = (row0 + j < M) ? mine[j * NT] : 0.0;
         const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
         float fh, fl, a, l;
         fg::split(f, off, fh, fl);
@@ -238,7 +245,7 @@ __global__ void __launch_bounds__(kBigThreads, 2)
       D2 a1{0.f, 0.f}, a2{0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < L; ++j) {
-        const double f = (row0 + j < M) ? mine[j * kBigThreads] : 0.0;
+        const double f = (row0 + j < M) ? mine[j * NT] : 0.0;
         const float4 c0 = __ldg(t + j * kSpK), c1 = __ldg(t + j * kSpK + 1);
         float fh, fl;
         fg::split(f, off, fh, fl);
@@ -397,27 +404,37 @@ __device__ __noinline__ void scale_rows(double* p, long long ld, int n, double f
 }
 
 template <int SPW, bool CYC, bool FG>
-__global__ void __launch_bounds__(kBigThreads)
+__global__ void __launch_bounds__(kLocalThreads, 4)
     k_big_fix(const float4* __restrict__ tab, const float2* __restrict__ ctab,
               const double* __restrict__ extra, const float2* __restrict__ sum, double* __restrict__ X,
               const unsigned* __restrict__ smag, const unsigned* __restrict__ sexp,
-              const int* __restrict__ cexp, int M, int P, int batch, int2 dup, float B) {
+              const int* __restrict__ cexp, int M, int P, int batch, int2 dup, float B, int4 groups) {
   constexpr int L = kBigL;
+  constexpr int NT = kLocalThreads;
   int s, c;
-  place<SPW>(s, c);
+  place<SPW, NT>(s, c);
   if (s >= batch || c >= P) return;
   const long long ld = batch;
   const int row0 = c * L;
   if (row0 >= M) return;
   double* p = X + (long long)row0 * ld + s;
+  const int nrow = M - row0 < L ? M - row0 : L;
   if (sexp[s] != 0u && (smag[s] >> 20) == 0x7FFu) {
     // an inf or NaN entry: the system's solution is not finite
-    fill_nan(p, ld, M - row0 < L ? M - row0 : L);
+    fill_nan(p, ld, nrow);
     if (CYC && c == 0) fill_nan(X + (long long)M * ld + s, ld, 2);
     return;
   }
   int E;
   if (!system_exp(smag, sexp, s, E)) return;      // all zero: already solved
+  // the chunk's x' (pairs) into this thread's shared-memory column, every row in
+  // flight while the chunk states are formed
+  extern __shared__ float2 sx[];                  // [L][NT]
+  float2* mine = sx + threadIdx.x;
+  const float2* q = reinterpret_cast<const float2*>(p);
+#pragma unroll
+  for (int j = 0; j < L; ++j)
+    if (j < nrow) cp_async8(mine + j * NT, q + (long long)j * ld);
   // the join to fp64 at 2^E, or at the edge of its window and then one fp64 product
   const int eo = E < (int)fg::kEMin ? (int)fg::kEMin : (E > (int)fg::kEMax ? (int)fg::kEMax : E);
   const uint32_t off = fg::out_offset((uint32_t)eo);
@@ -435,44 +452,77 @@ __global__ void __launch_bounds__(kBigThreads)
     X0 = df::from_double(-scale2(X[(long long)M * ld + s], 1023 - E));
     X1 = df::from_double(-scale2(X[(long long)(M + 1) * ld + s], 1023 - E));
   }
-  const float2* q = reinterpret_cast<const float2*>(p);
+  cp_async_wait_all();
   const float4* t = tab + (size_t)table_chunk(c, dup) * L * kSpK;
-  constexpr int G = 8;
-#pragma unroll
-  for (int j0 = 0; j0 < L; j0 += G) {
-    float2 xv[G];
-#pragma unroll
-    for (int u = 0; u < G; ++u) xv[u] = (row0 + j0 + u < M) ? q[(j0 + u) * ld] : make_float2(0.f, 0.f);
-#pragma unroll
-    for (int u = 0; u < G; ++u) {
-      const int j = j0 + u;
+  auto emit = [&](int j, D2 x) {
+    // three rows in four join through integers, off the slow fp64 pipe
+    const double xo = (j & 3) != 0 ? fg::join_int(x.h, x.l, off) : fg::join(x.h, x.l, off);
+    fg::store_cs_if(p + j * ld, xo, j < nrow);
+  };
+  if constexpr (FG) {
+    // on the plan's grid: x' (brought to the system's scale) onto it exactly, then
+    // the correction terms as fixed-grid multiply-adds, in 8-row groups whose kinds
+    // the plan fixed (2 full, 1 low word alone, 0 none; the M responses fall down a
+    // chunk, the K responses up it); one row with the kinds of its terms
+    // (compile-time in the common groups, tested per row in the others)
+    auto row = [&](int j, auto mk, auto kk) {
+      const float2 xv = j < nrow ? mine[j * NT] : make_float2(0.f, 0.f);
+      const float hs = xv.x * fx, ls = xv.y * fx;
+      float a = __fadd_rn(B, hs);
+      float l = __fadd_rn(ls, __fsub_rn(hs, __fsub_rn(a, B)));
       const float4 c3 = __ldg(t + j * kSpK + 3), c4 = __ldg(t + j * kSpK + 4);
-      D2 x;
-      if constexpr (FG) {
-        // on the plan's grid: x' (brought to the system's scale) onto it exactly,
-        // then the four correction terms as fixed-grid multiply-adds
-        const float hs = xv[u].x * fx, ls = xv[u].y * fx;
-        float a = __fadd_rn(B, hs);
-        float l = __fadd_rn(ls, __fsub_rn(hs, __fsub_rn(a, B)));
+      if (mk == 2) {
         fg::madd(a, l, c3.x, c3.y, S0.h, S0.l);
         fg::madd(a, l, c3.z, c3.w, S1.h, S1.l);
+      } else if (mk == 1) {
+        fg::madd_low(l, c3.x, S0.h);
+        fg::madd_low(l, c3.z, S1.h);
+      }
+      if (kk == 2) {
         fg::madd(a, l, c4.x, c4.y, T0.h, T0.l);
         fg::madd(a, l, c4.z, c4.w, T1.h, T1.l);
-        x = D2{__fsub_rn(a, B), l};
-      } else {
-        x = df::axpy(scaled(D2{xv[u].x, xv[u].y}, fx), D2{c3.x, c3.y}, S0);
-        x = df::axpy(x, D2{c3.z, c3.w}, S1);
-        x = df::axpy(x, D2{c4.x, c4.y}, T0);
-        x = df::axpy(x, D2{c4.z, c4.w}, T1);
-        if (CYC && needU) {
-          const float4 c1 = __ldg(t + j * kSpK + 1), c5 = __ldg(t + j * kSpK + 5);
-          x = df::axpy(x, D2{c1.z, c1.w}, X0);
-          x = df::axpy(x, D2{c5.x, c5.y}, X1);
-        }
+      } else if (kk == 1) {
+        fg::madd_low(l, c4.x, T0.h);
+        fg::madd_low(l, c4.z, T1.h);
       }
-      // three rows in four join through integers, off the slow fp64 pipe
-      const double xo = (j & 3) != 0 ? fg::join_int(x.h, x.l, off) : fg::join(x.h, x.l, off);
-      fg::store_cs_if(p + j * ld, xo, row0 + j < M);
+      emit(j, D2{__fsub_rn(a, B), l});
+    };
+    using K1 = std::integral_constant<int, 1>;
+    using K2 = std::integral_constant<int, 2>;
+#pragma unroll
+    for (int gi = 0; gi < L / 8; ++gi) {
+      const int mk = gi < groups.x ? 2 : (gi < groups.y ? 1 : 0);
+      const int kk = gi >= groups.w ? 2 : (gi >= groups.z ? 1 : 0);
+      const int j0 = gi * 8;
+      if (mk == 2 && kk == 2) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) row(j0 + u, K2{}, K2{});
+      } else if (mk == 2 && kk == 1) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) row(j0 + u, K2{}, K1{});
+      } else if (mk == 1 && kk == 2) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) row(j0 + u, K1{}, K2{});
+      } else {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) row(j0 + u, mk, kk);
+      }
+    }
+  } else {
+#pragma unroll 8
+    for (int j = 0; j < L; ++j) {
+      const float2 xv = j < nrow ? mine[j * NT] : make_float2(0.f, 0.f);
+      const float4 c3 = __ldg(t + j * kSpK + 3), c4 = __ldg(t + j * kSpK + 4);
+      D2 x = df::axpy(scaled(D2{xv.x, xv.y}, fx), D2{c3.x, c3.y}, S0);
+      x = df::axpy(x, D2{c3.z, c3.w}, S1);
+      x = df::axpy(x, D2{c4.x, c4.y}, T0);
+      x = df::axpy(x, D2{c4.z, c4.w}, T1);
+      if (CYC && needU) {
+        const float4 c1 = __ldg(t + j * kSpK + 1), c5 = __ldg(t + j * kSpK + 5);
+        x = df::axpy(x, D2{c1.z, c1.w}, X0);
+        x = df::axpy(x, D2{c5.x, c5.y}, X1);
+      }
+      emit(j, x);
     }
   }
   if (eo != E) {
@@ -486,7 +536,7 @@ __global__ void __launch_bounds__(kBigThreads)
 template <int SPW, bool CYC>
 cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   const int P = p.sp_P;
-  constexpr int CPB = (kBigThreads / 32) * (32 / SPW);     // chunks per CTA
+  constexpr int CPB = (kLocalThreads / 32) * (32 / SPW);   // chunks per CTA
   const dim3 grid((batch + SPW - 1) / SPW, (P + CPB - 1) / CPB);
   if (grid.y > 65535) return cudaErrorInvalidConfiguration;
   // scratch: summaries, x' at rows M-2, M-1, the two per-system words, chunk exponents
@@ -495,16 +545,18 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
   unsigned* sexp = smag + batch;
   int* cexp = reinterpret_cast<int*>(sexp + batch);
   const int2 dup = make_int2(p.dup_lo, p.dup_hi);
-  const size_t smem_local = (size_t)kBigL * kBigThreads * sizeof(double);
+  const size_t smem_local = (size_t)kBigL * kLocalThreads * sizeof(double);
+  const size_t smem_fix = (size_t)kBigL * kLocalThreads * sizeof(float2);
   // non-cyclic plans whose grid the plan derived: sweeps and fix-up on it
   const bool fgrid = !CYC && p.big_fg && p.fg_use;
   auto local = fgrid ? k_big_local<SPW, CYC, true> : k_big_local<SPW, CYC, false>;
   auto fix = fgrid ? k_big_fix<SPW, CYC, true> : k_big_fix<SPW, CYC, false>;
-  cudaError_t e = kernel_prepare((const void*)local, smem_local, kBigThreads, nullptr);
+  cudaError_t e = kernel_prepare((const void*)local, smem_local, kLocalThreads, nullptr);
+  if (e == cudaSuccess) e = kernel_prepare((const void*)fix, smem_fix, kLocalThreads, nullptr);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(smag, 0, 2 * (size_t)batch * sizeof(unsigned), st);
   if (e != cudaSuccess) return e;
-  local<<<grid, kBigThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, smag, sexp, cexp, p.M, P, batch, dup,
+  local<<<grid, kLocalThreads, smem_local, st>>>(p.sptab, X, p.spsum, xm, smag, sexp, cexp, p.M, P, batch, dup,
                                                p.fg_bias);
   note_launch();
   const long long n = (long long)P * batch;
@@ -517,8 +569,10 @@ cudaError_t run(pent_plan_s& p, double* X, int batch, cudaStream_t st) {
         p.spchunk, p.spchunk_df, p.spextra, sumd, xm, X, smag, sexp, cexp, p.M, P, batch, dup);
     note_launch();
   }
-  fix<<<grid, kBigThreads, 0, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, smag, sexp, cexp, p.M, P, batch,
-                                    dup, p.fg_bias);
+  // correction groups of the grid kernels (the TwoSum form applies every term)
+  const int4 groups = make_int4(p.fg_gm_full, p.fg_gm_none, p.fg_gk_none, p.fg_gk_full);
+  fix<<<grid, kLocalThreads, smem_fix, st>>>(p.sptab, p.spchunk_df, p.spextra, sumd, X, smag, sexp, cexp, p.M, P,
+                                             batch, dup, p.fg_bias, groups);
   note_launch();
   return cudaGetLastError();
 }
