@@ -266,12 +266,15 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   const int spL = p->M >= 256 ? 32 : 16;
   const int spP = ((p->M + 4 * spL - 1) / (4 * spL)) * 4;
   const size_t Mpad = (size_t)spL * spP;
-  const size_t o_work = off; off = round_up(off + 18 * (Mpad > (size_t)p->M ? Mpad : (size_t)p->M) * sizeof(double), 256);
+  // work: the partitioned tables' scratch (17 rows of Mpad), then the shared factor's
+  // (4 rows of M), so that the two factor kernels can run at once
+  const size_t wrow = Mpad > (size_t)p->M ? Mpad : (size_t)p->M;
+  const size_t o_work = off; off = round_up(off + 22 * wrow * sizeof(double), 256);
   const size_t o_sptab = off; off = round_up(off + Mpad * kSpK * sizeof(float4), 256);
   const size_t o_spchunk = off; off = round_up(off + (size_t)spP * kSpChunk * sizeof(double), 256);
   const size_t o_spchunkdf = off; off = round_up(off + (size_t)spP * kSpChunk * sizeof(float2), 256);
   const size_t o_spextra = off; off = round_up(off + kSpExtra * sizeof(double), 256);
-  const size_t o_status = off; off = round_up(off + sizeof(int), 256);
+  const size_t o_status = off; off = round_up(off + 2 * sizeof(int), 256);
   const size_t o_kerr = off; off = round_up(off + sizeof(int), 256);
   const size_t o_sched = off; off = round_up(off + 2 * sizeof(unsigned), 256);
   const size_t o_twtab = off; off = round_up(off + (size_t)p->M * kTwK * sizeof(float4), 256);
@@ -304,12 +307,32 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
   p->sched = reinterpret_cast<unsigned*>(arena + o_sched);
 
   int status = 0;
+  // The two factorisations (the native tables and the partitioned ones) are serial
+  // sweeps of one thread or one CTA each; they run at once on two streams, each
+  // with its own scratch and status word.
+  const bool split_tables = dtype == PENT_F64 && p->M >= 16;
+  int* d_status_split = d_status + 1;
+  cudaStream_t fs[2] = {nullptr, nullptr};
   e = cudaMemset(arena, 0, off);
   if (e == cudaSuccess)
     e = cudaMemcpy(d_bands, bands_host, 5 * (size_t)N * sizeof(double), cudaMemcpyHostToDevice);
-  if (e == cudaSuccess) e = factor_shared(d_bands, N, cyclic, p->coef64, p->tail64, d_work, d_status, 0);
+  // the non-blocking streams do not wait for the default stream's memset and copy
+  if (e == cudaSuccess) e = cudaStreamSynchronize(0);
+  for (auto& q : fs)
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking);
   if (e == cudaSuccess)
-    e = pack_coefficients(p->coef64, p->tail64, (int)nc, p->coef32, p->tail32, p->coefdf, p->taildf, 0);
+    e = factor_shared(d_bands, N, cyclic, p->coef64, p->tail64, d_work + 18 * wrow, d_status, fs[0]);
+  if (e == cudaSuccess)
+    e = pack_coefficients(p->coef64, p->tail64, (int)nc, p->coef32, p->tail32, p->coefdf, p->taildf, fs[0]);
+  if (e == cudaSuccess && split_tables)
+    e = factor_split(d_bands, N, cyclic, spL, (int)Mpad, p->sptab, p->spchunk, p->spextra, d_work,
+                     d_status_split, fs[1]);
+  for (auto& q : fs)
+    if (q) {
+      const cudaError_t es = cudaStreamSynchronize(q);
+      if (e == cudaSuccess) e = es;
+      cudaStreamDestroy(q);
+    }
   if (e == cudaSuccess) e = cudaMemcpy(&status, d_status, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -336,13 +359,12 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
                       !(cyclic && spL == 32 && spP > 32);
     // tables for every fp64 plan of 16 rows or more: one kernel (tables in shared
     // memory) where they fit, else the two-kernel form for long systems
-    if (dtype == PENT_F64 && p->M >= 16) {
+    if (split_tables) {
       p->sp_L = spL;
       p->sp_P = spP;
       int sstatus = 0;
-      e = factor_split(d_bands, N, cyclic, spL, (int)Mpad, p->sptab, p->spchunk, p->spextra, d_work,
-                       d_status, 0);
-      if (e == cudaSuccess) e = cudaMemcpy(&sstatus, d_status, sizeof(int), cudaMemcpyDeviceToHost);
+      // the tables were made above, alongside the native factorisation
+      e = cudaMemcpy(&sstatus, d_status_split, sizeof(int), cudaMemcpyDeviceToHost);
       if (e != cudaSuccess) {
         cudaGetLastError();
         pent_destroy(p);
