@@ -31,7 +31,9 @@
 // dropped (both decided when the plan is built).
 //
 // Warp layout: 8 consecutive systems x 4 chunks per warp, so every load or
-// store instruction moves four 64-byte runs of one row each.
+// store instruction moves four 64-byte runs of one row each.  A CTA holds 8
+// systems x P chunks; the grid is persistent, two CTAs per SM, and every block
+// of 8 systems after a CTA's first comes from an atomic queue in the plan.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
