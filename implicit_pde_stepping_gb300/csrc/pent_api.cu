@@ -417,8 +417,9 @@ pent_status pent_factor(const double* bands_host, int N, int batch, int cyclic, 
         p->cheap_k0 = p->cheap_k;
         p->cheap_m0 = p->cheap_m;
       }
-      // long systems: chunks with equal tables share one copy
-      if (p->split_big) {
+      // chunks with equal tables share one copy (long systems: in cache; the
+      // multi-step kernel: one shared-memory slot)
+      if (p->split_big || p->split_ok) {
         e = find_duplicate_chunks(*p, (int)Mpad);
         if (e != cudaSuccess) {
           cudaGetLastError();

@@ -81,9 +81,16 @@ __device__ __forceinline__ void mv2d(const float2* A, D2 x0, D2 x1, D2& y0, D2& 
   y1 = df::sum3(y1, unpack(A[2]), x0, unpack(A[3]), x1);
 }
 
-// Shared memory of one CTA (bytes), in the order the kernel carves it.
-__host__ __device__ inline size_t steps_smem(int L, int P, int SB, int rhs) {
-  size_t b = (size_t)P * (L * kSpK + 1) * sizeof(float4);        // row tables
+// Chunks dup_lo < c <= dup_hi have row and chunk tables bitwise equal to chunk
+// dup_lo's (found when the plan was built) and share its row-table slot.
+__host__ __device__ __forceinline__ int table_slot(int c, int lo, int hi) {
+  return c <= lo ? c : (c <= hi ? lo : c - (hi - lo));
+}
+
+// Shared memory of one CTA (bytes), in the order the kernel carves it; the row
+// tables in nslot slots (nslot = P without shared slots).
+__host__ __device__ inline size_t steps_smem(int L, int P, int SB, int rhs, int nslot) {
+  size_t b = (size_t)nslot * (L * kSpK + 1) * sizeof(float4);    // row tables
   b += ((size_t)P * kSpChunk + 2 * (size_t)SB * P * 2 + (size_t)SB * 8) * sizeof(double);
   b += kSpExtra * sizeof(float2);                                   // extras as (hi, lo)
   if (rhs == kStepCH) b += ((size_t)SB * P * 2 + SB) * sizeof(float2);   // halo, C_{M-1}
@@ -96,7 +103,7 @@ template <int L, int SB, int MAXT, int RHS, bool CHEAP>
 __global__ void __launch_bounds__(MAXT, 1)
     k_steps_df(const float4* __restrict__ growtab, const float2* __restrict__ gchunk,
                const double* __restrict__ gextra, double* __restrict__ X, int M, int P, int batch,
-               int nsteps, double k2d, int2 cheap, const NativeTabs nt) {
+               int nsteps, double k2d, int2 cheap, const NativeTabs nt, int dup_lo, int dup_hi) {
   constexpr bool CH = RHS == kStepCH;
   constexpr bool CN = RHS == kStepCN;
   constexpr int K4 = kSpK;
@@ -105,7 +112,8 @@ __global__ void __launch_bounds__(MAXT, 1)
   constexpr int LG = 8;                       // rows per load group
   extern __shared__ float4 smem4[];
   float4* rtab = smem4;                                              // [P][CS]
-  float2* ctab = reinterpret_cast<float2*>(rtab + (size_t)P * CS);   // [P][kSpChunk] (hi, lo)
+  const int nslot = P - (dup_hi - dup_lo);
+  float2* ctab = reinterpret_cast<float2*>(rtab + (size_t)nslot * CS);   // [P][kSpChunk] (hi, lo)
   float2* sE = ctab + (size_t)P * kSpChunk;      // [SB][P][2] local forward end values
   float2* sW = sE + (size_t)SB * P * 2;          // [SB][P][2] w_c
   float2* sX = sW + (size_t)SB * P * 2;         // [SB][8] y at 4 rows, x_t, tail state (hi, lo)
@@ -117,8 +125,9 @@ __global__ void __launch_bounds__(MAXT, 1)
   uint32_t* sgrow = smax + SB;                                                          // [SB]
 
   for (int t = threadIdx.x; t < P * L * K4; t += blockDim.x) {
-    const int row = t / K4, k = t % K4;
-    cp_async16(&rtab[(row / L) * CS + (row % L) * K4 + k], &growtab[(size_t)row * kSpK + k]);
+    const int row = t / K4, k = t % K4, cc = row / L;
+    if (cc > dup_lo && cc <= dup_hi) continue;                     // shares chunk dup_lo's slot
+    cp_async16(&rtab[table_slot(cc, dup_lo, dup_hi) * CS + (row % L) * K4 + k], &growtab[(size_t)row * kSpK + k]);
   }
   for (int t = threadIdx.x; t < P * kSpChunk / 2; t += blockDim.x) cp_async16(&ctab[2 * t], &gchunk[2 * t]);
   if (threadIdx.x < kSpExtra) sXe[threadIdx.x] = pack(df::from_double(gextra[threadIdx.x]));
@@ -132,7 +141,7 @@ __global__ void __launch_bounds__(MAXT, 1)
   const int sys = (w % SG) * 8 + (lane & 7);
   const int c = (w / SG) * 4 + (lane >> 3);
   const int row0 = c * L;
-  const float4* ctb = rtab + (size_t)c * CS;
+  const float4* ctb = rtab + (size_t)table_slot(c, dup_lo, dup_hi) * CS;
   const float2* ct = ctab + (size_t)c * kSpChunk;
   const long long ld = batch;
   const int nblk = (batch + SB - 1) / SB;
@@ -446,7 +455,8 @@ template <int L, int SB, int RHS, bool CHEAP>
 cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, double k2,
                    cudaStream_t st) {
   const int P = p.sp_P;
-  const size_t smem = steps_smem(L, P, SB, RHS);
+  const int nslot = P - (p.dup_hi - p.dup_lo);
+  const size_t smem = steps_smem(L, P, SB, RHS, nslot);
   auto kern = k_steps_df<L, SB, 512, RHS, CHEAP>;
   int per_sm = 0;
   const cudaError_t e = kernel_prepare((const void*)kern, smem, SB * P, &per_sm);
@@ -457,7 +467,7 @@ cudaError_t launch(const pent_plan_s& p, double* X, int batch, int nsteps, doubl
   if (grid > nblk) grid = nblk;
   const NativeTabs nt{p.coef64, p.tail64, p.bands};
   kern<<<grid, SB * P, smem, st>>>(p.sptab, p.spchunk_df, p.spextra, X, p.M, P, batch, nsteps, k2,
-                                   make_int2(p.cheap_k, p.cheap_m), nt);
+                                   make_int2(p.cheap_k, p.cheap_m), nt, p.dup_lo, p.dup_hi);
   note_launch();
   return cudaGetLastError();
 }
@@ -472,7 +482,7 @@ cudaError_t launch_kind(const pent_plan_s& p, double* X, int batch, int nsteps, 
   // has them is slower when none apply: measured 4% for Crank–Nicolson, 6% for
   // Cahn–Hilliard)
   const bool cheap = p.cheap_k > 0 || p.cheap_m < p.sp_L / 8;
-  const bool fits16 = p.sp_P <= 32 && steps_smem(32, p.sp_P, 16, RHS) <= kStepsSmemMax;
+  const bool fits16 = p.sp_P <= 32 && steps_smem(32, p.sp_P, 16, RHS, p.sp_P - (p.dup_hi - p.dup_lo)) <= kStepsSmemMax;
   const bool wide = p.steps_sb == 16 ? fits16 : p.steps_sb == 8 ? false : fits16 && batch > 16 * p.num_sms;
   if (wide)
     return cheap ? launch<32, 16, RHS, true>(p, X, batch, nsteps, k2, st)
@@ -486,7 +496,7 @@ cudaError_t launch_kind(const pent_plan_s& p, double* X, int batch, int nsteps, 
 bool steps_supported(const pent_plan_s& p, int kind) {
   if (!p.cyclic || !p.split_ok || p.sp_T <= 0 || p.sp_P > kSpMaxChunks) return false;
   const int rhs = kind == 1 ? kStepCH : kind == 2 ? kStepCN : kStepHyper;
-  return steps_smem(p.sp_L, p.sp_P, 8, rhs) <= kStepsSmemMax && 8 * p.sp_P <= 512;
+  return steps_smem(p.sp_L, p.sp_P, 8, rhs, p.sp_P - (p.dup_hi - p.dup_lo)) <= kStepsSmemMax && 8 * p.sp_P <= 512;
 }
 
 cudaError_t steps_df(const pent_plan_s& p, double* X, int batch, int nsteps, int kind, double k2,
